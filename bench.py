@@ -1,0 +1,408 @@
+#!/usr/bin/env python
+"""Benchmark of the ZeRO shard optimizer step on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+One step = one zero_shard_step call on the workload's stepped shard(s): the
+N-way gradient reduce + unscale + overflow check + global norm, the
+loss-scale / clip decision, and AdamW + cast into the flat buffer.  The
+default workload is the 10B FlatParameter's rank-7 shard (1.25e9 params,
+8 fp16 contributions, 60 GB resident).  Prints one JSON line on rank 0.
+
+value: Gparams/s stepped, device-timed (CUDA events on the step's stream)
+over K steps with inputs resident in HBM; the working set (tens of GB) is
+far larger than L2, so no flush is needed between steps.
+e2e: the same metric through the public API with the gradients copied from
+pinned host memory every step and the step result read back every step.
+roofline: the dominant kernel's algorithmic bytes per launch over its mean
+event-timed duration, against the measured HBM copy peak.
+cpu_baseline: the oracle (plain single-threaded C) on a bounded sample of the
+same workload, timed on this host.
+--impl reference: the oracle on the host cores as the reference arm.
+Under torchrun each rank runs an independent replica (weak scaling).
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "ZeRO shard AdamW step Gparams/s; achieved HBM GB/s as % of GB300 peak"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+RESULT_D2H_BYTES = 64            # the device state block read back with the result
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default="10b_rank7")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target length of the oracle's timed sample")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------- plumbing
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for name in ("zero_kernels.cu", "zero_kernels.cuh"):
+        with open(os.path.join(ROOT, "fsdp_sharded_mixed_zero_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel, workload))
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    sha = re.search(r"kernel_source_sha:\s*(\w+)", text)
+    tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not sha or not tr or sha.group(1) != kernel_source_sha():
+        return None
+    return float(tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for name, val in zip(self.NAMES, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------- CPU baseline
+def oracle_sample_step(w, k):
+    """Host inputs for one oracle step on k params of the workload's first
+    stepped shard (same flat indices, distributions and contributor count)."""
+    import numpy as np
+
+    import oracle
+    import synth
+    r = w.ranks[0]
+    S = w.shard_size
+    first = r * S
+    k = min(k, S)
+    scale = w.initial_scale if w.dynamic else 1.0
+    dtype = synth.BF16 if w.grad_dtype == 1 else synth.F16
+    g = synth.grads_host(w.seed, 0, w.world_size, first, k, w.sigma_g, w.sigma_n, scale, dtype,
+                         zero_from=w.full_numel)
+    g = np.ascontiguousarray(g)
+    master = synth.normal_host(w.seed, synth.MASTER, first, k, w.sigma_master)
+    m = (synth.normal_host(w.seed, synth.MOMENT_M, first, k, w.sigma_m) if w.sigma_m
+         else np.zeros(k, np.float32))
+    v = (synth.normal_host(w.seed, synth.MOMENT_V, first, k, w.sigma_v, absval=True)
+         if w.sigma_v else np.zeros(k, np.float32))
+    out = np.zeros(k, np.uint16)
+    hp = oracle.hparams(**w.hparams_kwargs())
+    st = oracle.scaler_init(hp)
+
+    def run():
+        # one shard of k params, N contributions of k elements each
+        return oracle.shard_step(hp, st, w.world_size, k * w.world_size, k, [0], g, k, 0,
+                                 [master], [m], [v], out, avg=w.op == 1,
+                                 grad_is_bf16=w.grad_dtype == 1,
+                                 param_is_bf16=w.grad_dtype == 1)
+    return run, k
+
+
+def cpu_baseline(w, target_s):
+    run, k0 = oracle_sample_step(w, 1 << 20)
+    t = time.perf_counter()
+    run()
+    t0 = time.perf_counter() - t
+    k = int(min(w.shard_size, 64 << 20, max(k0, k0 * target_s / max(t0, 1e-6))))
+    run, k = oracle_sample_step(w, k)
+    t = time.perf_counter()
+    run()
+    dt = time.perf_counter() - t
+    return {"value": k / dt / 1e9, "unit": "Gparams/s", "cores": 1, "kind": "oracle",
+            "sample": "%d params of the %s shard (%d fp16/bf16 contributions each), one full "
+                      "oracle step (reduce, norm, decision, AdamW, cast), single thread, "
+                      "%.1f s" % (k, w.name, w.world_size, dt)}
+
+
+# ---------------------------------------------------------------- arms
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    k = None
+    times = []
+    for i in range(args.warmup + args.steps):
+        if k is None:
+            run, k0 = oracle_sample_step(w, 1 << 20)
+            t = time.perf_counter()
+            run()
+            t0 = time.perf_counter() - t
+            per_step = max(0.2, min(5.0, 120.0 / max(1, args.warmup + args.steps)))
+            k = int(min(w.shard_size, max(k0, k0 * per_step / max(t0, 1e-6))))
+            run, k = oracle_sample_step(w, k)
+        t = time.perf_counter()
+        run()
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t)
+    total = sum(times)
+    value = k * len(times) / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "Gparams/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "sample_params_per_step": k},
+        "cpu_baseline": {"value": value, "unit": "Gparams/s", "cores": 1, "kind": "oracle",
+                         "sample": "%d params of the %s shard per step, single thread" %
+                                   (k, w.name)},
+        "e2e": {"value": value, "unit": "Gparams/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w):
+    import torch
+
+    world, rank, local = dist_env()
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+        pg = dist
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import fsdp_sharded_mixed_zero_gb300 as Z
+    from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    def max_over_ranks(x):
+        if pg is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        return float(t.item())
+
+    dw = DeviceWorkload(w, device=dev)
+    dw.gen_grads(0, dw.scaler().scale)
+    stream = torch.cuda.current_stream(dev)
+    params = dw.S * len(w.ranks)
+    n_batches = -(-len(w.ranks) // 64)
+    launches_per_step = 2 * n_batches + 1
+    torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        dw.step(want_result=False, stream=stream)
+    torch.cuda.synchronize(dev)
+
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = str(local)
+    sampler = ClockSampler(uuid)
+    Z.zero_flat_profile_enable(dw.flat.handle, True)
+    Z.zero_flat_profile_read(dw.flat.handle)              # clear
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        dw.step(want_result=False, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop()
+    Z.zero_flat_profile_enable(dw.flat.handle, False)
+    ms_red, ms_fin, ms_adam, nrec = Z.zero_flat_profile_read(dw.flat.handle)
+    elapsed_ms = max_over_ranks(e0.elapsed_time(e1))
+    res = dw.step(want_result=True, stream=stream)          # sanity: the step ran clean
+    assert res.skipped == 0 and res.overflow == 0, "benchmark inputs overflowed"
+
+    N = w.world_size
+    ms_step = elapsed_ms / args.steps
+    value = params * args.steps * world / (elapsed_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peaks()
+    # algorithmic bytes per parameter: reduce reads 2N and writes the fp32
+    # reduced gradient (4); AdamW reads it (4) and master/m/v (12), writes
+    # master/m/v (12) and the 16-bit param (2)
+    kernels = {
+        "reduce_kernel": {"ms_mean": ms_red / max(nrec, 1), "bytes_per_param": 2 * N + 4},
+        "adamw_kernel": {"ms_mean": ms_adam / max(nrec, 1), "bytes_per_param": 30},
+        "finalize_kernel": {"ms_mean": ms_fin / max(nrec, 1), "bytes_per_param": 0},
+    }
+    for k in kernels.values():
+        k["achieved_gbs"] = (k["bytes_per_param"] * params / (k["ms_mean"] / 1e3) / 1e9
+                             if k["ms_mean"] > 0 else None)
+    dom = max(("reduce_kernel", "adamw_kernel"), key=lambda n: kernels[n]["ms_mean"])
+    dk = kernels[dom]
+    traffic = profiled_traffic(dom, w.name)
+    min_bytes = (2 * N + 26) * params                       # spec minimum per step
+    step_gbs = min_bytes / (ms_step / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": dk["achieved_gbs"], "peak": peak,
+                "unit": "GB/s", "frac": dk["achieved_gbs"] / peak,
+                "peak_kind": peak_kind, "traffic": traffic,
+                "bytes_per_launch": dk["bytes_per_param"] * params}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(args, dw, stream, dev, params, barrier, max_over_ranks, world)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "Gparams/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "params_stepped_per_gpu": params,
+                       "emulated_world_size": N, "stepped_ranks": w.ranks,
+                       "storage": "%s grads and params, f32 master/m/v" %
+                                  ("bf16" if w.grad_dtype == 1 else "f16"),
+                       "l2": "inputs larger than L2 (%.0f GB resident vs 129 MB)" %
+                             (dw.flat.device_bytes() / 1e9 + (dw.grads.numel() * 2 +
+                              3 * params * 4 + dw.out.numel() * 2) / 1e9),
+                       "parallelism": "replicas%d" % world},
+            "step_hbm": {"min_bytes_per_param": 2 * N + 26, "achieved_gbs": step_gbs,
+                         "frac_of_measured": step_gbs / peak,
+                         "frac_of_nominal_8tbs": step_gbs / NOMINAL_HBM_GBS},
+            "kernels": kernels,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "clocks": clocks,
+            "gpu_launches": launches_per_step * args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    dw.close()
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def measure_e2e(args, dw, stream, dev, params, barrier, max_over_ranks, world):
+    """Gradients H2D from pinned host memory + step + result D2H, every step."""
+    import torch
+    try:
+        host = torch.empty(dw.grads.shape, dtype=dw.grads.dtype, pin_memory=True)
+    except RuntimeError as e:
+        return {"value": None, "unit": "Gparams/s", "error": "pinned host buffer: %s" % e}
+    host.copy_(dw.grads)
+    nbytes = host.numel() * host.element_size()
+    for _ in range(2):
+        dw.grads.copy_(host, non_blocking=True)
+        dw.step(want_result=True, stream=stream)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        dw.grads.copy_(host, non_blocking=True)
+        res = dw.step(want_result=True, stream=stream)
+        assert res.skipped == 0
+    torch.cuda.synchronize(dev)
+    dt = max_over_ranks(time.perf_counter() - t)
+    barrier()
+    del host
+    return {"value": params * args.e2e_steps * world / dt / 1e9, "unit": "Gparams/s",
+            "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": RESULT_D2H_BYTES,
+            "ms_per_step": 1e3 * dt / args.e2e_steps, "steps": args.e2e_steps}
+
+
+def main():
+    args = parse_args()
+    from synth.workloads import BY_NAME
+    w = BY_NAME[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

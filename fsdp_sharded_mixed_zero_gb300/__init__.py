@@ -1,0 +1,270 @@
+"""GB300 ZeRO shard optimizer step on a FlatParameter -- Python binding.
+
+A thin ctypes layer over ``libzero_gb300.so`` (the C ABI in include/zero.h):
+the functions keep the C names and only marshal arguments.  Every step of the
+path runs in the library's CUDA kernels; there is no CPU or PyTorch fallback,
+and importing this module fails loudly if the library has not been built
+(``python -m fsdp_sharded_mixed_zero_gb300.build`` or ``__graft_entry__.build()``).
+
+PyTorch is used only to hand over device pointers and CUDA streams.
+"""
+import ctypes as C
+import os
+
+__all__ = [
+    "ZERO_OK", "ZERO_F16", "ZERO_BF16", "ZERO_SUM", "ZERO_AVG", "ZeroError",
+    "ParamInfo", "Hparams", "ScalerState", "StepResult", "hparams", "param_infos",
+    "zero_flat_init", "zero_flat_layout", "zero_shard_step", "zero_loss_scaler_state",
+    "zero_set_loss_scaler_state", "zero_memory_bytes", "zero_flat_device_bytes",
+    "zero_flat_free", "zero_flat_profile_enable", "zero_flat_profile_read",
+    "zero_status_string", "zero_last_error", "ZeroFlat", "LIB_PATH",
+]
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libzero_gb300.so")
+
+ZERO_OK = 0
+ZERO_F16, ZERO_BF16 = 0, 1
+ZERO_SUM, ZERO_AVG = 0, 1
+
+
+class ZeroError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        msg = "%s: %s (%s)" % (where, _lib.zero_status_string(status).decode(),
+                               _lib.zero_last_error().decode())
+        super().__init__(msg)
+
+
+class ParamInfo(C.Structure):
+    _fields_ = [("offset", C.c_int64), ("numel", C.c_int64), ("ndim", C.c_int32),
+                ("dtype", C.c_int32), ("shape", C.c_int64 * 8)]
+
+
+class Hparams(C.Structure):
+    _fields_ = [("lr", C.c_double), ("beta1", C.c_double), ("beta2", C.c_double),
+                ("eps", C.c_double), ("weight_decay", C.c_double),
+                ("max_grad_norm", C.c_double), ("dynamic_loss_scale", C.c_int32),
+                ("initial_scale_power", C.c_int32), ("loss_scale_window", C.c_int32),
+                ("reserved", C.c_int32), ("static_loss_scale", C.c_double),
+                ("min_loss_scale", C.c_double)]
+
+
+class ScalerState(C.Structure):
+    _fields_ = [("scale", C.c_float), ("good_steps", C.c_int32), ("step_t", C.c_int64),
+                ("overflow_count", C.c_int64)]
+
+    def as_tuple(self):
+        return (self.scale, self.good_steps, self.step_t, self.overflow_count)
+
+
+class StepResult(C.Structure):
+    _fields_ = [("overflow", C.c_int32), ("skipped", C.c_int32), ("grad_norm", C.c_double),
+                ("clip_coef", C.c_float), ("scale_used", C.c_float)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libzero_gb300.so is not built (expected at %s); run "
+                          "fsdp_sharded_mixed_zero_gb300/build.py" % LIB_PATH)
+    L = C.CDLL(LIB_PATH)
+    vp, i32, i64, u64 = C.c_void_p, C.c_int32, C.c_int64, C.c_uint64
+    L.zero_flat_init.argtypes = [C.POINTER(ParamInfo), i32, i32, i32, i32, i32,
+                                 C.POINTER(Hparams), C.POINTER(vp)]
+    L.zero_flat_layout.argtypes = [vp, C.POINTER(i64), C.POINTER(i64), C.POINTER(i64)]
+    L.zero_shard_step.argtypes = [vp, C.POINTER(i32), i32, vp, i64, i64, C.POINTER(vp),
+                                  C.POINTER(vp), C.POINTER(vp), vp, C.c_double, vp,
+                                  C.POINTER(StepResult)]
+    L.zero_loss_scaler_state.argtypes = [vp, C.POINTER(ScalerState), vp]
+    L.zero_set_loss_scaler_state.argtypes = [vp, C.POINTER(ScalerState), vp]
+    L.zero_memory_bytes.argtypes = [i32, u64, i32] + [C.POINTER(u64)] * 4
+    L.zero_flat_device_bytes.argtypes = [vp, C.POINTER(u64)]
+    L.zero_flat_free.argtypes = [vp]
+    L.zero_flat_profile_enable.argtypes = [vp, i32]
+    L.zero_flat_profile_read.argtypes = [vp] + [C.POINTER(C.c_double)] * 3 + [C.POINTER(i64)]
+    L.zero_status_string.argtypes = [i32]
+    L.zero_status_string.restype = C.c_char_p
+    L.zero_last_error.argtypes = []
+    L.zero_last_error.restype = C.c_char_p
+    for name in ("zero_flat_init", "zero_flat_layout", "zero_shard_step",
+                 "zero_loss_scaler_state", "zero_set_loss_scaler_state", "zero_memory_bytes",
+                 "zero_flat_device_bytes", "zero_flat_free", "zero_flat_profile_enable",
+                 "zero_flat_profile_read"):
+        getattr(L, name).restype = i32
+    return L
+
+
+_lib = _load()
+
+
+def _check(status, where):
+    if status != ZERO_OK:
+        raise ZeroError(status, where)
+
+
+def hparams(lr=3e-5, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, max_grad_norm=1.0,
+            dynamic=True, initial_scale_power=16, window=1000, static_scale=1.0,
+            min_scale=1.0):
+    """Settings named after the DeepSpeed config keys (defaults: the AdamW,
+    fp16 dynamic loss-scale and gradient_clipping values of the config printed
+    in the ZeRO paper reading, §5.1)."""
+    return Hparams(lr, beta1, beta2, eps, weight_decay, max_grad_norm, 1 if dynamic else 0,
+                   initial_scale_power, window, 0, static_scale, min_scale)
+
+
+def param_infos(shapes, dtype=ZERO_F16):
+    """The FlatParameter's parameter table for parameters of the given shapes,
+    concatenated in order."""
+    arr = (ParamInfo * len(shapes))()
+    off = 0
+    for k, shp in enumerate(shapes):
+        shp = tuple(int(d) for d in shp)
+        numel = 1
+        for d in shp:
+            numel *= d
+        arr[k].offset = off
+        arr[k].numel = numel
+        arr[k].ndim = len(shp)
+        arr[k].dtype = dtype
+        for d, x in enumerate(shp):
+            arr[k].shape[d] = x
+        off += numel
+    return arr
+
+
+def zero_flat_init(infos, world_size, grad_dtype, param_dtype, op, hp):
+    h = C.c_void_p()
+    _check(_lib.zero_flat_init(infos, len(infos), world_size, grad_dtype, param_dtype, op,
+                               C.byref(hp), C.byref(h)), "zero_flat_init")
+    return h
+
+
+def zero_flat_layout(h):
+    out = [C.c_int64() for _ in range(3)]
+    _check(_lib.zero_flat_layout(h, *[C.byref(o) for o in out]), "zero_flat_layout")
+    return tuple(o.value for o in out)
+
+
+def zero_shard_step(h, ranks, grads_ptr, grad_ld, grad_rank_offset_mul, master_ptrs,
+                    m_ptrs, v_ptrs, out_ptr, extra_norm_sq=0.0, stream=0, want_result=True):
+    """Raw pointers in, status checked.  Returns a StepResult (synchronizes
+    the stream) when want_result, else None (fully asynchronous)."""
+    n = len(ranks)
+    r = (C.c_int32 * n)(*ranks)
+    mp = (C.c_void_p * n)(*master_ptrs)
+    mm = (C.c_void_p * n)(*m_ptrs)
+    vv = (C.c_void_p * n)(*v_ptrs)
+    res = StepResult() if want_result else None
+    _check(_lib.zero_shard_step(h, r, n, C.c_void_p(grads_ptr), grad_ld, grad_rank_offset_mul,
+                                mp, mm, vv, C.c_void_p(out_ptr), float(extra_norm_sq),
+                                C.c_void_p(stream), C.byref(res) if res is not None else None),
+           "zero_shard_step")
+    return res
+
+
+def zero_loss_scaler_state(h, stream=0):
+    st = ScalerState()
+    _check(_lib.zero_loss_scaler_state(h, C.byref(st), C.c_void_p(stream)),
+           "zero_loss_scaler_state")
+    return st
+
+
+def zero_set_loss_scaler_state(h, state, stream=0):
+    _check(_lib.zero_set_loss_scaler_state(h, C.byref(state), C.c_void_p(stream)),
+           "zero_set_loss_scaler_state")
+
+
+def zero_memory_bytes(stage, psi, world_size):
+    """(total, params, grads, optimizer) bytes per GPU."""
+    out = [C.c_uint64() for _ in range(4)]
+    _check(_lib.zero_memory_bytes(stage, psi, world_size, *[C.byref(o) for o in out]),
+           "zero_memory_bytes")
+    return tuple(o.value for o in out)
+
+
+def zero_flat_device_bytes(h):
+    b = C.c_uint64()
+    _check(_lib.zero_flat_device_bytes(h, C.byref(b)), "zero_flat_device_bytes")
+    return b.value
+
+
+def zero_flat_free(h):
+    _check(_lib.zero_flat_free(h), "zero_flat_free")
+
+
+def zero_flat_profile_enable(h, enable=True):
+    _check(_lib.zero_flat_profile_enable(h, 1 if enable else 0), "zero_flat_profile_enable")
+
+
+def zero_flat_profile_read(h):
+    """(ms_reduce, ms_finalize, ms_adamw, steps) summed since the last read."""
+    t = [C.c_double() for _ in range(3)]
+    n = C.c_int64()
+    _check(_lib.zero_flat_profile_read(h, *[C.byref(x) for x in t], C.byref(n)),
+           "zero_flat_profile_read")
+    return t[0].value, t[1].value, t[2].value, n.value
+
+
+def zero_status_string(status):
+    return _lib.zero_status_string(status).decode()
+
+
+def zero_last_error():
+    return _lib.zero_last_error().decode()
+
+
+class ZeroFlat:
+    """Owns a handle; steps torch CUDA tensors through the C ABI.
+
+    grads: 2-D 16-bit CUDA tensor [world_size, ld] (row stride ld); master, m,
+    v: lists of fp32 CUDA tensors, one per stepped rank; out: 1-D 16-bit CUDA
+    tensor of padded_numel elements.
+    """
+
+    def __init__(self, shapes_or_infos, world_size, grad_dtype=ZERO_F16, param_dtype=None,
+                 op=ZERO_AVG, hp=None):
+        if param_dtype is None:
+            param_dtype = grad_dtype
+        infos = (shapes_or_infos if isinstance(shapes_or_infos, C.Array)
+                 else param_infos(shapes_or_infos, param_dtype))
+        self.hp = hp if hp is not None else hparams()
+        self.world_size = world_size
+        self.handle = zero_flat_init(infos, world_size, grad_dtype, param_dtype, op, self.hp)
+        self.full_numel, self.shard_size, self.padded_numel = zero_flat_layout(self.handle)
+
+    def step(self, ranks, grads, master, m, v, out, grad_rank_offset_mul=None,
+             extra_norm_sq=0.0, stream=None, want_result=True):
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        assert grads.dim() == 2 and grads.stride(1) == 1 and grads.element_size() == 2
+        if grad_rank_offset_mul is None:
+            grad_rank_offset_mul = self.shard_size if len(ranks) > 1 else 0
+        return zero_shard_step(self.handle, list(ranks), grads.data_ptr(), grads.stride(0),
+                               grad_rank_offset_mul, [t.data_ptr() for t in master],
+                               [t.data_ptr() for t in m], [t.data_ptr() for t in v],
+                               out.data_ptr(), extra_norm_sq, stream.cuda_stream, want_result)
+
+    def scaler_state(self, stream=None):
+        import torch
+        s = stream if stream is not None else torch.cuda.current_stream()
+        return zero_loss_scaler_state(self.handle, s.cuda_stream)
+
+    def set_scaler_state(self, state, stream=None):
+        import torch
+        s = stream if stream is not None else torch.cuda.current_stream()
+        zero_set_loss_scaler_state(self.handle, state, s.cuda_stream)
+
+    def device_bytes(self):
+        return zero_flat_device_bytes(self.handle)
+
+    def close(self):
+        if self.handle is not None:
+            zero_flat_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,579 @@
+// zero_api.cu -- host side of the C ABI declared in include/zero.h: argument
+// validation, the flat-parameter layout, device state, scratch management and
+// the three launches of a step.  No arithmetic of the update happens here
+// beyond forming the per-step fp32 scalars from the fp64 hyper-parameters.
+#include "zero.h"
+#include "zero_kernels.cuh"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#define ZERO_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+zero_status fail(zero_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+zero_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(ZERO_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool mul_ok(int64_t a, int64_t b, int64_t *out) {
+    if (a < 0 || b < 0) return false;
+    if (a != 0 && b > INT64_MAX / a) return false;
+    *out = a * b;
+    return true;
+}
+bool add_ok(int64_t a, int64_t b, int64_t *out) {
+    if (a < 0 || b < 0 || a > INT64_MAX - b) return false;
+    *out = a + b;
+    return true;
+}
+
+// Switch to the handle's device for the duration of a call.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard() {
+        int cur;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+}  // namespace
+
+struct zero_flat {
+    int device = 0;
+    int sm_count = 0;
+    int reduce_bps = 1, adam_bps = 1;
+    int32_t world = 1;
+    zero_dtype grad_dtype = ZERO_F16, param_dtype = ZERO_F16;
+    zero_reduce_op op = ZERO_AVG;
+    zero_hparams hp{};
+    int64_t full_numel = 0, shard = 0, padded = 0;
+    // per-element fp32 scalars, each rounded once from fp64
+    float b1 = 0, b2 = 0, omb1 = 0, omb2 = 0, lr = 0, eps = 0, decay = 0, min_scale = 0;
+    zg::DevState *d_state = nullptr;
+    float2 *d_bc = nullptr;
+    int64_t bc_len = 0;
+    float *d_g = nullptr;             // reduced-gradient rows
+    int64_t g_stride = 0;             // floats per row (multiple of 4)
+    int64_t g_rows = 0;
+    double *d_part_ss = nullptr;
+    int32_t *d_part_of = nullptr;
+    int64_t parts_cap = 0;
+    zg::DevState *h_state = nullptr;  // pinned staging for state reads
+    uint64_t device_bytes = 0;
+    // per-kernel timing (zero_flat_profile_enable)
+    bool profile = false;
+    std::vector<cudaEvent_t> ev;      // 4 events per recorded step
+    size_t ev_used = 0;
+};
+
+namespace {
+
+// Bias-correction table: entry t = {(float)(1 - b1^t), (float)(1 - b2^t)} with
+// pow in fp64, for t = 0 .. until both round to 1.0f (from there on they stay
+// 1.0f, which the finalize kernel uses past the end of the table).
+zero_status build_bc_table(zero_flat *h) {
+    const int64_t kCap = int64_t(1) << 24;
+    std::vector<float2> tab;
+    tab.reserve(1 << 15);
+    for (int64_t t = 0;; ++t) {
+        if (t >= kCap)
+            return fail(ZERO_ERR_INVALID_ARG,
+                        "betas too close to 1: bias corrections do not reach 1.0f within 2^24 steps");
+        const float c1 = (float)(1.0 - std::pow(h->hp.beta1, (double)t));
+        const float c2 = (float)(1.0 - std::pow(h->hp.beta2, (double)t));
+        tab.push_back(make_float2(c1, c2));
+        if (t > 0 && c1 == 1.0f && c2 == 1.0f) break;
+    }
+    h->bc_len = (int64_t)tab.size();
+    const size_t bytes = tab.size() * sizeof(float2);
+    cudaError_t e = cudaMalloc(&h->d_bc, bytes);
+    if (e) return cuda_fail(e, "cudaMalloc(bias-correction table)");
+    h->device_bytes += bytes;
+    e = cudaMemcpy(h->d_bc, tab.data(), bytes, cudaMemcpyHostToDevice);
+    if (e) return cuda_fail(e, "cudaMemcpy(bias-correction table)");
+    return ZERO_OK;
+}
+
+zero_status validate_hparams(const zero_hparams *hp) {
+    if (!hp) return fail(ZERO_ERR_INVALID_ARG, "hparams is NULL");
+    auto finite = [](double x) { return std::isfinite(x); };
+    if (!finite(hp->lr) || hp->lr < 0) return fail(ZERO_ERR_INVALID_ARG, "lr must be finite and >= 0");
+    if (!finite(hp->beta1) || hp->beta1 < 0 || hp->beta1 >= 1)
+        return fail(ZERO_ERR_INVALID_ARG, "beta1 must be in [0, 1)");
+    if (!finite(hp->beta2) || hp->beta2 < 0 || hp->beta2 >= 1)
+        return fail(ZERO_ERR_INVALID_ARG, "beta2 must be in [0, 1)");
+    if (!finite(hp->eps) || hp->eps <= 0) return fail(ZERO_ERR_INVALID_ARG, "eps must be > 0");
+    if (!finite(hp->weight_decay) || hp->weight_decay < 0)
+        return fail(ZERO_ERR_INVALID_ARG, "weight_decay must be >= 0");
+    if (!finite(hp->max_grad_norm)) return fail(ZERO_ERR_INVALID_ARG, "max_grad_norm must be finite");
+    if (hp->dynamic_loss_scale != 0 && hp->dynamic_loss_scale != 1)
+        return fail(ZERO_ERR_INVALID_ARG, "dynamic_loss_scale must be 0 or 1");
+    if (hp->initial_scale_power < 0 || hp->initial_scale_power > 126)
+        return fail(ZERO_ERR_INVALID_ARG, "initial_scale_power must be in [0, 126]");
+    if (hp->loss_scale_window < 1) return fail(ZERO_ERR_INVALID_ARG, "loss_scale_window must be >= 1");
+    if (hp->reserved != 0) return fail(ZERO_ERR_INVALID_ARG, "reserved must be 0");
+    if (!hp->dynamic_loss_scale &&
+        (!finite(hp->static_loss_scale) || hp->static_loss_scale <= 0 ||
+         !std::isfinite((float)hp->static_loss_scale) || (float)hp->static_loss_scale <= 0))
+        return fail(ZERO_ERR_INVALID_ARG, "static_loss_scale must be a positive fp32 value");
+    if (!finite(hp->min_loss_scale) || hp->min_loss_scale <= 0 || (float)hp->min_loss_scale <= 0)
+        return fail(ZERO_ERR_INVALID_ARG, "min_loss_scale must be > 0");
+    return ZERO_OK;
+}
+
+zero_status ensure_scratch(zero_flat *h, int64_t rows, int64_t parts) {
+    if (rows > h->g_rows) {
+        int64_t bytes;
+        if (!mul_ok(rows, h->g_stride, &bytes) || !mul_ok(bytes, 4, &bytes))
+            return fail(ZERO_ERR_OVERFLOW_SIZE, "scratch size overflows");
+        if (h->d_g) {
+            cudaFree(h->d_g);
+            h->device_bytes -= (uint64_t)(h->g_rows * h->g_stride * 4);
+            h->d_g = nullptr;
+            h->g_rows = 0;
+        }
+        if (bytes > 0) {
+            cudaError_t e = cudaMalloc(&h->d_g, (size_t)bytes);
+            if (e == cudaErrorMemoryAllocation) {
+                cudaGetLastError();
+                return fail(ZERO_ERR_NO_MEMORY, "cannot allocate %lld bytes of gradient scratch",
+                            (long long)bytes);
+            }
+            if (e) return cuda_fail(e, "cudaMalloc(gradient scratch)");
+        }
+        h->g_rows = rows;
+        h->device_bytes += (uint64_t)bytes;
+    }
+    if (parts > h->parts_cap) {
+        if (h->d_part_ss) cudaFree(h->d_part_ss);
+        if (h->d_part_of) cudaFree(h->d_part_of);
+        h->device_bytes -= (uint64_t)(h->parts_cap * 12);
+        h->d_part_ss = nullptr;
+        h->d_part_of = nullptr;
+        h->parts_cap = 0;
+        cudaError_t e = cudaMalloc(&h->d_part_ss, (size_t)parts * sizeof(double));
+        if (!e) e = cudaMalloc(&h->d_part_of, (size_t)parts * sizeof(int32_t));
+        if (e) return cuda_fail(e, "cudaMalloc(norm partials)");
+        h->parts_cap = parts;
+        h->device_bytes += (uint64_t)(parts * 12);
+    }
+    return ZERO_OK;
+}
+
+// Next free event of the timing record (created on demand, reused).
+cudaError_t next_event(zero_flat *h, cudaEvent_t *out) {
+    if (h->ev_used == h->ev.size()) {
+        cudaEvent_t e;
+        cudaError_t err = cudaEventCreate(&e);
+        if (err) return err;
+        h->ev.push_back(e);
+    }
+    *out = h->ev[h->ev_used++];
+    return cudaSuccess;
+}
+
+cudaError_t mark(zero_flat *h, cudaStream_t s) {
+    if (!h->profile) return cudaSuccess;
+    cudaEvent_t e;
+    cudaError_t err = next_event(h, &e);
+    if (err) return err;
+    return cudaEventRecord(e, s);
+}
+
+void release(zero_flat *h) {
+    if (!h) return;
+    DeviceGuard g(h->device);
+    for (cudaEvent_t e : h->ev) cudaEventDestroy(e);
+    cudaFree(h->d_state);
+    cudaFree(h->d_bc);
+    cudaFree(h->d_g);
+    cudaFree(h->d_part_ss);
+    cudaFree(h->d_part_of);
+    if (h->h_state) cudaFreeHost(h->h_state);
+    delete h;
+}
+
+}  // namespace
+
+ZERO_API const char *zero_status_string(zero_status s) {
+    switch (s) {
+        case ZERO_OK: return "ok";
+        case ZERO_ERR_INVALID_ARG: return "invalid argument";
+        case ZERO_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
+        case ZERO_ERR_ALIGNMENT: return "misaligned pointer";
+        case ZERO_ERR_CUDA: return "CUDA error";
+        case ZERO_ERR_OVERFLOW_SIZE: return "size overflows int64";
+        case ZERO_ERR_TIMEOUT: return "timeout";
+        case ZERO_ERR_NO_MEMORY: return "out of memory";
+    }
+    return "unknown status";
+}
+
+ZERO_API const char *zero_last_error(void) { return g_last_error; }
+
+ZERO_API zero_status zero_memory_bytes(int32_t stage, uint64_t psi, int32_t world_size,
+                                       uint64_t *total, uint64_t *params, uint64_t *grads,
+                                       uint64_t *optim) {
+    if (stage < 0 || stage > 3) return fail(ZERO_ERR_INVALID_ARG, "stage must be 0..3");
+    if (world_size < 1) return fail(ZERO_ERR_INVALID_ARG, "world_size must be >= 1");
+    // bytes/param of fp16 params, fp16 grads, fp32 master+m+v; which are split N ways
+    static const unsigned kBytes[3] = {2, 2, 12};
+    const bool split[3] = {stage >= 3, stage >= 2, stage >= 1};
+    using u128 = unsigned __int128;
+    const u128 n = (u128)(uint64_t)world_size;
+    u128 num = 0;                               // total * n
+    uint64_t part[3];
+    for (int k = 0; k < 3; ++k) {
+        const u128 b = (u128)kBytes[k] * psi;
+        u128 p = split[k] ? (b + n - 1) / n : b;
+        if (p > (u128)UINT64_MAX) return fail(ZERO_ERR_OVERFLOW_SIZE, "byte count overflows");
+        part[k] = (uint64_t)p;
+        num += split[k] ? b : b * n;
+    }
+    const u128 t = (num + n - 1) / n;
+    if (t > (u128)UINT64_MAX) return fail(ZERO_ERR_OVERFLOW_SIZE, "byte count overflows");
+    if (total) *total = (uint64_t)t;
+    if (params) *params = part[0];
+    if (grads) *grads = part[1];
+    if (optim) *optim = part[2];
+    return ZERO_OK;
+}
+
+ZERO_API zero_status zero_flat_init(const zero_param_info *infos, int32_t n_infos,
+                                    int32_t world_size, zero_dtype grad_dtype,
+                                    zero_dtype param_dtype, zero_reduce_op op,
+                                    const zero_hparams *hp, zero_flat **out) {
+    if (!out) return fail(ZERO_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!infos || n_infos < 1) return fail(ZERO_ERR_INVALID_ARG, "need at least one param_info");
+    if (world_size < 1) return fail(ZERO_ERR_INVALID_ARG, "world_size must be >= 1");
+    if ((grad_dtype != ZERO_F16 && grad_dtype != ZERO_BF16) ||
+        (param_dtype != ZERO_F16 && param_dtype != ZERO_BF16))
+        return fail(ZERO_ERR_UNSUPPORTED_DTYPE, "dtypes must be ZERO_F16 or ZERO_BF16");
+    if (op != ZERO_SUM && op != ZERO_AVG) return fail(ZERO_ERR_INVALID_ARG, "op must be SUM or AVG");
+    zero_status s = validate_hparams(hp);
+    if (s) return s;
+
+    int64_t total = 0;
+    for (int32_t k = 0; k < n_infos; ++k) {
+        const zero_param_info &p = infos[k];
+        if (p.offset != total)
+            return fail(ZERO_ERR_INVALID_ARG, "param_info %d: offset %lld, expected %lld", k,
+                        (long long)p.offset, (long long)total);
+        if (p.numel < 0) return fail(ZERO_ERR_INVALID_ARG, "param_info %d: negative numel", k);
+        if (p.ndim < 0 || p.ndim > 8) return fail(ZERO_ERR_INVALID_ARG, "param_info %d: ndim", k);
+        if (p.dtype != ZERO_F16 && p.dtype != ZERO_BF16)
+            return fail(ZERO_ERR_UNSUPPORTED_DTYPE, "param_info %d: dtype", k);
+        int64_t prod = 1;
+        for (int d = 0; d < p.ndim; ++d)
+            if (!mul_ok(prod, p.shape[d], &prod))
+                return fail(ZERO_ERR_OVERFLOW_SIZE, "param_info %d: shape product", k);
+        if (prod != p.numel)
+            return fail(ZERO_ERR_INVALID_ARG, "param_info %d: numel %lld != prod(shape) %lld", k,
+                        (long long)p.numel, (long long)prod);
+        if (!add_ok(total, p.numel, &total))
+            return fail(ZERO_ERR_OVERFLOW_SIZE, "total numel overflows int64");
+    }
+    const int64_t S = total / world_size + (total % world_size != 0);
+    int64_t padded;
+    if (!mul_ok(S, world_size, &padded)) return fail(ZERO_ERR_OVERFLOW_SIZE, "padded numel overflows");
+
+    zero_flat *h = new (std::nothrow) zero_flat;
+    if (!h) return fail(ZERO_ERR_NO_MEMORY, "host allocation failed");
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e) { delete h; return cuda_fail(e, "cudaGetDevice"); }
+    e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device);
+    if (e) { delete h; return cuda_fail(e, "cudaDeviceGetAttribute"); }
+    e = zg::blocks_per_sm(&h->reduce_bps, &h->adam_bps);
+    if (e) { delete h; return cuda_fail(e, "occupancy query"); }
+    h->world = world_size;
+    h->grad_dtype = grad_dtype;
+    h->param_dtype = param_dtype;
+    h->op = op;
+    h->hp = *hp;
+    h->full_numel = total;
+    h->shard = S;
+    h->padded = padded;
+    h->g_stride = (S + 3) / 4 * 4;
+    h->b1 = (float)hp->beta1;
+    h->b2 = (float)hp->beta2;
+    h->omb1 = (float)(1.0 - hp->beta1);
+    h->omb2 = (float)(1.0 - hp->beta2);
+    h->lr = (float)hp->lr;
+    h->eps = (float)hp->eps;
+    h->decay = (float)(1.0 - hp->lr * hp->weight_decay);
+    h->min_scale = (float)hp->min_loss_scale;
+
+    zg::DevState init{};
+    init.scaler.scale = hp->dynamic_loss_scale ? (float)std::ldexp(1.0, hp->initial_scale_power)
+                                               : (float)hp->static_loss_scale;
+    init.bc1 = init.bc2 = 1.0f;
+    e = cudaMalloc(&h->d_state, sizeof(zg::DevState));
+    if (e) { release(h); return cuda_fail(e, "cudaMalloc(state)"); }
+    h->device_bytes += sizeof(zg::DevState);
+    e = cudaMemcpy(h->d_state, &init, sizeof(init), cudaMemcpyHostToDevice);
+    if (e) { release(h); return cuda_fail(e, "cudaMemcpy(state)"); }
+    e = cudaMallocHost(&h->h_state, sizeof(zg::DevState));
+    if (e) { h->h_state = nullptr; release(h); return cuda_fail(e, "cudaMallocHost(state)"); }
+    s = build_bc_table(h);
+    if (s) { release(h); return s; }
+    *out = h;
+    return ZERO_OK;
+}
+
+ZERO_API zero_status zero_flat_layout(const zero_flat *h, int64_t *full_numel, int64_t *shard_size,
+                                      int64_t *padded_numel) {
+    if (!h) return fail(ZERO_ERR_INVALID_ARG, "handle is NULL");
+    if (full_numel) *full_numel = h->full_numel;
+    if (shard_size) *shard_size = h->shard;
+    if (padded_numel) *padded_numel = h->padded;
+    return ZERO_OK;
+}
+
+ZERO_API zero_status zero_flat_device_bytes(const zero_flat *h, uint64_t *bytes) {
+    if (!h || !bytes) return fail(ZERO_ERR_INVALID_ARG, "NULL argument");
+    *bytes = h->device_bytes;
+    return ZERO_OK;
+}
+
+ZERO_API zero_status zero_shard_step(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                                     const void *grads, int64_t grad_ld,
+                                     int64_t grad_rank_offset_mul, float *const *master,
+                                     float *const *m, float *const *v, void *flat_param_out,
+                                     double extra_norm_sq, void *stream, zero_step_result *res) {
+    if (!h) return fail(ZERO_ERR_INVALID_ARG, "handle is NULL");
+    if (!ranks || n_ranks < 1 || n_ranks > h->world)
+        return fail(ZERO_ERR_INVALID_ARG, "need 1..world_size stepped ranks");
+    if (!master || !m || !v) return fail(ZERO_ERR_INVALID_ARG, "master/m/v arrays are NULL");
+    if (!flat_param_out) return fail(ZERO_ERR_INVALID_ARG, "flat_param_out is NULL");
+    if (!std::isfinite(extra_norm_sq) || extra_norm_sq < 0)
+        return fail(ZERO_ERR_INVALID_ARG, "extra_norm_sq must be finite and >= 0");
+    if (grad_ld < 0 || grad_rank_offset_mul < 0)
+        return fail(ZERO_ERR_INVALID_ARG, "grad_ld and grad_rank_offset_mul must be >= 0");
+    const int64_t S = h->shard;
+    if (S > 0 && !grads) return fail(ZERO_ERR_INVALID_ARG, "grads is NULL");
+    if (h->world > 1 && grad_ld < S)
+        return fail(ZERO_ERR_INVALID_ARG, "grad_ld must be >= shard_size");
+    if ((uintptr_t)grads % 2 || (uintptr_t)flat_param_out % 2)
+        return fail(ZERO_ERR_ALIGNMENT, "grads and flat_param_out must be 2-byte aligned");
+
+    std::vector<int32_t> sorted(ranks, ranks + n_ranks);
+    std::sort(sorted.begin(), sorted.end());
+    for (int32_t j = 0; j < n_ranks; ++j) {
+        if (sorted[j] < 0 || sorted[j] >= h->world)
+            return fail(ZERO_ERR_INVALID_ARG, "rank %d out of range", sorted[j]);
+        if (j && sorted[j] == sorted[j - 1])
+            return fail(ZERO_ERR_INVALID_ARG, "rank %d listed twice", sorted[j]);
+    }
+    // the largest element index read, (N-1)*ld + r_max*mul + S - 1, must fit int64
+    int64_t rows_span, rank_span, span;
+    if (!mul_ok((int64_t)(h->world - 1), grad_ld, &rows_span) ||
+        !mul_ok((int64_t)sorted.back(), grad_rank_offset_mul, &rank_span) ||
+        !add_ok(rows_span, rank_span, &span) || !add_ok(span, S, &span))
+        return fail(ZERO_ERR_OVERFLOW_SIZE, "gradient addressing overflows int64");
+    for (int32_t j = 0; j < n_ranks; ++j) {
+        if (S > 0 && (!master[j] || !m[j] || !v[j]))
+            return fail(ZERO_ERR_INVALID_ARG, "master/m/v pointer %d is NULL", j);
+        if ((uintptr_t)master[j] % 4 || (uintptr_t)m[j] % 4 || (uintptr_t)v[j] % 4)
+            return fail(ZERO_ERR_ALIGNMENT, "master/m/v must be 4-byte aligned");
+    }
+
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the handle's device");
+    cudaStream_t st = (cudaStream_t)stream;
+
+    // launch geometry: one resident wave of blocks, split across stepped ranks
+    const int64_t batch = std::min<int64_t>(n_ranks, zg::kMaxRanksPerLaunch);
+    const int64_t chunks = (S + zg::kVec - 1) / zg::kVec;
+    const int64_t want = (chunks + zg::kBlock - 1) / zg::kBlock;
+    auto grid_for = [&](int bps) {
+        int64_t cap = (int64_t)h->sm_count * std::max(bps, 1) / batch;
+        return (int)std::max<int64_t>(1, std::min<int64_t>(want, std::max<int64_t>(cap, 1)));
+    };
+    const int gx1 = grid_for(h->reduce_bps);
+    const int gx3 = grid_for(h->adam_bps);
+    const int64_t parts = (int64_t)gx1 * n_ranks;
+    zero_status s = ensure_scratch(h, n_ranks, parts);
+    if (s) return s;
+
+    const bool gbf16 = h->grad_dtype == ZERO_BF16;
+    const bool pbf16 = h->param_dtype == ZERO_BF16;
+    cudaError_t e;
+    if ((e = mark(h, st))) return cuda_fail(e, "timing event");
+    for (int32_t b0 = 0; b0 < n_ranks; b0 += (int32_t)batch) {
+        const int32_t nb = (int32_t)std::min<int64_t>(batch, n_ranks - b0);
+        zg::ReduceArgs a{};
+        a.grads = static_cast<const uint16_t *>(grads);
+        a.ld = grad_ld;
+        a.S = S;
+        a.full_numel = h->full_numel;
+        a.g = h->d_g + (int64_t)b0 * h->g_stride;
+        a.g_stride = h->g_stride;
+        a.part_ss = h->d_part_ss;
+        a.part_of = h->d_part_of;
+        a.part_base = (int32_t)((int64_t)b0 * gx1);
+        a.n_contrib = h->world;
+        a.avg = h->op == ZERO_AVG;
+        a.n_ranks = nb;
+        a.st = h->d_state;
+        for (int32_t j = 0; j < nb; ++j) {
+            const int64_t r = ranks[b0 + j];
+            a.goff[j] = r * grad_rank_offset_mul;
+            a.first[j] = r * S;
+            a.vec[j] = ((uintptr_t)grads % 16 == 0) && (grad_ld % 8 == 0) && (a.goff[j] % 8 == 0);
+        }
+        if (S > 0 && (e = zg::launch_reduce(a, gx1, gbf16, st)))
+            return cuda_fail(e, "reduce kernel launch");
+    }
+    zg::FinalizeArgs f{};
+    f.part_ss = h->d_part_ss;
+    f.part_of = h->d_part_of;
+    f.n_parts = S > 0 ? (int32_t)parts : 0;
+    f.dynamic = h->hp.dynamic_loss_scale;
+    f.window = h->hp.loss_scale_window;
+    f.min_scale = h->min_scale;
+    f.extra_norm_sq = extra_norm_sq;
+    f.max_grad_norm = h->hp.max_grad_norm;
+    f.bc_table = h->d_bc;
+    f.bc_len = h->bc_len;
+    f.st = h->d_state;
+    if ((e = mark(h, st))) return cuda_fail(e, "timing event");
+    if ((e = zg::launch_finalize(f, st))) return cuda_fail(e, "finalize kernel launch");
+    if ((e = mark(h, st))) return cuda_fail(e, "timing event");
+    for (int32_t b0 = 0; b0 < n_ranks && S > 0; b0 += (int32_t)batch) {
+        const int32_t nb = (int32_t)std::min<int64_t>(batch, n_ranks - b0);
+        zg::AdamArgs a{};
+        a.g = h->d_g + (int64_t)b0 * h->g_stride;
+        a.g_stride = h->g_stride;
+        a.S = S;
+        a.b1 = h->b1; a.b2 = h->b2; a.omb1 = h->omb1; a.omb2 = h->omb2;
+        a.lr = h->lr; a.eps = h->eps; a.decay = h->decay;
+        a.n_ranks = nb;
+        a.st = h->d_state;
+        a.out = flat_param_out;
+        for (int32_t j = 0; j < nb; ++j) {
+            const int64_t r = ranks[b0 + j];
+            a.master[j] = master[b0 + j];
+            a.m[j] = m[b0 + j];
+            a.v[j] = v[b0 + j];
+            a.out_off[j] = r * S;
+            a.vec[j] = ((uintptr_t)master[b0 + j] % 16 == 0) && ((uintptr_t)m[b0 + j] % 16 == 0) &&
+                       ((uintptr_t)v[b0 + j] % 16 == 0);
+            const uintptr_t addr = (uintptr_t)flat_param_out + (uintptr_t)(r * S) * 2;
+            a.out_align[j] = addr % 16 == 0 ? 16 : (addr % 4 == 0 ? 4 : 2);
+        }
+        if ((e = zg::launch_adamw(a, gx3, pbf16, st))) return cuda_fail(e, "adamw kernel launch");
+    }
+    if ((e = mark(h, st))) return cuda_fail(e, "timing event");
+    if (res) {
+        e = cudaMemcpyAsync(h->h_state, h->d_state, sizeof(zg::DevState), cudaMemcpyDeviceToHost, st);
+        if (!e) e = cudaStreamSynchronize(st);
+        if (e) return cuda_fail(e, "reading the step result");
+        res->overflow = h->h_state->res.overflow;
+        res->skipped = h->h_state->res.skipped;
+        res->grad_norm = h->h_state->res.grad_norm;
+        res->clip_coef = h->h_state->res.clip_coef;
+        res->scale_used = h->h_state->res.scale_used;
+    }
+    return ZERO_OK;
+}
+
+ZERO_API zero_status zero_loss_scaler_state(zero_flat *h, zero_scaler_state *out, void *stream) {
+    if (!h || !out) return fail(ZERO_ERR_INVALID_ARG, "NULL argument");
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the handle's device");
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(h->h_state, h->d_state, sizeof(zg::DevState),
+                                    cudaMemcpyDeviceToHost, st);
+    if (!e) e = cudaStreamSynchronize(st);
+    if (e) return cuda_fail(e, "reading the loss-scale state");
+    out->scale = h->h_state->scaler.scale;
+    out->good_steps = h->h_state->scaler.good_steps;
+    out->step_t = h->h_state->scaler.step_t;
+    out->overflow_count = h->h_state->scaler.overflow_count;
+    return ZERO_OK;
+}
+
+ZERO_API zero_status zero_set_loss_scaler_state(zero_flat *h, const zero_scaler_state *in,
+                                                void *stream) {
+    if (!h || !in) return fail(ZERO_ERR_INVALID_ARG, "NULL argument");
+    if (!(in->scale > 0.0f) || !std::isfinite(in->scale) || in->good_steps < 0 ||
+        in->step_t < 0 || in->overflow_count < 0)
+        return fail(ZERO_ERR_INVALID_ARG, "invalid loss-scale state");
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the handle's device");
+    cudaStream_t st = (cudaStream_t)stream;
+    // stage through the pinned buffer after earlier work on the stream is done
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e) return cuda_fail(e, "cudaStreamSynchronize");
+    zg::ScalerDev sc{in->scale, in->good_steps, in->step_t, in->overflow_count};
+    memcpy(&h->h_state->scaler, &sc, sizeof(sc));
+    e = cudaMemcpyAsync(&h->d_state->scaler, &h->h_state->scaler, sizeof(sc),
+                        cudaMemcpyHostToDevice, st);
+    if (!e) e = cudaStreamSynchronize(st);
+    if (e) return cuda_fail(e, "writing the loss-scale state");
+    return ZERO_OK;
+}
+
+ZERO_API zero_status zero_flat_profile_enable(zero_flat *h, int32_t enable) {
+    if (!h) return fail(ZERO_ERR_INVALID_ARG, "handle is NULL");
+    if (h->ev_used % 4) return fail(ZERO_ERR_INVALID_ARG, "timing record is inconsistent");
+    h->profile = enable != 0;
+    return ZERO_OK;
+}
+
+ZERO_API zero_status zero_flat_profile_read(zero_flat *h, double *ms_reduce, double *ms_finalize,
+                                            double *ms_adamw, int64_t *steps) {
+    if (!h) return fail(ZERO_ERR_INVALID_ARG, "handle is NULL");
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the handle's device");
+    double t[3] = {0, 0, 0};
+    const size_t n = h->ev_used / 4;
+    for (size_t k = 0; k < n; ++k) {
+        cudaError_t e = cudaEventSynchronize(h->ev[4 * k + 3]);
+        if (e) return cuda_fail(e, "cudaEventSynchronize");
+        for (int i = 0; i < 3; ++i) {
+            float ms = 0;
+            e = cudaEventElapsedTime(&ms, h->ev[4 * k + i], h->ev[4 * k + i + 1]);
+            if (e) return cuda_fail(e, "cudaEventElapsedTime");
+            t[i] += ms;
+        }
+    }
+    h->ev_used = 0;
+    if (ms_reduce) *ms_reduce = t[0];
+    if (ms_finalize) *ms_finalize = t[1];
+    if (ms_adamw) *ms_adamw = t[2];
+    if (steps) *steps = (int64_t)n;
+    return ZERO_OK;
+}
+
+ZERO_API zero_status zero_flat_free(zero_flat *h) {
+    if (!h) return ZERO_OK;
+    {
+        DeviceGuard guard(h->device);
+        cudaDeviceSynchronize();
+    }
+    release(h);
+    return ZERO_OK;
+}

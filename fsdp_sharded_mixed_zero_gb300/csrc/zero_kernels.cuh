@@ -1,0 +1,102 @@
+// zero_kernels.cuh -- device-side data structures and launch entry points of
+// the ZeRO shard step (sm_103a).  See zero_kernels.cu for the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace zg {
+
+// Stepped ranks handled by one launch (kernel-parameter tables stay < 4 KB;
+// more ranks are processed in several launches).
+constexpr int kMaxRanksPerLaunch = 64;
+// Elements per thread-chunk: one 16-byte load of 16-bit gradients, two of fp32.
+constexpr int kVec = 8;
+constexpr int kBlock = 256;           // threads per block, reduce and AdamW kernels
+constexpr int kFinalizeThreads = 1024;
+
+// Device-resident state of a handle.  `scaler` persists across steps; `res`
+// and the fields after it are written by the finalize kernel of each step and
+// read by the AdamW kernel of the same step.  The first two members have the
+// layout of zero_scaler_state and zero_step_result.
+struct ScalerDev {
+    float scale;
+    int32_t good_steps;
+    int64_t step_t;
+    int64_t overflow_count;
+};
+struct ResultDev {
+    int32_t overflow;
+    int32_t skipped;
+    double grad_norm;
+    float clip_coef;
+    float scale_used;
+};
+struct DevState {
+    ScalerDev scaler;
+    ResultDev res;
+    float bc1, bc2;                   // bias corrections of this step (1 - beta^t)
+    int32_t bc_saturated;             // t ran past the table: both corrections are 1
+    int32_t pad;
+};
+
+// K1: reduce of the N contributions + AVG + unscale + overflow + norm partials.
+struct ReduceArgs {
+    const uint16_t *grads;            // contributor c, element i: grads[c*ld + goff[j] + i]
+    int64_t ld;
+    int64_t S;                        // shard size
+    int64_t full_numel;
+    float *g;                         // reduced gradient rows, row j at g + j*g_stride
+    int64_t g_stride;
+    double *part_ss;                  // per-block partial sums of squares
+    int32_t *part_of;                 // per-block overflow flags
+    int32_t part_base;                // partial index = part_base + j*gridDim.x + blockIdx.x
+    int32_t n_contrib;
+    int32_t avg;
+    int32_t n_ranks;
+    const DevState *st;
+    int64_t goff[kMaxRanksPerLaunch];     // r * grad_rank_offset_mul
+    int64_t first[kMaxRanksPerLaunch];    // r * S (flat index of the shard's element 0)
+    uint8_t vec[kMaxRanksPerLaunch];      // 16-byte-aligned rows: vector path
+};
+
+// K2: one block; deterministic total of the partials, norm, clip, loss scale.
+struct FinalizeArgs {
+    const double *part_ss;
+    const int32_t *part_of;
+    int32_t n_parts;
+    int32_t dynamic;
+    int32_t window;
+    float min_scale;
+    double extra_norm_sq;
+    double max_grad_norm;
+    const float2 *bc_table;           // bc_table[t] = {1 - b1^t, 1 - b2^t} as fp32
+    int64_t bc_len;                   // entries t >= bc_len are {1, 1}
+    DevState *st;
+};
+
+// K3: AdamW + cast into the flat buffer.
+struct AdamArgs {
+    const float *g;
+    int64_t g_stride;
+    int64_t S;
+    float b1, b2, omb1, omb2, lr, eps, decay;
+    int32_t n_ranks;
+    const DevState *st;
+    void *out;                        // flat 16-bit buffer
+    float *master[kMaxRanksPerLaunch];
+    float *m[kMaxRanksPerLaunch];
+    float *v[kMaxRanksPerLaunch];
+    int64_t out_off[kMaxRanksPerLaunch];  // r * S
+    uint8_t vec[kMaxRanksPerLaunch];      // master/m/v 16-byte aligned
+    uint8_t out_align[kMaxRanksPerLaunch];// byte alignment of the output slot: 16, 4 or 2
+};
+
+cudaError_t launch_reduce(const ReduceArgs &a, int grid_x, bool bf16, cudaStream_t s);
+cudaError_t launch_finalize(const FinalizeArgs &a, cudaStream_t s);
+cudaError_t launch_adamw(const AdamArgs &a, int grid_x, bool bf16_out, cudaStream_t s);
+
+// Resident blocks per SM of the reduce and AdamW kernels (occupancy API).
+cudaError_t blocks_per_sm(int *reduce_bps, int *adam_bps);
+
+}  // namespace zg

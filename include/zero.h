@@ -1,0 +1,221 @@
+/*
+ * zero.h -- C ABI of the GB300 ZeRO shard optimizer step on a FlatParameter.
+ *
+ * One call of zero_shard_step performs, for the stepped shard(s) of a flat
+ * parameter split N ways:
+ *   1. the reduce of the N per-rank fp16/bf16 gradient contributions of the
+ *      shard (SUM or AVG, accumulated in fp32) -- the reduce half of a
+ *      reduce-scatter, with all N contributions already in this GPU's memory;
+ *   2. division by the loss scale and an inf/NaN overflow check;
+ *   3. the global L2 gradient norm and the clip coefficient;
+ *   4. the dynamic-loss-scale decision (overflow: skip the step and halve the
+ *      scale; after `loss_scale_window` clean steps: double it);
+ *   5. AdamW with bias correction and decoupled weight decay on the fp32
+ *      master weights, m and v;
+ *   6. the round-to-nearest cast of the updated shard into its slot of the
+ *      flat, all-gather-shaped 16-bit parameter buffer.
+ *
+ * Sources (web pages, by title and section):
+ *   "DeepSpeed 与 FSDP" (docs.ifdog.com): §逐步推导 (16 bytes per parameter),
+ *     §ZeRO-1/2/3 and §ZeRO-3 的数学总结 (sharded update, reduce-scatter,
+ *     all-gather, per-stage memory), §ZeRO-Offload (Adam equations),
+ *     §FSDP 的分片粒度与 FlatParameter (flat buffer, chunk per rank).
+ *   "PyTorch FSDP（Fully Sharded Data Parallel）源码级深度解析" (tbr8.org):
+ *     §3.1 (FlatParameter and its per-parameter {start, end, shape, dtype}
+ *     table), §3.3 (reduce_scatter_tensor with op AVG or SUM, shard_size),
+ *     §4 (ShardingStrategy), §7.2 (fp32 master weights under bf16 compute).
+ *   The ZeRO paper reading at 2kiu.com/news/5312103: §5.1 (DeepSpeed config:
+ *     AdamW lr/betas/eps/weight_decay, fp16 loss_scale 0 = dynamic,
+ *     loss_scale_window, initial_scale_power, gradient_clipping), §5.3
+ *     (overflow detection and clipping are one global decision).
+ *
+ * Conventions for every function:
+ *   - Returns a zero_status; never aborts, never throws, never exits.
+ *   - On an error nothing is launched and no state changes.
+ *   - Device pointers are plain CUDA device addresses on the device the
+ *     handle was created on; the caller owns every buffer it passes and keeps
+ *     it alive until the work queued on `stream` has finished.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *   - The library needs the CUDA driver; it contains no CPU fallback.
+ */
+#ifndef ZERO_GB300_H
+#define ZERO_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ZERO_OK = 0,
+    ZERO_ERR_INVALID_ARG = 1,       /* null pointer, bad size, rank out of range ... */
+    ZERO_ERR_UNSUPPORTED_DTYPE = 2, /* dtype not fp16/bf16 */
+    ZERO_ERR_ALIGNMENT = 3,         /* pointer not aligned to its element size */
+    ZERO_ERR_CUDA = 4,              /* a CUDA runtime call failed (see zero_last_error) */
+    ZERO_ERR_OVERFLOW_SIZE = 5,     /* a size or offset does not fit in int64 */
+    ZERO_ERR_TIMEOUT = 6,           /* reserved for bounded device waits */
+    ZERO_ERR_NO_MEMORY = 7          /* host or device allocation failed */
+} zero_status;
+
+typedef enum { ZERO_F16 = 0, ZERO_BF16 = 1 } zero_dtype;
+
+/* reduce_scatter_tensor's op ("PyTorch FSDP ... 深度解析" §3.3). */
+typedef enum { ZERO_SUM = 0, ZERO_AVG = 1 } zero_reduce_op;
+
+/* One row of the FlatParameter's parameter table ("PyTorch FSDP ... 深度解析"
+ * §3.1: start = offset, end = offset + numel, shape, dtype).  Rows must be
+ * contiguous and in order: offset[0] == 0, offset[k] == offset[k-1] +
+ * numel[k-1]; numel == prod(shape[0..ndim)) (ndim 0 means a scalar,
+ * numel 1); 0 <= ndim <= 8; dtype is the parameter's 16-bit dtype. */
+typedef struct {
+    int64_t offset;
+    int64_t numel;
+    int32_t ndim;
+    int32_t dtype;                  /* zero_dtype */
+    int64_t shape[8];
+} zero_param_info;
+
+/* Optimizer and loss-scale settings, named after the DeepSpeed config keys
+ * (ZeRO reading §5.1).  Reals are fp64 as a config file holds them; every
+ * per-element scalar is rounded to fp32 once from fp64: beta1, beta2,
+ * 1-beta1, 1-beta2, lr, eps, 1-lr*weight_decay, and the bias corrections
+ * 1-beta^t (t = number of applied steps, computed with pow in fp64). */
+typedef struct {
+    double lr;                      /* 3e-5 in the printed config */
+    double beta1, beta2;            /* 0.9, 0.999 */
+    double eps;                     /* 1e-8 */
+    double weight_decay;            /* 0.01, decoupled: theta *= 1 - lr*wd */
+    double max_grad_norm;           /* gradient_clipping, 1.0; <= 0 disables */
+    int32_t dynamic_loss_scale;     /* 1: "loss_scale": 0 (dynamic); 0: static */
+    int32_t initial_scale_power;    /* 16: initial scale 2^16 */
+    int32_t loss_scale_window;      /* 1000 clean steps before doubling (>= 1) */
+    int32_t reserved;               /* must be 0 */
+    double static_loss_scale;       /* used when dynamic_loss_scale == 0 (> 0) */
+    double min_loss_scale;          /* floor of the dynamic scale (> 0), 1.0 */
+} zero_hparams;
+
+/* Loss-scale state (lives on the device). */
+typedef struct {
+    float scale;                    /* scale applied to the next step's gradients */
+    int32_t good_steps;             /* consecutive clean steps since the last change */
+    int64_t step_t;                 /* applied (not skipped) steps: Adam's t */
+    int64_t overflow_count;         /* skipped steps so far */
+} zero_scaler_state;
+
+/* What one step did. */
+typedef struct {
+    int32_t overflow;               /* 1 if any reduced gradient was inf/NaN */
+    int32_t skipped;                /* 1 if the update was skipped */
+    double grad_norm;               /* global L2 norm of the unscaled gradient */
+    float clip_coef;                /* factor applied to the gradient (1 = no clip) */
+    float scale_used;               /* loss scale the gradients were divided by */
+} zero_step_result;
+
+typedef struct zero_flat zero_flat; /* opaque handle */
+
+/* Create a handle for a FlatParameter sharded `world_size` ways.
+ * Layout ("PyTorch FSDP ... 深度解析" §3.1, §3.3; "DeepSpeed 与 FSDP"
+ * §FSDP 的分片粒度与 FlatParameter): full_numel = sum of numel;
+ * shard_size S = ceil(full_numel / world_size); padded_numel = world_size*S;
+ * rank r owns flat elements [r*S, (r+1)*S); elements >= full_numel are
+ * padding and carry a zero gradient.
+ * grad_dtype / param_dtype: ZERO_F16 or ZERO_BF16.  op: ZERO_SUM / ZERO_AVG.
+ * The handle binds to the current CUDA device and allocates there the
+ * loss-scale state, the per-step scalars and the bias-correction table
+ * (a few hundred KB).  The scratch of a step (an fp32 reduced-gradient row of
+ * S floats per stepped rank, plus norm partials) is allocated on the first
+ * step that needs it and kept: do the first step before any stream capture.
+ * *out receives the handle; free it with zero_flat_free.
+ * Errors: INVALID_ARG (null, n_infos < 1, world_size < 1, table not
+ * contiguous, shape/numel mismatch, bad hparams), UNSUPPORTED_DTYPE,
+ * OVERFLOW_SIZE, NO_MEMORY, CUDA. */
+zero_status zero_flat_init(const zero_param_info *infos, int32_t n_infos, int32_t world_size,
+                           zero_dtype grad_dtype, zero_dtype param_dtype, zero_reduce_op op,
+                           const zero_hparams *hp, zero_flat **out);
+
+/* full_numel, shard_size and padded_numel of the handle (any may be NULL). */
+zero_status zero_flat_layout(const zero_flat *h, int64_t *full_numel, int64_t *shard_size,
+                             int64_t *padded_numel);
+
+/* One optimizer step on the stepped ranks ranks[0..n_ranks) (distinct, each
+ * in [0, world_size); one rank for a real rank's step, or all N to emulate
+ * the whole group on one GPU -- the norm and the overflow flag are then
+ * global over every stepped shard).
+ *
+ * grads: device, grad_dtype; contributor c's gradient for flat element
+ *   (rank r, i) is grads[c*grad_ld + r*grad_rank_offset_mul + i],
+ *   c in [0, world_size), i in [0, S).  Use grad_ld = padded_numel,
+ *   grad_rank_offset_mul = S when each contributor holds the whole padded
+ *   flat gradient (the reduce-scatter input), or grad_ld >= S,
+ *   grad_rank_offset_mul = 0 when the buffer holds only the stepped rank's
+ *   slice of each contribution.  Every addressed element must be readable;
+ *   padding elements are not read.  16-byte aligned rows take the vector path.
+ * master[j], m[j], v[j]: device fp32, S elements each, rank ranks[j]'s
+ *   shard, updated in place (host arrays of n_ranks device pointers).
+ * flat_param_out: device, param_dtype, padded_numel elements; rank r's
+ *   slot [r*S, (r+1)*S) is overwritten with the cast master shard.  Other
+ *   slots are not touched.
+ * extra_norm_sq: sum of squared norms of shards not stepped here (other
+ *   ranks' share of the global norm); 0 when every shard is stepped or in a
+ *   one-rank emulation.
+ * res: NULL for a fully asynchronous step; otherwise the step's result is
+ *   copied back and `stream` is synchronized before returning.
+ * A skipped (overflowed) step leaves master, m, v, step_t and the flat
+ * buffer untouched.  Results are deterministic for a given device.
+ * Errors: INVALID_ARG, ALIGNMENT (grads/out not 2-byte or master/m/v not
+ * 4-byte aligned), OVERFLOW_SIZE, NO_MEMORY, CUDA. */
+zero_status zero_shard_step(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                            const void *grads, int64_t grad_ld, int64_t grad_rank_offset_mul,
+                            float *const *master, float *const *m, float *const *v,
+                            void *flat_param_out, double extra_norm_sq, void *stream,
+                            zero_step_result *res);
+
+/* Copy the loss-scale state to the host; synchronizes `stream`. */
+zero_status zero_loss_scaler_state(zero_flat *h, zero_scaler_state *out, void *stream);
+
+/* Overwrite the loss-scale state (resume from a checkpoint): stream-ordered
+ * before later steps on `stream`.  scale > 0, good_steps >= 0, step_t >= 0,
+ * overflow_count >= 0, else INVALID_ARG. */
+zero_status zero_set_loss_scaler_state(zero_flat *h, const zero_scaler_state *in, void *stream);
+
+/* Model-state bytes per GPU for Psi parameters and N ranks in mixed
+ * precision ("DeepSpeed 与 FSDP" §逐步推导 and §ZeRO-3 的数学总结):
+ *   stage 0 (plain data parallel): 2Psi + 2Psi + 12Psi = 16Psi
+ *   stage 1: 2Psi + 2Psi + 12Psi/N      stage 2: 2Psi + 2Psi/N + 12Psi/N
+ *   stage 3: 2Psi/N + 2Psi/N + 12Psi/N
+ * (fp16 params, fp16 grads, fp32 master+m+v).  Each part is rounded up to a
+ * whole byte; *total is the exact sum rounded up once.  Any output may be
+ * NULL.  Host only; needs no GPU.
+ * Errors: INVALID_ARG (stage not 0..3, world_size < 1), OVERFLOW_SIZE. */
+zero_status zero_memory_bytes(int32_t stage, uint64_t psi, int32_t world_size, uint64_t *total,
+                              uint64_t *params, uint64_t *grads, uint64_t *optim);
+
+/* Device bytes the handle holds now (state + scratch). */
+zero_status zero_flat_device_bytes(const zero_flat *h, uint64_t *bytes);
+
+/* Per-kernel timing, for measurement tools.  While enabled, every
+ * zero_shard_step records CUDA events on its stream around its reduce,
+ * finalize and AdamW launches (a few microseconds per step).
+ * zero_flat_profile_read waits for the recorded events, returns the summed
+ * device milliseconds of each kernel class and the number of steps recorded,
+ * and clears the record.  Any output may be NULL. */
+zero_status zero_flat_profile_enable(zero_flat *h, int32_t enable);
+zero_status zero_flat_profile_read(zero_flat *h, double *ms_reduce, double *ms_finalize,
+                                   double *ms_adamw, int64_t *steps);
+
+/* Release the handle and its device memory (after the work queued with it
+ * has finished; this call synchronizes the handle's device).  NULL is OK. */
+zero_status zero_flat_free(zero_flat *h);
+
+/* Static description of a status code. */
+const char *zero_status_string(zero_status s);
+
+/* Message of the last error raised on this thread ("" if none). */
+const char *zero_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO_GB300_H */

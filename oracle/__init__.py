@@ -176,10 +176,11 @@ def scaler_init(hp):
 
 
 def reduce_unscale(grads_u16, ld, rank_off, n_contrib, count, first_flat_index,
-                   full_numel, avg, scale, grad_is_bf16=False):
-    """Reduced, unscaled fp32 gradient of `count` elements."""
+                   full_numel, avg, scale, grad_is_bf16=False, out=None):
+    """Reduced, unscaled fp32 gradient of `count` elements (into `out` if given)."""
     _check(grads_u16, np.uint16)
-    g = np.empty(max(count, 1), dtype=np.float32)
+    g = np.empty(max(count, 1), dtype=np.float32) if out is None else _check(out, np.float32)
+    assert g.size >= count
     lib().ora_reduce_unscale(int(grad_is_bf16), _ptr(grads_u16), ld, rank_off, n_contrib,
                              count, first_flat_index, full_numel, int(avg), scale, _ptr(g))
     return g[:count]
@@ -201,12 +202,18 @@ def scaler_decide(hp, st, overflow, norm):
     return coef.value, skip.value
 
 
-def adamw_cast(hp, t, coef, g, theta, m, v, param_is_bf16=False):
-    """In-place AdamW on theta, m, v (fp32); returns the 16-bit cast as uint16."""
+def adamw_cast(hp, t, coef, g, theta, m, v, param_is_bf16=False, out=None):
+    """In-place AdamW on theta, m, v (fp32); returns the 16-bit cast as uint16
+    (written into `out` if given)."""
     for a in (g, theta, m, v):
         _check(a, np.float32)
     n = g.size
-    out = np.empty(max(n, 1), dtype=np.uint16)
+    assert theta.size == n and m.size == n and v.size == n
+    if out is None:
+        out = np.empty(max(n, 1), dtype=np.uint16)
+    else:
+        _check(out, np.uint16)
+        assert out.size >= n
     lib().ora_adamw_cast(C.byref(hp), t, coef, _ptr(g), _ptr(theta), _ptr(m), _ptr(v),
                          n, _ptr(out), int(param_is_bf16))
     return out[:n]

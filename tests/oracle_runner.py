@@ -1,0 +1,66 @@
+"""Run the oracle's own pieces (reduce-scatter + unscale, norm, decision,
+AdamW + cast) over a large shard with host threads: the same arithmetic as
+ora_shard_step, in the same order (the norm is chained through the stepped
+ranks and elements in global order), only spread over cores.  The equality
+with ora_shard_step is itself a CPU test (test_oracle_runner.py).
+"""
+import math
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+import oracle
+
+CHUNK = 1 << 22
+_POOL = None
+
+
+def _pool():
+    global _POOL
+    if _POOL is None:
+        _POOL = ThreadPoolExecutor(max_workers=max(1, min(32, os.cpu_count() or 1)))
+    return _POOL
+
+
+def _chunks(n):
+    return [(a, min(a + CHUNK, n)) for a in range(0, n, CHUNK)]
+
+
+def reduce_rank(grads, ld, rank_off, n_contrib, S, first, full, avg, scale, bf16, g):
+    """g[:] = reduced, unscaled gradient of one shard, computed chunk-parallel."""
+    flat = grads.reshape(-1)
+
+    def job(ab):
+        a, b = ab
+        oracle.reduce_unscale(flat, ld, rank_off + a, n_contrib, b - a, first + a, full, avg,
+                              scale, grad_is_bf16=bf16, out=g[a:b])
+
+    list(_pool().map(job, _chunks(S)))
+
+
+def shard_step(hp, st, world_size, full, S, ranks, grads, ld, mul, master, m, v, out,
+               avg=True, grad_is_bf16=False, param_is_bf16=False, extra_norm_sq=0.0):
+    """Equivalent of oracle.shard_step; returns (overflow, skipped, norm, coef, scale_used)."""
+    scale = st.scale
+    gs = []
+    for r in ranks:
+        g = np.empty(max(S, 1), np.float32)[:S]
+        reduce_rank(grads, ld, r * mul, world_size, S, r * S, full, avg, scale, grad_is_bf16, g)
+        gs.append(g)
+    ss, of = 0.0, 0
+    for g in gs:                                  # global element order
+        ss, of = oracle.norm_accumulate(g, ss, of)
+    norm = math.sqrt(ss + extra_norm_sq)
+    coef, skip = oracle.scaler_decide(hp, st, of, norm)
+    if not skip:
+        t = st.step_t
+
+        def job(args):
+            j, a, b = args
+            r = ranks[j]
+            oracle.adamw_cast(hp, t, coef, gs[j][a:b], master[j][a:b], m[j][a:b], v[j][a:b],
+                              param_is_bf16=param_is_bf16, out=out[r * S + a:r * S + b])
+
+        list(_pool().map(job, [(j, a, b) for j in range(len(ranks)) for a, b in _chunks(S)]))
+    return of, skip, norm, coef, scale

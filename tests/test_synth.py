@@ -1,0 +1,57 @@
+"""The seeded input generator: Philox4x32-10 against the published
+known-answer vectors, the Irwin-Hall normal's moments, counter-based
+regeneration of single elements, thread-count independence."""
+import numpy as np
+import pytest
+
+import synth
+
+# Known-answer tests distributed with Random123 (Salmon et al., SC'11) for
+# philox4x32 with 10 rounds: (counter, key) -> output.
+KAT = [
+    ((0, 0, 0, 0), (0, 0), (0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8)),
+    ((0xFFFFFFFF,) * 4, (0xFFFFFFFF,) * 2, (0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD)),
+    ((0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344), (0xA4093822, 0x299F31D0),
+     (0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1)),
+]
+
+
+@pytest.mark.parametrize("ctr,key,want", KAT)
+def test_philox_known_answers(ctr, key, want):
+    assert tuple(synth.philox(ctr, key)) == want
+
+
+def test_irwin_hall_moments():
+    x = synth.normal_host(0, synth.MASTER, 0, 2_000_000, 1.0).astype(np.float64)
+    assert abs(x.mean()) < 3e-3
+    assert abs(x.var() - 1.0) < 5e-3
+    kurt = ((x - x.mean()) ** 4).mean() / x.var() ** 2 - 3.0
+    assert abs(kurt - (-0.3)) < 0.02                  # Irwin-Hall, n=4: -6/(5n)
+    assert np.abs(x).max() <= 2 * np.sqrt(3) + 1e-6
+    y = synth.normal_host(0, synth.MASTER, 0, 1000, 0.02)
+    assert np.allclose(y, (x[:1000] * 0.02).astype(np.float32), rtol=1e-6, atol=0)
+
+
+def test_counter_based_regeneration_and_threads():
+    big = synth.normal_host(7, synth.GRAD_SHARED, 10 ** 9, 300_000, 1e-3)
+    for k in (0, 1, 12345, 299_999):
+        one = synth.normal_host(7, synth.GRAD_SHARED, 10 ** 9 + k, 1, 1e-3)
+        assert one[0] == big[k]
+    g = synth.grads_host(3, 2, 4, 5_000_000, 200_000, 1e-3, 1e-3, scale=65536.0)
+    g2 = np.concatenate([synth.grads_host(3, 2, 4, 5_000_000 + a, 50_000, 1e-3, 1e-3,
+                                          scale=65536.0) for a in range(0, 200_000, 50_000)],
+                        axis=1)
+    assert np.array_equal(g, g2)
+
+
+def test_grads_recipe():
+    # grad[c][i] = fp16((g_i + n_{c,i}) * scale): shared part identical across c
+    n, N = 100_000, 4
+    g = synth.grads_host(5, 1, N, 0, n, 1e-3, 0.0, scale=1024.0)
+    assert all(np.array_equal(g[0], g[c]) for c in range(N))
+    shared = synth.normal_host(5, synth.GRAD_SHARED, 0, n, 1e-3, step=1)
+    assert np.array_equal(g[0], (shared * np.float32(1024.0)).astype(np.float16).view(np.uint16))
+    b = synth.grads_host(5, 1, 2, 0, n, 1e-3, 1e-3, dtype=synth.BF16)
+    assert b.shape == (2, n) and b.dtype == np.uint16
+    z = synth.grads_host(5, 1, 2, 0, 10, 1.0, 1.0, zero_from=6)
+    assert not z[:, 6:].any() and z[:, :6].all()
