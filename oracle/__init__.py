@@ -31,6 +31,11 @@ class Scaler(C.Structure):
         return (self.scale, self.good_steps, self.step_t, self.overflow_count)
 
 
+class ExactAcc(C.Structure):
+    """Exact fixed-point accumulator of squares (640 bits, unit 2^-298)."""
+    _fields_ = [("w", C.c_uint64 * 10)]
+
+
 class Result(C.Structure):
     _fields_ = [("overflow", C.c_int32), ("skipped", C.c_int32),
                 ("grad_norm", C.c_double), ("clip_coef", C.c_float),
@@ -69,8 +74,11 @@ def lib():
         L.ora_reduce_unscale.argtypes = [C.c_int32, C.c_void_p, C.c_int64, C.c_int64,
                                          C.c_int32, C.c_int64, C.c_int64, C.c_int64,
                                          C.c_int32, C.c_float, C.c_void_p]
-        L.ora_norm_accumulate.argtypes = [C.c_void_p, C.c_int64,
-                                          C.POINTER(C.c_double), C.POINTER(C.c_int32)]
+        L.ora_norm_accumulate.argtypes = [C.c_void_p, C.c_int64, C.POINTER(ExactAcc),
+                                          C.POINTER(C.c_int32)]
+        L.ora_norm_sum.argtypes = [C.POINTER(ExactAcc)]
+        L.ora_norm_sum.restype = C.c_double
+        L.ora_acc_merge.argtypes = [C.POINTER(ExactAcc), C.POINTER(ExactAcc)]
         L.ora_scaler_decide.argtypes = [C.POINTER(Hparams), C.POINTER(Scaler), C.c_int32,
                                         C.c_double, C.POINTER(C.c_float),
                                         C.POINTER(C.c_int32)]
@@ -186,12 +194,29 @@ def reduce_unscale(grads_u16, ld, rank_off, n_contrib, count, first_flat_index,
     return g[:count]
 
 
-def norm_accumulate(g, sum_sq=0.0, overflow=0):
+def norm_accumulate(g, acc=None, overflow=0):
+    """Add the exact squares of g to `acc` (a new accumulator if None);
+    returns (acc, overflow)."""
     _check(g, np.float32)
-    ss = C.c_double(sum_sq)
+    acc = ExactAcc() if acc is None else acc
     of = C.c_int32(overflow)
-    lib().ora_norm_accumulate(_ptr(g), g.size, C.byref(ss), C.byref(of))
-    return ss.value, of.value
+    lib().ora_norm_accumulate(_ptr(g), g.size, C.byref(acc), C.byref(of))
+    return acc, of.value
+
+
+def norm_sum(acc):
+    """The accumulated sum of squares rounded to the nearest double."""
+    return lib().ora_norm_sum(C.byref(acc))
+
+
+def acc_merge(dst, src):
+    lib().ora_acc_merge(C.byref(dst), C.byref(src))
+    return dst
+
+
+def sum_of_squares(g):
+    acc, of = norm_accumulate(g)
+    return norm_sum(acc), of
 
 
 def scaler_decide(hp, st, overflow, norm):

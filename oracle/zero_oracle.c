@@ -19,9 +19,8 @@
  * reduce_dtype=float32).  So every floating-point operation of the update is
  * one IEEE-754 binary32 operation rounded to nearest-even, in the order the
  * code states; the library is built with -ffp-contract=off so that no
- * multiply-add is fused.  The gradient norm is accumulated in fp64 in global
- * element order, so the result does not depend on how the flat buffer is
- * sharded.
+ * multiply-add is fused.  The squared gradient norm is summed exactly and
+ * rounded once, so it does not depend on how the flat buffer is sharded.
  *
  * Parity pins (tests/test_oracle_*.py): closed forms of the Adam update,
  * special cases, brute force on tiny buffers, the ZeRO == DDP invariant, the
@@ -274,18 +273,106 @@ void ora_reduce_unscale(int32_t grad_is_bf16, const uint16_t *grads, int64_t ld,
     }
 }
 
-/* Overflow check and squared L2 norm, accumulated in fp64 in element order.
+/* Overflow check and the squared L2 norm, computed exactly.
  * [P3] §5.3 (second pitfall): the overflow decision and the clipping must be
- * one global decision, taken on the whole gradient.                         */
-void ora_norm_accumulate(const float *g, int64_t n, double *sum_sq, int32_t *overflow)
+ * one global decision, taken on the whole gradient.
+ * The norm's plain definition, sqrt(sum g_i^2), is evaluated exactly: the
+ * square of a binary32 value is exact in binary64 (24 + 24 significant bits)
+ * and its lowest set bit weighs no less than 2^-298 (the square of the
+ * smallest subnormal).  A sum of up to 2^40 squares, each below 2^256, stays
+ * below 2^297, so a 640-bit fixed-point integer whose unit is 2^-298 holds
+ * every partial sum exactly, in any order.  ora_norm_sum rounds it once to
+ * the nearest binary64 (ties to even).  Non-finite values only raise the
+ * overflow flag (the step is skipped; the norm is then not used).          */
+#define ORA_ACC_LIMBS 10
+#define ORA_ACC_UNIT_EXP (-298)
+typedef struct {
+    uint64_t w[ORA_ACC_LIMBS];   /* little-endian 64-bit limbs */
+} ora_exact_acc;
+
+static void acc_add_at(ora_exact_acc *a, int limb, uint64_t x)
 {
-    double ss = *sum_sq;
+    for (int k = limb; k < ORA_ACC_LIMBS && x; ++k) {
+        const uint64_t before = a->w[k];
+        a->w[k] = before + x;
+        x = a->w[k] < before;               /* carry */
+    }
+}
+
+static void acc_add_square(ora_exact_acc *a, float gf)
+{
+    const double x = (double)gf * (double)gf;      /* exact */
+    if (x == 0.0) return;
+    int q;
+    const double f = frexp(x, &q);                 /* x = f * 2^q, f in [0.5, 1) */
+    uint64_t m = (uint64_t)ldexp(f, 53);           /* x = m * 2^(q-53), m < 2^53 */
+    int off = q - 53 - ORA_ACC_UNIT_EXP;           /* bit position of m's unit */
+    if (off < 0) {                                 /* the dropped low bits are 0 */
+        m >>= -off;
+        off = 0;
+    }
+    const int limb = off / 64, sh = off % 64;
+    acc_add_at(a, limb, m << sh);
+    if (sh) acc_add_at(a, limb + 1, m >> (64 - sh));
+}
+
+void ora_acc_clear(ora_exact_acc *a)
+{
+    memset(a, 0, sizeof(*a));
+}
+
+/* dst += src, exactly. */
+void ora_acc_merge(ora_exact_acc *dst, const ora_exact_acc *src)
+{
+    uint64_t carry = 0;
+    for (int k = 0; k < ORA_ACC_LIMBS; ++k) {
+        const uint64_t a = dst->w[k], b = src->w[k];
+        const uint64_t s1 = a + b;
+        const uint64_t c1 = s1 < a;
+        const uint64_t s2 = s1 + carry;
+        const uint64_t c2 = s2 < s1;
+        dst->w[k] = s2;
+        carry = c1 | c2;
+    }
+}
+
+static int acc_bit(const ora_exact_acc *a, int i)
+{
+    return (int)((a->w[i / 64] >> (i % 64)) & 1u);
+}
+
+/* The accumulated sum rounded to the nearest binary64, ties to even. */
+double ora_norm_sum(const ora_exact_acc *a)
+{
+    int top = -1;
+    for (int i = 64 * ORA_ACC_LIMBS - 1; i >= 0; --i)
+        if (acc_bit(a, i)) { top = i; break; }
+    if (top < 0) return 0.0;
+    if (top < 53) {                               /* fits in 53 bits: exact */
+        uint64_t v = 0;
+        for (int i = top; i >= 0; --i) v = (v << 1) | (uint64_t)acc_bit(a, i);
+        return ldexp((double)v, ORA_ACC_UNIT_EXP);
+    }
+    uint64_t mant = 0;                            /* the top 53 bits */
+    for (int i = top; i > top - 53; --i) mant = (mant << 1) | (uint64_t)acc_bit(a, i);
+    const int low = top - 53;                     /* highest discarded bit */
+    const int round = acc_bit(a, low);
+    int sticky = 0;
+    for (int i = low - 1; i >= 0 && !sticky; --i) sticky = acc_bit(a, i);
+    if (round && (sticky || (mant & 1u))) mant += 1;   /* may carry to 2^53: exact */
+    return ldexp((double)mant, low + 1 + ORA_ACC_UNIT_EXP);
+}
+
+void ora_norm_accumulate(const float *g, int64_t n, ora_exact_acc *acc, int32_t *overflow)
+{
     int32_t of = *overflow;
     for (int64_t i = 0; i < n; ++i) {
-        if (!isfinite(g[i])) of = 1;
-        ss += (double)g[i] * (double)g[i];
+        if (!isfinite(g[i])) {
+            of = 1;
+            continue;
+        }
+        acc_add_square(acc, g[i]);
     }
-    *sum_sq = ss;
     *overflow = of;
 }
 
@@ -401,18 +488,17 @@ int ora_shard_step(const ora_hparams *hp, ora_scaler *st, int32_t world_size,
     if (!g) return ORA_EOVERFLOW;
 
     const float scale_used = st->scale;
-    double ss = 0.0;
+    ora_exact_acc acc;
+    ora_acc_clear(&acc);
     int32_t overflow = 0;
-    /* global element order: stepped ranks in the order given (the tests pass
-       them ascending), elements ascending within each shard                 */
     for (int32_t j = 0; j < n_ranks; ++j) {
         const int64_t r = ranks[j];
         float *gj = g + (int64_t)j * shard_size;
         ora_reduce_unscale(grad_is_bf16, grads, ld, r * rank_mul, world_size,
                            shard_size, r * shard_size, full_numel, avg, scale_used, gj);
-        ora_norm_accumulate(gj, shard_size, &ss, &overflow);
+        ora_norm_accumulate(gj, shard_size, &acc, &overflow);
     }
-    const double norm = sqrt(ss + extra_norm_sq);
+    const double norm = sqrt(ora_norm_sum(&acc) + extra_norm_sq);
     float coef;
     int32_t skip;
     ora_scaler_decide(hp, st, overflow, norm, &coef, &skip);
@@ -463,10 +549,11 @@ int ora_ddp_step(const ora_hparams *hp, ora_scaler *st, int32_t n_contrib,
     const float scale_used = st->scale;
     ora_reduce_unscale(grad_is_bf16, grads, ld, 0, n_contrib, full_numel, 0,
                        full_numel, avg, scale_used, g);
-    double ss = 0.0;
+    ora_exact_acc acc;
+    ora_acc_clear(&acc);
     int32_t overflow = 0;
-    ora_norm_accumulate(g, full_numel, &ss, &overflow);
-    const double norm = sqrt(ss);
+    ora_norm_accumulate(g, full_numel, &acc, &overflow);
+    const double norm = sqrt(ora_norm_sum(&acc));
     float coef;
     int32_t skip;
     ora_scaler_decide(hp, st, overflow, norm, &coef, &skip);

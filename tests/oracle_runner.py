@@ -1,7 +1,7 @@
 """Run the oracle's own pieces (reduce-scatter + unscale, norm, decision,
 AdamW + cast) over a large shard with host threads: the same arithmetic as
-ora_shard_step, in the same order (the norm is chained through the stepped
-ranks and elements in global order), only spread over cores.  The equality
+ora_shard_step, only spread over cores (the squared norm is an exact sum,
+so its order does not matter).  The equality
 with ora_shard_step is itself a CPU test (test_oracle_runner.py).
 """
 import math
@@ -39,6 +39,22 @@ def reduce_rank(grads, ld, rank_off, n_contrib, S, first, full, avg, scale, bf16
     list(_pool().map(job, _chunks(S)))
 
 
+def norm_exact(arrays, acc=None, overflow=0):
+    """Exact accumulation of the squares of every array (chunk-parallel; the
+    exact sum does not depend on the order)."""
+    jobs = [(a, lo, hi) for a in arrays for lo, hi in _chunks(a.size)]
+
+    def job(x):
+        a, lo, hi = x
+        return oracle.norm_accumulate(a[lo:hi])
+
+    acc = oracle.ExactAcc() if acc is None else acc
+    for part, of in _pool().map(job, jobs):
+        oracle.acc_merge(acc, part)
+        overflow |= of
+    return acc, overflow
+
+
 def shard_step(hp, st, world_size, full, S, ranks, grads, ld, mul, master, m, v, out,
                avg=True, grad_is_bf16=False, param_is_bf16=False, extra_norm_sq=0.0):
     """Equivalent of oracle.shard_step; returns (overflow, skipped, norm, coef, scale_used)."""
@@ -48,10 +64,8 @@ def shard_step(hp, st, world_size, full, S, ranks, grads, ld, mul, master, m, v,
         g = np.empty(max(S, 1), np.float32)[:S]
         reduce_rank(grads, ld, r * mul, world_size, S, r * S, full, avg, scale, grad_is_bf16, g)
         gs.append(g)
-    ss, of = 0.0, 0
-    for g in gs:                                  # global element order
-        ss, of = oracle.norm_accumulate(g, ss, of)
-    norm = math.sqrt(ss + extra_norm_sq)
+    acc, of = norm_exact(gs)
+    norm = math.sqrt(oracle.norm_sum(acc) + extra_norm_sq)
     coef, skip = oracle.scaler_decide(hp, st, of, norm)
     if not skip:
         t = st.step_t

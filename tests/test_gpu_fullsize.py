@@ -1,8 +1,8 @@
 """Full-size parity for the 7B (rank 0 of 8, 842,301,952 params) and 10B
 (rank 7 of 8, 1.25e9 params) shards, in the launch configuration the
 benchmark times.  Every step: the oracle reduces the whole gradient (chunks
-copied to the host, reduced by the oracle's own code on host threads, norm
-chained in global element order), takes the loss-scale / clip decision, and
+copied to the host, reduced by the oracle's own code on host threads, squared
+norm summed exactly), takes the loss-scale / clip decision, and
 computes the AdamW update one by one for ~1M sampled elements (both ends of
 the shard and random positions); those are compared with the GPU's state and
 flat-buffer slot.  The buffer outside the slot must keep its fill."""
@@ -35,7 +35,7 @@ def oracle_reduce(ora, dw, w, scale, idx):
     """(sum of squares, overflow, reduced gradient at idx) by the oracle."""
     S, N, r = dw.S, w.world_size, w.ranks[0]
     bf16 = w.grad_dtype == BF16
-    ss, of = 0.0, 0
+    acc, of = ora.ExactAcc(), 0
     g_s = np.empty(idx.size, np.float32)
     for a in range(0, S, CHUNK):
         b = min(S, a + CHUNK)
@@ -43,10 +43,10 @@ def oracle_reduce(ora, dw, w, scale, idx):
         g = np.empty(b - a, np.float32)
         runner.reduce_rank(gh, b - a, 0, N, b - a, r * S + a, dw.full, w.op == AVG, scale,
                            bf16, g)
-        ss, of = ora.norm_accumulate(g, ss, of)
+        acc, of = runner.norm_exact([g], acc, of)
         lo, hi = np.searchsorted(idx, [a, b])
         g_s[lo:hi] = g[idx[lo:hi] - a]
-    return ss, of, g_s
+    return ora.norm_sum(acc), of, g_s
 
 
 @pytest.mark.parametrize("w", [W.LLAMA_7B, W.TEN_B], ids=lambda w: w.name)

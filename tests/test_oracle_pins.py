@@ -260,16 +260,37 @@ def test_reduce_order_ld_offset_and_padding(ora):
         assert np.all(g[~valid] == 0)
 
 
-def test_norm_accumulate_is_exact_sum_of_squares(ora):
+def test_sum_of_squares_is_exact(ora):
+    # the exact sum of the exact squares, rounded once: math.fsum's answer
     rng = np.random.default_rng(2)
-    g = rng.standard_normal(10_000).astype(np.float32)
-    ss, of = ora.norm_accumulate(g)
-    exact = math.fsum(float(x) * float(x) for x in g)
-    assert of == 0 and abs(ss - exact) <= 1e-12 * exact
+    g = rng.standard_normal(100_000).astype(np.float32)
+    ss, of = ora.sum_of_squares(g)
+    assert of == 0 and ss == math.fsum(float(x) * float(x) for x in g)
+    # extreme magnitudes: subnormal, tiny, huge and mixed scales
+    ext = np.array([2.0 ** -149, 2.0 ** -126, 3.0e-30, 1.0, 1.0e30, 3.4e38, 2.0 ** -149,
+                    7.0, 1e-20], np.float32)
+    exact = sum((Fr(float(x)) ** 2 for x in ext), Fr(0))
+    assert ora.sum_of_squares(ext)[0] == float(exact)        # Fraction -> nearest double
+    acc, _ = ora.norm_accumulate(np.ones(3, np.float32))
+    assert ora.norm_sum(acc) == 3.0
+    # order and splitting do not matter
+    parts = [ora.norm_accumulate(c)[0] for c in np.array_split(g, 7)]
+    tot = ora.ExactAcc()
+    for p_ in parts[::-1]:
+        ora.acc_merge(tot, p_)
+    assert ora.norm_sum(tot) == ss
     g[123] = np.nan
-    assert ora.norm_accumulate(g)[1] == 1
+    assert ora.sum_of_squares(g)[1] == 1
     g[123] = -np.inf
-    assert ora.norm_accumulate(g)[1] == 1
+    assert ora.sum_of_squares(g)[1] == 1
+
+
+def test_sum_of_squares_rounding_ties(ora):
+    # (2^26)^2 + (2^26)^2 + 1 = 2^53 + 1 is halfway between two doubles
+    x = np.array([2.0 ** 26, 2.0 ** 26, 1.0], np.float32)   # 2^53 + 1 exactly
+    assert ora.sum_of_squares(x)[0] == float(Fr(2 ** 53 + 1))   # ties to even: 2^53
+    y = np.array([2.0 ** 26, 2.0 ** 26, 1.0, 1.0, 1.0], np.float32)  # 2^53 + 3
+    assert ora.sum_of_squares(y)[0] == float(Fr(2 ** 53 + 3))   # ties to even: 2^53 + 4
 
 
 # --------------------------------------------------------------------------
