@@ -25,7 +25,8 @@
 // Arithmetic: every fp32 operation is an explicit round-to-nearest intrinsic
 // (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn), so nothing is contracted
 // into an FMA and each result is the IEEE-754 binary32 result of the written
-// expression in the written order.  Division by a power of two is done as a
+// expression in the written order (the only FMAs are the explicit ones that
+// give the exact rounding error of a square in the norm).  Division by a power of two is done as a
 // multiplication by its exact reciprocal, which has the same exact value and
 // therefore the same correctly rounded result.
 #include "zero_kernels.cuh"
@@ -119,6 +120,34 @@ __device__ __forceinline__ float divide(float x, const Divisor &q) {
     return q.pow2 ? __fmul_rn(x, q.inv) : __fdiv_rn(x, q.d);
 }
 
+// ------------------------------------------------------------------ norm
+// The squared norm must be accurate to ~1e-14 so that the fp32 clip
+// coefficient derived from it rounds like the exactly computed one.  Per
+// 8-element chunk the squares are summed without error in fp32 pairs: the
+// exact square of x is p + e with p = x*x and e = fma(x, x, -p) (exact), and
+// Knuth's TwoSum gives the exact error of every addition.  Only the small
+// correction term `lo` is rounded (relative error ~ eps^2), and the chunk's
+// hi + lo enters the thread's fp64 sum once.
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &err) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+__device__ __forceinline__ double chunk_sum_of_squares(const float x[kVec]) {
+    float hi = __fmul_rn(x[0], x[0]);
+    float lo = __fmaf_rn(x[0], x[0], -hi);
+#pragma unroll
+    for (int k = 1; k < kVec; ++k) {
+        const float p = __fmul_rn(x[k], x[k]);
+        const float e = __fmaf_rn(x[k], x[k], -p);
+        float t;
+        two_sum(hi, p, hi, t);
+        lo = __fadd_rn(lo, __fadd_rn(t, e));
+    }
+    return (double)hi + (double)lo;
+}
+
 // ------------------------------------------------------------------ reduction
 // Block total of per-thread fp64 sums and flags, in a fixed order.
 __device__ __forceinline__ void block_partial(double ss, int of, double *out_ss,
@@ -186,7 +215,6 @@ __global__ void __launch_bounds__(kBlock) reduce_kernel(const __grid_constant__ 
 #pragma unroll
                 for (int e = 0; e < kVec; ++e) acc[e] = __fadd_rn(acc[e], f[e]);
             }
-            float sq[kVec];
 #pragma unroll
             for (int e = 0; e < kVec; ++e) {
                 float x = acc[e];
@@ -194,11 +222,8 @@ __global__ void __launch_bounds__(kBlock) reduce_kernel(const __grid_constant__ 
                 x = divide(x, ds);
                 acc[e] = x;
                 of |= !isfinite(x);
-                sq[e] = __fmul_rn(x, x);
             }
-            const float s = __fadd_rn(__fadd_rn(__fadd_rn(sq[0], sq[1]), __fadd_rn(sq[2], sq[3])),
-                                      __fadd_rn(__fadd_rn(sq[4], sq[5]), __fadd_rn(sq[6], sq[7])));
-            ss += (double)s;
+            ss += chunk_sum_of_squares(acc);
             st_f4(g + i0, make_float4(acc[0], acc[1], acc[2], acc[3]));
             st_f4(g + i0 + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
         }
@@ -210,7 +235,7 @@ __global__ void __launch_bounds__(kBlock) reduce_kernel(const __grid_constant__ 
         if (avg) acc = divide(acc, dn);
         acc = divide(acc, ds);
         of |= !isfinite(acc);
-        ss += (double)__fmul_rn(acc, acc);
+        ss += (double)acc * (double)acc;          // exact square in fp64
         g[i] = acc;
     }
     for (int64_t i = valid + tid; i < S; i += nthreads) g[i] = 0.0f;   // padding

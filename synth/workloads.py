@@ -147,5 +147,14 @@ TEN_B = Workload(
     shapes=[(10_000_000_000,)], world_size=8, ranks=[7], grad_dtype=F16, op=AVG,
     dynamic=True, steps=5, sigma_g=2e-4, sigma_n=2e-4, seed=4, grads_layout="slice")
 
+# A smaller case of the 10B rank-7 step (same kernels and launch shape, ~5 GB
+# resident: still far larger than L2) for hardware-counter captures.
+FLAT_800M = Workload(
+    name="flat800m_rank7", description="800M params in one flat buffer, N=8, rank 7's shard "
+    "(1e8 params), fp16 AVG at loss scale 2^16 (profiling size of the 10B step)",
+    shapes=[(800_000_000,)], world_size=8, ranks=[7], grad_dtype=F16, op=AVG, dynamic=True,
+    steps=5, sigma_g=2e-4, sigma_n=2e-4, seed=5, grads_layout="slice")
+
 ALL = [TINY, GPT2, GPT_1P5B, LLAMA_7B, TEN_B]
-BY_NAME = {w.name: w for w in ALL}
+EXTRA = [FLAT_800M]
+BY_NAME = {w.name: w for w in ALL + EXTRA}
