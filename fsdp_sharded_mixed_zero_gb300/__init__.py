@@ -17,7 +17,8 @@ __all__ = [
     "zero_flat_init", "zero_flat_layout", "zero_shard_step", "zero_loss_scaler_state",
     "zero_set_loss_scaler_state", "zero_memory_bytes", "zero_flat_device_bytes",
     "zero_flat_free", "zero_flat_profile_enable", "zero_flat_profile_read",
-    "zero_status_string", "zero_last_error", "ZeroFlat", "LIB_PATH",
+    "zero_shard_step_noalloc", "zero_status_string", "zero_last_error", "ZeroFlat",
+    "LIB_PATH",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -82,6 +83,10 @@ def _load():
     L.zero_flat_free.argtypes = [vp]
     L.zero_flat_profile_enable.argtypes = [vp, i32]
     L.zero_flat_profile_read.argtypes = [vp] + [C.POINTER(C.c_double)] * 3 + [C.POINTER(i64)]
+    L.zero_shard_step_noalloc.argtypes = [i64, i32, i32, i32, i32, C.POINTER(Hparams),
+                                          C.POINTER(ScalerState), C.POINTER(i32), i32, vp, i64,
+                                          i64, C.POINTER(vp), C.POINTER(vp), C.POINTER(vp), vp,
+                                          C.c_double, vp, C.POINTER(StepResult)]
     L.zero_status_string.argtypes = [i32]
     L.zero_status_string.restype = C.c_char_p
     L.zero_last_error.argtypes = []
@@ -89,7 +94,7 @@ def _load():
     for name in ("zero_flat_init", "zero_flat_layout", "zero_shard_step",
                  "zero_loss_scaler_state", "zero_set_loss_scaler_state", "zero_memory_bytes",
                  "zero_flat_device_bytes", "zero_flat_free", "zero_flat_profile_enable",
-                 "zero_flat_profile_read"):
+                 "zero_flat_profile_read", "zero_shard_step_noalloc"):
         getattr(L, name).restype = i32
     return L
 
@@ -159,6 +164,28 @@ def zero_shard_step(h, ranks, grads_ptr, grad_ld, grad_rank_offset_mul, master_p
                                 mp, mm, vv, C.c_void_p(out_ptr), float(extra_norm_sq),
                                 C.c_void_p(stream), C.byref(res) if res is not None else None),
            "zero_shard_step")
+    return res
+
+
+def zero_shard_step_noalloc(full_numel, world_size, grad_dtype, param_dtype, op, hp, state,
+                            ranks, grads_ptr, grad_ld, grad_rank_offset_mul, master_ptrs,
+                            m_ptrs, v_ptrs, out_ptr, extra_norm_sq=0.0, stream=0):
+    """The shard step without a handle and without any allocation, for
+    callers that must not allocate device memory (see include/zero.h).
+    `state` is a ScalerState in host memory, updated in place; returns the
+    StepResult.  Synchronous."""
+    n = len(ranks)
+    r = (C.c_int32 * n)(*ranks)
+    mp = (C.c_void_p * n)(*master_ptrs)
+    mm = (C.c_void_p * n)(*m_ptrs)
+    vv = (C.c_void_p * n)(*v_ptrs)
+    res = StepResult()
+    _check(_lib.zero_shard_step_noalloc(full_numel, world_size, grad_dtype, param_dtype, op,
+                                        C.byref(hp), C.byref(state), r, n, C.c_void_p(grads_ptr),
+                                        grad_ld, grad_rank_offset_mul, mp, mm, vv,
+                                        C.c_void_p(out_ptr), float(extra_norm_sq),
+                                        C.c_void_p(stream), C.byref(res)),
+           "zero_shard_step_noalloc")
     return res
 
 

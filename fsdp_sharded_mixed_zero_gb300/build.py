@@ -11,7 +11,7 @@ from concurrent.futures import ThreadPoolExecutor
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
-SOURCES = ["zero_kernels.cu", "zero_api.cu"]
+SOURCES = ["zero_kernels.cu", "zero_api.cu", "zero_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "zero_kernels.cuh"), os.path.join(ROOT, "include", "zero.h")]
 LIB = os.path.join(HERE, "libzero_gb300.so")
 BUILD = os.path.join(HERE, "_build")

@@ -216,6 +216,11 @@ void release(zero_flat *h) {
 
 }  // namespace
 
+// Lets the other translation units of the library set zero_last_error().
+void zero_internal_set_error(const char *msg) {
+    snprintf(g_last_error, sizeof(g_last_error), "%s", msg);
+}
+
 ZERO_API const char *zero_status_string(zero_status s) {
     switch (s) {
         case ZERO_OK: return "ok";

@@ -204,6 +204,43 @@ zero_status zero_flat_profile_enable(zero_flat *h, int32_t enable);
 zero_status zero_flat_profile_read(zero_flat *h, double *ms_reduce, double *ms_finalize,
                                    double *ms_adamw, int64_t *steps);
 
+/* Size of the device array that zero_shard_step_noalloc uses as scratch. */
+#define ZERO_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* The shard step for callers that may not allocate device memory.
+ * The pages have no counterpart of this entry point: it exists for callers
+ * that run where allocating is forbidden or unsafe -- inside a framework
+ * whose caching allocator owns all device memory, in runtimes that plan every
+ * byte in advance, or in service loops where a cudaMalloc would synchronize
+ * the device or fail at a bad moment.  Such callers cannot create a
+ * zero_flat handle, because zero_flat_init allocates.
+ * Same arithmetic and kernels as zero_shard_step; no handle.  Arguments as
+ * for zero_flat_init / zero_shard_step, except:
+ *   full_numel: elements of the FlatParameter (shard_size = ceil(full/N));
+ *   state: the loss-scale state in HOST memory, read and updated by the call
+ *     (start from scale = 2^initial_scale_power, or the static scale, and
+ *     zeros); n_ranks <= 64.
+ * It calls no cudaMalloc / cudaFree and allocates no host memory.  Its
+ * scratch (fp32 reduced-gradient rows, norm partials, step scalars) is one
+ * file-scope __device__ array of ZERO_NOALLOC_SCRATCH_BYTES that every GPU
+ * which loads this library holds until the process exits; stepped shards
+ * needing more than about 8.3M fp32 scratch elements in total
+ * (n_ranks * roundup(shard_size, 4)) are rejected with ZERO_ERR_INVALID_ARG
+ * and a message in zero_last_error().  Every call shares that array (it keeps
+ * the last call's contents; nothing in it needs to start at zero), so calls
+ * whose GPU work overlaps race: order them.  The call is synchronous: it
+ * waits for `stream` before returning the new state (and `res`, if not NULL).
+ * The first call on a device looks up the array's address and the launch
+ * geometry with that device current; make it before any stream capture. */
+zero_status zero_shard_step_noalloc(int64_t full_numel, int32_t world_size, zero_dtype grad_dtype,
+                                    zero_dtype param_dtype, zero_reduce_op op,
+                                    const zero_hparams *hp, zero_scaler_state *state,
+                                    const int32_t *ranks, int32_t n_ranks, const void *grads,
+                                    int64_t grad_ld, int64_t grad_rank_offset_mul,
+                                    float *const *master, float *const *m, float *const *v,
+                                    void *flat_param_out, double extra_norm_sq, void *stream,
+                                    zero_step_result *res);
+
 /* Release the handle and its device memory (after the work queued with it
  * has finished; this call synchronizes the handle's device).  NULL is OK. */
 zero_status zero_flat_free(zero_flat *h);
