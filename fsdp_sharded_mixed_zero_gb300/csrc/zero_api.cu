@@ -62,7 +62,7 @@ struct DeviceGuard {
 struct zero_flat {
     int device = 0;
     int sm_count = 0;
-    int reduce_bps = 1, adam_bps = 1;
+    int reduce_bps = 1;               // resident reduce blocks per SM
     int32_t world = 1;
     zero_dtype grad_dtype = ZERO_F16, param_dtype = ZERO_F16;
     zero_reduce_op op = ZERO_AVG;
@@ -310,7 +310,7 @@ ZERO_API zero_status zero_flat_init(const zero_param_info *infos, int32_t n_info
     if (e) { delete h; return cuda_fail(e, "cudaGetDevice"); }
     e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device);
     if (e) { delete h; return cuda_fail(e, "cudaDeviceGetAttribute"); }
-    e = zg::blocks_per_sm(&h->reduce_bps, &h->adam_bps);
+    e = zg::reduce_blocks_per_sm(&h->reduce_bps);
     if (e) { delete h; return cuda_fail(e, "occupancy query"); }
     h->world = world_size;
     h->grad_dtype = grad_dtype;
@@ -408,16 +408,10 @@ ZERO_API zero_status zero_shard_step(zero_flat *h, const int32_t *ranks, int32_t
     if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the handle's device");
     cudaStream_t st = (cudaStream_t)stream;
 
-    // launch geometry: one resident wave of blocks, split across stepped ranks
+    // launch geometry (measured per kernel), split across the stepped ranks
     const int64_t batch = std::min<int64_t>(n_ranks, zg::kMaxRanksPerLaunch);
-    const int64_t chunks = (S + zg::kVec - 1) / zg::kVec;
-    const int64_t want = (chunks + zg::kBlock - 1) / zg::kBlock;
-    auto grid_for = [&](int bps) {
-        int64_t cap = (int64_t)h->sm_count * std::max(bps, 1) / batch;
-        return (int)std::max<int64_t>(1, std::min<int64_t>(want, std::max<int64_t>(cap, 1)));
-    };
-    const int gx1 = grid_for(h->reduce_bps);
-    const int gx3 = grid_for(h->adam_bps);
+    const int gx1 = zg::grid_x_for(S, batch, h->sm_count, h->reduce_bps);
+    const int gx3 = zg::grid_x_for(S, batch, h->sm_count, zg::kAdamBlocksPerSm);
     const int64_t parts = (int64_t)gx1 * n_ranks;
     zero_status s = ensure_scratch(h, n_ranks, parts);
     if (s) return s;

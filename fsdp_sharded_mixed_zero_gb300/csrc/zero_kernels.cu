@@ -169,7 +169,7 @@ __device__ __forceinline__ void block_partial(double ss, int of, double *out_ss,
 
 // ------------------------------------------------------------------ K1
 template <bool kBf16>
-__global__ void __launch_bounds__(kBlock) reduce_kernel(const __grid_constant__ ReduceArgs a) {
+__global__ void __launch_bounds__(kBlock, 5) reduce_kernel(const __grid_constant__ ReduceArgs a) {
     const int j = blockIdx.y;
     const int64_t S = a.S;
     int64_t valid = a.full_numel - a.first[j];   // elements [valid, S) are padding
@@ -411,15 +411,14 @@ cudaError_t launch_adamw(const AdamArgs &a, int grid_x, bool bf16_out, cudaStrea
     return cudaGetLastError();
 }
 
-cudaError_t blocks_per_sm(int *reduce_bps, int *adam_bps) {
-    int r0 = 0, r1 = 0, a0 = 0, a1 = 0;
+
+cudaError_t reduce_blocks_per_sm(int *bps) {
+    int r0 = 0, r1 = 0;
     cudaError_t e;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r0, reduce_kernel<false>, kBlock, 0))) return e;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r1, reduce_kernel<true>, kBlock, 0))) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a0, adamw_kernel<false>, kBlock, 0))) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a1, adamw_kernel<true>, kBlock, 0))) return e;
-    *reduce_bps = r0 < r1 ? r0 : r1;
-    *adam_bps = a0 < a1 ? a0 : a1;
+    *bps = r0 < r1 ? r0 : r1;
+    if (*bps < 1) *bps = 1;
     return cudaSuccess;
 }
 

@@ -96,7 +96,26 @@ cudaError_t launch_reduce(const ReduceArgs &a, int grid_x, bool bf16, cudaStream
 cudaError_t launch_finalize(const FinalizeArgs &a, cudaStream_t s);
 cudaError_t launch_adamw(const AdamArgs &a, int grid_x, bool bf16_out, cudaStream_t s);
 
-// Resident blocks per SM of the reduce and AdamW kernels (occupancy API).
-cudaError_t blocks_per_sm(int *reduce_bps, int *adam_bps);
+// Launch geometry, measured on GB300 (152 SMs) on the 10B rank-7 step.  The
+// AdamW kernel streams four arrays in and four out and is fastest with exactly
+// two 256-thread blocks per SM (5.67 ms; 6.50 ms with four, 6.3 ms with three,
+// and grids between whole multiples of the SM count are worse).  The
+// read-dominated reduce is fastest with one full wave of resident blocks (its
+// 48 registers allow five per SM; a partial second wave costs ~15 %).  A
+// launch's blocks are split across the stepped ranks it handles and never
+// exceed the work there is.
+constexpr int kAdamBlocksPerSm = 2;
+
+// Resident blocks per SM of the reduce kernel (occupancy API).
+cudaError_t reduce_blocks_per_sm(int *bps);
+
+inline int grid_x_for(int64_t S, int64_t ranks_in_launch, int sm_count, int blocks_per_sm) {
+    const int64_t chunks = (S + kVec - 1) / kVec;
+    const int64_t want = (chunks + kBlock - 1) / kBlock;
+    int64_t cap = (int64_t)sm_count * blocks_per_sm / (ranks_in_launch > 0 ? ranks_in_launch : 1);
+    if (cap < 1) cap = 1;
+    const int64_t g = want < cap ? want : cap;
+    return (int)(g < 1 ? 1 : g);
+}
 
 }  // namespace zg

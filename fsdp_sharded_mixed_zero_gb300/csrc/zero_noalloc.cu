@@ -61,7 +61,6 @@ struct DeviceSetup {
     unsigned char *base;              // device address of g_noalloc_scratch
     int sm_count;
     int reduce_bps;
-    int adam_bps;
 };
 DeviceSetup g_setup[kMaxDevices];
 std::mutex g_setup_mu;
@@ -90,7 +89,7 @@ zero_status setup_device(int dev, const DeviceSetup **out) {
         if (!p) return fail(ZERO_ERR_CUDA, "static scratch has no device address");
         e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-        e = zg::blocks_per_sm(&d.reduce_bps, &d.adam_bps);
+        e = zg::reduce_blocks_per_sm(&d.reduce_bps);
         if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
         d.base = static_cast<unsigned char *>(p);
         d.done = true;
@@ -253,16 +252,8 @@ ZERO_API zero_status zero_shard_step_noalloc(
     if (s != ZERO_OK) return s;
 
     // ---- launch geometry (as zero_shard_step computes it)
-    const int64_t chunks = (S + zg::kVec - 1) / zg::kVec;
-    const int64_t want = (chunks + zg::kBlock - 1) / zg::kBlock;
-    auto grid_for = [&](int bps) {
-        int64_t cap = (int64_t)d->sm_count * (bps > 1 ? bps : 1) / n_ranks;
-        if (cap < 1) cap = 1;
-        int64_t g = want < cap ? want : cap;
-        return (int)(g < 1 ? 1 : g);
-    };
-    const int gx1 = grid_for(d->reduce_bps);
-    const int gx3 = grid_for(d->adam_bps);
+    const int gx1 = zg::grid_x_for(S, n_ranks, d->sm_count, d->reduce_bps);
+    const int gx3 = zg::grid_x_for(S, n_ranks, d->sm_count, zg::kAdamBlocksPerSm);
     const int64_t parts = (int64_t)gx1 * n_ranks;
     if (parts > kMaxParts) return fail(ZERO_ERR_INVALID_ARG, "too many norm partials");
 
