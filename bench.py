@@ -55,6 +55,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target length of the oracle's timed sample")
+    p.add_argument("--ref-seconds", type=float, default=120.0,
+                   help="target length of the whole --impl reference run")
     return p.parse_args()
 
 
@@ -64,6 +66,49 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+class RankGroup:
+    """The ranks of a torchrun launch (one process per GPU): rendezvous from
+    RANK / WORLD_SIZE / MASTER_ADDR / MASTER_PORT, a barrier, and the maximum
+    of a host value over ranks.  Each rank runs an independent replica of the
+    step; nothing on the data path is exchanged.  backend: "nccl" for GPU
+    ranks, "gloo" for CPU ranks."""
+
+    def __init__(self, backend=None, device=None):
+        self.world, self.rank, self.local = dist_env()
+        self.device = device
+        self.dist = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+            if backend is None:
+                backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend=backend)
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, x):
+        if self.dist is None:
+            return float(x)
+        import torch
+        t = torch.tensor([float(x)], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+            self.dist = None
+
+
+def whole_job_value(params_per_rank, steps, world, max_elapsed_ms):
+    """Gparams/s of the whole job: every rank's stepped parameters over the
+    slowest rank's time."""
+    return params_per_rank * steps * world / (max_elapsed_ms / 1e3) / 1e9
 
 
 def measured_peaks():
@@ -217,7 +262,7 @@ def run_reference(args, w):
             t = time.perf_counter()
             run()
             t0 = time.perf_counter() - t
-            per_step = max(0.2, min(5.0, 120.0 / max(1, args.warmup + args.steps)))
+            per_step = max(0.05, min(5.0, args.ref_seconds / max(1, args.warmup + args.steps)))
             k = int(min(w.shard_size, max(k0, k0 * per_step / max(t0, 1e-6))))
             run, k = oracle_sample_step(w, k)
         t = time.perf_counter()
@@ -245,27 +290,13 @@ def run_ours(args, w):
     import torch
 
     world, rank, local = dist_env()
-    pg = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
-        pg = dist
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    group = RankGroup(backend="nccl", device=dev)
+    barrier, max_over_ranks = group.barrier, group.max
 
     import fsdp_sharded_mixed_zero_gb300 as Z
     from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
-
-    def barrier():
-        if pg is not None:
-            pg.barrier()
-
-    def max_over_ranks(x):
-        if pg is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        return float(t.item())
 
     dw = DeviceWorkload(w, device=dev)
     dw.gen_grads(0, dw.scaler().scale)
@@ -306,7 +337,7 @@ def run_ours(args, w):
 
     N = w.world_size
     ms_step = elapsed_ms / args.steps
-    value = params * args.steps * world / (elapsed_ms / 1e3) / 1e9
+    value = whole_job_value(params, args.steps, world, elapsed_ms)
     peak, peak_kind = measured_peaks()
     # algorithmic bytes per parameter: reduce reads 2N and writes the fp32
     # reduced gradient (4); AdamW reads it (4) and master/m/v (12), writes
@@ -362,8 +393,7 @@ def run_ours(args, w):
         }
         print(json.dumps(line), flush=True)
     dw.close()
-    if pg is not None:
-        pg.destroy_process_group()
+    group.close()
 
 
 def measure_e2e(args, dw, stream, dev, params, barrier, max_over_ranks, world):
