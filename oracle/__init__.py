@@ -93,12 +93,39 @@ def lib():
                                      C.c_void_p, C.c_double, C.POINTER(Result)]
         L.ora_cast_array.argtypes = [C.c_void_p, C.c_int64, C.c_void_p, C.c_int32]
         L.ora_decode_array.argtypes = [C.c_void_p, C.c_int64, C.c_void_p, C.c_int32]
+        L.ora_grad_accumulate.argtypes = [C.c_int32, C.c_int64, C.c_int64, C.c_int32, C.c_int32,
+                                          C.POINTER(C.c_int32), C.c_int32, C.c_void_p,
+                                          C.c_int64, C.c_int64, C.POINTER(C.c_void_p),
+                                          C.c_int32]
+        L.ora_shard_step_acc.argtypes = [C.POINTER(Hparams), C.POINTER(Scaler), C.c_int32,
+                                         C.c_int64, C.c_int64, C.c_int32, C.POINTER(C.c_int32),
+                                         C.c_int32, C.POINTER(C.c_void_p),
+                                         C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
+                                         C.POINTER(C.c_void_p), C.c_void_p, C.c_double,
+                                         C.POINTER(Result)]
         L.ora_ddp_step.argtypes = [C.POINTER(Hparams), C.POINTER(Scaler), C.c_int32,
                                    C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
                                    C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p,
                                    C.c_void_p, C.POINTER(Result)]
         _lib = L
     return _lib
+
+
+def _grad_kind(grads, grad_is_bf16):
+    """Contribution encoding: 0 fp16 / 1 bf16 (uint16 arrays), 2 fp32."""
+    if isinstance(grads, np.ndarray) and grads.dtype == np.float32:
+        assert grads.flags.c_contiguous
+        return 2
+    _check(grads, np.uint16)
+    return 1 if grad_is_bf16 else 0
+
+
+def _ptr_array(arrs, n=None, dtype=np.float32):
+    for a in arrs:
+        _check(a, dtype)
+        if n is not None:
+            assert a.size == n
+    return (C.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
 
 
 def _ptr(a):
@@ -185,11 +212,12 @@ def scaler_init(hp):
 
 def reduce_unscale(grads_u16, ld, rank_off, n_contrib, count, first_flat_index,
                    full_numel, avg, scale, grad_is_bf16=False, out=None):
-    """Reduced, unscaled fp32 gradient of `count` elements (into `out` if given)."""
-    _check(grads_u16, np.uint16)
+    """Reduced, unscaled fp32 gradient of `count` elements (into `out` if given).
+    grads_u16: uint16 fp16/bf16 encodings, or a float32 array of fp32 contributions."""
+    kind = _grad_kind(grads_u16, grad_is_bf16)
     g = np.empty(max(count, 1), dtype=np.float32) if out is None else _check(out, np.float32)
     assert g.size >= count
-    lib().ora_reduce_unscale(int(grad_is_bf16), _ptr(grads_u16), ld, rank_off, n_contrib,
+    lib().ora_reduce_unscale(kind, _ptr(grads_u16), ld, rank_off, n_contrib,
                              count, first_flat_index, full_numel, int(avg), scale, _ptr(g))
     return g[:count]
 
@@ -248,8 +276,9 @@ def shard_step(hp, st, world_size, full_numel, shard_size, ranks, grads_u16, ld,
                rank_mul, master, m, v, flat_out, avg=True, grad_is_bf16=False,
                param_is_bf16=False, extra_norm_sq=0.0):
     """One ZeRO shard step on the listed ranks; master/m/v are lists of fp32
-    arrays (one per stepped rank), flat_out a uint16 array of padded_numel."""
-    _check(grads_u16, np.uint16)
+    arrays (one per stepped rank), flat_out a uint16 array of padded_numel.
+    grads_u16: uint16 fp16/bf16 encodings, or float32 fp32 contributions."""
+    kind = _grad_kind(grads_u16, grad_is_bf16)
     _check(flat_out, np.uint16)
     ranks_a = (C.c_int32 * len(ranks))(*ranks)
     arrs = []
@@ -261,7 +290,7 @@ def shard_step(hp, st, world_size, full_numel, shard_size, ranks, grads_u16, ld,
         arrs.append((C.c_void_p * len(lst))(*[a.ctypes.data for a in lst]))
     res = Result()
     rc = lib().ora_shard_step(C.byref(hp), C.byref(st), world_size, full_numel,
-                              shard_size, int(grad_is_bf16), int(param_is_bf16), int(avg),
+                              shard_size, kind, int(param_is_bf16), int(avg),
                               ranks_a, len(ranks), _ptr(grads_u16), ld, rank_mul,
                               arrs[0], arrs[1], arrs[2], _ptr(flat_out),
                               float(extra_norm_sq), C.byref(res))
@@ -270,15 +299,44 @@ def shard_step(hp, st, world_size, full_numel, shard_size, ranks, grads_u16, ld,
     return res
 
 
+def grad_accumulate(world_size, full_numel, shard_size, ranks, grads, ld, rank_mul, acc,
+                    first, avg=True, grad_is_bf16=False):
+    """acc[j] (fp32 arrays, one per stepped rank) = reduce(grads) if first,
+    else acc[j] + reduce(grads)."""
+    kind = _grad_kind(grads, grad_is_bf16)
+    ranks_a = (C.c_int32 * len(ranks))(*ranks)
+    rc = lib().ora_grad_accumulate(world_size, full_numel, shard_size, kind, int(avg), ranks_a,
+                                   len(ranks), _ptr(grads), ld, rank_mul,
+                                   _ptr_array(acc, shard_size), int(bool(first)))
+    if rc:
+        raise ValueError("ora_grad_accumulate failed: %d" % rc)
+
+
+def shard_step_acc(hp, st, world_size, full_numel, shard_size, ranks, acc, master, m, v,
+                   flat_out, param_is_bf16=False, extra_norm_sq=0.0):
+    """The optimizer step on accumulated fp32 shards acc[j]."""
+    _check(flat_out, np.uint16)
+    ranks_a = (C.c_int32 * len(ranks))(*ranks)
+    res = Result()
+    rc = lib().ora_shard_step_acc(C.byref(hp), C.byref(st), world_size, full_numel, shard_size,
+                                  int(param_is_bf16), ranks_a, len(ranks),
+                                  _ptr_array(acc, shard_size), _ptr_array(master, shard_size),
+                                  _ptr_array(m, shard_size), _ptr_array(v, shard_size),
+                                  _ptr(flat_out), float(extra_norm_sq), C.byref(res))
+    if rc:
+        raise ValueError("ora_shard_step_acc failed: %d" % rc)
+    return res
+
+
 def ddp_step(hp, st, n_contrib, full_numel, grads_u16, ld, master, m, v, out,
              avg=True, grad_is_bf16=False, param_is_bf16=False):
     for a in (master, m, v):
         _check(a, np.float32)
-    _check(grads_u16, np.uint16)
+    kind = _grad_kind(grads_u16, grad_is_bf16)
     _check(out, np.uint16)
     res = Result()
     rc = lib().ora_ddp_step(C.byref(hp), C.byref(st), n_contrib, full_numel,
-                            int(grad_is_bf16), int(param_is_bf16), int(avg),
+                            kind, int(param_is_bf16), int(avg),
                             _ptr(grads_u16), ld, _ptr(master), _ptr(m), _ptr(v),
                             _ptr(out), C.byref(res))
     if rc:

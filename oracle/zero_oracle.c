@@ -252,8 +252,17 @@ void ora_scaler_init(const ora_hparams *hp, ora_scaler *st)
  * grads[c*ld + rank_off + i] with rank_off = r*mul.  Elements whose flat
  * index is >= full_numel are padding: their gradient is zero.
  * For each element: acc = 0; acc += f32(grad_c) for c = 0..N-1 in order;
- * AVG divides by N; then g = acc / scale.                                    */
-void ora_reduce_unscale(int32_t grad_is_bf16, const uint16_t *grads, int64_t ld,
+ * AVG divides by N; then g = acc / scale.
+ * grad_kind: 0 fp16, 1 bf16, 2 fp32 contributions (fp32 when the reduce runs
+ * in reduce_dtype=float32 end to end).                                      */
+static float contribution(const void *grads, int32_t grad_kind, int64_t idx)
+{
+    if (grad_kind == 2) return ((const float *)grads)[idx];
+    const uint16_t h = ((const uint16_t *)grads)[idx];
+    return grad_kind == 1 ? ora_bf16_to_f32(h) : ora_f16_to_f32(h);
+}
+
+void ora_reduce_unscale(int32_t grad_kind, const void *grads, int64_t ld,
                         int64_t rank_off, int32_t n_contrib, int64_t count,
                         int64_t first_flat_index, int64_t full_numel, int32_t avg,
                         float scale, float *g_out)
@@ -264,10 +273,8 @@ void ora_reduce_unscale(int32_t grad_is_bf16, const uint16_t *grads, int64_t ld,
             continue;
         }
         float acc = 0.0f;
-        for (int32_t c = 0; c < n_contrib; ++c) {
-            const uint16_t h = grads[(int64_t)c * ld + rank_off + i];
-            acc = acc + (grad_is_bf16 ? ora_bf16_to_f32(h) : ora_f16_to_f32(h));
-        }
+        for (int32_t c = 0; c < n_contrib; ++c)
+            acc = acc + contribution(grads, grad_kind, (int64_t)c * ld + rank_off + i);
         if (avg) acc = acc / (float)n_contrib;
         g_out[i] = acc / scale;
     }
@@ -464,40 +471,23 @@ void ora_adamw_cast(const ora_hparams *hp, int64_t t, float coef, const float *g
 }
 
 /* ------------------------------------------------------------------------- */
-/* One ZeRO shard step for the stepped ranks ranks[0..n_ranks) (one rank, or
- * all N in an emulation of the whole group), composed from the pieces above:
- * reduce-scatter + unscale -> overflow check and global norm over every
- * stepped shard (plus extra_norm_sq, the other ranks' share) -> loss-scale
- * decision and clip coefficient -> AdamW + cast into the flat buffer.
- * A skipped step leaves master, m, v, t and the flat buffer untouched.
- * master[j], m[j], v[j] point at rank ranks[j]'s shard_size elements.       */
-int ora_shard_step(const ora_hparams *hp, ora_scaler *st, int32_t world_size,
-                   int64_t full_numel, int64_t shard_size, int32_t grad_is_bf16,
-                   int32_t param_is_bf16, int32_t avg, const int32_t *ranks,
-                   int32_t n_ranks, const uint16_t *grads, int64_t ld,
-                   int64_t rank_mul, float *const *master, float *const *m,
-                   float *const *v, uint16_t *flat_out, double extra_norm_sq,
-                   ora_result *res)
+/* The part of a step after the reduce: overflow check and global norm over
+ * every stepped shard's reduced gradient g (plus extra_norm_sq, the other
+ * ranks' share) -> loss-scale decision and clip coefficient -> AdamW + cast
+ * into each rank's slot of the flat buffer.  g holds n_ranks rows of
+ * shard_size.  A skipped step leaves master, m, v, t and the flat buffer
+ * untouched.                                                               */
+static void apply_step(const ora_hparams *hp, ora_scaler *st, int64_t shard_size,
+                       int32_t param_is_bf16, const int32_t *ranks, int32_t n_ranks,
+                       const float *g, float *const *master, float *const *m,
+                       float *const *v, uint16_t *flat_out, double extra_norm_sq,
+                       float scale_used, ora_result *res)
 {
-    if (!hp || !st || !ranks || n_ranks < 1 || world_size < 1 || shard_size < 0)
-        return ORA_EINVAL;
-    for (int32_t j = 0; j < n_ranks; ++j)
-        if (ranks[j] < 0 || ranks[j] >= world_size) return ORA_EINVAL;
-    float *g = (float *)malloc(sizeof(float) * (size_t)(shard_size ? shard_size : 1)
-                               * (size_t)n_ranks);
-    if (!g) return ORA_EOVERFLOW;
-
-    const float scale_used = st->scale;
     ora_exact_acc acc;
     ora_acc_clear(&acc);
     int32_t overflow = 0;
-    for (int32_t j = 0; j < n_ranks; ++j) {
-        const int64_t r = ranks[j];
-        float *gj = g + (int64_t)j * shard_size;
-        ora_reduce_unscale(grad_is_bf16, grads, ld, r * rank_mul, world_size,
-                           shard_size, r * shard_size, full_numel, avg, scale_used, gj);
-        ora_norm_accumulate(gj, shard_size, &acc, &overflow);
-    }
+    for (int32_t j = 0; j < n_ranks; ++j)
+        ora_norm_accumulate(g + (int64_t)j * shard_size, shard_size, &acc, &overflow);
     const double norm = sqrt(ora_norm_sum(&acc) + extra_norm_sq);
     float coef;
     int32_t skip;
@@ -517,6 +507,100 @@ int ora_shard_step(const ora_hparams *hp, ora_scaler *st, int32_t world_size,
         res->clip_coef = coef;
         res->scale_used = scale_used;
     }
+}
+
+static int check_ranks(const int32_t *ranks, int32_t n_ranks, int32_t world_size)
+{
+    if (!ranks || n_ranks < 1 || world_size < 1) return ORA_EINVAL;
+    for (int32_t j = 0; j < n_ranks; ++j)
+        if (ranks[j] < 0 || ranks[j] >= world_size) return ORA_EINVAL;
+    return ORA_OK;
+}
+
+static float *alloc_rows(int64_t shard_size, int32_t n_ranks)
+{
+    return (float *)malloc(sizeof(float) * (size_t)(shard_size ? shard_size : 1) *
+                           (size_t)n_ranks);
+}
+
+/* One ZeRO shard step for the stepped ranks ranks[0..n_ranks) (one rank, or
+ * all N in an emulation of the whole group): reduce-scatter + unscale of each
+ * stepped shard, then apply_step.  master[j], m[j], v[j] point at rank
+ * ranks[j]'s shard_size elements.                                           */
+int ora_shard_step(const ora_hparams *hp, ora_scaler *st, int32_t world_size,
+                   int64_t full_numel, int64_t shard_size, int32_t grad_kind,
+                   int32_t param_is_bf16, int32_t avg, const int32_t *ranks,
+                   int32_t n_ranks, const void *grads, int64_t ld,
+                   int64_t rank_mul, float *const *master, float *const *m,
+                   float *const *v, uint16_t *flat_out, double extra_norm_sq,
+                   ora_result *res)
+{
+    if (!hp || !st || shard_size < 0 || check_ranks(ranks, n_ranks, world_size))
+        return ORA_EINVAL;
+    float *g = alloc_rows(shard_size, n_ranks);
+    if (!g) return ORA_EOVERFLOW;
+    const float scale_used = st->scale;
+    for (int32_t j = 0; j < n_ranks; ++j) {
+        const int64_t r = ranks[j];
+        ora_reduce_unscale(grad_kind, grads, ld, r * rank_mul, world_size, shard_size,
+                           r * shard_size, full_numel, avg, scale_used,
+                           g + (int64_t)j * shard_size);
+    }
+    apply_step(hp, st, shard_size, param_is_bf16, ranks, n_ranks, g, master, m, v,
+               flat_out, extra_norm_sq, scale_used, res);
+    free(g);
+    return ORA_OK;
+}
+
+/* Gradient accumulation across micro-steps.  [P1] §实践要点 (gradient
+ * accumulation): the loss is divided by the number of micro-steps and the
+ * micro-steps' gradients add up before one optimizer step; [P3] §5.1
+ * (contiguous_gradients) and §5.3: the reduced gradient partitions live in
+ * one contiguous buffer and accumulate there.  Reading: every micro-step's
+ * contributions are reduced exactly as in the step (fp32, contributor order,
+ * AVG) and added into the rank's fp32 accumulator:
+ *     r = reduce(grads);  acc = first ? r : acc + r.
+ * The loss scale stays in the accumulator until the optimizer step.         */
+int ora_grad_accumulate(int32_t world_size, int64_t full_numel, int64_t shard_size,
+                        int32_t grad_kind, int32_t avg, const int32_t *ranks,
+                        int32_t n_ranks, const void *grads, int64_t ld, int64_t rank_mul,
+                        float *const *acc, int32_t first)
+{
+    if (shard_size < 0 || check_ranks(ranks, n_ranks, world_size)) return ORA_EINVAL;
+    float *r = alloc_rows(shard_size, 1);
+    if (!r) return ORA_EOVERFLOW;
+    for (int32_t j = 0; j < n_ranks; ++j) {
+        const int64_t rk = ranks[j];
+        ora_reduce_unscale(grad_kind, grads, ld, rk * rank_mul, world_size, shard_size,
+                           rk * shard_size, full_numel, avg, 1.0f, r);
+        for (int64_t i = 0; i < shard_size; ++i)
+            acc[j][i] = first ? r[i] : acc[j][i] + r[i];
+    }
+    free(r);
+    return ORA_OK;
+}
+
+/* The optimizer step on accumulated shards: g = acc / scale (padding
+ * elements, flat index >= full_numel, count as zero), then apply_step.      */
+int ora_shard_step_acc(const ora_hparams *hp, ora_scaler *st, int32_t world_size,
+                       int64_t full_numel, int64_t shard_size, int32_t param_is_bf16,
+                       const int32_t *ranks, int32_t n_ranks, const float *const *acc,
+                       float *const *master, float *const *m, float *const *v,
+                       uint16_t *flat_out, double extra_norm_sq, ora_result *res)
+{
+    if (!hp || !st || shard_size < 0 || check_ranks(ranks, n_ranks, world_size))
+        return ORA_EINVAL;
+    float *g = alloc_rows(shard_size, n_ranks);
+    if (!g) return ORA_EOVERFLOW;
+    const float scale_used = st->scale;
+    for (int32_t j = 0; j < n_ranks; ++j) {
+        const int64_t first = (int64_t)ranks[j] * shard_size;
+        for (int64_t i = 0; i < shard_size; ++i)
+            g[(int64_t)j * shard_size + i] =
+                first + i >= full_numel ? 0.0f : acc[j][i] / scale_used;
+    }
+    apply_step(hp, st, shard_size, param_is_bf16, ranks, n_ranks, g, master, m, v,
+               flat_out, extra_norm_sq, scale_used, res);
     free(g);
     return ORA_OK;
 }
@@ -539,34 +623,19 @@ void ora_decode_array(const uint16_t *in, int64_t n, float *out, int32_t from_bf
  * all-reduced, and the whole flat parameter is updated on one replica.
  * grads: N rows of at least full_numel elements, row stride ld.            */
 int ora_ddp_step(const ora_hparams *hp, ora_scaler *st, int32_t n_contrib,
-                 int64_t full_numel, int32_t grad_is_bf16, int32_t param_is_bf16,
-                 int32_t avg, const uint16_t *grads, int64_t ld, float *master,
+                 int64_t full_numel, int32_t grad_kind, int32_t param_is_bf16,
+                 int32_t avg, const void *grads, int64_t ld, float *master,
                  float *m, float *v, uint16_t *out, ora_result *res)
 {
     if (!hp || !st || n_contrib < 1 || full_numel < 0) return ORA_EINVAL;
-    float *g = (float *)malloc(sizeof(float) * (size_t)(full_numel ? full_numel : 1));
+    float *g = alloc_rows(full_numel, 1);
     if (!g) return ORA_EOVERFLOW;
     const float scale_used = st->scale;
-    ora_reduce_unscale(grad_is_bf16, grads, ld, 0, n_contrib, full_numel, 0,
-                       full_numel, avg, scale_used, g);
-    ora_exact_acc acc;
-    ora_acc_clear(&acc);
-    int32_t overflow = 0;
-    ora_norm_accumulate(g, full_numel, &acc, &overflow);
-    const double norm = sqrt(ora_norm_sum(&acc));
-    float coef;
-    int32_t skip;
-    ora_scaler_decide(hp, st, overflow, norm, &coef, &skip);
-    if (!skip)
-        ora_adamw_cast(hp, st->step_t, coef, g, master, m, v, full_numel, out,
-                       param_is_bf16);
-    if (res) {
-        res->overflow = overflow;
-        res->skipped = skip;
-        res->grad_norm = norm;
-        res->clip_coef = coef;
-        res->scale_used = scale_used;
-    }
+    ora_reduce_unscale(grad_kind, grads, ld, 0, n_contrib, full_numel, 0, full_numel, avg,
+                       scale_used, g);
+    const int32_t rank0 = 0;
+    apply_step(hp, st, full_numel, param_is_bf16, &rank0, 1, g, &master, &m, &v, out, 0.0,
+               scale_used, res);
     free(g);
     return ORA_OK;
 }

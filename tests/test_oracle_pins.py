@@ -628,3 +628,127 @@ def test_zero_equals_ddp(ora, N, n, bf16, avg):
         assert np.array_equal(zout[:full], dout)
         assert not np.concatenate(zm)[full:].any()             # padding stays zero
     assert st_z.step_t == (5 if bf16 else 4)
+
+
+# --------------------------------------------------------------------------
+# fp32 contributions (reduce_dtype=float32, DS-FSDP §PyTorch FSDP 使用) and
+# gradient accumulation across micro-steps (DS-FSDP §实践要点; ZeRO reading
+# §5.1 contiguous_gradients).
+
+def test_fp32_contributions_sum_then_split(ora):
+    rng = np.random.default_rng(21)
+    N, n = 4, 40
+    ints = rng.integers(-2 ** 20, 2 ** 20, size=(N, n))       # exact in fp32, sums too
+    grads = ints.astype(np.float32)
+    full, S, padded = ora.layout([n], N)
+    want = np.array_split(ints.sum(axis=0), N)
+    for r in range(N):
+        g = ora.reduce_unscale(grads, n, r * S, N, S, r * S, full, avg=False, scale=1.0)
+        assert np.array_equal(g, want[r].astype(np.float32))
+
+
+def test_fp32_contributions_sequential_order(ora):
+    rng = np.random.default_rng(22)
+    N, S = 5, 1000
+    grads = rng.standard_normal((N, S)).astype(np.float32) * np.float32(1e3)
+    g = ora.reduce_unscale(grads, S, 0, N, S, 0, S, avg=True, scale=4.0)
+    acc = np.zeros(S, np.float32)
+    for c in range(N):
+        acc = acc + grads[c]
+    assert np.array_equal(g, (acc / np.float32(N)) / np.float32(4.0))
+
+
+def test_accumulation_is_the_sum_of_micro_steps(ora):
+    rng = np.random.default_rng(23)
+    N, n, K = 4, 64, 5
+    full, S, padded = ora.layout([n], N)
+    acc = [np.full(S, 7.0, np.float32) for _ in range(N)]     # overwritten by first=True
+    total = np.zeros((N, padded), np.int64)
+    for k in range(K):
+        ints = rng.integers(-1000, 1000, size=(N, padded))
+        total += ints
+        ora.grad_accumulate(N, full, S, list(range(N)), ints.astype(np.float16).view(np.uint16),
+                            padded, S, acc, first=(k == 0), avg=True)
+    want = total.sum(axis=0) / N                              # exact: N is a power of two
+    for r in range(N):
+        assert np.array_equal(acc[r], want[r * S:(r + 1) * S].astype(np.float32))
+
+
+@pytest.mark.parametrize("kind", ["f16", "bf16", "f32"])
+def test_one_micro_step_equals_the_direct_step(ora, kind):
+    # accumulate once (first=True), then step from the accumulator: the same
+    # bits as the direct step on the same contributions
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(24)
+    N, n = 3, 1001
+    full, S, padded = ora.layout([n], N)
+    x = rng.standard_normal((N, padded)) * 100.0
+    if kind == "f16":
+        grads, bf = x.astype(np.float16).view(np.uint16), False
+    elif kind == "bf16":
+        grads = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).view(
+            torch.int16).numpy().view(np.uint16)
+        bf = True
+    else:
+        grads, bf = x.astype(np.float32), False
+    hp = ora.hparams(lr=1e-3, max_grad_norm=1.0, initial_scale_power=3)
+    sa, sb = ora.scaler_init(hp), ora.scaler_init(hp)
+    th = [(rng.standard_normal(S) * 0.02).astype(np.float32) for _ in range(N)]
+    A = [[t.copy() for t in th], [np.zeros(S, np.float32) for _ in range(N)],
+         [np.zeros(S, np.float32) for _ in range(N)], np.zeros(padded, np.uint16)]
+    B = [[t.copy() for t in th], [np.zeros(S, np.float32) for _ in range(N)],
+         [np.zeros(S, np.float32) for _ in range(N)], np.zeros(padded, np.uint16)]
+    ra = ora.shard_step(hp, sa, N, full, S, list(range(N)), grads, padded, S, A[0], A[1], A[2],
+                        A[3], avg=True, grad_is_bf16=bf)
+    acc = [np.zeros(S, np.float32) for _ in range(N)]
+    ora.grad_accumulate(N, full, S, list(range(N)), grads, padded, S, acc, first=True,
+                        avg=True, grad_is_bf16=bf)
+    rb = ora.shard_step_acc(hp, sb, N, full, S, list(range(N)), acc, B[0], B[1], B[2], B[3])
+    assert (ra.overflow, ra.skipped, ra.grad_norm, ra.clip_coef, ra.scale_used) == \
+           (rb.overflow, rb.skipped, rb.grad_norm, rb.clip_coef, rb.scale_used)
+    assert sa.as_tuple() == sb.as_tuple()
+    for xa, xb in zip(A[0] + A[1] + A[2] + [A[3]], B[0] + B[1] + B[2] + [B[3]]):
+        assert np.array_equal(xa, xb)
+
+
+def test_cancelling_micro_steps_give_pure_decay(ora):
+    # micro-steps G and -G accumulate to exactly zero: the step is theta*decay
+    rng = np.random.default_rng(25)
+    N, n = 2, 500
+    full, S, padded = ora.layout([n], N)
+    G = (rng.standard_normal((N, padded)) * 1000).astype(np.float16)
+    acc = [np.zeros(S, np.float32) for _ in range(N)]
+    ora.grad_accumulate(N, full, S, [0, 1], G.view(np.uint16), padded, S, acc, first=True)
+    ora.grad_accumulate(N, full, S, [0, 1], (-G).view(np.uint16), padded, S, acc, first=False)
+    assert all(not a.any() for a in acc)
+    hp = ora.hparams(lr=1e-2, weight_decay=0.1)
+    st = ora.scaler_init(hp)
+    th0 = [(rng.standard_normal(S) * 0.3).astype(np.float32) for _ in range(N)]
+    th = [t.copy() for t in th0]
+    m = [np.zeros(S, np.float32) for _ in range(N)]
+    v = [np.zeros(S, np.float32) for _ in range(N)]
+    res = ora.shard_step_acc(hp, st, N, full, S, [0, 1], acc, th, m, v,
+                             np.zeros(padded, np.uint16))
+    assert res.grad_norm == 0.0 and res.skipped == 0
+    decay = np.float32(1.0 - 1e-2 * 0.1)
+    for a, b in zip(th, th0):
+        assert np.array_equal(a, b * decay)
+
+
+def test_step_from_accumulator_overflow_and_padding(ora):
+    N, n = 3, 10
+    full, S, padded = ora.layout([n], N)                      # S=4, two padding elements
+    hp = ora.hparams(initial_scale_power=4)
+    st = ora.scaler_init(hp)
+    acc = [np.ones(S, np.float32) for _ in range(N)]
+    acc[2][3] = np.inf                                        # padding: ignored
+    th = [np.zeros(S, np.float32) for _ in range(N)]
+    m = [np.zeros(S, np.float32) for _ in range(N)]
+    v = [np.zeros(S, np.float32) for _ in range(N)]
+    res = ora.shard_step_acc(hp, st, N, full, S, [0, 1, 2], acc, th, m, v,
+                             np.zeros(padded, np.uint16))
+    assert res.overflow == 0 and abs(res.grad_norm - np.sqrt(10) / 16) < 1e-15
+    acc[1][0] = np.nan
+    res = ora.shard_step_acc(hp, st, N, full, S, [0, 1, 2], acc, th, m, v,
+                             np.zeros(padded, np.uint16))
+    assert res.overflow == 1 and res.skipped == 1 and st.scale == 8.0
