@@ -51,6 +51,10 @@ def parse_args():
     p.add_argument("--workload", default="10b_rank7")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--micro-steps", type=int, default=1,
+                   help="K > 1: each step accumulates K micro-steps' contributions into an "
+                        "fp32 shard (zero_grad_accumulate) and steps from it "
+                        "(zero_shard_step_accumulated)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -303,11 +307,30 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
     params = dw.S * len(w.ranks)
     n_batches = -(-len(w.ranks) // 64)
-    launches_per_step = 2 * n_batches + 1
-    torch.cuda.synchronize(dev)
+    K = max(1, args.micro_steps)
+    launches_per_step = 2 * n_batches + 1 + (K * n_batches if K > 1 else 0)
+    acc_events = []
+    if K > 1:
+        dw.alloc_acc()
 
+    def one_step(timed=False):
+        if K == 1:
+            dw.step(want_result=False, stream=stream)
+            return
+        if timed:
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+        for k in range(K):
+            dw.accumulate(first=(k == 0), stream=stream)
+        if timed:
+            a1.record(stream)
+            acc_events.append((a0, a1))
+        dw.step_accumulated(want_result=False, stream=stream)
+
+    torch.cuda.synchronize(dev)
     for _ in range(args.warmup):
-        dw.step(want_result=False, stream=stream)
+        one_step()
     torch.cuda.synchronize(dev)
 
     try:
@@ -324,7 +347,7 @@ def run_ours(args, w):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        dw.step(want_result=False, stream=stream)
+        one_step(timed=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -332,28 +355,39 @@ def run_ours(args, w):
     Z.zero_flat_profile_enable(dw.flat.handle, False)
     ms_red, ms_fin, ms_adam, nrec = Z.zero_flat_profile_read(dw.flat.handle)
     elapsed_ms = max_over_ranks(e0.elapsed_time(e1))
-    res = dw.step(want_result=True, stream=stream)          # sanity: the step ran clean
+    res = (dw.step(want_result=True, stream=stream) if K == 1 else
+           dw.step_accumulated(want_result=True, stream=stream))   # sanity: a clean step
     assert res.skipped == 0 and res.overflow == 0, "benchmark inputs overflowed"
+    ms_acc = sum(a0.elapsed_time(a1) for a0, a1 in acc_events)
 
     N = w.world_size
+    esize = 4 if w.grad_dtype == 2 else 2
     ms_step = elapsed_ms / args.steps
     value = whole_job_value(params, args.steps, world, elapsed_ms)
     peak, peak_kind = measured_peaks()
-    # algorithmic bytes per parameter: reduce reads 2N and writes the fp32
-    # reduced gradient (4); AdamW reads it (4) and master/m/v (12), writes
-    # master/m/v (12) and the 16-bit param (2)
+    # algorithmic bytes per parameter: the reduce reads the N contributions
+    # (N*esize) and writes the fp32 reduced gradient (4); AdamW reads it (4)
+    # and master/m/v (12), writes master/m/v (12) and the 16-bit param (2).
+    # With micro-steps the reduce kernel is the norm pass over the fp32
+    # accumulator (4) and the accumulate launches read N*esize, read (after
+    # the first) and write the accumulator.
     kernels = {
-        "reduce_kernel": {"ms_mean": ms_red / max(nrec, 1), "bytes_per_param": 2 * N + 4},
+        "reduce_kernel": {"ms_mean": ms_red / max(nrec, 1),
+                          "bytes_per_param": N * esize + 4 if K == 1 else 4},
         "adamw_kernel": {"ms_mean": ms_adam / max(nrec, 1), "bytes_per_param": 30},
         "finalize_kernel": {"ms_mean": ms_fin / max(nrec, 1), "bytes_per_param": 0},
     }
+    if K > 1:
+        kernels["accumulate_launch"] = {
+            "ms_mean": ms_acc / max(len(acc_events), 1) / K,
+            "bytes_per_param": N * esize + (4 + 8 * (K - 1)) / K}
     for k in kernels.values():
         k["achieved_gbs"] = (k["bytes_per_param"] * params / (k["ms_mean"] / 1e3) / 1e9
                              if k["ms_mean"] > 0 else None)
-    dom = max(("reduce_kernel", "adamw_kernel"), key=lambda n: kernels[n]["ms_mean"])
+    dom = max(kernels, key=lambda n: kernels[n]["ms_mean"] * (K if n == "accumulate_launch" else 1))
     dk = kernels[dom]
     traffic = profiled_traffic(dom, w.name)
-    min_bytes = (2 * N + 26) * params                       # spec minimum per step
+    min_bytes = (K * N * esize + 26) * params               # the method's minimum per step
     step_gbs = min_bytes / (ms_step / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": dk["achieved_gbs"], "peak": peak,
                 "unit": "GB/s", "frac": dk["achieved_gbs"] / peak,
@@ -361,7 +395,7 @@ def run_ours(args, w):
                 "bytes_per_launch": dk["bytes_per_param"] * params}
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and K == 1:
         e2e = measure_e2e(args, dw, stream, dev, params, barrier, max_over_ranks, world)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -375,13 +409,15 @@ def run_ours(args, w):
             "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "params_stepped_per_gpu": params,
                        "emulated_world_size": N, "stepped_ranks": w.ranks,
-                       "storage": "%s grads and params, f32 master/m/v" %
-                                  ("bf16" if w.grad_dtype == 1 else "f16"),
+                       "storage": "%s grads, %s params, f32 master/m/v" %
+                                  (("f16", "bf16", "f32")[w.grad_dtype],
+                                   ("f16", "bf16")[w.param_dtype]),
+                       "micro_steps": K,
                        "l2": "inputs larger than L2 (%.0f GB resident vs 129 MB)" %
-                             (dw.flat.device_bytes() / 1e9 + (dw.grads.numel() * 2 +
-                              3 * params * 4 + dw.out.numel() * 2) / 1e9),
+                             (dw.flat.device_bytes() / 1e9 + (dw.grads.numel() * esize +
+                              (3 + (K > 1)) * params * 4 + dw.out.numel() * 2) / 1e9),
                        "parallelism": "replicas%d" % world},
-            "step_hbm": {"min_bytes_per_param": 2 * N + 26, "achieved_gbs": step_gbs,
+            "step_hbm": {"min_bytes_per_param": K * N * esize + 26, "achieved_gbs": step_gbs,
                          "frac_of_measured": step_gbs / peak,
                          "frac_of_nominal_8tbs": step_gbs / NOMINAL_HBM_GBS},
             "kernels": kernels,

@@ -12,12 +12,13 @@ import ctypes as C
 import os
 
 __all__ = [
-    "ZERO_OK", "ZERO_F16", "ZERO_BF16", "ZERO_SUM", "ZERO_AVG", "ZeroError",
+    "ZERO_OK", "ZERO_F16", "ZERO_BF16", "ZERO_F32", "ZERO_SUM", "ZERO_AVG", "ZeroError",
     "ParamInfo", "Hparams", "ScalerState", "StepResult", "hparams", "param_infos",
     "zero_flat_init", "zero_flat_layout", "zero_shard_step", "zero_loss_scaler_state",
     "zero_set_loss_scaler_state", "zero_memory_bytes", "zero_flat_device_bytes",
     "zero_flat_free", "zero_flat_profile_enable", "zero_flat_profile_read",
-    "zero_shard_step_noalloc", "zero_status_string", "zero_last_error", "ZeroFlat",
+    "zero_shard_step_noalloc", "zero_grad_accumulate", "zero_shard_step_accumulated",
+    "zero_status_string", "zero_last_error", "ZeroFlat",
     "LIB_PATH",
 ]
 
@@ -25,7 +26,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libzero_gb300.so")
 
 ZERO_OK = 0
-ZERO_F16, ZERO_BF16 = 0, 1
+ZERO_F16, ZERO_BF16, ZERO_F32 = 0, 1, 2
 ZERO_SUM, ZERO_AVG = 0, 1
 
 
@@ -87,6 +88,11 @@ def _load():
                                           C.POINTER(ScalerState), C.POINTER(i32), i32, vp, i64,
                                           i64, C.POINTER(vp), C.POINTER(vp), C.POINTER(vp), vp,
                                           C.c_double, vp, C.POINTER(StepResult)]
+    L.zero_grad_accumulate.argtypes = [vp, C.POINTER(i32), i32, vp, i64, i64, C.POINTER(vp), i32,
+                                       vp]
+    L.zero_shard_step_accumulated.argtypes = [vp, C.POINTER(i32), i32, C.POINTER(vp),
+                                              C.POINTER(vp), C.POINTER(vp), C.POINTER(vp), vp,
+                                              C.c_double, vp, C.POINTER(StepResult)]
     L.zero_status_string.argtypes = [i32]
     L.zero_status_string.restype = C.c_char_p
     L.zero_last_error.argtypes = []
@@ -94,7 +100,8 @@ def _load():
     for name in ("zero_flat_init", "zero_flat_layout", "zero_shard_step",
                  "zero_loss_scaler_state", "zero_set_loss_scaler_state", "zero_memory_bytes",
                  "zero_flat_device_bytes", "zero_flat_free", "zero_flat_profile_enable",
-                 "zero_flat_profile_read", "zero_shard_step_noalloc"):
+                 "zero_flat_profile_read", "zero_shard_step_noalloc", "zero_grad_accumulate",
+                 "zero_shard_step_accumulated"):
         getattr(L, name).restype = i32
     return L
 
@@ -189,6 +196,32 @@ def zero_shard_step_noalloc(full_numel, world_size, grad_dtype, param_dtype, op,
     return res
 
 
+def zero_grad_accumulate(h, ranks, grads_ptr, grad_ld, grad_rank_offset_mul, acc_ptrs,
+                         first_micro_step, stream=0):
+    """acc[j] = reduce(contributions) on the first micro-step, else
+    acc[j] + reduce(contributions).  Asynchronous."""
+    n = len(ranks)
+    r = (C.c_int32 * n)(*ranks)
+    aa = (C.c_void_p * n)(*acc_ptrs)
+    _check(_lib.zero_grad_accumulate(h, r, n, C.c_void_p(grads_ptr), grad_ld,
+                                     grad_rank_offset_mul, aa, 1 if first_micro_step else 0,
+                                     C.c_void_p(stream)), "zero_grad_accumulate")
+
+
+def zero_shard_step_accumulated(h, ranks, acc_ptrs, master_ptrs, m_ptrs, v_ptrs, out_ptr,
+                                extra_norm_sq=0.0, stream=0, want_result=True):
+    """The optimizer step on accumulated fp32 shards (g = acc / loss scale)."""
+    n = len(ranks)
+    r = (C.c_int32 * n)(*ranks)
+    arrs = [(C.c_void_p * n)(*p) for p in (acc_ptrs, master_ptrs, m_ptrs, v_ptrs)]
+    res = StepResult() if want_result else None
+    _check(_lib.zero_shard_step_accumulated(h, r, n, *arrs, C.c_void_p(out_ptr),
+                                            float(extra_norm_sq), C.c_void_p(stream),
+                                            C.byref(res) if res is not None else None),
+           "zero_shard_step_accumulated")
+    return res
+
+
 def zero_loss_scaler_state(h, stream=0):
     st = ScalerState()
     _check(_lib.zero_loss_scaler_state(h, C.byref(st), C.c_void_p(stream)),
@@ -251,7 +284,7 @@ class ZeroFlat:
     def __init__(self, shapes_or_infos, world_size, grad_dtype=ZERO_F16, param_dtype=None,
                  op=ZERO_AVG, hp=None):
         if param_dtype is None:
-            param_dtype = grad_dtype
+            param_dtype = grad_dtype if grad_dtype != ZERO_F32 else ZERO_F16
         infos = (shapes_or_infos if isinstance(shapes_or_infos, C.Array)
                  else param_infos(shapes_or_infos, param_dtype))
         self.hp = hp if hp is not None else hparams()
@@ -264,13 +297,36 @@ class ZeroFlat:
         import torch
         if stream is None:
             stream = torch.cuda.current_stream()
-        assert grads.dim() == 2 and grads.stride(1) == 1 and grads.element_size() == 2
+        assert grads.dim() == 2 and grads.stride(1) == 1
         if grad_rank_offset_mul is None:
             grad_rank_offset_mul = self.shard_size if len(ranks) > 1 else 0
         return zero_shard_step(self.handle, list(ranks), grads.data_ptr(), grads.stride(0),
                                grad_rank_offset_mul, [t.data_ptr() for t in master],
                                [t.data_ptr() for t in m], [t.data_ptr() for t in v],
                                out.data_ptr(), extra_norm_sq, stream.cuda_stream, want_result)
+
+    def accumulate(self, ranks, grads, acc, first_micro_step, grad_rank_offset_mul=None,
+                   stream=None):
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        assert grads.dim() == 2 and grads.stride(1) == 1
+        if grad_rank_offset_mul is None:
+            grad_rank_offset_mul = self.shard_size if len(ranks) > 1 else 0
+        zero_grad_accumulate(self.handle, list(ranks), grads.data_ptr(), grads.stride(0),
+                             grad_rank_offset_mul, [t.data_ptr() for t in acc],
+                             first_micro_step, stream.cuda_stream)
+
+    def step_accumulated(self, ranks, acc, master, m, v, out, extra_norm_sq=0.0, stream=None,
+                         want_result=True):
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        return zero_shard_step_accumulated(self.handle, list(ranks), [t.data_ptr() for t in acc],
+                                           [t.data_ptr() for t in master],
+                                           [t.data_ptr() for t in m], [t.data_ptr() for t in v],
+                                           out.data_ptr(), extra_norm_sq, stream.cuda_stream,
+                                           want_result)
 
     def scaler_state(self, stream=None):
         import torch

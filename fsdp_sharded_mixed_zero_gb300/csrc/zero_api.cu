@@ -62,7 +62,7 @@ struct DeviceGuard {
 struct zero_flat {
     int device = 0;
     int sm_count = 0;
-    int reduce_bps = 1;               // resident reduce blocks per SM
+    int reduce_bps[4] = {1, 1, 1, 1}; // resident reduce blocks per SM, per ReduceMode
     int32_t world = 1;
     zero_dtype grad_dtype = ZERO_F16, param_dtype = ZERO_F16;
     zero_reduce_op op = ZERO_AVG;
@@ -273,9 +273,10 @@ ZERO_API zero_status zero_flat_init(const zero_param_info *infos, int32_t n_info
     *out = nullptr;
     if (!infos || n_infos < 1) return fail(ZERO_ERR_INVALID_ARG, "need at least one param_info");
     if (world_size < 1) return fail(ZERO_ERR_INVALID_ARG, "world_size must be >= 1");
-    if ((grad_dtype != ZERO_F16 && grad_dtype != ZERO_BF16) ||
+    if ((grad_dtype != ZERO_F16 && grad_dtype != ZERO_BF16 && grad_dtype != ZERO_F32) ||
         (param_dtype != ZERO_F16 && param_dtype != ZERO_BF16))
-        return fail(ZERO_ERR_UNSUPPORTED_DTYPE, "dtypes must be ZERO_F16 or ZERO_BF16");
+        return fail(ZERO_ERR_UNSUPPORTED_DTYPE,
+                    "grad dtype must be ZERO_F16, ZERO_BF16 or ZERO_F32; param dtype ZERO_F16 or ZERO_BF16");
     if (op != ZERO_SUM && op != ZERO_AVG) return fail(ZERO_ERR_INVALID_ARG, "op must be SUM or AVG");
     zero_status s = validate_hparams(hp);
     if (s) return s;
@@ -310,8 +311,14 @@ ZERO_API zero_status zero_flat_init(const zero_param_info *infos, int32_t n_info
     if (e) { delete h; return cuda_fail(e, "cudaGetDevice"); }
     e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device);
     if (e) { delete h; return cuda_fail(e, "cudaDeviceGetAttribute"); }
-    e = zg::reduce_blocks_per_sm(&h->reduce_bps);
-    if (e) { delete h; return cuda_fail(e, "occupancy query"); }
+    {
+        const int kind = grad_dtype == ZERO_F32 ? zg::kInF32
+                       : (grad_dtype == ZERO_BF16 ? zg::kInBF16 : zg::kInF16);
+        for (int mode = 0; mode < 4; ++mode) {
+            e = zg::reduce_blocks_per_sm(kind, mode, &h->reduce_bps[mode]);
+            if (e) { delete h; return cuda_fail(e, "occupancy query"); }
+        }
+    }
     h->world = world_size;
     h->grad_dtype = grad_dtype;
     h->param_dtype = param_dtype;
@@ -362,27 +369,13 @@ ZERO_API zero_status zero_flat_device_bytes(const zero_flat *h, uint64_t *bytes)
     return ZERO_OK;
 }
 
-ZERO_API zero_status zero_shard_step(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
-                                     const void *grads, int64_t grad_ld,
-                                     int64_t grad_rank_offset_mul, float *const *master,
-                                     float *const *m, float *const *v, void *flat_param_out,
-                                     double extra_norm_sq, void *stream, zero_step_result *res) {
-    if (!h) return fail(ZERO_ERR_INVALID_ARG, "handle is NULL");
+namespace {
+
+// The stepped ranks: 1..world_size distinct ranks in range.
+zero_status check_ranks(const zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                        int32_t *max_rank) {
     if (!ranks || n_ranks < 1 || n_ranks > h->world)
         return fail(ZERO_ERR_INVALID_ARG, "need 1..world_size stepped ranks");
-    if (!master || !m || !v) return fail(ZERO_ERR_INVALID_ARG, "master/m/v arrays are NULL");
-    if (!flat_param_out) return fail(ZERO_ERR_INVALID_ARG, "flat_param_out is NULL");
-    if (!std::isfinite(extra_norm_sq) || extra_norm_sq < 0)
-        return fail(ZERO_ERR_INVALID_ARG, "extra_norm_sq must be finite and >= 0");
-    if (grad_ld < 0 || grad_rank_offset_mul < 0)
-        return fail(ZERO_ERR_INVALID_ARG, "grad_ld and grad_rank_offset_mul must be >= 0");
-    const int64_t S = h->shard;
-    if (S > 0 && !grads) return fail(ZERO_ERR_INVALID_ARG, "grads is NULL");
-    if (h->world > 1 && grad_ld < S)
-        return fail(ZERO_ERR_INVALID_ARG, "grad_ld must be >= shard_size");
-    if ((uintptr_t)grads % 2 || (uintptr_t)flat_param_out % 2)
-        return fail(ZERO_ERR_ALIGNMENT, "grads and flat_param_out must be 2-byte aligned");
-
     std::vector<int32_t> sorted(ranks, ranks + n_ranks);
     std::sort(sorted.begin(), sorted.end());
     for (int32_t j = 0; j < n_ranks; ++j) {
@@ -391,60 +384,102 @@ ZERO_API zero_status zero_shard_step(zero_flat *h, const int32_t *ranks, int32_t
         if (j && sorted[j] == sorted[j - 1])
             return fail(ZERO_ERR_INVALID_ARG, "rank %d listed twice", sorted[j]);
     }
+    *max_rank = sorted.back();
+    return ZERO_OK;
+}
+
+size_t grad_elem_size(const zero_flat *h) { return h->grad_dtype == ZERO_F32 ? 4 : 2; }
+
+// The contributions of the stepped ranks (element (c, r, i) at
+// grads[c*ld + r*mul + i]): present, aligned to their element size, and
+// addressable in int64.
+zero_status check_grads(const zero_flat *h, const void *grads, int64_t grad_ld,
+                        int64_t grad_rank_offset_mul, int32_t max_rank) {
+    const int64_t S = h->shard;
+    if (grad_ld < 0 || grad_rank_offset_mul < 0)
+        return fail(ZERO_ERR_INVALID_ARG, "grad_ld and grad_rank_offset_mul must be >= 0");
+    if (S > 0 && !grads) return fail(ZERO_ERR_INVALID_ARG, "grads is NULL");
+    if (h->world > 1 && grad_ld < S)
+        return fail(ZERO_ERR_INVALID_ARG, "grad_ld must be >= shard_size");
+    if ((uintptr_t)grads % grad_elem_size(h))
+        return fail(ZERO_ERR_ALIGNMENT, "grads must be aligned to their element size");
     // the largest element index read, (N-1)*ld + r_max*mul + S - 1, must fit int64
     int64_t rows_span, rank_span, span;
     if (!mul_ok((int64_t)(h->world - 1), grad_ld, &rows_span) ||
-        !mul_ok((int64_t)sorted.back(), grad_rank_offset_mul, &rank_span) ||
-        !add_ok(rows_span, rank_span, &span) || !add_ok(span, S, &span))
+        !mul_ok((int64_t)max_rank, grad_rank_offset_mul, &rank_span) ||
+        !add_ok(rows_span, rank_span, &span) || !add_ok(span, S, &span) ||
+        !mul_ok(span, (int64_t)grad_elem_size(h), &span))
         return fail(ZERO_ERR_OVERFLOW_SIZE, "gradient addressing overflows int64");
+    return ZERO_OK;
+}
+
+// Per-rank fp32 arrays (master, m, v, accumulators): present and 4-byte aligned.
+zero_status check_rows(const zero_flat *h, float *const *rows, int32_t n_ranks, const char *what) {
+    if (!rows) return fail(ZERO_ERR_INVALID_ARG, "%s array is NULL", what);
     for (int32_t j = 0; j < n_ranks; ++j) {
-        if (S > 0 && (!master[j] || !m[j] || !v[j]))
-            return fail(ZERO_ERR_INVALID_ARG, "master/m/v pointer %d is NULL", j);
-        if ((uintptr_t)master[j] % 4 || (uintptr_t)m[j] % 4 || (uintptr_t)v[j] % 4)
-            return fail(ZERO_ERR_ALIGNMENT, "master/m/v must be 4-byte aligned");
+        if (h->shard > 0 && !rows[j]) return fail(ZERO_ERR_INVALID_ARG, "%s pointer %d is NULL", what, j);
+        if ((uintptr_t)rows[j] % 4) return fail(ZERO_ERR_ALIGNMENT, "%s must be 4-byte aligned", what);
     }
+    return ZERO_OK;
+}
 
-    DeviceGuard guard(h->device);
-    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the handle's device");
-    cudaStream_t st = (cudaStream_t)stream;
+zero_status check_update(const zero_flat *h, int32_t n_ranks, float *const *master,
+                         float *const *m, float *const *v, void *flat_param_out,
+                         double extra_norm_sq) {
+    zero_status s;
+    if ((s = check_rows(h, master, n_ranks, "master"))) return s;
+    if ((s = check_rows(h, m, n_ranks, "m"))) return s;
+    if ((s = check_rows(h, v, n_ranks, "v"))) return s;
+    if (!flat_param_out) return fail(ZERO_ERR_INVALID_ARG, "flat_param_out is NULL");
+    if ((uintptr_t)flat_param_out % 2)
+        return fail(ZERO_ERR_ALIGNMENT, "flat_param_out must be 2-byte aligned");
+    if (!std::isfinite(extra_norm_sq) || extra_norm_sq < 0)
+        return fail(ZERO_ERR_INVALID_ARG, "extra_norm_sq must be finite and >= 0");
+    return ZERO_OK;
+}
 
-    // launch geometry (measured per kernel), split across the stepped ranks
-    const int64_t batch = std::min<int64_t>(n_ranks, zg::kMaxRanksPerLaunch);
-    const int gx1 = zg::grid_x_for(S, batch, h->sm_count, h->reduce_bps);
-    const int gx3 = zg::grid_x_for(S, batch, h->sm_count, zg::kAdamBlocksPerSm);
-    const int64_t parts = (int64_t)gx1 * n_ranks;
-    zero_status s = ensure_scratch(h, n_ranks, parts);
+int in_kind_of(const zero_flat *h) {
+    return h->grad_dtype == ZERO_F32 ? zg::kInF32 : (h->grad_dtype == ZERO_BF16 ? zg::kInBF16 : zg::kInF16);
+}
+
+// K1 as planned (contributions -> scratch rows, or an accumulator norm pass),
+// K2, K3 (from the scratch rows, or from the accumulators), with the timing
+// marks and the optional result read-back.  Called on the handle's device.
+zero_status launch_step(zero_flat *h, zg::ReducePlan rp, zg::AdamPlan ap, double extra_norm_sq,
+                        cudaStream_t st, zero_step_result *res) {
+    const int64_t S = h->shard;
+    const int64_t batch = std::min<int64_t>(rp.n_ranks, zg::kMaxRanksPerLaunch);
+    rp.grid_x = zg::grid_x_for(S, batch, h->sm_count, h->reduce_bps[rp.mode]);
+    ap.grid_x = zg::grid_x_for(S, batch, h->sm_count, zg::kAdamBlocksPerSm);
+    const int64_t parts = (int64_t)rp.grid_x * rp.n_ranks;
+    const int64_t rows = rp.mode == zg::kModeStep ? rp.n_ranks : 0;
+    zero_status s = ensure_scratch(h, rows, parts);
     if (s) return s;
+    rp.g = h->d_g;
+    rp.g_stride = h->g_stride;
+    rp.part_ss = h->d_part_ss;
+    rp.part_of = h->d_part_of;
+    rp.S = S;
+    rp.full_numel = h->full_numel;
+    rp.n_contrib = h->world;
+    rp.avg = h->op == ZERO_AVG;
+    rp.st = h->d_state;
+    if (!ap.acc) {
+        ap.g = h->d_g;
+        ap.g_stride = h->g_stride;
+    }
+    ap.bf16_out = h->param_dtype == ZERO_BF16;
+    ap.ranks = rp.ranks;
+    ap.n_ranks = rp.n_ranks;
+    ap.S = S;
+    ap.full_numel = h->full_numel;
+    ap.b1 = h->b1; ap.b2 = h->b2; ap.omb1 = h->omb1; ap.omb2 = h->omb2;
+    ap.lr = h->lr; ap.eps = h->eps; ap.decay = h->decay;
+    ap.st = h->d_state;
 
-    const bool gbf16 = h->grad_dtype == ZERO_BF16;
-    const bool pbf16 = h->param_dtype == ZERO_BF16;
     cudaError_t e;
     if ((e = mark(h, st))) return cuda_fail(e, "timing event");
-    for (int32_t b0 = 0; b0 < n_ranks; b0 += (int32_t)batch) {
-        const int32_t nb = (int32_t)std::min<int64_t>(batch, n_ranks - b0);
-        zg::ReduceArgs a{};
-        a.grads = static_cast<const uint16_t *>(grads);
-        a.ld = grad_ld;
-        a.S = S;
-        a.full_numel = h->full_numel;
-        a.g = h->d_g + (int64_t)b0 * h->g_stride;
-        a.g_stride = h->g_stride;
-        a.part_ss = h->d_part_ss;
-        a.part_of = h->d_part_of;
-        a.part_base = (int32_t)((int64_t)b0 * gx1);
-        a.n_contrib = h->world;
-        a.avg = h->op == ZERO_AVG;
-        a.n_ranks = nb;
-        a.st = h->d_state;
-        for (int32_t j = 0; j < nb; ++j) {
-            const int64_t r = ranks[b0 + j];
-            a.goff[j] = r * grad_rank_offset_mul;
-            a.first[j] = r * S;
-            a.vec[j] = ((uintptr_t)grads % 16 == 0) && (grad_ld % 8 == 0) && (a.goff[j] % 8 == 0);
-        }
-        if (S > 0 && (e = zg::launch_reduce(a, gx1, gbf16, st)))
-            return cuda_fail(e, "reduce kernel launch");
-    }
+    if ((e = zg::run_reduce(rp, st))) return cuda_fail(e, "reduce kernel launch");
     zg::FinalizeArgs f{};
     f.part_ss = h->d_part_ss;
     f.part_of = h->d_part_of;
@@ -460,30 +495,7 @@ ZERO_API zero_status zero_shard_step(zero_flat *h, const int32_t *ranks, int32_t
     if ((e = mark(h, st))) return cuda_fail(e, "timing event");
     if ((e = zg::launch_finalize(f, st))) return cuda_fail(e, "finalize kernel launch");
     if ((e = mark(h, st))) return cuda_fail(e, "timing event");
-    for (int32_t b0 = 0; b0 < n_ranks && S > 0; b0 += (int32_t)batch) {
-        const int32_t nb = (int32_t)std::min<int64_t>(batch, n_ranks - b0);
-        zg::AdamArgs a{};
-        a.g = h->d_g + (int64_t)b0 * h->g_stride;
-        a.g_stride = h->g_stride;
-        a.S = S;
-        a.b1 = h->b1; a.b2 = h->b2; a.omb1 = h->omb1; a.omb2 = h->omb2;
-        a.lr = h->lr; a.eps = h->eps; a.decay = h->decay;
-        a.n_ranks = nb;
-        a.st = h->d_state;
-        a.out = flat_param_out;
-        for (int32_t j = 0; j < nb; ++j) {
-            const int64_t r = ranks[b0 + j];
-            a.master[j] = master[b0 + j];
-            a.m[j] = m[b0 + j];
-            a.v[j] = v[b0 + j];
-            a.out_off[j] = r * S;
-            a.vec[j] = ((uintptr_t)master[b0 + j] % 16 == 0) && ((uintptr_t)m[b0 + j] % 16 == 0) &&
-                       ((uintptr_t)v[b0 + j] % 16 == 0);
-            const uintptr_t addr = (uintptr_t)flat_param_out + (uintptr_t)(r * S) * 2;
-            a.out_align[j] = addr % 16 == 0 ? 16 : (addr % 4 == 0 ? 4 : 2);
-        }
-        if ((e = zg::launch_adamw(a, gx3, pbf16, st))) return cuda_fail(e, "adamw kernel launch");
-    }
+    if ((e = zg::run_adamw(ap, st))) return cuda_fail(e, "adamw kernel launch");
     if ((e = mark(h, st))) return cuda_fail(e, "timing event");
     if (res) {
         e = cudaMemcpyAsync(h->h_state, h->d_state, sizeof(zg::DevState), cudaMemcpyDeviceToHost, st);
@@ -496,6 +508,99 @@ ZERO_API zero_status zero_shard_step(zero_flat *h, const int32_t *ranks, int32_t
         res->scale_used = h->h_state->res.scale_used;
     }
     return ZERO_OK;
+}
+
+}  // namespace
+
+ZERO_API zero_status zero_shard_step(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                                     const void *grads, int64_t grad_ld,
+                                     int64_t grad_rank_offset_mul, float *const *master,
+                                     float *const *m, float *const *v, void *flat_param_out,
+                                     double extra_norm_sq, void *stream, zero_step_result *res) {
+    if (!h) return fail(ZERO_ERR_INVALID_ARG, "handle is NULL");
+    int32_t max_rank = 0;
+    zero_status s;
+    if ((s = check_ranks(h, ranks, n_ranks, &max_rank))) return s;
+    if ((s = check_update(h, n_ranks, master, m, v, flat_param_out, extra_norm_sq))) return s;
+    if ((s = check_grads(h, grads, grad_ld, grad_rank_offset_mul, max_rank))) return s;
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the handle's device");
+    zg::ReducePlan rp;
+    rp.mode = zg::kModeStep;
+    rp.grads = grads;
+    rp.in_kind = in_kind_of(h);
+    rp.ld = grad_ld;
+    rp.rank_mul = grad_rank_offset_mul;
+    rp.ranks = ranks;
+    rp.n_ranks = n_ranks;
+    zg::AdamPlan ap;
+    ap.master = master;
+    ap.m = m;
+    ap.v = v;
+    ap.out = flat_param_out;
+    return launch_step(h, rp, ap, extra_norm_sq, (cudaStream_t)stream, res);
+}
+
+ZERO_API zero_status zero_grad_accumulate(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                                          const void *grads, int64_t grad_ld,
+                                          int64_t grad_rank_offset_mul, float *const *acc,
+                                          int32_t first_micro_step, void *stream) {
+    if (!h) return fail(ZERO_ERR_INVALID_ARG, "handle is NULL");
+    int32_t max_rank = 0;
+    zero_status s;
+    if ((s = check_ranks(h, ranks, n_ranks, &max_rank))) return s;
+    if ((s = check_rows(h, acc, n_ranks, "acc"))) return s;
+    if ((s = check_grads(h, grads, grad_ld, grad_rank_offset_mul, max_rank))) return s;
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the handle's device");
+    zg::ReducePlan rp;
+    rp.mode = first_micro_step ? zg::kModeAccFirst : zg::kModeAccAdd;
+    rp.grads = grads;
+    rp.in_kind = in_kind_of(h);
+    rp.ld = grad_ld;
+    rp.rank_mul = grad_rank_offset_mul;
+    rp.acc_out = acc;
+    rp.ranks = ranks;
+    rp.n_ranks = n_ranks;
+    rp.S = h->shard;
+    rp.full_numel = h->full_numel;
+    rp.n_contrib = h->world;
+    rp.avg = h->op == ZERO_AVG;
+    rp.st = h->d_state;
+    const int64_t batch = std::min<int64_t>(n_ranks, zg::kMaxRanksPerLaunch);
+    rp.grid_x = zg::grid_x_for(h->shard, batch, h->sm_count, h->reduce_bps[rp.mode]);
+    const cudaError_t e = zg::run_reduce(rp, (cudaStream_t)stream);
+    if (e) return cuda_fail(e, "accumulate kernel launch");
+    return ZERO_OK;
+}
+
+ZERO_API zero_status zero_shard_step_accumulated(zero_flat *h, const int32_t *ranks,
+                                                 int32_t n_ranks, const float *const *acc,
+                                                 float *const *master, float *const *m,
+                                                 float *const *v, void *flat_param_out,
+                                                 double extra_norm_sq, void *stream,
+                                                 zero_step_result *res) {
+    if (!h) return fail(ZERO_ERR_INVALID_ARG, "handle is NULL");
+    int32_t max_rank = 0;
+    zero_status s;
+    if ((s = check_ranks(h, ranks, n_ranks, &max_rank))) return s;
+    if ((s = check_rows(h, const_cast<float *const *>(acc), n_ranks, "acc"))) return s;
+    if ((s = check_update(h, n_ranks, master, m, v, flat_param_out, extra_norm_sq))) return s;
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the handle's device");
+    zg::ReducePlan rp;
+    rp.mode = zg::kModeNormOnly;
+    rp.in_kind = zg::kInF32;
+    rp.acc_in = acc;
+    rp.ranks = ranks;
+    rp.n_ranks = n_ranks;
+    zg::AdamPlan ap;
+    ap.acc = acc;
+    ap.master = master;
+    ap.m = m;
+    ap.v = v;
+    ap.out = flat_param_out;
+    return launch_step(h, rp, ap, extra_norm_sq, (cudaStream_t)stream, res);
 }
 
 ZERO_API zero_status zero_loss_scaler_state(zero_flat *h, zero_scaler_state *out, void *stream) {

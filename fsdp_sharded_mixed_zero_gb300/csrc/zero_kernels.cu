@@ -1,6 +1,6 @@
 // zero_kernels.cu -- the three kernels of one ZeRO shard step on sm_103a.
 //
-//   K1 reduce_kernel    N-way reduce of the 16-bit gradient contributions of
+//   K1 reduce_kernel    N-way reduce of the fp16/bf16/fp32 gradient contributions of
 //                       each stepped shard, AVG, loss-scale division, inf/NaN
 //                       check and per-block partial sums of squares; writes
 //                       the fp32 reduced gradient row (the reduce half of a
@@ -124,29 +124,64 @@ __device__ __forceinline__ float divide(float x, const Divisor &q) {
 // The squared norm must be accurate to ~1e-14 so that the fp32 clip
 // coefficient derived from it rounds like the exactly computed one.  Per
 // 8-element chunk the squares are summed without error in fp32 pairs: the
-// exact square of x is p + e with p = x*x and e = fma(x, x, -p) (exact), and
-// Knuth's TwoSum gives the exact error of every addition.  Only the small
-// correction term `lo` is rounded (relative error ~ eps^2), and the chunk's
-// hi + lo enters the thread's fp64 sum once.
+// exact square of x is p + e with p = x*x and e = fma(x, x, -p), and Knuth's
+// TwoSum gives the exact error of every addition; only the small correction
+// term is rounded (relative error ~ eps^2).  A thread carries that pair over
+// eight chunks before one fp64 addition, because GB300's fp64 rate is low
+// enough that an fp64 add per chunk would bound a read-only pass.  Chunks
+// whose sum lies outside [2^-100, 2^100] (where fp32 squares could overflow
+// or lose their low bits), or that hold inf/NaN, are summed exactly in fp64.
 __device__ __forceinline__ void two_sum(float a, float b, float &s, float &err) {
     s = __fadd_rn(a, b);
     const float bb = __fsub_rn(s, a);
     err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
-__device__ __forceinline__ double chunk_sum_of_squares(const float x[kVec]) {
-    float hi = __fmul_rn(x[0], x[0]);
-    float lo = __fmaf_rn(x[0], x[0], -hi);
-#pragma unroll
-    for (int k = 1; k < kVec; ++k) {
-        const float p = __fmul_rn(x[k], x[k]);
-        const float e = __fmaf_rn(x[k], x[k], -p);
-        float t;
-        two_sum(hi, p, hi, t);
-        lo = __fadd_rn(lo, __fadd_rn(t, e));
+struct NormAcc {
+    double ss = 0.0;                  // flushed total
+    float hi = 0.0f, lo = 0.0f;       // carried pair
+    int n = 0;                        // chunks in the pair
+
+    __device__ __forceinline__ void flush() {
+        ss += (double)hi + (double)lo;
+        hi = 0.0f;
+        lo = 0.0f;
+        n = 0;
     }
-    return (double)hi + (double)lo;
-}
+    __device__ __forceinline__ void add_chunk(const float x[kVec]) {
+        float ch = __fmul_rn(x[0], x[0]);
+        float cl = __fmaf_rn(x[0], x[0], -ch);
+#pragma unroll
+        for (int k = 1; k < kVec; ++k) {
+            const float p = __fmul_rn(x[k], x[k]);
+            const float e = __fmaf_rn(x[k], x[k], -p);
+            float t;
+            two_sum(ch, p, ch, t);
+            cl = __fadd_rn(cl, __fadd_rn(t, e));
+        }
+        if (ch >= 0x1p-100f && ch <= 0x1p100f) {
+            float t;
+            two_sum(hi, ch, hi, t);
+            lo = __fadd_rn(lo, __fadd_rn(t, cl));
+            if (++n == 8) flush();
+        } else {
+            // out of range, inf/NaN, or zero squares: zero squares may come
+            // from nonzero values below 2^-75, so test the values themselves
+            bool any = false;
+#pragma unroll
+            for (int k = 0; k < kVec; ++k) any |= x[k] != 0.0f;
+            if (any) {
+#pragma unroll
+                for (int k = 0; k < kVec; ++k) ss += (double)x[k] * (double)x[k];
+            }
+        }
+    }
+    __device__ __forceinline__ void add_exact(float x) { ss += (double)x * (double)x; }
+    __device__ __forceinline__ double total() {
+        flush();
+        return ss;
+    }
+};
 
 // ------------------------------------------------------------------ reduction
 // Block total of per-thread fp64 sums and flags, in a fixed order.
@@ -168,80 +203,204 @@ __device__ __forceinline__ void block_partial(double ss, int of, double *out_ss,
 }
 
 // ------------------------------------------------------------------ K1
-template <bool kBf16>
-__global__ void __launch_bounds__(kBlock, 5) reduce_kernel(const __grid_constant__ ReduceArgs a) {
+// Element traits of a contribution encoding: 16-byte words per 8 elements and
+// contributor rows kept in flight per batch.
+template <int kIn> struct InTraits {
+    using T = uint16_t;
+    static constexpr int kWords = 1;
+    static constexpr int kBatch = 8;
+};
+template <> struct InTraits<kInF32> {
+    using T = float;
+    static constexpr int kWords = 2;
+    static constexpr int kBatch = 4;
+};
+
+// Register budget: five resident blocks per SM (48 registers) except for the
+// fp32-contribution reduce, whose four rows in flight need four (64).
+template <int kIn, int kMode>
+constexpr int reduce_min_blocks() {
+    return (kIn == kInF32 && kMode != kModeNormOnly) ? 4 : 5;
+}
+
+template <int kIn>
+__device__ __forceinline__ void load_words(const typename InTraits<kIn>::T *p, uint4 w[]) {
+    w[0] = ld_nc_u4(p);
+    if constexpr (InTraits<kIn>::kWords == 2) w[1] = ld_nc_u4(p + 4);
+}
+
+template <int kIn>
+__device__ __forceinline__ void words_to_f32(const uint4 w[], float f[kVec]) {
+    if constexpr (kIn == kInF32) {
+        f[0] = __uint_as_float(w[0].x); f[1] = __uint_as_float(w[0].y);
+        f[2] = __uint_as_float(w[0].z); f[3] = __uint_as_float(w[0].w);
+        f[4] = __uint_as_float(w[1].x); f[5] = __uint_as_float(w[1].y);
+        f[6] = __uint_as_float(w[1].z); f[7] = __uint_as_float(w[1].w);
+    } else {
+        unpack8<kIn == kInBF16>(w[0], f);
+    }
+}
+
+template <int kIn>
+__device__ __forceinline__ float elem_to_f32(const typename InTraits<kIn>::T *p) {
+    if constexpr (kIn == kInF32) return *p;
+    else return to_f32<kIn == kInBF16>(*p);
+}
+
+template <int kIn, int kMode>
+__global__ void __launch_bounds__(kBlock, (reduce_min_blocks<kIn, kMode>()))
+reduce_kernel(const __grid_constant__ ReduceArgs a) {
+    using T = typename InTraits<kIn>::T;
+    constexpr int kW = InTraits<kIn>::kWords;
+    constexpr int kB = InTraits<kIn>::kBatch;
+    constexpr bool kNorm = kMode == kModeStep || kMode == kModeNormOnly;
     const int j = blockIdx.y;
     const int64_t S = a.S;
     int64_t valid = a.full_numel - a.first[j];   // elements [valid, S) are padding
     valid = valid < 0 ? 0 : (valid > S ? S : valid);
-    const uint16_t *base = a.grads + a.goff[j];
+    const T *base = static_cast<const T *>(a.in[j]);
     float *g = a.g + (int64_t)j * a.g_stride;
+    float *acc_out = a.acc[j];
     const int N = a.n_contrib;
     const int64_t ld = a.ld;
     const bool avg = a.avg != 0;
     const Divisor dn = make_divisor((float)N);
-    const Divisor ds = make_divisor(a.st->scaler.scale);
+    const Divisor ds = make_divisor(kNorm ? a.st->scaler.scale : 1.0f);
 
-    double ss = 0.0;
+    // r of one element from its contributions, in contributor order from 0.
+    auto finish = [&](float x) { return avg ? divide(x, dn) : x; };
+
+    NormAcc na;
     int of = 0;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
     int64_t done = 0;
-    if (a.vec[j]) {
+    if constexpr (kMode == kModeNormOnly) {
+        // A pure read stream of 4 bytes per element: keep two chunks (64
+        // bytes) in flight per thread.  Chunks are still summed in the order
+        // of the plain grid-stride loop: ch, ch + T, ch + 2T, ...
+        if (a.vec[j]) {
+            const float *acc_in = reinterpret_cast<const float *>(base);
+            const int64_t nch = valid / kVec;
+            int64_t ch = tid;
+            for (; ch + nthreads < nch; ch += 2 * nthreads) {
+                uint4 w[2][2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) load_words<kInF32>(acc_in + (ch + u * nthreads) * kVec, w[u]);
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    float x[kVec];
+                    words_to_f32<kInF32>(w[u], x);
+#pragma unroll
+                    for (int e = 0; e < kVec; ++e) {
+                        x[e] = divide(x[e], ds);
+                        of |= !isfinite(x[e]);
+                    }
+                    na.add_chunk(x);
+                }
+            }
+            for (; ch < nch; ch += nthreads) {
+                uint4 w[2];
+                load_words<kInF32>(acc_in + ch * kVec, w);
+                float x[kVec];
+                words_to_f32<kInF32>(w, x);
+#pragma unroll
+                for (int e = 0; e < kVec; ++e) {
+                    x[e] = divide(x[e], ds);
+                    of |= !isfinite(x[e]);
+                }
+                na.add_chunk(x);
+            }
+            done = nch * kVec;
+        }
+    } else if (a.vec[j]) {
         const int64_t nch = valid / kVec;
         for (int64_t ch = tid; ch < nch; ch += nthreads) {
             const int64_t i0 = ch * kVec;
-            const uint16_t *p = base + i0;
-            float acc[kVec];
+            float x[kVec];
+            if constexpr (kMode == kModeNormOnly) {
+                uint4 w[2];
+                load_words<kInF32>(reinterpret_cast<const float *>(base) + i0, w);
+                words_to_f32<kInF32>(w, x);
+            } else {
+                const T *p = base + i0;
 #pragma unroll
-            for (int e = 0; e < kVec; ++e) acc[e] = 0.0f;
-            int c = 0;
-            for (; c + 8 <= N; c += 8) {          // eight rows in flight
-                uint4 w[8];
+                for (int e = 0; e < kVec; ++e) x[e] = 0.0f;
+                int c = 0;
+                for (; c + kB <= N; c += kB) {           // kB rows in flight
+                    uint4 w[kB][kW];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) w[k] = ld_nc_u4(p + (int64_t)(c + k) * ld);
+                    for (int k = 0; k < kB; ++k) load_words<kIn>(p + (int64_t)(c + k) * ld, w[k]);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    float f[kVec];
-                    unpack8<kBf16>(w[k], f);
+                    for (int k = 0; k < kB; ++k) {
+                        float f[kVec];
+                        words_to_f32<kIn>(w[k], f);
 #pragma unroll
-                    for (int e = 0; e < kVec; ++e) acc[e] = __fadd_rn(acc[e], f[e]);
+                        for (int e = 0; e < kVec; ++e) x[e] = __fadd_rn(x[e], f[e]);
+                    }
                 }
-            }
-            for (; c < N; ++c) {
-                const uint4 w = ld_nc_u4(p + (int64_t)c * ld);
-                float f[kVec];
-                unpack8<kBf16>(w, f);
+                for (; c < N; ++c) {
+                    uint4 w[kW];
+                    load_words<kIn>(p + (int64_t)c * ld, w);
+                    float f[kVec];
+                    words_to_f32<kIn>(w, f);
 #pragma unroll
-                for (int e = 0; e < kVec; ++e) acc[e] = __fadd_rn(acc[e], f[e]);
-            }
+                    for (int e = 0; e < kVec; ++e) x[e] = __fadd_rn(x[e], f[e]);
+                }
 #pragma unroll
-            for (int e = 0; e < kVec; ++e) {
-                float x = acc[e];
-                if (avg) x = divide(x, dn);
-                x = divide(x, ds);
-                acc[e] = x;
-                of |= !isfinite(x);
+                for (int e = 0; e < kVec; ++e) x[e] = finish(x[e]);
             }
-            ss += chunk_sum_of_squares(acc);
-            st_f4(g + i0, make_float4(acc[0], acc[1], acc[2], acc[3]));
-            st_f4(g + i0 + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
+            if constexpr (kNorm) {
+#pragma unroll
+                for (int e = 0; e < kVec; ++e) {
+                    x[e] = divide(x[e], ds);
+                    of |= !isfinite(x[e]);
+                }
+                na.add_chunk(x);
+            }
+            if constexpr (kMode == kModeStep) {
+                st_f4(g + i0, make_float4(x[0], x[1], x[2], x[3]));
+                st_f4(g + i0 + 4, make_float4(x[4], x[5], x[6], x[7]));
+            } else if constexpr (kMode == kModeAccFirst || kMode == kModeAccAdd) {
+                if constexpr (kMode == kModeAccAdd) {
+                    const float4 o0 = ld_f4(acc_out + i0), o1 = ld_f4(acc_out + i0 + 4);
+                    const float o[kVec] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+#pragma unroll
+                    for (int e = 0; e < kVec; ++e) x[e] = __fadd_rn(o[e], x[e]);
+                }
+                st_f4(acc_out + i0, make_float4(x[0], x[1], x[2], x[3]));
+                st_f4(acc_out + i0 + 4, make_float4(x[4], x[5], x[6], x[7]));
+            }
         }
         done = nch * kVec;
     }
     for (int64_t i = done + tid; i < valid; i += nthreads) {   // ragged tail / unaligned rows
-        float acc = 0.0f;
-        for (int c = 0; c < N; ++c) acc = __fadd_rn(acc, to_f32<kBf16>(base[(int64_t)c * ld + i]));
-        if (avg) acc = divide(acc, dn);
-        acc = divide(acc, ds);
-        of |= !isfinite(acc);
-        ss += (double)acc * (double)acc;          // exact square in fp64
-        g[i] = acc;
+        float x;
+        if constexpr (kMode == kModeNormOnly) {
+            x = reinterpret_cast<const float *>(base)[i];
+        } else {
+            x = 0.0f;
+            for (int c = 0; c < N; ++c) x = __fadd_rn(x, elem_to_f32<kIn>(base + (int64_t)c * ld + i));
+            x = finish(x);
+        }
+        if constexpr (kNorm) {
+            x = divide(x, ds);
+            of |= !isfinite(x);
+            na.add_exact(x);                          // exact square in fp64
+        }
+        if constexpr (kMode == kModeStep) g[i] = x;
+        if constexpr (kMode == kModeAccFirst) acc_out[i] = x;
+        if constexpr (kMode == kModeAccAdd) acc_out[i] = __fadd_rn(acc_out[i], x);
     }
-    for (int64_t i = valid + tid; i < S; i += nthreads) g[i] = 0.0f;   // padding
-
-    const int64_t pidx = a.part_base + (int64_t)j * gridDim.x + blockIdx.x;
-    block_partial(ss, of, a.part_ss + pidx, a.part_of + pidx);
+    for (int64_t i = valid + tid; i < S; i += nthreads) {     // padding: zero gradient
+        if constexpr (kMode == kModeStep) g[i] = 0.0f;
+        if constexpr (kMode == kModeAccFirst) acc_out[i] = 0.0f;
+        if constexpr (kMode == kModeAccAdd) acc_out[i] = __fadd_rn(acc_out[i], 0.0f);
+    }
+    if constexpr (kNorm) {
+        const int64_t pidx = a.part_base + (int64_t)j * gridDim.x + blockIdx.x;
+        block_partial(na.total(), of, a.part_ss + pidx, a.part_of + pidx);
+    }
 }
 
 // ------------------------------------------------------------------ K2
@@ -319,7 +478,10 @@ __device__ __forceinline__ void adam_elem(float g, float &th, float &m, float &v
     th = __fsub_rn(th, __fdiv_rn(__fmul_rn(k.lr, mh), __fadd_rn(__fsqrt_rn(vh), k.eps)));
 }
 
-template <bool kBf16>
+// kFromAcc: the gradient rows are micro-step accumulators that still carry
+// the loss scale: g = acc / scale_used (the same division the reduce kernel
+// applies), padding elements (flat index >= full_numel) are zero.
+template <bool kBf16, bool kFromAcc>
 __global__ void __launch_bounds__(kBlock) adamw_kernel(const __grid_constant__ AdamArgs a) {
     const DevState *st = a.st;
     if (st->res.skipped) return;
@@ -334,9 +496,16 @@ __global__ void __launch_bounds__(kBlock) adamw_kernel(const __grid_constant__ A
     float *th = a.master[j];
     float *mm = a.m[j];
     float *vv = a.v[j];
-    const float *g = a.g + (int64_t)j * a.g_stride;
+    const float *g = a.g[j];
     uint16_t *out = reinterpret_cast<uint16_t *>(a.out) + a.out_off[j];
     const int64_t S = a.S;
+    const Divisor ds = make_divisor(kFromAcc ? st->res.scale_used : 1.0f);
+    int64_t valid = a.full_numel - a.out_off[j];
+    valid = valid < 0 ? 0 : (valid > S ? S : valid);
+    auto grad = [&](float x, int64_t i) {
+        if constexpr (kFromAcc) return i < valid ? divide(x, ds) : 0.0f;
+        else return x;
+    };
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
     int64_t done = 0;
@@ -354,7 +523,7 @@ __global__ void __launch_bounds__(kBlock) adamw_kernel(const __grid_constant__ A
             float M[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
             float V[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) adam_elem(G[e], T[e], M[e], V[e], k);
+            for (int e = 0; e < 8; ++e) adam_elem(grad(G[e], i0 + e), T[e], M[e], V[e], k);
             st_f4(th + i0, make_float4(T[0], T[1], T[2], T[3]));
             st_f4(th + i0 + 4, make_float4(T[4], T[5], T[6], T[7]));
             st_f4(mm + i0, make_float4(M[0], M[1], M[2], M[3]));
@@ -382,7 +551,7 @@ __global__ void __launch_bounds__(kBlock) adamw_kernel(const __grid_constant__ A
     }
     for (int64_t i = done + tid; i < S; i += nthreads) {   // ragged tail / unaligned shards
         float t = th[i], m = mm[i], v = vv[i];
-        adam_elem(g[i], t, m, v, k);
+        adam_elem(grad(g[i], i), t, m, v, k);
         th[i] = t;
         mm[i] = m;
         vv[i] = v;
@@ -392,11 +561,29 @@ __global__ void __launch_bounds__(kBlock) adamw_kernel(const __grid_constant__ A
 
 }  // namespace
 
-cudaError_t launch_reduce(const ReduceArgs &a, int grid_x, bool bf16, cudaStream_t s) {
-    const dim3 grid((unsigned)grid_x, (unsigned)a.n_ranks);
-    if (bf16) reduce_kernel<true><<<grid, kBlock, 0, s>>>(a);
-    else reduce_kernel<false><<<grid, kBlock, 0, s>>>(a);
+template <int kIn>
+static cudaError_t launch_reduce_in(const ReduceArgs &a, dim3 grid, int mode, cudaStream_t s) {
+    switch (mode) {
+        case kModeStep: reduce_kernel<kIn, kModeStep><<<grid, kBlock, 0, s>>>(a); break;
+        case kModeAccFirst: reduce_kernel<kIn, kModeAccFirst><<<grid, kBlock, 0, s>>>(a); break;
+        case kModeAccAdd: reduce_kernel<kIn, kModeAccAdd><<<grid, kBlock, 0, s>>>(a); break;
+        default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
+}
+
+cudaError_t launch_reduce(const ReduceArgs &a, int grid_x, int in_kind, int mode, cudaStream_t s) {
+    const dim3 grid((unsigned)grid_x, (unsigned)a.n_ranks);
+    if (mode == kModeNormOnly) {
+        reduce_kernel<kInF32, kModeNormOnly><<<grid, kBlock, 0, s>>>(a);
+        return cudaGetLastError();
+    }
+    switch (in_kind) {
+        case kInF16: return launch_reduce_in<kInF16>(a, grid, mode, s);
+        case kInBF16: return launch_reduce_in<kInBF16>(a, grid, mode, s);
+        case kInF32: return launch_reduce_in<kInF32>(a, grid, mode, s);
+    }
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_finalize(const FinalizeArgs &a, cudaStream_t s) {
@@ -404,22 +591,115 @@ cudaError_t launch_finalize(const FinalizeArgs &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_adamw(const AdamArgs &a, int grid_x, bool bf16_out, cudaStream_t s) {
+cudaError_t launch_adamw(const AdamArgs &a, int grid_x, bool bf16_out, bool from_acc,
+                         cudaStream_t s) {
     const dim3 grid((unsigned)grid_x, (unsigned)a.n_ranks);
-    if (bf16_out) adamw_kernel<true><<<grid, kBlock, 0, s>>>(a);
-    else adamw_kernel<false><<<grid, kBlock, 0, s>>>(a);
+    if (from_acc) {
+        if (bf16_out) adamw_kernel<true, true><<<grid, kBlock, 0, s>>>(a);
+        else adamw_kernel<false, true><<<grid, kBlock, 0, s>>>(a);
+    } else {
+        if (bf16_out) adamw_kernel<true, false><<<grid, kBlock, 0, s>>>(a);
+        else adamw_kernel<false, false><<<grid, kBlock, 0, s>>>(a);
+    }
     return cudaGetLastError();
 }
 
 
-cudaError_t reduce_blocks_per_sm(int *bps) {
-    int r0 = 0, r1 = 0;
-    cudaError_t e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r0, reduce_kernel<false>, kBlock, 0))) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r1, reduce_kernel<true>, kBlock, 0))) return e;
-    *bps = r0 < r1 ? r0 : r1;
-    if (*bps < 1) *bps = 1;
+cudaError_t run_reduce(const ReducePlan &p, cudaStream_t s) {
+    if (p.S <= 0) return cudaSuccess;
+    const size_t esize = p.in_kind == kInF32 ? 4 : 2;
+    for (int32_t b0 = 0; b0 < p.n_ranks; b0 += kMaxRanksPerLaunch) {
+        const int32_t nb = p.n_ranks - b0 < kMaxRanksPerLaunch ? p.n_ranks - b0 : kMaxRanksPerLaunch;
+        ReduceArgs a{};
+        a.ld = p.ld;
+        a.S = p.S;
+        a.full_numel = p.full_numel;
+        a.g = p.g ? p.g + (int64_t)b0 * p.g_stride : nullptr;
+        a.g_stride = p.g_stride;
+        a.part_ss = p.part_ss;
+        a.part_of = p.part_of;
+        a.part_base = b0 * p.grid_x;
+        a.n_contrib = p.mode == kModeNormOnly ? 1 : p.n_contrib;
+        a.avg = p.mode == kModeNormOnly ? 0 : p.avg;
+        a.n_ranks = nb;
+        a.st = p.st;
+        for (int32_t j = 0; j < nb; ++j) {
+            const int64_t r = p.ranks[b0 + j];
+            bool vec;
+            if (p.mode == kModeNormOnly) {
+                a.in[j] = p.acc_in[b0 + j];
+                vec = (uintptr_t)a.in[j] % 16 == 0;
+            } else {
+                a.in[j] = static_cast<const char *>(p.grads) + (size_t)(r * p.rank_mul) * esize;
+                vec = (uintptr_t)a.in[j] % 16 == 0 && ((size_t)p.ld * esize) % 16 == 0;
+            }
+            if (p.mode == kModeAccFirst || p.mode == kModeAccAdd) {
+                a.acc[j] = p.acc_out[b0 + j];
+                vec = vec && (uintptr_t)a.acc[j] % 16 == 0;
+            }
+            a.first[j] = r * p.S;
+            a.vec[j] = vec;
+        }
+        const cudaError_t e = launch_reduce(a, p.grid_x, p.in_kind, p.mode, s);
+        if (e != cudaSuccess) return e;
+    }
     return cudaSuccess;
+}
+
+cudaError_t run_adamw(const AdamPlan &p, cudaStream_t s) {
+    if (p.S <= 0) return cudaSuccess;
+    for (int32_t b0 = 0; b0 < p.n_ranks; b0 += kMaxRanksPerLaunch) {
+        const int32_t nb = p.n_ranks - b0 < kMaxRanksPerLaunch ? p.n_ranks - b0 : kMaxRanksPerLaunch;
+        AdamArgs a{};
+        a.S = p.S;
+        a.full_numel = p.full_numel;
+        a.b1 = p.b1; a.b2 = p.b2; a.omb1 = p.omb1; a.omb2 = p.omb2;
+        a.lr = p.lr; a.eps = p.eps; a.decay = p.decay;
+        a.n_ranks = nb;
+        a.st = p.st;
+        a.out = p.out;
+        for (int32_t j = 0; j < nb; ++j) {
+            const int64_t r = p.ranks[b0 + j];
+            a.g[j] = p.acc ? p.acc[b0 + j] : p.g + (int64_t)(b0 + j) * p.g_stride;
+            a.master[j] = p.master[b0 + j];
+            a.m[j] = p.m[b0 + j];
+            a.v[j] = p.v[b0 + j];
+            a.out_off[j] = r * p.S;
+            a.vec[j] = (uintptr_t)a.g[j] % 16 == 0 && (uintptr_t)a.master[j] % 16 == 0 &&
+                       (uintptr_t)a.m[j] % 16 == 0 && (uintptr_t)a.v[j] % 16 == 0;
+            const uintptr_t addr = (uintptr_t)p.out + (uintptr_t)(r * p.S) * 2;
+            a.out_align[j] = addr % 16 == 0 ? 16 : (addr % 4 == 0 ? 4 : 2);
+        }
+        const cudaError_t e = launch_adamw(a, p.grid_x, p.bf16_out, p.acc != nullptr, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+template <int kIn, int kMode>
+static cudaError_t occ(int *bps) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, reduce_kernel<kIn, kMode>, kBlock, 0);
+}
+
+cudaError_t reduce_blocks_per_sm(int in_kind, int mode, int *bps) {
+    cudaError_t e = cudaErrorInvalidValue;
+    *bps = 1;
+    if (mode == kModeNormOnly) {
+        e = occ<kInF32, kModeNormOnly>(bps);
+    } else {
+#define ZG_OCC(K)                                                    \
+        switch (mode) {                                              \
+            case kModeStep: e = occ<K, kModeStep>(bps); break;       \
+            case kModeAccFirst: e = occ<K, kModeAccFirst>(bps); break; \
+            case kModeAccAdd: e = occ<K, kModeAccAdd>(bps); break;   \
+        }
+        if (in_kind == kInF16) { ZG_OCC(kInF16) }
+        else if (in_kind == kInBF16) { ZG_OCC(kInBF16) }
+        else if (in_kind == kInF32) { ZG_OCC(kInF32) }
+#undef ZG_OCC
+    }
+    if (*bps < 1) *bps = 1;
+    return e;
 }
 
 }  // namespace zg

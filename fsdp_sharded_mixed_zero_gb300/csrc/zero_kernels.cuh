@@ -40,13 +40,24 @@ struct DevState {
     int32_t pad;
 };
 
+// Contribution encodings of the reduce kernel.
+enum InKind : int { kInF16 = 0, kInBF16 = 1, kInF32 = 2 };
+
+// What the reduce kernel does with the reduced value r of each element
+// (r = sum of the N contributions in contributor order, / N for AVG):
+//   kModeStep:     g = r / scale -> the fp32 gradient rows, overflow, norm
+//   kModeAccFirst: acc = r                      (first micro-step)
+//   kModeAccAdd:   acc = acc + r                (later micro-steps)
+//   kModeNormOnly: g = acc / scale read from the accumulator: overflow and
+//                  norm only (the AdamW kernel re-derives g from acc)
+enum ReduceMode : int { kModeStep = 0, kModeAccFirst = 1, kModeAccAdd = 2, kModeNormOnly = 3 };
+
 // K1: reduce of the N contributions + AVG + unscale + overflow + norm partials.
 struct ReduceArgs {
-    const uint16_t *grads;            // contributor c, element i: grads[c*ld + goff[j] + i]
-    int64_t ld;
+    int64_t ld;                       // contributor row stride, elements
     int64_t S;                        // shard size
     int64_t full_numel;
-    float *g;                         // reduced gradient rows, row j at g + j*g_stride
+    float *g;                         // kModeStep: reduced gradient rows, row j at g + j*g_stride
     int64_t g_stride;
     double *part_ss;                  // per-block partial sums of squares
     int32_t *part_of;                 // per-block overflow flags
@@ -55,7 +66,9 @@ struct ReduceArgs {
     int32_t avg;
     int32_t n_ranks;
     const DevState *st;
-    int64_t goff[kMaxRanksPerLaunch];     // r * grad_rank_offset_mul
+    const void *in[kMaxRanksPerLaunch];   // contributor 0's element 0 of rank j's slice
+                                          // (kModeNormOnly: the rank's accumulator)
+    float *acc[kMaxRanksPerLaunch];       // kModeAccFirst / kModeAccAdd: rank j's accumulator
     int64_t first[kMaxRanksPerLaunch];    // r * S (flat index of the shard's element 0)
     uint8_t vec[kMaxRanksPerLaunch];      // 16-byte-aligned rows: vector path
 };
@@ -77,24 +90,68 @@ struct FinalizeArgs {
 
 // K3: AdamW + cast into the flat buffer.
 struct AdamArgs {
-    const float *g;
-    int64_t g_stride;
     int64_t S;
+    int64_t full_numel;
     float b1, b2, omb1, omb2, lr, eps, decay;
     int32_t n_ranks;
     const DevState *st;
     void *out;                        // flat 16-bit buffer
+    const float *g[kMaxRanksPerLaunch];   // reduced gradient row of rank j (or its accumulator)
     float *master[kMaxRanksPerLaunch];
     float *m[kMaxRanksPerLaunch];
     float *v[kMaxRanksPerLaunch];
     int64_t out_off[kMaxRanksPerLaunch];  // r * S
-    uint8_t vec[kMaxRanksPerLaunch];      // master/m/v 16-byte aligned
+    uint8_t vec[kMaxRanksPerLaunch];      // g/master/m/v 16-byte aligned
     uint8_t out_align[kMaxRanksPerLaunch];// byte alignment of the output slot: 16, 4 or 2
 };
 
-cudaError_t launch_reduce(const ReduceArgs &a, int grid_x, bool bf16, cudaStream_t s);
+// in_kind: InKind; mode: ReduceMode.  from_acc: g = acc / scale_used, with
+// padding elements (flat index >= full_numel) taken as zero.
+cudaError_t launch_reduce(const ReduceArgs &a, int grid_x, int in_kind, int mode, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeArgs &a, cudaStream_t s);
-cudaError_t launch_adamw(const AdamArgs &a, int grid_x, bool bf16_out, cudaStream_t s);
+cudaError_t launch_adamw(const AdamArgs &a, int grid_x, bool bf16_out, bool from_acc,
+                         cudaStream_t s);
+
+
+// Host-side planning of one kernel class over any number of stepped ranks
+// (one launch per kMaxRanksPerLaunch ranks), shared by every entry point.
+struct ReducePlan {
+    int mode = kModeStep;             // ReduceMode
+    const void *grads = nullptr;      // contributions: rank r, contributor c, element i at
+    int in_kind = kInF16;             //   grads[c*ld + r*rank_mul + i] (InKind encoding)
+    int64_t ld = 0;
+    int64_t rank_mul = 0;
+    const float *const *acc_in = nullptr;  // kModeNormOnly: per-rank accumulators
+    float *const *acc_out = nullptr;       // kModeAccFirst / kModeAccAdd
+    float *g = nullptr;               // kModeStep: rows of g_stride floats per stepped rank
+    int64_t g_stride = 0;
+    double *part_ss = nullptr;        // kModeStep / kModeNormOnly: grid_x partials per rank
+    int32_t *part_of = nullptr;
+    const int32_t *ranks = nullptr;
+    int32_t n_ranks = 0;
+    int64_t S = 0, full_numel = 0;
+    int32_t n_contrib = 1;
+    int32_t avg = 0;
+    const DevState *st = nullptr;
+    int grid_x = 1;
+};
+cudaError_t run_reduce(const ReducePlan &p, cudaStream_t s);
+
+struct AdamPlan {
+    const float *g = nullptr;         // scratch rows (g_stride floats per stepped rank), or
+    int64_t g_stride = 0;
+    const float *const *acc = nullptr;    // per-rank accumulators (then g = acc / scale)
+    float *const *master = nullptr, *const *m = nullptr, *const *v = nullptr;
+    void *out = nullptr;
+    bool bf16_out = false;
+    const int32_t *ranks = nullptr;
+    int32_t n_ranks = 0;
+    int64_t S = 0, full_numel = 0;
+    float b1 = 0, b2 = 0, omb1 = 0, omb2 = 0, lr = 0, eps = 0, decay = 0;
+    const DevState *st = nullptr;
+    int grid_x = 1;
+};
+cudaError_t run_adamw(const AdamPlan &p, cudaStream_t s);
 
 // Launch geometry, measured on GB300 (152 SMs) on the 10B rank-7 step.  The
 // AdamW kernel streams four arrays in and four out and is fastest with exactly
@@ -106,8 +163,8 @@ cudaError_t launch_adamw(const AdamArgs &a, int grid_x, bool bf16_out, cudaStrea
 // exceed the work there is.
 constexpr int kAdamBlocksPerSm = 2;
 
-// Resident blocks per SM of the reduce kernel (occupancy API).
-cudaError_t reduce_blocks_per_sm(int *bps);
+// Resident blocks per SM of one reduce-kernel instance (occupancy API).
+cudaError_t reduce_blocks_per_sm(int in_kind, int mode, int *bps);
 
 inline int grid_x_for(int64_t S, int64_t ranks_in_launch, int sm_count, int blocks_per_sm) {
     const int64_t chunks = (S + kVec - 1) / kVec;

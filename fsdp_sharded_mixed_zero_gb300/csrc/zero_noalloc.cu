@@ -60,7 +60,7 @@ struct DeviceSetup {
     bool done;
     unsigned char *base;              // device address of g_noalloc_scratch
     int sm_count;
-    int reduce_bps;
+    int reduce_bps[3];                // per contribution encoding (InKind)
 };
 DeviceSetup g_setup[kMaxDevices];
 std::mutex g_setup_mu;
@@ -89,8 +89,10 @@ zero_status setup_device(int dev, const DeviceSetup **out) {
         if (!p) return fail(ZERO_ERR_CUDA, "static scratch has no device address");
         e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-        e = zg::reduce_blocks_per_sm(&d.reduce_bps);
-        if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+        for (int kind = 0; kind < 3; ++kind) {
+            e = zg::reduce_blocks_per_sm(kind, zg::kModeStep, &d.reduce_bps[kind]);
+            if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+        }
         d.base = static_cast<unsigned char *>(p);
         d.done = true;
     }
@@ -195,9 +197,10 @@ ZERO_API zero_status zero_shard_step_noalloc(
     double extra_norm_sq, void *stream, zero_step_result *res) {
     // ---- arguments (host only; nothing is launched on an error)
     if (full_numel < 0 || world_size < 1) return fail(ZERO_ERR_INVALID_ARG, "bad layout");
-    if ((grad_dtype != ZERO_F16 && grad_dtype != ZERO_BF16) ||
+    if ((grad_dtype != ZERO_F16 && grad_dtype != ZERO_BF16 && grad_dtype != ZERO_F32) ||
         (param_dtype != ZERO_F16 && param_dtype != ZERO_BF16))
-        return fail(ZERO_ERR_UNSUPPORTED_DTYPE, "dtypes must be ZERO_F16 or ZERO_BF16");
+        return fail(ZERO_ERR_UNSUPPORTED_DTYPE,
+                    "grad dtype must be ZERO_F16, ZERO_BF16 or ZERO_F32; param dtype ZERO_F16 or ZERO_BF16");
     if (op != ZERO_SUM && op != ZERO_AVG) return fail(ZERO_ERR_INVALID_ARG, "op must be SUM or AVG");
     if (!hparams_ok(hp)) return fail(ZERO_ERR_INVALID_ARG, "invalid hyper-parameters");
     if (!state || !(state->scale > 0.0f) || !std::isfinite(state->scale) ||
@@ -220,8 +223,10 @@ ZERO_API zero_status zero_shard_step_noalloc(
     if (grad_ld < 0 || grad_rank_offset_mul < 0 || (world_size > 1 && grad_ld < S))
         return fail(ZERO_ERR_INVALID_ARG, "grad_ld must be >= shard_size");
     if (S > 0 && !grads) return fail(ZERO_ERR_INVALID_ARG, "grads is NULL");
-    if ((uintptr_t)grads % 2 || (uintptr_t)flat_param_out % 2)
-        return fail(ZERO_ERR_ALIGNMENT, "grads and flat_param_out must be 2-byte aligned");
+    const size_t esize = grad_dtype == ZERO_F32 ? 4 : 2;
+    if ((uintptr_t)grads % esize || (uintptr_t)flat_param_out % 2)
+        return fail(ZERO_ERR_ALIGNMENT,
+                    "grads must be aligned to their element size, flat_param_out to 2 bytes");
     int32_t rmax = 0;
     for (int32_t j = 0; j < n_ranks; ++j) {
         if (ranks[j] > rmax) rmax = ranks[j];
@@ -252,7 +257,9 @@ ZERO_API zero_status zero_shard_step_noalloc(
     if (s != ZERO_OK) return s;
 
     // ---- launch geometry (as zero_shard_step computes it)
-    const int gx1 = zg::grid_x_for(S, n_ranks, d->sm_count, d->reduce_bps);
+    const int in_kind = grad_dtype == ZERO_F32 ? zg::kInF32
+                      : (grad_dtype == ZERO_BF16 ? zg::kInBF16 : zg::kInF16);
+    const int gx1 = zg::grid_x_for(S, n_ranks, d->sm_count, d->reduce_bps[in_kind]);
     const int gx3 = zg::grid_x_for(S, n_ranks, d->sm_count, zg::kAdamBlocksPerSm);
     const int64_t parts = (int64_t)gx1 * n_ranks;
     if (parts > kMaxParts) return fail(ZERO_ERR_INVALID_ARG, "too many norm partials");
@@ -274,32 +281,25 @@ ZERO_API zero_status zero_shard_step_noalloc(
     e = cudaMemcpyAsync(&dstate->scaler, &sc, sizeof(sc), cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return cuda_fail(e, "writing the loss-scale state");
 
-    const bool gbf16 = grad_dtype == ZERO_BF16;
-    const bool pbf16 = param_dtype == ZERO_BF16;
-    if (S > 0) {
-        zg::ReduceArgs a{};
-        a.grads = static_cast<const uint16_t *>(grads);
-        a.ld = grad_ld;
-        a.S = S;
-        a.full_numel = full_numel;
-        a.g = gbuf;
-        a.g_stride = g_stride;
-        a.part_ss = part_ss;
-        a.part_of = part_of;
-        a.part_base = 0;
-        a.n_contrib = world_size;
-        a.avg = op == ZERO_AVG;
-        a.n_ranks = n_ranks;
-        a.st = dstate;
-        for (int32_t j = 0; j < n_ranks; ++j) {
-            const int64_t r = ranks[j];
-            a.goff[j] = r * grad_rank_offset_mul;
-            a.first[j] = r * S;
-            a.vec[j] = ((uintptr_t)grads % 16 == 0) && (grad_ld % 8 == 0) && (a.goff[j] % 8 == 0);
-        }
-        if ((e = zg::launch_reduce(a, gx1, gbf16, st)) != cudaSuccess)
-            return cuda_fail(e, "reduce kernel launch");
-    }
+    zg::ReducePlan rp;
+    rp.mode = zg::kModeStep;
+    rp.grads = grads;
+    rp.in_kind = in_kind;
+    rp.ld = grad_ld;
+    rp.rank_mul = grad_rank_offset_mul;
+    rp.g = gbuf;
+    rp.g_stride = g_stride;
+    rp.part_ss = part_ss;
+    rp.part_of = part_of;
+    rp.ranks = ranks;
+    rp.n_ranks = n_ranks;
+    rp.S = S;
+    rp.full_numel = full_numel;
+    rp.n_contrib = world_size;
+    rp.avg = op == ZERO_AVG;
+    rp.st = dstate;
+    rp.grid_x = gx1;
+    if ((e = zg::run_reduce(rp, st)) != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
     FinalizeGivenArgs f{};
     f.part_ss = part_ss;
     f.part_of = part_of;
@@ -314,35 +314,28 @@ ZERO_API zero_status zero_shard_step_noalloc(
     f.st = dstate;
     finalize_given_bc_kernel<<<1, zg::kFinalizeThreads, 0, st>>>(f);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "finalize kernel launch");
-    if (S > 0) {
-        zg::AdamArgs a{};
-        a.g = gbuf;
-        a.g_stride = g_stride;
-        a.S = S;
-        a.b1 = (float)hp->beta1;
-        a.b2 = (float)hp->beta2;
-        a.omb1 = (float)(1.0 - hp->beta1);
-        a.omb2 = (float)(1.0 - hp->beta2);
-        a.lr = (float)hp->lr;
-        a.eps = (float)hp->eps;
-        a.decay = (float)(1.0 - hp->lr * hp->weight_decay);
-        a.n_ranks = n_ranks;
-        a.st = dstate;
-        a.out = flat_param_out;
-        for (int32_t j = 0; j < n_ranks; ++j) {
-            const int64_t r = ranks[j];
-            a.master[j] = master[j];
-            a.m[j] = m[j];
-            a.v[j] = v[j];
-            a.out_off[j] = r * S;
-            a.vec[j] = ((uintptr_t)master[j] % 16 == 0) && ((uintptr_t)m[j] % 16 == 0) &&
-                       ((uintptr_t)v[j] % 16 == 0);
-            const uintptr_t addr = (uintptr_t)flat_param_out + (uintptr_t)(r * S) * 2;
-            a.out_align[j] = addr % 16 == 0 ? 16 : (addr % 4 == 0 ? 4 : 2);
-        }
-        if ((e = zg::launch_adamw(a, gx3, pbf16, st)) != cudaSuccess)
-            return cuda_fail(e, "adamw kernel launch");
-    }
+    zg::AdamPlan ap;
+    ap.g = gbuf;
+    ap.g_stride = g_stride;
+    ap.master = master;
+    ap.m = m;
+    ap.v = v;
+    ap.out = flat_param_out;
+    ap.bf16_out = param_dtype == ZERO_BF16;
+    ap.ranks = ranks;
+    ap.n_ranks = n_ranks;
+    ap.S = S;
+    ap.full_numel = full_numel;
+    ap.b1 = (float)hp->beta1;
+    ap.b2 = (float)hp->beta2;
+    ap.omb1 = (float)(1.0 - hp->beta1);
+    ap.omb2 = (float)(1.0 - hp->beta2);
+    ap.lr = (float)hp->lr;
+    ap.eps = (float)hp->eps;
+    ap.decay = (float)(1.0 - hp->lr * hp->weight_decay);
+    ap.st = dstate;
+    ap.grid_x = gx3;
+    if ((e = zg::run_adamw(ap, st)) != cudaSuccess) return cuda_fail(e, "adamw kernel launch");
 
     // ---- the new loss-scale state and the result back to the caller
     zg::DevState out_state;

@@ -8,11 +8,11 @@ step of the optimizer runs in libzero_gb300's kernels.
 import torch
 
 import synth
-from synth.workloads import BF16, Workload
+from synth.workloads import Workload
 
 from . import ZeroFlat, hparams
 
-_TORCH_DTYPE = {0: torch.float16, 1: torch.bfloat16}
+_TORCH_DTYPE = {0: torch.float16, 1: torch.bfloat16, 2: torch.float32}
 
 
 class DeviceWorkload:
@@ -20,12 +20,13 @@ class DeviceWorkload:
         self.w = w
         self.device = torch.device(device)
         hp = hparams(**w.hparams_kwargs())
-        self.flat = ZeroFlat(w.shapes, w.world_size, w.grad_dtype, w.grad_dtype, w.op, hp)
+        self.flat = ZeroFlat(w.shapes, w.world_size, w.grad_dtype, w.param_dtype, w.op, hp)
         self.S = self.flat.shard_size
         self.full = self.flat.full_numel
         self.padded = self.flat.padded_numel
-        dt = _TORCH_DTYPE[w.grad_dtype]
-        self.grads = torch.empty((w.world_size, w.grad_ld), dtype=dt, device=self.device)
+        self.grads = torch.empty((w.world_size, w.grad_ld), dtype=_TORCH_DTYPE[w.grad_dtype],
+                                 device=self.device)
+        dt = _TORCH_DTYPE[w.param_dtype]
         self.master = [torch.empty(self.S, dtype=torch.float32, device=self.device)
                        for _ in w.ranks]
         self.m = [torch.zeros(self.S, dtype=torch.float32, device=self.device) for _ in w.ranks]
@@ -59,7 +60,7 @@ class DeviceWorkload:
     def gen_grads(self, step, scale):
         """Contributions of `step`: fp16((g + n_c) * scale) or bf16(g + n_c)."""
         w = self.w
-        dtype = synth.BF16 if w.grad_dtype == BF16 else synth.F16
+        dtype = {0: synth.F16, 1: synth.BF16, 2: synth.F32}[w.grad_dtype]
         if w.grads_layout == "full":
             synth.grads_device(self.grads, w.seed, step, 0, self.padded, w.sigma_g, w.sigma_n,
                                scale, dtype, zero_from=self.full)
@@ -79,6 +80,22 @@ class DeviceWorkload:
                               grad_rank_offset_mul=self.w.grad_rank_mul,
                               extra_norm_sq=extra_norm_sq, stream=stream,
                               want_result=want_result)
+
+    # ------------------------------------------------------------ micro-steps
+    def alloc_acc(self):
+        """Per-rank fp32 accumulators, views of one contiguous buffer."""
+        buf = torch.empty(len(self.w.ranks) * self.S, dtype=torch.float32, device=self.device)
+        self.acc = [buf[j * self.S:(j + 1) * self.S] for j in range(len(self.w.ranks))]
+        return self.acc
+
+    def accumulate(self, first, stream=None):
+        self.flat.accumulate(self.w.ranks, self.grads, self.acc, first,
+                             grad_rank_offset_mul=self.w.grad_rank_mul, stream=stream)
+
+    def step_accumulated(self, want_result=True, stream=None, extra_norm_sq=0.0):
+        return self.flat.step_accumulated(self.w.ranks, self.acc, self.master, self.m, self.v,
+                                          self.out, extra_norm_sq=extra_norm_sq, stream=stream,
+                                          want_result=want_result)
 
     def scaler(self):
         return self.flat.scaler_state()

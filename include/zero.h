@@ -58,7 +58,10 @@ typedef enum {
     ZERO_ERR_NO_MEMORY = 7          /* host or device allocation failed */
 } zero_status;
 
-typedef enum { ZERO_F16 = 0, ZERO_BF16 = 1 } zero_dtype;
+/* ZERO_F32 is a gradient dtype only: fp32 contributions, as a reduce-scatter
+ * in reduce_dtype=float32 delivers them ("DeepSpeed 与 FSDP", MixedPrecision
+ * example).  Parameters are always 16-bit. */
+typedef enum { ZERO_F16 = 0, ZERO_BF16 = 1, ZERO_F32 = 2 } zero_dtype;
 
 /* reduce_scatter_tensor's op ("PyTorch FSDP ... 深度解析" §3.3). */
 typedef enum { ZERO_SUM = 0, ZERO_AVG = 1 } zero_reduce_op;
@@ -120,7 +123,8 @@ typedef struct zero_flat zero_flat; /* opaque handle */
  * shard_size S = ceil(full_numel / world_size); padded_numel = world_size*S;
  * rank r owns flat elements [r*S, (r+1)*S); elements >= full_numel are
  * padding and carry a zero gradient.
- * grad_dtype / param_dtype: ZERO_F16 or ZERO_BF16.  op: ZERO_SUM / ZERO_AVG.
+ * grad_dtype: ZERO_F16, ZERO_BF16 or ZERO_F32; param_dtype: ZERO_F16 or
+ * ZERO_BF16.  op: ZERO_SUM / ZERO_AVG.
  * The handle binds to the current CUDA device and allocates there the
  * loss-scale state, the per-step scalars and the bias-correction table
  * (a few hundred KB).  The scratch of a step (an fp32 reduced-gradient row of
@@ -143,7 +147,8 @@ zero_status zero_flat_layout(const zero_flat *h, int64_t *full_numel, int64_t *s
  * the whole group on one GPU -- the norm and the overflow flag are then
  * global over every stepped shard).
  *
- * grads: device, grad_dtype; contributor c's gradient for flat element
+ * grads: device, grad_dtype (aligned to its element size); contributor c's
+ * gradient for flat element
  *   (rank r, i) is grads[c*grad_ld + r*grad_rank_offset_mul + i],
  *   c in [0, world_size), i in [0, S).  Use grad_ld = padded_numel,
  *   grad_rank_offset_mul = S when each contributor holds the whole padded
@@ -163,13 +168,41 @@ zero_status zero_flat_layout(const zero_flat *h, int64_t *full_numel, int64_t *s
  *   copied back and `stream` is synchronized before returning.
  * A skipped (overflowed) step leaves master, m, v, step_t and the flat
  * buffer untouched.  Results are deterministic for a given device.
- * Errors: INVALID_ARG, ALIGNMENT (grads/out not 2-byte or master/m/v not
- * 4-byte aligned), OVERFLOW_SIZE, NO_MEMORY, CUDA. */
+ * Errors: INVALID_ARG, ALIGNMENT (grads not aligned to their element size,
+ * out not 2-byte or master/m/v not 4-byte aligned), OVERFLOW_SIZE,
+ * NO_MEMORY, CUDA. */
 zero_status zero_shard_step(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
                             const void *grads, int64_t grad_ld, int64_t grad_rank_offset_mul,
                             float *const *master, float *const *m, float *const *v,
                             void *flat_param_out, double extra_norm_sq, void *stream,
                             zero_step_result *res);
+
+/* Gradient accumulation across micro-steps ("DeepSpeed 与 FSDP" §实践要点,
+ * gradient accumulation: the loss is divided by the number of micro-steps
+ * and their gradients add up before one optimizer step; ZeRO reading §5.1,
+ * contiguous_gradients: the reduced gradient partitions live in one
+ * contiguous buffer).  For each stepped rank j the micro-step's N
+ * contributions are reduced exactly as zero_shard_step reduces them (fp32,
+ * contributor order, AVG per the handle's op) and
+ *     acc[j][i] = first_micro_step ? r : acc[j][i] + r.
+ * The loss scale is not divided out here; zero_shard_step_accumulated does
+ * that.  grads: as for zero_shard_step.  acc[j]: device fp32, shard_size
+ * elements per stepped rank, caller-owned (one contiguous buffer of
+ * n_ranks * shard_size works).  Padding elements accumulate zero.
+ * Asynchronous on `stream`; no norm, no state change.
+ * Errors: INVALID_ARG, ALIGNMENT, OVERFLOW_SIZE, CUDA. */
+zero_status zero_grad_accumulate(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                                 const void *grads, int64_t grad_ld, int64_t grad_rank_offset_mul,
+                                 float *const *acc, int32_t first_micro_step, void *stream);
+
+/* The optimizer step on accumulated shards: g = acc[j] / scale (padding
+ * elements count as zero), then the overflow check, global norm, loss-scale
+ * decision, AdamW and cast exactly as in zero_shard_step.  acc is only read.
+ * Other arguments and errors as for zero_shard_step. */
+zero_status zero_shard_step_accumulated(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                                        const float *const *acc, float *const *master,
+                                        float *const *m, float *const *v, void *flat_param_out,
+                                        double extra_norm_sq, void *stream, zero_step_result *res);
 
 /* Copy the loss-scale state to the host; synchronizes `stream`. */
 zero_status zero_loss_scaler_state(zero_flat *h, zero_scaler_state *out, void *stream);

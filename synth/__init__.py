@@ -14,7 +14,7 @@ import numpy as np
 from . import build as _build
 
 MASTER, MOMENT_M, MOMENT_V, GRAD_SHARED, GRAD_NOISE = 1, 2, 3, 4, 5
-F16, BF16 = 0, 1
+F16, BF16, F32 = 0, 1, 2
 
 _lib = None
 
@@ -69,7 +69,8 @@ def normal_host(seed, kind, first, n, sigma, absval=False, step=0, contrib=0):
 def grads_host(seed, step, n_contrib, first, n, sigma_g, sigma_n, scale=1.0, dtype=F16,
                zero_from=None, c0=0):
     """uint16 encodings [n_contrib, n] (fp16 via the compiler's conversion,
-    bf16 via torch's conversion of the fp32 pre-cast values)."""
+    bf16 via torch's conversion of the fp32 pre-cast values), or the fp32
+    values themselves for dtype F32."""
     zero_from = (1 << 64) - 1 if zero_from is None else zero_from
     if dtype == F16:
         out = np.empty((n_contrib, max(n, 1)), np.uint16)
@@ -84,6 +85,8 @@ def grads_host(seed, step, n_contrib, first, n, sigma_g, sigma_n, scale=1.0, dty
                                 first, n, zero_from, f.ctypes.data_as(C.c_void_p),
                                 f.shape[1], _threads())
     assert rc == 0
+    if dtype == F32:
+        return np.ascontiguousarray(f[:, :n])
     b = torch.from_numpy(f[:, :n].copy()).to(torch.bfloat16)
     return b.view(torch.int16).numpy().view(np.uint16)
 
@@ -102,10 +105,11 @@ def normal_device(tensor, seed, kind, first, sigma, absval=False, step=0, contri
 
 def grads_device(tensor, seed, step, first, n, sigma_g, sigma_n, scale=1.0, dtype=F16,
                  zero_from=None, c0=0, n_contrib=None, stream=None):
-    """Fill rows of a 2-D 16-bit CUDA tensor [n_contrib, ld] (uses the first n
-    columns of each row)."""
+    """Fill rows of a 2-D CUDA tensor [n_contrib, ld] (16-bit for F16/BF16,
+    float32 for F32; uses the first n columns of each row)."""
     import torch
-    assert tensor.dim() == 2 and tensor.is_cuda and tensor.element_size() == 2
+    assert tensor.dim() == 2 and tensor.is_cuda
+    assert tensor.element_size() == (4 if dtype == F32 else 2)
     assert tensor.stride(1) == 1
     nc = tensor.shape[0] if n_contrib is None else n_contrib
     zero_from = (1 << 64) - 1 if zero_from is None else zero_from

@@ -109,9 +109,10 @@ __global__ void k_normal_f32(uint32_t seed, uint32_t stream, uint64_t first, int
     }
 }
 
+// dtype: 0 fp16, 1 bf16, 2 fp32 (the pre-cast value itself).
 __global__ void k_grads(uint32_t seed, uint32_t step, int32_t c0, int32_t nc, double sg,
-                        double sn, float scale, int bf16, uint64_t first, int64_t n,
-                        uint64_t zero_from, uint16_t *out, int64_t ld) {
+                        double sn, float scale, int dtype, uint64_t first, int64_t n,
+                        uint64_t zero_from, void *out, int64_t ld) {
     const int64_t total = n * (int64_t)nc;
     for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
          e += (int64_t)gridDim.x * blockDim.x) {
@@ -119,15 +120,19 @@ __global__ void k_grads(uint32_t seed, uint32_t step, int32_t c0, int32_t nc, do
         const uint64_t idx = first + (uint64_t)i;
         float x = 0.0f;
         if (idx < zero_from) x = grad_value(seed, step, (uint32_t)(c0 + c), idx, sg, sn, scale);
+        if (dtype == 2) {
+            static_cast<float *>(out)[c * ld + i] = x;
+            continue;
+        }
         uint16_t h;
-        if (bf16) {
+        if (dtype == 1) {
             __nv_bfloat16 b = __float2bfloat16_rn(x);
             memcpy(&h, &b, 2);
         } else {
             __half b = __float2half_rn(x);
             memcpy(&h, &b, 2);
         }
-        out[c * ld + i] = h;
+        static_cast<uint16_t *>(out)[c * ld + i] = h;
     }
 }
 
@@ -214,14 +219,14 @@ SYNTH_API int synth_normal_f32_device(uint32_t seed, uint32_t stream, uint64_t f
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
 
-// dtype 0 = fp16, 1 = bf16; out is uint16 [nc rows, stride ld].
+// dtype 0 = fp16, 1 = bf16 (out: uint16), 2 = fp32 (out: float); [nc rows, stride ld].
 SYNTH_API int synth_grads_device(uint32_t seed, uint32_t step, int32_t c0, int32_t nc,
                                  double sg, double sn, float scale, int dtype, uint64_t first,
                                  int64_t n, uint64_t zero_from, void *out, int64_t ld,
                                  void *cuda_stream) {
-    if (n < 0 || nc < 0 || (n && nc && !out) || ld < n || (dtype != 0 && dtype != 1)) return 1;
+    if (n < 0 || nc < 0 || (n && nc && !out) || ld < n || dtype < 0 || dtype > 2) return 1;
     if (n == 0 || nc == 0) return 0;
     k_grads<<<grid_for(n * (int64_t)nc), 256, 0, (cudaStream_t)cuda_stream>>>(
-        seed, step, c0, nc, sg, sn, scale, dtype, first, n, zero_from, (uint16_t *)out, ld);
+        seed, step, c0, nc, sg, sn, scale, dtype, first, n, zero_from, out, ld);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }

@@ -12,7 +12,7 @@ no weights): see each field for the distribution.
 from dataclasses import dataclass, field
 from typing import List, Optional, Tuple
 
-F16, BF16 = 0, 1
+F16, BF16, F32 = 0, 1, 2
 SUM, AVG = 0, 1
 
 
@@ -73,6 +73,12 @@ class Workload:
     inf_at: Optional[Tuple[int, int, int]] = None   # (step, contributor, shard index): +inf
     hp: dict = field(default_factory=dict)
     grads_layout: str = "full"       # "full": [N, padded], mul = S; "slice": [N, ld], mul = 0
+    micro_steps: int = 1             # >1: contributions accumulated over micro-steps per step
+
+    @property
+    def param_dtype(self):
+        """16-bit parameter dtype (the grad dtype, or fp16 under fp32 contributions)."""
+        return self.grad_dtype if self.grad_dtype in (F16, BF16) else F16
 
     @property
     def full_numel(self):
@@ -91,7 +97,7 @@ class Workload:
     def grad_ld(self):
         if self.grads_layout == "full":
             return self.padded_numel
-        return -(-self.shard_size // 8) * 8          # rows padded to 16 bytes
+        return -(-self.shard_size // 8) * 8          # rows padded to 16 (fp32: 32) bytes
 
     @property
     def grad_rank_mul(self):
@@ -155,6 +161,14 @@ FLAT_800M = Workload(
     shapes=[(800_000_000,)], world_size=8, ranks=[7], grad_dtype=F16, op=AVG, dynamic=True,
     steps=5, sigma_g=2e-4, sigma_n=2e-4, seed=5, grads_layout="slice")
 
+# The 10B rank-7 step with fp32 contributions (reduce_dtype=float32): 40 GB of
+# contributions, fp16 parameters.
+TEN_B_F32 = Workload(
+    name="10b_rank7_fp32", description="10B params, N=8, rank 7's shard, fp32 contributions "
+    "(reduce_dtype=float32), fp16 params, dynamic loss scale 2^16",
+    shapes=[(10_000_000_000,)], world_size=8, ranks=[7], grad_dtype=F32, op=AVG,
+    dynamic=True, steps=5, sigma_g=2e-4, sigma_n=2e-4, seed=6, grads_layout="slice")
+
 ALL = [TINY, GPT2, GPT_1P5B, LLAMA_7B, TEN_B]
-EXTRA = [FLAT_800M]
+EXTRA = [FLAT_800M, TEN_B_F32]
 BY_NAME = {w.name: w for w in ALL + EXTRA}

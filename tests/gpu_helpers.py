@@ -19,6 +19,15 @@ def u16(t):
     return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
+def host_grads(t):
+    """Gradient contributions as the oracle takes them: uint16 encodings of a
+    16-bit tensor, or the float32 values of an fp32 one."""
+    import torch
+    if t.dtype == torch.float32:
+        return t.detach().cpu().numpy()
+    return u16(t)
+
+
 def f32(t):
     return t.detach().cpu().numpy()
 

@@ -14,7 +14,7 @@ from synth.workloads import AVG, BF16, F16, SUM, Workload  # noqa: E402
 
 import tests.oracle_runner as runner  # noqa: E402
 from tests.gpu_helpers import (assert_params_close, assert_result, assert_state, f32,  # noqa: E402
-                               u16)
+                               host_grads, u16)
 
 pytestmark = pytest.mark.gpu
 
@@ -38,17 +38,18 @@ def run_parity(ora, w, steps=None, out_fill=SENTINEL, extra_norm_sq=0.0):
         v = [f32(t).copy() for t in dw.v]
         out = u16(dw.out).copy()
         st = ora.scaler_init(hp)
-        bf16 = w.grad_dtype == BF16
+        gbf16 = w.grad_dtype == BF16
+        bf16 = w.param_dtype == BF16
         results = []
         for step in range(steps if steps is not None else w.warm_steps + w.steps):
             sc = dw.scaler()
             assert sc.as_tuple() == st.as_tuple(), (step, sc.as_tuple(), st.as_tuple())
             dw.gen_grads(step, sc.scale)
-            g = u16(dw.grads)
+            g = host_grads(dw.grads)
             res = dw.step(extra_norm_sq=extra_norm_sq)
             want = runner.shard_step(hp, st, w.world_size, dw.full, dw.S, w.ranks, g,
                                      w.grad_ld, w.grad_rank_mul, master, m, v, out,
-                                     avg=w.op == AVG, grad_is_bf16=bf16, param_is_bf16=bf16,
+                                     avg=w.op == AVG, grad_is_bf16=gbf16, param_is_bf16=bf16,
                                      extra_norm_sq=extra_norm_sq)
             assert_result(res, want)
             for j in range(len(w.ranks)):
