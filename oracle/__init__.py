@@ -103,6 +103,7 @@ def lib():
                                          C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
                                          C.POINTER(C.c_void_p), C.c_void_p, C.c_double,
                                          C.POINTER(Result)]
+        L.ora_quantize_q8.argtypes = [C.c_void_p, C.c_int64, C.c_int32, C.c_void_p, C.c_void_p]
         L.ora_ddp_step.argtypes = [C.POINTER(Hparams), C.POINTER(Scaler), C.c_int32,
                                    C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
                                    C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p,
@@ -202,6 +203,16 @@ def decode_array(h, from_bf16=False):
     out = np.empty(max(h.size, 1), dtype=np.float32)
     lib().ora_decode_array(_ptr(h), h.size, _ptr(out), int(from_bf16))
     return out[:h.size]
+
+
+def quantize_q8(p, block=256):
+    """(codes int8 [n], scales float32 [ceil(n/block)]) of decoded params p."""
+    _check(p, np.float32)
+    n = p.size
+    q = np.empty(max(n, 1), np.int8)
+    sc = np.empty(max(-(-n // block), 1), np.float32)
+    lib().ora_quantize_q8(_ptr(p), n, block, _ptr(q), _ptr(sc))
+    return q[:n], sc[:-(-n // block)]
 
 
 def scaler_init(hp):

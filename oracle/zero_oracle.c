@@ -605,6 +605,43 @@ int ora_shard_step_acc(const ora_hparams *hp, ora_scaler *st, int32_t world_size
     return ORA_OK;
 }
 
+/* ZeRO++ quantized weight communication ([P1] §ZeRO++: the parameter shard
+ * is quantized to int8/int4 before the all-gather and dequantized by the
+ * receiver, halving the traffic; [P3] §4.2: the 2-byte fp16 weights go out
+ * as INT8 and are restored before local use).  The pages give no scheme.
+ * Reading: symmetric absmax int8 over blocks of `block` consecutive elements
+ * of each rank's shard (the last block may be short), applied to the 16-bit
+ * parameter value that would otherwise be all-gathered (decoded exactly to
+ * fp32):
+ *     amax = max |p| over the block (NaN ignored);  scale = amax / 127;
+ *     q = 0 if scale == 0 or p/scale is NaN, else clamp(rint(p/scale), -127, 127)
+ * with rint rounding half to even; the receiver uses q * scale.
+ * p: n decoded parameter values; q: n codes; scales: ceil(n/block) floats. */
+void ora_quantize_q8(const float *p, int64_t n, int32_t block, int8_t *q, float *scales)
+{
+    for (int64_t b0 = 0, k = 0; b0 < n; b0 += block, ++k) {
+        const int64_t b1 = b0 + block < n ? b0 + block : n;
+        float amax = 0.0f;
+        for (int64_t i = b0; i < b1; ++i) {
+            const float a = fabsf(p[i]);
+            if (a > amax) amax = a;                   /* NaN compares false: ignored */
+        }
+        const float scale = amax / 127.0f;
+        scales[k] = scale;
+        for (int64_t i = b0; i < b1; ++i) {
+            int32_t code = 0;
+            if (scale != 0.0f) {
+                const float v = p[i] / scale;
+                if (!isnan(v)) {
+                    const float r = rintf(v);         /* default mode: half to even */
+                    code = r > 127.0f ? 127 : (r < -127.0f ? -127 : (int32_t)r);
+                }
+            }
+            q[i] = (int8_t)code;
+        }
+    }
+}
+
 /* Array form of the casts, for exhaustive checks. */
 void ora_cast_array(const float *in, int64_t n, uint16_t *out, int32_t to_bf16)
 {

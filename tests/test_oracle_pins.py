@@ -752,3 +752,66 @@ def test_step_from_accumulator_overflow_and_padding(ora):
     res = ora.shard_step_acc(hp, st, N, full, S, [0, 1, 2], acc, th, m, v,
                              np.zeros(padded, np.uint16))
     assert res.overflow == 1 and res.skipped == 1 and st.scale == 8.0
+
+
+# --------------------------------------------------------------------------
+# ZeRO++ quantized weight all-gather payload (DS-FSDP §ZeRO++; ZeRO reading
+# §4.2): int8 codes halve the fp16 payload; the receiver dequantizes.
+
+def _q8_exact(p, block):
+    """Rational re-derivation: scale = RN32(amax / 127), code = round-half-even
+    of the fp32-rounded quotient, clamped."""
+    codes, scales = [], []
+    for b0 in range(0, len(p), block):
+        blk = [Fr(float(x)) for x in p[b0:b0 + block]]
+        amax = max(abs(x) for x in blk)
+        scale = _rf32(amax / 127) if amax else Fr(0)
+        scales.append(float(scale))
+        for x in blk:
+            if scale == 0:
+                codes.append(0)
+                continue
+            v = _rf32(x / scale)
+            k = v.numerator // v.denominator
+            rem = v - k
+            if rem > Fr(1, 2) or (rem == Fr(1, 2) and k % 2 == 1):
+                k += 1
+            codes.append(max(-127, min(127, int(k))))
+    return np.array(codes, np.int8), np.array(scales, np.float32)
+
+
+@pytest.mark.parametrize("n,block", [(1000, 256), (256, 256), (77, 32), (5, 8)])
+def test_q8_matches_exact_rounding(ora, n, block):
+    rng = np.random.default_rng(n)
+    p = (rng.standard_normal(n) * 0.05).astype(np.float16).astype(np.float32)
+    p[::17] = 0.0
+    q, sc = ora.quantize_q8(p, block)
+    wq, wsc = _q8_exact(p, block)
+    assert np.array_equal(q, wq) and np.array_equal(sc, wsc)
+
+
+def test_q8_properties(ora):
+    rng = np.random.default_rng(40)
+    p = (rng.standard_normal(100_000) * np.exp(rng.standard_normal(100_000))).astype(
+        np.float16).astype(np.float32)
+    q, sc = ora.quantize_q8(p, 256)
+    assert q.min() >= -127 and q.max() <= 127
+    deq = q.astype(np.float64) * np.repeat(sc.astype(np.float64), 256)[:p.size]
+    # every block's largest magnitude maps to +-127, and the error is at most
+    # half a quantization step (plus fp32 rounding of the quotient)
+    for k in range(sc.size):
+        blk = np.abs(p[k * 256:(k + 1) * 256])
+        assert np.abs(q[k * 256:(k + 1) * 256]).max() == (127 if blk.max() > 0 else 0)
+    step = np.repeat(sc.astype(np.float64), 256)[:p.size]
+    assert np.all(np.abs(deq - p) <= step * (0.5 + 1e-5))
+    # payload: 1 byte per parameter + one fp32 scale per 256 -> about half of fp16
+    assert abs((p.size + 4 * sc.size) / (2 * p.size) - 0.5078) < 1e-3
+
+
+def test_q8_special_values(ora):
+    z, sz = ora.quantize_q8(np.zeros(10, np.float32), 4)
+    assert not z.any() and not sz.any()
+    p = np.array([1.0, -1.0, 0.5, np.nan, np.inf, -2.0, 3.0, 0.0], np.float32)
+    q, sc = ora.quantize_q8(p, 4)
+    assert list(q[:3]) == [127, -127, 64] and q[3] == 0        # 63.5 -> 64 (even)
+    assert sc[1] == np.inf and list(q[4:]) == [0, 0, 0, 0]     # inf block: inf/inf -> NaN -> 0
