@@ -51,6 +51,8 @@ def parse_args():
     p.add_argument("--workload", default="10b_rank7")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--q8", action="store_true",
+                   help="also write the int8 all-gather payload (zero_shard_step_q8)")
     p.add_argument("--micro-steps", type=int, default=1,
                    help="K > 1: each step accumulates K micro-steps' contributions into an "
                         "fp32 shard (zero_grad_accumulate) and steps from it "
@@ -312,8 +314,18 @@ def run_ours(args, w):
     acc_events = []
     if K > 1:
         dw.alloc_acc()
+    q8 = q8_scales = None
+    if args.q8:
+        assert K == 1, "--q8 applies to the plain step"
+        q8 = torch.empty(dw.padded, dtype=torch.int8, device=dev)
+        q8_scales = torch.empty(w.world_size * -(-dw.S // 256), device=dev)
 
     def one_step(timed=False):
+        if q8 is not None:
+            dw.flat.step_q8(w.ranks, dw.grads, dw.master, dw.m, dw.v, dw.out, q8, q8_scales,
+                            grad_rank_offset_mul=w.grad_rank_mul, stream=stream,
+                            want_result=False)
+            return
         if K == 1:
             dw.step(want_result=False, stream=stream)
             return
@@ -374,7 +386,8 @@ def run_ours(args, w):
     kernels = {
         "reduce_kernel": {"ms_mean": ms_red / max(nrec, 1),
                           "bytes_per_param": N * esize + 4 if K == 1 else 4},
-        "adamw_kernel": {"ms_mean": ms_adam / max(nrec, 1), "bytes_per_param": 30},
+        "adamw_kernel": {"ms_mean": ms_adam / max(nrec, 1),
+                         "bytes_per_param": 30 + (1 + 4 / 256 if args.q8 else 0)},
         "finalize_kernel": {"ms_mean": ms_fin / max(nrec, 1), "bytes_per_param": 0},
     }
     if K > 1:
@@ -395,7 +408,7 @@ def run_ours(args, w):
                 "bytes_per_launch": dk["bytes_per_param"] * params}
 
     e2e = None
-    if not args.no_e2e and K == 1:
+    if not args.no_e2e and K == 1 and not args.q8:
         e2e = measure_e2e(args, dw, stream, dev, params, barrier, max_over_ranks, world)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -413,6 +426,7 @@ def run_ours(args, w):
                                   (("f16", "bf16", "f32")[w.grad_dtype],
                                    ("f16", "bf16")[w.param_dtype]),
                        "micro_steps": K,
+                       "q8_payload": bool(args.q8),
                        "l2": "inputs larger than L2 (%.0f GB resident vs 129 MB)" %
                              (dw.flat.device_bytes() / 1e9 + (dw.grads.numel() * esize +
                               (3 + (K > 1)) * params * 4 + dw.out.numel() * 2) / 1e9),

@@ -18,6 +18,7 @@ __all__ = [
     "zero_set_loss_scaler_state", "zero_memory_bytes", "zero_flat_device_bytes",
     "zero_flat_free", "zero_flat_profile_enable", "zero_flat_profile_read",
     "zero_shard_step_noalloc", "zero_grad_accumulate", "zero_shard_step_accumulated",
+    "zero_shard_step_q8", "ZERO_Q8_BLOCK",
     "zero_status_string", "zero_last_error", "ZeroFlat",
     "LIB_PATH",
 ]
@@ -28,6 +29,7 @@ LIB_PATH = os.path.join(HERE, "libzero_gb300.so")
 ZERO_OK = 0
 ZERO_F16, ZERO_BF16, ZERO_F32 = 0, 1, 2
 ZERO_SUM, ZERO_AVG = 0, 1
+ZERO_Q8_BLOCK = 256
 
 
 class ZeroError(RuntimeError):
@@ -88,6 +90,9 @@ def _load():
                                           C.POINTER(ScalerState), C.POINTER(i32), i32, vp, i64,
                                           i64, C.POINTER(vp), C.POINTER(vp), C.POINTER(vp), vp,
                                           C.c_double, vp, C.POINTER(StepResult)]
+    L.zero_shard_step_q8.argtypes = [vp, C.POINTER(i32), i32, vp, i64, i64, C.POINTER(vp),
+                                     C.POINTER(vp), C.POINTER(vp), vp, vp, vp, C.c_double, vp,
+                                     C.POINTER(StepResult)]
     L.zero_grad_accumulate.argtypes = [vp, C.POINTER(i32), i32, vp, i64, i64, C.POINTER(vp), i32,
                                        vp]
     L.zero_shard_step_accumulated.argtypes = [vp, C.POINTER(i32), i32, C.POINTER(vp),
@@ -101,6 +106,7 @@ def _load():
                  "zero_loss_scaler_state", "zero_set_loss_scaler_state", "zero_memory_bytes",
                  "zero_flat_device_bytes", "zero_flat_free", "zero_flat_profile_enable",
                  "zero_flat_profile_read", "zero_shard_step_noalloc", "zero_grad_accumulate",
+                 "zero_shard_step_q8",
                  "zero_shard_step_accumulated"):
         getattr(L, name).restype = i32
     return L
@@ -193,6 +199,23 @@ def zero_shard_step_noalloc(full_numel, world_size, grad_dtype, param_dtype, op,
                                         C.c_void_p(out_ptr), float(extra_norm_sq),
                                         C.c_void_p(stream), C.byref(res)),
            "zero_shard_step_noalloc")
+    return res
+
+
+def zero_shard_step_q8(h, ranks, grads_ptr, grad_ld, grad_rank_offset_mul, master_ptrs,
+                       m_ptrs, v_ptrs, out_ptr, q8_ptr, scales_ptr, extra_norm_sq=0.0,
+                       stream=0, want_result=True):
+    """zero_shard_step that also writes the int8 all-gather payload (codes +
+    one fp32 scale per 256 elements); out_ptr may be 0."""
+    n = len(ranks)
+    r = (C.c_int32 * n)(*ranks)
+    arrs = [(C.c_void_p * n)(*p) for p in (master_ptrs, m_ptrs, v_ptrs)]
+    res = StepResult() if want_result else None
+    _check(_lib.zero_shard_step_q8(h, r, n, C.c_void_p(grads_ptr), grad_ld, grad_rank_offset_mul,
+                                   *arrs, C.c_void_p(out_ptr or None), C.c_void_p(q8_ptr),
+                                   C.c_void_p(scales_ptr), float(extra_norm_sq),
+                                   C.c_void_p(stream), C.byref(res) if res is not None else None),
+           "zero_shard_step_q8")
     return res
 
 
@@ -304,6 +327,22 @@ class ZeroFlat:
                                grad_rank_offset_mul, [t.data_ptr() for t in master],
                                [t.data_ptr() for t in m], [t.data_ptr() for t in v],
                                out.data_ptr(), extra_norm_sq, stream.cuda_stream, want_result)
+
+    def step_q8(self, ranks, grads, master, m, v, out, q8, q8_scales, grad_rank_offset_mul=None,
+                extra_norm_sq=0.0, stream=None, want_result=True):
+        """Step and write the int8 payload: q8 int8 [padded_numel], q8_scales
+        float32 [world_size * ceil(shard_size / 256)]; out may be None."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        if grad_rank_offset_mul is None:
+            grad_rank_offset_mul = self.shard_size if len(ranks) > 1 else 0
+        return zero_shard_step_q8(self.handle, list(ranks), grads.data_ptr(), grads.stride(0),
+                                  grad_rank_offset_mul, [t.data_ptr() for t in master],
+                                  [t.data_ptr() for t in m], [t.data_ptr() for t in v],
+                                  out.data_ptr() if out is not None else 0, q8.data_ptr(),
+                                  q8_scales.data_ptr(), extra_norm_sq, stream.cuda_stream,
+                                  want_result)
 
     def accumulate(self, ranks, grads, acc, first_micro_step, grad_rank_offset_mul=None,
                    stream=None):

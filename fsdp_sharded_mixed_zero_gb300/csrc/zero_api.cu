@@ -425,12 +425,12 @@ zero_status check_rows(const zero_flat *h, float *const *rows, int32_t n_ranks, 
 
 zero_status check_update(const zero_flat *h, int32_t n_ranks, float *const *master,
                          float *const *m, float *const *v, void *flat_param_out,
-                         double extra_norm_sq) {
+                         double extra_norm_sq, bool out_optional = false) {
     zero_status s;
     if ((s = check_rows(h, master, n_ranks, "master"))) return s;
     if ((s = check_rows(h, m, n_ranks, "m"))) return s;
     if ((s = check_rows(h, v, n_ranks, "v"))) return s;
-    if (!flat_param_out) return fail(ZERO_ERR_INVALID_ARG, "flat_param_out is NULL");
+    if (!flat_param_out && !out_optional) return fail(ZERO_ERR_INVALID_ARG, "flat_param_out is NULL");
     if ((uintptr_t)flat_param_out % 2)
         return fail(ZERO_ERR_ALIGNMENT, "flat_param_out must be 2-byte aligned");
     if (!std::isfinite(extra_norm_sq) || extra_norm_sq < 0)
@@ -450,7 +450,8 @@ zero_status launch_step(zero_flat *h, zg::ReducePlan rp, zg::AdamPlan ap, double
     const int64_t S = h->shard;
     const int64_t batch = std::min<int64_t>(rp.n_ranks, zg::kMaxRanksPerLaunch);
     rp.grid_x = zg::grid_x_for(S, batch, h->sm_count, h->reduce_bps[rp.mode]);
-    ap.grid_x = zg::grid_x_for(S, batch, h->sm_count, zg::kAdamBlocksPerSm);
+    ap.grid_x = zg::grid_x_for(S, batch, h->sm_count,
+                               ap.q8 ? zg::kAdamQ8BlocksPerSm : zg::kAdamBlocksPerSm);
     const int64_t parts = (int64_t)rp.grid_x * rp.n_ranks;
     const int64_t rows = rp.mode == zg::kModeStep ? rp.n_ranks : 0;
     zero_status s = ensure_scratch(h, rows, parts);
@@ -538,6 +539,41 @@ ZERO_API zero_status zero_shard_step(zero_flat *h, const int32_t *ranks, int32_t
     ap.m = m;
     ap.v = v;
     ap.out = flat_param_out;
+    return launch_step(h, rp, ap, extra_norm_sq, (cudaStream_t)stream, res);
+}
+
+ZERO_API zero_status zero_shard_step_q8(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                                        const void *grads, int64_t grad_ld,
+                                        int64_t grad_rank_offset_mul, float *const *master,
+                                        float *const *m, float *const *v, void *flat_param_out,
+                                        int8_t *flat_q8_out, float *q8_scales,
+                                        double extra_norm_sq, void *stream,
+                                        zero_step_result *res) {
+    if (!h) return fail(ZERO_ERR_INVALID_ARG, "handle is NULL");
+    int32_t max_rank = 0;
+    zero_status s;
+    if ((s = check_ranks(h, ranks, n_ranks, &max_rank))) return s;
+    if ((s = check_update(h, n_ranks, master, m, v, flat_param_out, extra_norm_sq, true))) return s;
+    if ((s = check_grads(h, grads, grad_ld, grad_rank_offset_mul, max_rank))) return s;
+    if (!flat_q8_out || !q8_scales) return fail(ZERO_ERR_INVALID_ARG, "int8 outputs are NULL");
+    if ((uintptr_t)q8_scales % 4) return fail(ZERO_ERR_ALIGNMENT, "q8_scales must be 4-byte aligned");
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the handle's device");
+    zg::ReducePlan rp;
+    rp.mode = zg::kModeStep;
+    rp.grads = grads;
+    rp.in_kind = in_kind_of(h);
+    rp.ld = grad_ld;
+    rp.rank_mul = grad_rank_offset_mul;
+    rp.ranks = ranks;
+    rp.n_ranks = n_ranks;
+    zg::AdamPlan ap;
+    ap.master = master;
+    ap.m = m;
+    ap.v = v;
+    ap.out = flat_param_out;
+    ap.q8 = flat_q8_out;
+    ap.q8_scales = q8_scales;
     return launch_step(h, rp, ap, extra_norm_sq, (cudaStream_t)stream, res);
 }
 

@@ -559,6 +559,156 @@ __global__ void __launch_bounds__(kBlock) adamw_kernel(const __grid_constant__ A
     }
 }
 
+// ------------------------------------------------------------------ K3q
+// AdamW + cast + the int8 all-gather payload (ZeRO++ quantized weights:
+// "DeepSpeed 与 FSDP" §ZeRO++, ZeRO reading §4.2).  Each warp owns one
+// kQ8Block-element block of the shard per iteration (lane L: elements
+// 8L..8L+7), so the block's absmax is a warp reduction.  The quantized value
+// is the 16-bit parameter as it would be gathered (decoded exactly to fp32):
+// scale = amax / 127, q = clamp(rint(p / scale), -127, 127), NaN -> 0.
+template <bool kBf16>
+__device__ __forceinline__ float decode16(float x) {
+    if constexpr (kBf16) return __bfloat162float(__float2bfloat16_rn(x));
+    else return __half2float(__float2half_rn(x));
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kBlock) adamw_q8_kernel(const __grid_constant__ AdamArgs a) {
+    const DevState *st = a.st;
+    if (st->res.skipped) return;
+    AdamConst k;
+    k.b1 = a.b1; k.b2 = a.b2; k.omb1 = a.omb1; k.omb2 = a.omb2;
+    k.lr = a.lr; k.eps = a.eps; k.decay = a.decay;
+    k.coef = st->res.clip_coef;
+    k.bc1 = st->bc1;
+    k.bc2 = st->bc2;
+
+    const int j = blockIdx.y;
+    float *th = a.master[j];
+    float *mm = a.m[j];
+    float *vv = a.v[j];
+    const float *g = a.g[j];
+    uint16_t *out = a.out ? reinterpret_cast<uint16_t *>(a.out) + a.out_off[j] : nullptr;
+    int8_t *q8 = a.q8 + a.out_off[j];
+    float *scales = a.q8_scales + a.q8_scale_off[j];
+    const int64_t S = a.S;
+    const bool vec = a.vec[j] != 0;
+    const int oal = a.out_align[j];
+    const bool q8vec = a.q8_align[j] == 8;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t nblk = (S + kQ8Block - 1) / kQ8Block;
+
+    for (int64_t b = warp; b < nblk; b += n_warps) {          // warp-uniform
+        const int64_t i0 = b * kQ8Block + (int64_t)lane * kVec;
+        const int64_t rem = S - i0;
+        const int cnt = rem <= 0 ? 0 : (rem >= kVec ? kVec : (int)rem);
+        float P[kVec];
+        if (cnt == kVec && vec) {
+            const float4 g0 = ld_nc_f4(g + i0), g1 = ld_nc_f4(g + i0 + 4);
+            const float4 t0 = ld_f4(th + i0), t1 = ld_f4(th + i0 + 4);
+            const float4 m0 = ld_f4(mm + i0), m1 = ld_f4(mm + i0 + 4);
+            const float4 v0 = ld_f4(vv + i0), v1 = ld_f4(vv + i0 + 4);
+            float G[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            float T[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+            float M[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+            float V[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) adam_elem(G[e], T[e], M[e], V[e], k);
+            st_f4(th + i0, make_float4(T[0], T[1], T[2], T[3]));
+            st_f4(th + i0 + 4, make_float4(T[4], T[5], T[6], T[7]));
+            st_f4(mm + i0, make_float4(M[0], M[1], M[2], M[3]));
+            st_f4(mm + i0 + 4, make_float4(M[4], M[5], M[6], M[7]));
+            st_f4(vv + i0, make_float4(V[0], V[1], V[2], V[3]));
+            st_f4(vv + i0 + 4, make_float4(V[4], V[5], V[6], V[7]));
+            if (out) {
+                const uint32_t w0 = pack2<kBf16>(T[0], T[1]), w1 = pack2<kBf16>(T[2], T[3]);
+                const uint32_t w2 = pack2<kBf16>(T[4], T[5]), w3 = pack2<kBf16>(T[6], T[7]);
+                uint16_t *o = out + i0;
+                if (oal == 16) {
+                    *reinterpret_cast<uint4 *>(o) = make_uint4(w0, w1, w2, w3);
+                } else if (oal == 4) {
+                    uint32_t *o32 = reinterpret_cast<uint32_t *>(o);
+                    o32[0] = w0; o32[1] = w1; o32[2] = w2; o32[3] = w3;
+                } else {
+                    const uint32_t w[4] = {w0, w1, w2, w3};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        o[2 * e] = (uint16_t)(w[e] & 0xFFFFu);
+                        o[2 * e + 1] = (uint16_t)(w[e] >> 16);
+                    }
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < kVec; ++e) P[e] = decode16<kBf16>(T[e]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < kVec; ++e) {
+                P[e] = 0.0f;
+                if (e < cnt) {
+                    const int64_t i = i0 + e;
+                    float t = th[i], m = mm[i], v = vv[i];
+                    adam_elem(g[i], t, m, v, k);
+                    th[i] = t;
+                    mm[i] = m;
+                    vv[i] = v;
+                    if (out) out[i] = from_f32<kBf16>(t);
+                    P[e] = decode16<kBf16>(t);
+                }
+            }
+        }
+        float amax = 0.0f;                                     // NaN ignored (fmaxf)
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) amax = fmaxf(amax, fabsf(P[e]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const float scale = __fdiv_rn(amax, 127.0f);
+        // p / scale, correctly rounded, by Markstein's correction (P. Markstein,
+        // IBM J. Res. Dev. 34(1), 1990): with y = RN(1/scale) and q0 = RN(p*y)
+        // within an ulp of p/scale, RN(q0 + r*y) with the exact remainder
+        // r = p - q0*scale (one fma) is the IEEE quotient.  Used when scale,
+        // 1/scale and the quotients stay normal; IEEE division otherwise.
+        const bool fast = scale >= 0x1p-100f && scale <= 0x1p100f;
+        const float y = fast ? __frcp_rn(scale) : 0.0f;
+        int8_t q[kVec];
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+            int code = 0;
+            if (scale != 0.0f) {
+                float v;
+                const float pe = P[e];
+                if (fast && fabsf(pe) >= 0x1p-100f) {
+                    const float q0 = __fmul_rn(pe, y);
+                    const float r = __fmaf_rn(-q0, scale, pe);
+                    v = __fmaf_rn(r, y, q0);
+                } else {
+                    v = __fdiv_rn(pe, scale);
+                }
+                if (!isnan(v)) {
+                    code = __float2int_rn(v);                  // half to even; saturates
+                    code = code > 127 ? 127 : (code < -127 ? -127 : code);
+                }
+            }
+            q[e] = (int8_t)code;
+        }
+        if (cnt == kVec && q8vec) {
+            uint32_t lo = 0, hi = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                lo |= (uint32_t)(uint8_t)q[e] << (8 * e);
+                hi |= (uint32_t)(uint8_t)q[e + 4] << (8 * e);
+            }
+            *reinterpret_cast<uint2 *>(q8 + i0) = make_uint2(lo, hi);
+        } else {
+#pragma unroll
+            for (int e = 0; e < kVec; ++e)
+                if (e < cnt) q8[i0 + e] = q[e];
+        }
+        if (lane == 0) scales[b] = scale;
+    }
+}
+
 }  // namespace
 
 template <int kIn>
@@ -646,8 +796,16 @@ cudaError_t run_reduce(const ReducePlan &p, cudaStream_t s) {
     return cudaSuccess;
 }
 
+cudaError_t launch_adamw_q8(const AdamArgs &a, int grid_x, bool bf16_out, cudaStream_t s) {
+    const dim3 grid((unsigned)grid_x, (unsigned)a.n_ranks);
+    if (bf16_out) adamw_q8_kernel<true><<<grid, kBlock, 0, s>>>(a);
+    else adamw_q8_kernel<false><<<grid, kBlock, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
 cudaError_t run_adamw(const AdamPlan &p, cudaStream_t s) {
     if (p.S <= 0) return cudaSuccess;
+    if (p.q8 && p.acc) return cudaErrorInvalidValue;   // no quantizing variant reads accumulators
     for (int32_t b0 = 0; b0 < p.n_ranks; b0 += kMaxRanksPerLaunch) {
         const int32_t nb = p.n_ranks - b0 < kMaxRanksPerLaunch ? p.n_ranks - b0 : kMaxRanksPerLaunch;
         AdamArgs a{};
@@ -669,8 +827,15 @@ cudaError_t run_adamw(const AdamPlan &p, cudaStream_t s) {
                        (uintptr_t)a.m[j] % 16 == 0 && (uintptr_t)a.v[j] % 16 == 0;
             const uintptr_t addr = (uintptr_t)p.out + (uintptr_t)(r * p.S) * 2;
             a.out_align[j] = addr % 16 == 0 ? 16 : (addr % 4 == 0 ? 4 : 2);
+            if (p.q8) {
+                a.q8_scale_off[j] = r * ((p.S + kQ8Block - 1) / kQ8Block);
+                a.q8_align[j] = ((uintptr_t)(p.q8 + r * p.S)) % 8 == 0 ? 8 : 1;
+            }
         }
-        const cudaError_t e = launch_adamw(a, p.grid_x, p.bf16_out, p.acc != nullptr, s);
+        a.q8 = p.q8;
+        a.q8_scales = p.q8_scales;
+        const cudaError_t e = p.q8 ? launch_adamw_q8(a, p.grid_x, p.bf16_out, s)
+                                   : launch_adamw(a, p.grid_x, p.bf16_out, p.acc != nullptr, s);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

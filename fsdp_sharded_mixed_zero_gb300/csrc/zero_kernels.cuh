@@ -40,6 +40,10 @@ struct DevState {
     int32_t pad;
 };
 
+// Elements per int8 quantization block of the all-gather payload (one warp's
+// 32 x 8 elements in the quantizing AdamW kernel).
+constexpr int kQ8Block = 256;
+
 // Contribution encodings of the reduce kernel.
 enum InKind : int { kInF16 = 0, kInBF16 = 1, kInF32 = 2 };
 
@@ -103,6 +107,12 @@ struct AdamArgs {
     int64_t out_off[kMaxRanksPerLaunch];  // r * S
     uint8_t vec[kMaxRanksPerLaunch];      // g/master/m/v 16-byte aligned
     uint8_t out_align[kMaxRanksPerLaunch];// byte alignment of the output slot: 16, 4 or 2
+    // int8 all-gather payload (adamw_q8_kernel only): codes in the flat int8
+    // buffer at out_off, one fp32 scale per kQ8Block elements of the shard
+    int8_t *q8;
+    float *q8_scales;
+    int64_t q8_scale_off[kMaxRanksPerLaunch];  // r * ceil(S / kQ8Block)
+    uint8_t q8_align[kMaxRanksPerLaunch];      // 8: 8-byte code stores, else byte stores
 };
 
 // in_kind: InKind; mode: ReduceMode.  from_acc: g = acc / scale_used, with
@@ -111,6 +121,8 @@ cudaError_t launch_reduce(const ReduceArgs &a, int grid_x, int in_kind, int mode
 cudaError_t launch_finalize(const FinalizeArgs &a, cudaStream_t s);
 cudaError_t launch_adamw(const AdamArgs &a, int grid_x, bool bf16_out, bool from_acc,
                          cudaStream_t s);
+// AdamW + cast + int8 block quantization of the cast values (a.out may be NULL).
+cudaError_t launch_adamw_q8(const AdamArgs &a, int grid_x, bool bf16_out, cudaStream_t s);
 
 
 // Host-side planning of one kernel class over any number of stepped ranks
@@ -149,6 +161,8 @@ struct AdamPlan {
     int64_t S = 0, full_numel = 0;
     float b1 = 0, b2 = 0, omb1 = 0, omb2 = 0, lr = 0, eps = 0, decay = 0;
     const DevState *st = nullptr;
+    int8_t *q8 = nullptr;             // non-NULL: also write the int8 payload and its scales
+    float *q8_scales = nullptr;
     int grid_x = 1;
 };
 cudaError_t run_adamw(const AdamPlan &p, cudaStream_t s);
@@ -162,6 +176,7 @@ cudaError_t run_adamw(const AdamPlan &p, cudaStream_t s);
 // launch's blocks are split across the stepped ranks it handles and never
 // exceed the work there is.
 constexpr int kAdamBlocksPerSm = 2;
+constexpr int kAdamQ8BlocksPerSm = 3;    // AdamW + int8 payload (72 registers): 6.10 ms vs 6.90 at two
 
 // Resident blocks per SM of one reduce-kernel instance (occupancy API).
 cudaError_t reduce_blocks_per_sm(int in_kind, int mode, int *bps);

@@ -177,6 +177,29 @@ zero_status zero_shard_step(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
                             void *flat_param_out, double extra_norm_sq, void *stream,
                             zero_step_result *res);
 
+/* Elements per int8 quantization block of the all-gather payload. */
+#define ZERO_Q8_BLOCK 256
+
+/* zero_shard_step that also writes the ZeRO++ quantized weight payload
+ * ("DeepSpeed 与 FSDP" §ZeRO++: the parameter shard is quantized to int8
+ * before the all-gather and dequantized by the receiver, halving the fp16
+ * traffic; ZeRO reading §4.2).  Scheme (the pages give none): for every
+ * block of ZERO_Q8_BLOCK consecutive elements of a rank's shard (the last
+ * block may be short), with p the 16-bit parameter value decoded to fp32,
+ *     amax = max |p| (NaN ignored); scale = amax / 127;
+ *     q = 0 if scale == 0 or p/scale is NaN, else clamp(rint(p/scale), +-127)
+ * (rint: half to even); the receiver uses q * scale.
+ * flat_q8_out: device int8, padded_numel elements; rank r's codes go to
+ *   [r*S, (r+1)*S).  q8_scales: device fp32, world_size * ceil(S/256)
+ *   elements; rank r's scales at [r*nb, (r+1)*nb), nb = ceil(S/256).
+ * flat_param_out may be NULL (then only the int8 payload is written).
+ * Other arguments, skip semantics and errors as for zero_shard_step. */
+zero_status zero_shard_step_q8(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                               const void *grads, int64_t grad_ld, int64_t grad_rank_offset_mul,
+                               float *const *master, float *const *m, float *const *v,
+                               void *flat_param_out, int8_t *flat_q8_out, float *q8_scales,
+                               double extra_norm_sq, void *stream, zero_step_result *res);
+
 /* Gradient accumulation across micro-steps ("DeepSpeed 与 FSDP" §实践要点,
  * gradient accumulation: the loss is divided by the number of micro-steps
  * and their gradients add up before one optimizer step; ZeRO reading §5.1,
