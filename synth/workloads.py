@@ -74,10 +74,13 @@ class Workload:
     hp: dict = field(default_factory=dict)
     grads_layout: str = "full"       # "full": [N, padded], mul = S; "slice": [N, ld], mul = 0
     micro_steps: int = 1             # >1: contributions accumulated over micro-steps per step
+    pdtype: Optional[int] = None     # parameter dtype if it differs from the default below
 
     @property
     def param_dtype(self):
         """16-bit parameter dtype (the grad dtype, or fp16 under fp32 contributions)."""
+        if self.pdtype is not None:
+            return self.pdtype
         return self.grad_dtype if self.grad_dtype in (F16, BF16) else F16
 
     @property
