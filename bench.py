@@ -51,6 +51,8 @@ def parse_args():
     p.add_argument("--workload", default="10b_rank7")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--graph", action="store_true",
+                   help="capture one step in a CUDA graph and replay it (no per-kernel split)")
     p.add_argument("--q8", action="store_true",
                    help="also write the int8 all-gather payload (zero_shard_step_q8)")
     p.add_argument("--micro-steps", type=int, default=1,
@@ -344,6 +346,20 @@ def run_ours(args, w):
     for _ in range(args.warmup):
         one_step()
     torch.cuda.synchronize(dev)
+    graph = None
+    if args.graph:
+        # the warm-up steps above allocated the handle's scratch; capture one step
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            saved = stream
+            stream = cap
+            one_step()
+            stream = saved
+        stream.wait_stream(cap)
+        graph.replay()
+        torch.cuda.synchronize(dev)
 
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -359,7 +375,10 @@ def run_ours(args, w):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        one_step(timed=True)
+        if graph is not None:
+            graph.replay()
+        else:
+            one_step(timed=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -403,7 +422,7 @@ def run_ours(args, w):
     min_bytes = (K * N * esize + 26) * params               # the method's minimum per step
     step_gbs = min_bytes / (ms_step / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": dk["achieved_gbs"], "peak": peak,
-                "unit": "GB/s", "frac": dk["achieved_gbs"] / peak,
+                "unit": "GB/s", "frac": dk["achieved_gbs"] / peak if dk["achieved_gbs"] else None,
                 "peak_kind": peak_kind, "traffic": traffic,
                 "bytes_per_launch": dk["bytes_per_param"] * params}
 
@@ -427,6 +446,7 @@ def run_ours(args, w):
                                    ("f16", "bf16")[w.param_dtype]),
                        "micro_steps": K,
                        "q8_payload": bool(args.q8),
+                       "cuda_graph": bool(args.graph),
                        "l2": "inputs larger than L2 (%.0f GB resident vs 129 MB)" %
                              (dw.flat.device_bytes() / 1e9 + (dw.grads.numel() * esize +
                               (3 + (K > 1)) * params * 4 + dw.out.numel() * 2) / 1e9),
