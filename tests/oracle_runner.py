@@ -78,3 +78,17 @@ def shard_step(hp, st, world_size, full, S, ranks, grads, ld, mul, master, m, v,
 
         list(_pool().map(job, [(j, a, b) for j in range(len(ranks)) for a, b in _chunks(S)]))
     return of, skip, norm, coef, scale
+
+
+def accumulate_rows(grads, ld, n_contrib, count, full, avg, bf16, acc, first):
+    """The oracle's grad_accumulate over `count` columns of a [n_contrib, ld]
+    contribution block (flat indices from 0, no padding inside), into the
+    fp32 slice acc, chunk-parallel."""
+    flat = grads.reshape(-1)
+
+    def job(ab):
+        a, b = ab
+        oracle.grad_accumulate(n_contrib, full, b - a, [0], flat[a:], ld, 0, [acc[a:b]],
+                               first, avg=avg, grad_is_bf16=bf16)
+
+    list(_pool().map(job, _chunks(count)))
