@@ -87,3 +87,26 @@ def test_bf16_grads_fp16_params(ora):
                  shapes=[(40_001,), (7,)], world_size=4, ranks=[0, 1, 2, 3], grad_dtype=BF16,
                  op=AVG, dynamic=False, steps=3, sigma_g=1e-3, sigma_n=1e-3, pdtype=F16)
     run_parity(ora, w)
+
+
+def test_gradients_in_pinned_host_memory():
+    """The contributions read straight from page-locked host memory (no copy):
+    the bits of the device-resident step."""
+    _need_gpu()
+    from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
+    w = Workload(name="hostgrads", description="hostgrads", shapes=[(2_000_017,)], world_size=8,
+                 ranks=[5], grad_dtype=F16, op=AVG, dynamic=True, steps=3, sigma_g=1e-3,
+                 sigma_n=1e-3, grads_layout="slice")
+    dev, hst = DeviceWorkload(w), DeviceWorkload(w)
+    pinned = torch.empty(dev.grads.shape, dtype=dev.grads.dtype, pin_memory=True)
+    for step in range(w.steps):
+        dev.gen_grads(step, dev.scaler().scale)
+        pinned.copy_(dev.grads)
+        ra = dev.step()
+        rb = hst.flat.step(w.ranks, pinned, hst.master, hst.m, hst.v, hst.out,
+                           grad_rank_offset_mul=0)
+        assert (ra.overflow, ra.skipped, ra.grad_norm, ra.clip_coef) == \
+               (rb.overflow, rb.skipped, rb.grad_norm, rb.clip_coef)
+    _same(dev.master + dev.m + dev.v + [dev.out], hst.master + hst.m + hst.v + [hst.out])
+    dev.close()
+    hst.close()
