@@ -18,7 +18,7 @@ __all__ = [
     "zero_set_loss_scaler_state", "zero_memory_bytes", "zero_flat_device_bytes",
     "zero_flat_free", "zero_flat_profile_enable", "zero_flat_profile_read",
     "zero_shard_step_noalloc", "zero_grad_accumulate", "zero_shard_step_accumulated",
-    "zero_shard_step_q8", "ZERO_Q8_BLOCK",
+    "zero_shard_step_q8", "ZERO_Q8_BLOCK", "zero_flat_set_lr",
     "zero_status_string", "zero_last_error", "ZeroFlat",
     "LIB_PATH",
 ]
@@ -98,6 +98,7 @@ def _load():
     L.zero_shard_step_accumulated.argtypes = [vp, C.POINTER(i32), i32, C.POINTER(vp),
                                               C.POINTER(vp), C.POINTER(vp), C.POINTER(vp), vp,
                                               C.c_double, vp, C.POINTER(StepResult)]
+    L.zero_flat_set_lr.argtypes = [vp, C.c_double]
     L.zero_status_string.argtypes = [i32]
     L.zero_status_string.restype = C.c_char_p
     L.zero_last_error.argtypes = []
@@ -106,7 +107,7 @@ def _load():
                  "zero_loss_scaler_state", "zero_set_loss_scaler_state", "zero_memory_bytes",
                  "zero_flat_device_bytes", "zero_flat_free", "zero_flat_profile_enable",
                  "zero_flat_profile_read", "zero_shard_step_noalloc", "zero_grad_accumulate",
-                 "zero_shard_step_q8",
+                 "zero_shard_step_q8", "zero_flat_set_lr",
                  "zero_shard_step_accumulated"):
         getattr(L, name).restype = i32
     return L
@@ -245,6 +246,11 @@ def zero_shard_step_accumulated(h, ranks, acc_ptrs, master_ptrs, m_ptrs, v_ptrs,
     return res
 
 
+def zero_flat_set_lr(h, lr):
+    """Learning rate of the steps launched from now on."""
+    _check(_lib.zero_flat_set_lr(h, float(lr)), "zero_flat_set_lr")
+
+
 def zero_loss_scaler_state(h, stream=0):
     st = ScalerState()
     _check(_lib.zero_loss_scaler_state(h, C.byref(st), C.c_void_p(stream)),
@@ -366,6 +372,10 @@ class ZeroFlat:
                                            [t.data_ptr() for t in m], [t.data_ptr() for t in v],
                                            out.data_ptr(), extra_norm_sq, stream.cuda_stream,
                                            want_result)
+
+    def set_lr(self, lr):
+        zero_flat_set_lr(self.handle, lr)
+        self.hp.lr = lr
 
     def scaler_state(self, stream=None):
         import torch

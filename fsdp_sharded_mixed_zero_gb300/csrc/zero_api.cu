@@ -639,6 +639,15 @@ ZERO_API zero_status zero_shard_step_accumulated(zero_flat *h, const int32_t *ra
     return launch_step(h, rp, ap, extra_norm_sq, (cudaStream_t)stream, res);
 }
 
+ZERO_API zero_status zero_flat_set_lr(zero_flat *h, double lr) {
+    if (!h) return fail(ZERO_ERR_INVALID_ARG, "handle is NULL");
+    if (!std::isfinite(lr) || lr < 0) return fail(ZERO_ERR_INVALID_ARG, "lr must be finite and >= 0");
+    h->hp.lr = lr;
+    h->lr = (float)lr;
+    h->decay = (float)(1.0 - lr * h->hp.weight_decay);
+    return ZERO_OK;
+}
+
 ZERO_API zero_status zero_loss_scaler_state(zero_flat *h, zero_scaler_state *out, void *stream) {
     if (!h || !out) return fail(ZERO_ERR_INVALID_ARG, "NULL argument");
     DeviceGuard guard(h->device);

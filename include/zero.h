@@ -37,6 +37,7 @@
  *     it alive until the work queued on `stream` has finished.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
  *   - The library needs the CUDA driver; it contains no CPU fallback.
+ *   - A handle is not thread-safe: calls on one handle must not overlap.
  */
 #ifndef ZERO_GB300_H
 #define ZERO_GB300_H
@@ -226,6 +227,14 @@ zero_status zero_shard_step_accumulated(zero_flat *h, const int32_t *ranks, int3
                                         const float *const *acc, float *const *master,
                                         float *const *m, float *const *v, void *flat_param_out,
                                         double extra_norm_sq, void *stream, zero_step_result *res);
+
+/* Change the learning rate for the steps launched after this call (a
+ * schedule's warm-up or decay; the ZeRO reading §5.3 warns that warm-up must
+ * be re-tuned when the effective batch changes).  lr is fp64 as in
+ * zero_hparams; lr and 1 - lr*weight_decay are rounded to fp32 once, as at
+ * init.  Host only: steps already queued keep the rate they were launched
+ * with.  Errors: INVALID_ARG (NULL handle, lr negative or not finite). */
+zero_status zero_flat_set_lr(zero_flat *h, double lr);
 
 /* Copy the loss-scale state to the host; synchronizes `stream`. */
 zero_status zero_loss_scaler_state(zero_flat *h, zero_scaler_state *out, void *stream);

@@ -262,3 +262,38 @@ def test_step_argument_errors(ora):
         f.set_scaler_state(bad)
     assert f.scaler_state().step_t == 0                # nothing ran
     f.close()
+
+
+def test_learning_rate_schedule(ora):
+    """A warm-up then decay schedule set between steps (zero_flat_set_lr)
+    matches the oracle stepping with the same rates."""
+    _need_gpu()
+    from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
+    w = _wl("lr_sched", [(60_001,)], 4, [0, 1, 2, 3], steps=5)
+    lrs = [1e-5, 2e-5, 3e-5, 1.5e-5, 0.0]
+    dw = DeviceWorkload(w)
+    try:
+        master = [f32(t).copy() for t in dw.master]
+        m = [f32(t).copy() for t in dw.m]
+        v = [f32(t).copy() for t in dw.v]
+        out = u16(dw.out).copy()
+        kw = w.hparams_kwargs()
+        st = ora.scaler_init(ora.hparams(**kw))
+        for step, lr in enumerate(lrs):
+            dw.flat.set_lr(lr)
+            kw["lr"] = lr
+            hp = ora.hparams(**kw)
+            dw.gen_grads(step, dw.scaler().scale)
+            g = host_grads(dw.grads)
+            res = dw.step()
+            want = runner.shard_step(hp, st, w.world_size, dw.full, dw.S, w.ranks, g, w.grad_ld,
+                                     w.grad_rank_mul, master, m, v, out, avg=True)
+            assert_result(res, want)
+            for j in range(len(w.ranks)):
+                assert_state(f32(dw.master[j]), f32(dw.m[j]), f32(dw.v[j]), master[j], m[j],
+                             v[j], tag=" (lr %g)" % lr)
+        import fsdp_sharded_mixed_zero_gb300 as Z
+        with pytest.raises(Z.ZeroError):
+            dw.flat.set_lr(float("nan"))
+    finally:
+        dw.close()
