@@ -21,6 +21,10 @@ event-timed duration, against the measured HBM copy peak.
 cpu_baseline: the oracle (plain single-threaded C) on a bounded sample of the
 same workload, timed on this host.
 --impl reference: the oracle on the host cores as the reference arm.
+--offload: the ZeRO-Offload step instead (zero_shard_step_offload: reduce and
+decision on the GPU, AdamW over host-resident fp32 state on the host cores),
+its own JSON line with the per-phase times and the host update against the
+host copy bandwidth measured in the same run.
 Under torchrun each rank runs an independent replica (weak scaling).
 """
 import argparse
@@ -60,6 +64,10 @@ def parse_args():
                    help="K > 1: each step accumulates K micro-steps' contributions into an "
                         "fp32 shard (zero_grad_accumulate) and steps from it "
                         "(zero_shard_step_accumulated)")
+    p.add_argument("--offload", action="store_true",
+                   help="time the ZeRO-Offload step (optimizer on the host cores)")
+    p.add_argument("--offload-threads", type=int, default=0,
+                   help="host threads of the offload update (0: every available CPU)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -513,12 +521,130 @@ def measure_e2e(args, dw, stream, dev, params, barrier, max_over_ranks, world):
             "copy_then_step_ms": 1e3 * timings["copy_then_step"] / args.e2e_steps}
 
 
+def host_copy_gbs(nbytes=2 << 30, reps=3):
+    """Host memory bandwidth of a multi-threaded torch CPU copy (bytes read +
+    written per second, best of `reps`), the peak the host update is held to."""
+    import torch
+    n = nbytes // 4
+    src = torch.ones(n, dtype=torch.float32)
+    dst = torch.empty_like(src)
+    best = 0.0
+    for _ in range(reps + 1):
+        t = time.perf_counter()
+        dst.copy_(src)
+        dt = time.perf_counter() - t
+        best = max(best, 2 * n * 4 / dt / 1e9)
+    return best, torch.get_num_threads()
+
+
+def run_offload(args, w):
+    """The ZeRO-Offload step on the workload: K1 reduces on the GPU and writes
+    the fp32 gradient rows into pinned host memory, K2 decides, the host
+    threads update master/m/v (host memory) and the 16-bit parameters are
+    copied back into the device flat buffer."""
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    group = RankGroup(backend="nccl", device=dev)
+    barrier, max_over_ranks = group.barrier, group.max
+
+    import fsdp_sharded_mixed_zero_gb300 as Z
+    from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
+
+    dw = DeviceWorkload(w, device=dev)
+    dw.gen_grads(0, dw.scaler().scale)
+    stream = torch.cuda.current_stream(dev)
+    hm, hmm, hv = ([t.cpu() for t in ts] for ts in (dw.master, dw.m, dw.v))
+    dw.master = dw.m = dw.v = None                       # the state lives on the host
+    torch.cuda.empty_cache()
+    params = dw.S * len(w.ranks)
+    n_batches = -(-len(w.ranks) // 64)
+
+    def one_step():
+        return dw.flat.step_offload(w.ranks, dw.grads, hm, hmm, hv, dw.out,
+                                    grad_rank_offset_mul=w.grad_rank_mul,
+                                    n_threads=args.offload_threads, stream=stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize(dev)
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = str(local)
+    sampler = ClockSampler(uuid)
+    Z.zero_flat_profile_enable(dw.flat.handle, True)
+    Z.zero_flat_profile_read(dw.flat.handle)
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        res = one_step()
+        assert res.skipped == 0 and res.overflow == 0, "benchmark inputs overflowed"
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop()
+    Z.zero_flat_profile_enable(dw.flat.handle, False)
+    ms_red, ms_fin, ms_host, nrec = Z.zero_flat_profile_read(dw.flat.handle)
+    elapsed_ms = max_over_ranks(e0.elapsed_time(e1))
+    peak, threads = host_copy_gbs()
+
+    N = w.world_size
+    esize = 4 if w.grad_dtype == 2 else 2
+    # K1 reads the N contributions from HBM and writes the fp32 gradient rows
+    # (4 B/param) over the host link; the host update reads the gradient (4)
+    # and master/m/v (12), writes master/m/v (12) and the 16-bit param (2),
+    # whose copy to the device overlaps it.
+    kernels = {
+        "reduce_kernel": {"ms_mean": ms_red / max(nrec, 1), "bytes_per_param": N * esize + 4,
+                          "link_bytes_per_param": 4},
+        "finalize_kernel": {"ms_mean": ms_fin / max(nrec, 1), "bytes_per_param": 0},
+        "host_update": {"ms_mean": ms_host / max(nrec, 1), "bytes_per_param": 30,
+                        "link_bytes_per_param": 2},
+    }
+    for k in kernels.values():
+        k["achieved_gbs"] = (k["bytes_per_param"] * params / (k["ms_mean"] / 1e3) / 1e9
+                             if k["ms_mean"] > 0 else None)
+    hu = kernels["host_update"]
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": whole_job_value(params, args.steps, world, elapsed_ms),
+            "unit": "Gparams/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "params_stepped_per_gpu": params,
+                       "emulated_world_size": N, "stepped_ranks": w.ranks,
+                       "offload": "AdamW on host cores, fp32 master/m/v in host memory",
+                       "host_threads": args.offload_threads or len(os.sched_getaffinity(0)),
+                       "parallelism": "replicas%d" % world},
+            "kernels": kernels,
+            "roofline": {"bound": "host-memory", "kernel": "host_update",
+                         "achieved": hu["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                         "frac": hu["achieved_gbs"] / peak if hu["achieved_gbs"] else None,
+                         "peak_kind": "measured here: torch CPU copy on %d threads" % threads,
+                         "traffic": None, "bytes_per_launch": 30 * params},
+            "cpu_baseline": None, "e2e": None, "clocks": clocks,
+            "gpu_launches": (n_batches + 1) * args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    dw.close()
+    group.close()
+
+
 def main():
     args = parse_args()
     from synth.workloads import BY_NAME
     w = BY_NAME[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.offload:
+        run_offload(args, w)
     else:
         run_ours(args, w)
 

@@ -18,7 +18,8 @@ __all__ = [
     "zero_set_loss_scaler_state", "zero_memory_bytes", "zero_flat_device_bytes",
     "zero_flat_free", "zero_flat_profile_enable", "zero_flat_profile_read",
     "zero_shard_step_noalloc", "zero_grad_accumulate", "zero_shard_step_accumulated",
-    "zero_shard_step_q8", "ZERO_Q8_BLOCK", "zero_flat_set_lr",
+    "zero_shard_step_q8", "ZERO_Q8_BLOCK", "zero_flat_set_lr", "zero_shard_step_offload",
+    "zero_offload_adamw_host",
     "zero_status_string", "zero_last_error", "ZeroFlat",
     "LIB_PATH",
 ]
@@ -99,6 +100,11 @@ def _load():
                                               C.POINTER(vp), C.POINTER(vp), C.POINTER(vp), vp,
                                               C.c_double, vp, C.POINTER(StepResult)]
     L.zero_flat_set_lr.argtypes = [vp, C.c_double]
+    L.zero_shard_step_offload.argtypes = [vp, C.POINTER(i32), i32, vp, i64, i64, C.POINTER(vp),
+                                          C.POINTER(vp), C.POINTER(vp), vp, C.c_double, i32, vp,
+                                          C.POINTER(StepResult)]
+    L.zero_offload_adamw_host.argtypes = [C.POINTER(Hparams), i64, C.c_float, vp, vp, vp, vp,
+                                          vp, i64, i32, i32]
     L.zero_status_string.argtypes = [i32]
     L.zero_status_string.restype = C.c_char_p
     L.zero_last_error.argtypes = []
@@ -107,7 +113,8 @@ def _load():
                  "zero_loss_scaler_state", "zero_set_loss_scaler_state", "zero_memory_bytes",
                  "zero_flat_device_bytes", "zero_flat_free", "zero_flat_profile_enable",
                  "zero_flat_profile_read", "zero_shard_step_noalloc", "zero_grad_accumulate",
-                 "zero_shard_step_q8", "zero_flat_set_lr",
+                 "zero_shard_step_q8", "zero_flat_set_lr", "zero_shard_step_offload",
+                 "zero_offload_adamw_host",
                  "zero_shard_step_accumulated"):
         getattr(L, name).restype = i32
     return L
@@ -246,6 +253,34 @@ def zero_shard_step_accumulated(h, ranks, acc_ptrs, master_ptrs, m_ptrs, v_ptrs,
     return res
 
 
+def zero_shard_step_offload(h, ranks, grads_ptr, grad_ld, grad_rank_offset_mul, master_ptrs,
+                            m_ptrs, v_ptrs, out_ptr, extra_norm_sq=0.0, n_threads=0, stream=0,
+                            want_result=True):
+    """The offload step: master/m/v pointers are HOST memory; returns a
+    StepResult when want_result (the call synchronizes the stream either way)."""
+    n = len(ranks)
+    r = (C.c_int32 * n)(*ranks)
+    arrs = [(C.c_void_p * n)(*p) for p in (master_ptrs, m_ptrs, v_ptrs)]
+    res = StepResult() if want_result else None
+    _check(_lib.zero_shard_step_offload(h, r, n, C.c_void_p(grads_ptr), grad_ld,
+                                        grad_rank_offset_mul, *arrs, C.c_void_p(out_ptr),
+                                        float(extra_norm_sq), int(n_threads), C.c_void_p(stream),
+                                        C.byref(res) if res is not None else None),
+           "zero_shard_step_offload")
+    return res
+
+
+def zero_offload_adamw_host(hp, step_t, clip_coef, g_ptr, master_ptr, m_ptr, v_ptr, out_ptr, n,
+                            param_dtype=ZERO_F16, n_threads=0):
+    """The host AdamW + 16-bit cast of the offload step on n elements of host
+    arrays (no GPU involved)."""
+    _check(_lib.zero_offload_adamw_host(C.byref(hp), int(step_t), C.c_float(clip_coef),
+                                        C.c_void_p(g_ptr), C.c_void_p(master_ptr),
+                                        C.c_void_p(m_ptr), C.c_void_p(v_ptr), C.c_void_p(out_ptr),
+                                        int(n), int(param_dtype), int(n_threads)),
+           "zero_offload_adamw_host")
+
+
 def zero_flat_set_lr(h, lr):
     """Learning rate of the steps launched from now on."""
     _check(_lib.zero_flat_set_lr(h, float(lr)), "zero_flat_set_lr")
@@ -372,6 +407,24 @@ class ZeroFlat:
                                            [t.data_ptr() for t in m], [t.data_ptr() for t in v],
                                            out.data_ptr(), extra_norm_sq, stream.cuda_stream,
                                            want_result)
+
+    def step_offload(self, ranks, grads, master, m, v, out, grad_rank_offset_mul=None,
+                     extra_norm_sq=0.0, n_threads=0, stream=None, want_result=True):
+        """The ZeRO-Offload step: master, m, v are fp32 CPU tensors (pinned or
+        not); grads and out are CUDA tensors as for step()."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        assert grads.dim() == 2 and grads.stride(1) == 1
+        for t in list(master) + list(m) + list(v):
+            assert t.device.type == "cpu" and t.dtype == torch.float32 and t.is_contiguous()
+        if grad_rank_offset_mul is None:
+            grad_rank_offset_mul = self.shard_size if len(ranks) > 1 else 0
+        return zero_shard_step_offload(self.handle, list(ranks), grads.data_ptr(),
+                                       grads.stride(0), grad_rank_offset_mul,
+                                       [t.data_ptr() for t in master], [t.data_ptr() for t in m],
+                                       [t.data_ptr() for t in v], out.data_ptr(), extra_norm_sq,
+                                       n_threads, stream.cuda_stream, want_result)
 
     def set_lr(self, lr):
         zero_flat_set_lr(self.handle, lr)

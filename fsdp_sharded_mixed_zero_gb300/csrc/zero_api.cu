@@ -4,12 +4,15 @@
 // beyond forming the per-step fp32 scalars from the fp64 hyper-parameters.
 #include "zero.h"
 #include "zero_kernels.cuh"
+#include "host_adam.h"
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <memory>
 #include <new>
 #include <vector>
 
@@ -81,6 +84,14 @@ struct zero_flat {
     int64_t parts_cap = 0;
     zg::DevState *h_state = nullptr;  // pinned staging for state reads
     uint64_t device_bytes = 0;
+    // offload step: pinned host gradient rows and 16-bit staging, the host
+    // worker pool, and an event after the last parameter copy
+    float *h_g = nullptr;
+    int64_t h_g_rows = 0;
+    uint16_t *h_out = nullptr;
+    int64_t h_out_rows = 0;
+    std::unique_ptr<zh::Pool> pool;
+    cudaEvent_t out_done = nullptr;
     // per-kernel timing (zero_flat_profile_enable)
     bool profile = false;
     std::vector<cudaEvent_t> ev;      // 4 events per recorded step
@@ -204,6 +215,13 @@ cudaError_t mark(zero_flat *h, cudaStream_t s) {
 void release(zero_flat *h) {
     if (!h) return;
     DeviceGuard g(h->device);
+    h->pool.reset();
+    if (h->out_done) {
+        cudaEventSynchronize(h->out_done);        // copies may still read h_out
+        cudaEventDestroy(h->out_done);
+    }
+    if (h->h_g) cudaFreeHost(h->h_g);
+    if (h->h_out) cudaFreeHost(h->h_out);
     for (cudaEvent_t e : h->ev) cudaEventDestroy(e);
     cudaFree(h->d_state);
     cudaFree(h->d_bc);
@@ -444,19 +462,21 @@ int in_kind_of(const zero_flat *h) {
 
 // K1 as planned (contributions -> scratch rows, or an accumulator norm pass),
 // K2, K3 (from the scratch rows, or from the accumulators), with the timing
-// marks and the optional result read-back.  Called on the handle's device.
+// marks and the optional result read-back.  With host_g (the offload step)
+// K1 writes the gradient rows there and K3 and the last timing mark are left
+// to the caller.  Called on the handle's device.
 zero_status launch_step(zero_flat *h, zg::ReducePlan rp, zg::AdamPlan ap, double extra_norm_sq,
-                        cudaStream_t st, zero_step_result *res) {
+                        cudaStream_t st, zero_step_result *res, float *host_g = nullptr) {
     const int64_t S = h->shard;
     const int64_t batch = std::min<int64_t>(rp.n_ranks, zg::kMaxRanksPerLaunch);
     rp.grid_x = zg::grid_x_for(S, batch, h->sm_count, h->reduce_bps[rp.mode]);
     ap.grid_x = zg::grid_x_for(S, batch, h->sm_count,
                                ap.q8 ? zg::kAdamQ8BlocksPerSm : zg::kAdamBlocksPerSm);
     const int64_t parts = (int64_t)rp.grid_x * rp.n_ranks;
-    const int64_t rows = rp.mode == zg::kModeStep ? rp.n_ranks : 0;
+    const int64_t rows = rp.mode == zg::kModeStep && !host_g ? rp.n_ranks : 0;
     zero_status s = ensure_scratch(h, rows, parts);
     if (s) return s;
-    rp.g = h->d_g;
+    rp.g = host_g ? host_g : h->d_g;
     rp.g_stride = h->g_stride;
     rp.part_ss = h->d_part_ss;
     rp.part_of = h->d_part_of;
@@ -496,6 +516,7 @@ zero_status launch_step(zero_flat *h, zg::ReducePlan rp, zg::AdamPlan ap, double
     if ((e = mark(h, st))) return cuda_fail(e, "timing event");
     if ((e = zg::launch_finalize(f, st))) return cuda_fail(e, "finalize kernel launch");
     if ((e = mark(h, st))) return cuda_fail(e, "timing event");
+    if (host_g) return ZERO_OK;
     if ((e = zg::run_adamw(ap, st))) return cuda_fail(e, "adamw kernel launch");
     if ((e = mark(h, st))) return cuda_fail(e, "timing event");
     if (res) {
@@ -637,6 +658,205 @@ ZERO_API zero_status zero_shard_step_accumulated(zero_flat *h, const int32_t *ra
     ap.v = v;
     ap.out = flat_param_out;
     return launch_step(h, rp, ap, extra_norm_sq, (cudaStream_t)stream, res);
+}
+
+namespace {
+
+// Pinned host buffers and worker threads of the offload step, grown on demand.
+zero_status ensure_offload(zero_flat *h, int32_t n_ranks, int32_t n_threads) {
+    const int64_t S = h->shard;
+    if (n_ranks > h->h_g_rows) {
+        if (h->out_done) cudaEventSynchronize(h->out_done);
+        if (h->h_g) cudaFreeHost(h->h_g);
+        h->h_g = nullptr;
+        h->h_g_rows = 0;
+        int64_t bytes;
+        if (!mul_ok((int64_t)n_ranks, h->g_stride, &bytes) || !mul_ok(bytes, 4, &bytes))
+            return fail(ZERO_ERR_OVERFLOW_SIZE, "host gradient buffer size overflows");
+        if (bytes > 0) {
+            cudaError_t e = cudaHostAlloc((void **)&h->h_g, (size_t)bytes, cudaHostAllocPortable);
+            if (e) {
+                cudaGetLastError();
+                h->h_g = nullptr;
+                return fail(ZERO_ERR_NO_MEMORY, "cannot pin %lld bytes of host gradient rows: %s",
+                            (long long)bytes, cudaGetErrorString(e));
+            }
+        }
+        h->h_g_rows = n_ranks;
+    }
+    if (n_ranks > h->h_out_rows) {
+        if (h->out_done) cudaEventSynchronize(h->out_done);
+        if (h->h_out) cudaFreeHost(h->h_out);
+        h->h_out = nullptr;
+        h->h_out_rows = 0;
+        int64_t bytes;
+        if (!mul_ok((int64_t)n_ranks, S, &bytes) || !mul_ok(bytes, 2, &bytes))
+            return fail(ZERO_ERR_OVERFLOW_SIZE, "host parameter staging size overflows");
+        if (bytes > 0) {
+            cudaError_t e = cudaHostAlloc((void **)&h->h_out, (size_t)bytes, cudaHostAllocPortable);
+            if (e) {
+                cudaGetLastError();
+                h->h_out = nullptr;
+                return fail(ZERO_ERR_NO_MEMORY, "cannot pin %lld bytes of parameter staging: %s",
+                            (long long)bytes, cudaGetErrorString(e));
+            }
+        }
+        h->h_out_rows = n_ranks;
+    }
+    if (!h->out_done) {
+        cudaError_t e = cudaEventCreateWithFlags(&h->out_done, cudaEventDisableTiming);
+        if (e) { h->out_done = nullptr; return cuda_fail(e, "cudaEventCreate"); }
+    }
+    const int want = n_threads > 0 ? n_threads : zh::available_cpus();
+    if (!h->pool || h->pool->size() != want) {
+        h->pool.reset();
+        h->pool.reset(new (std::nothrow) zh::Pool(want));
+        if (!h->pool) return fail(ZERO_ERR_NO_MEMORY, "host thread pool");
+    }
+    return ZERO_OK;
+}
+
+// Elements per host task, and per parameter copy back to the device.
+constexpr int64_t kHostChunk = int64_t(1) << 16;
+constexpr int64_t kHostSegment = int64_t(1) << 24;
+
+// The host update of every stepped rank; each segment's 16-bit parameters are
+// copied to the device as soon as its last chunk is done.  Returns the first
+// copy error, if any.
+cudaError_t host_update(zero_flat *h, const zh::AdamScalars &k, const int32_t *ranks,
+                        int32_t n_ranks, float *const *master, float *const *m, float *const *v,
+                        void *flat_param_out, cudaStream_t st) {
+    const int64_t S = h->shard;
+    if (S == 0) return cudaSuccess;
+    const bool bf16 = h->param_dtype == ZERO_BF16;
+    const int64_t chunks_per_seg = kHostSegment / kHostChunk;
+    const int64_t segs = (S + kHostSegment - 1) / kHostSegment;
+    const int64_t chunks = (S + kHostChunk - 1) / kHostChunk;
+    std::unique_ptr<std::atomic<int64_t>[]> left(new std::atomic<int64_t>[n_ranks * segs]);
+    for (int64_t j = 0; j < n_ranks; ++j)
+        for (int64_t q = 0; q < segs; ++q) {
+            const int64_t c0 = q * chunks_per_seg;
+            left[j * segs + q].store(std::min(chunks_per_seg, chunks - c0));
+        }
+    std::atomic<int> err{0};
+    const int dev = h->device;
+    uint16_t *out16 = static_cast<uint16_t *>(flat_param_out);
+    const std::function<void(int64_t)> task = [&](int64_t t) {
+        const int64_t j = t / chunks, c = t % chunks;
+        const int64_t i0 = c * kHostChunk;
+        const int64_t n = std::min(kHostChunk, S - i0);
+        uint16_t *stage = h->h_out + j * S;
+        zh::adamw_cast_range(k, h->h_g + j * h->g_stride + i0, master[j] + i0, m[j] + i0,
+                             v[j] + i0, stage + i0, n, bf16);
+        const int64_t q = c / chunks_per_seg;
+        if (left[j * segs + q].fetch_sub(1) == 1) {           // segment complete
+            const int64_t s0 = q * kHostSegment;
+            const int64_t len = std::min(kHostSegment, S - s0);
+            cudaError_t e = cudaSetDevice(dev);
+            if (!e) e = cudaMemcpyAsync(out16 + (int64_t)ranks[j] * S + s0, stage + s0,
+                                        (size_t)len * 2, cudaMemcpyHostToDevice, st);
+            int none = 0;
+            if (e) err.compare_exchange_strong(none, (int)e);
+        }
+    };
+    h->pool->run(n_ranks * chunks, task);
+    return (cudaError_t)err.load();
+}
+
+}  // namespace
+
+ZERO_API zero_status zero_shard_step_offload(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                                             const void *grads, int64_t grad_ld,
+                                             int64_t grad_rank_offset_mul, float *const *master,
+                                             float *const *m, float *const *v,
+                                             void *flat_param_out, double extra_norm_sq,
+                                             int32_t n_threads, void *stream,
+                                             zero_step_result *res) {
+    if (!h) return fail(ZERO_ERR_INVALID_ARG, "handle is NULL");
+    int32_t max_rank = 0;
+    zero_status s;
+    if ((s = check_ranks(h, ranks, n_ranks, &max_rank))) return s;
+    if ((s = check_update(h, n_ranks, master, m, v, flat_param_out, extra_norm_sq))) return s;
+    if ((s = check_grads(h, grads, grad_ld, grad_rank_offset_mul, max_rank))) return s;
+    if (n_threads < 0) return fail(ZERO_ERR_INVALID_ARG, "n_threads must be >= 0");
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the handle's device");
+    if ((s = ensure_offload(h, n_ranks, n_threads))) return s;
+    const cudaStream_t st = (cudaStream_t)stream;
+    zg::ReducePlan rp;
+    rp.mode = zg::kModeStep;
+    rp.grads = grads;
+    rp.in_kind = in_kind_of(h);
+    rp.ld = grad_ld;
+    rp.rank_mul = grad_rank_offset_mul;
+    rp.ranks = ranks;
+    rp.n_ranks = n_ranks;
+    zg::AdamPlan ap;
+    if ((s = launch_step(h, rp, ap, extra_norm_sq, st, nullptr, h->h_g))) return s;
+    cudaError_t e = cudaMemcpyAsync(h->h_state, h->d_state, sizeof(zg::DevState),
+                                    cudaMemcpyDeviceToHost, st);
+    if (!e) e = cudaStreamSynchronize(st);
+    if (e) return cuda_fail(e, "reading the step decision");
+    const zg::DevState ds = *h->h_state;
+    if (!ds.res.skipped) {
+        // the previous call's copies (perhaps on another stream) read h_out
+        if ((e = cudaEventSynchronize(h->out_done))) return cuda_fail(e, "waiting for the last copies");
+        const zh::AdamScalars k{h->b1, h->b2, h->omb1, h->omb2, h->lr, h->eps, h->decay,
+                                ds.res.clip_coef, ds.bc1, ds.bc2};
+        if ((e = host_update(h, k, ranks, n_ranks, master, m, v, flat_param_out, st)))
+            return cuda_fail(e, "copying parameters to the device");
+        if ((e = cudaSetDevice(h->device))) return cuda_fail(e, "cudaSetDevice");
+        if ((e = cudaEventRecord(h->out_done, st))) return cuda_fail(e, "cudaEventRecord");
+    }
+    if ((e = mark(h, st))) return cuda_fail(e, "timing event");
+    if (res) {
+        res->overflow = ds.res.overflow;
+        res->skipped = ds.res.skipped;
+        res->grad_norm = ds.res.grad_norm;
+        res->clip_coef = ds.res.clip_coef;
+        res->scale_used = ds.res.scale_used;
+    }
+    return ZERO_OK;
+}
+
+ZERO_API zero_status zero_offload_adamw_host(const zero_hparams *hp, int64_t step_t,
+                                             float clip_coef, const float *g, float *master,
+                                             float *m, float *v, void *param_out, int64_t n,
+                                             zero_dtype param_dtype, int32_t n_threads) {
+    zero_status s;
+    if ((s = validate_hparams(hp))) return s;
+    if (n < 0) return fail(ZERO_ERR_INVALID_ARG, "n must be >= 0");
+    if (step_t < 1) return fail(ZERO_ERR_INVALID_ARG, "step_t must be >= 1");
+    if (n_threads < 0) return fail(ZERO_ERR_INVALID_ARG, "n_threads must be >= 0");
+    if (param_dtype != ZERO_F16 && param_dtype != ZERO_BF16)
+        return fail(ZERO_ERR_UNSUPPORTED_DTYPE, "param dtype must be ZERO_F16 or ZERO_BF16");
+    if (n > 0 && (!g || !master || !m || !v || !param_out))
+        return fail(ZERO_ERR_INVALID_ARG, "NULL array");
+    if ((uintptr_t)g % 4 || (uintptr_t)master % 4 || (uintptr_t)m % 4 || (uintptr_t)v % 4 ||
+        (uintptr_t)param_out % 2)
+        return fail(ZERO_ERR_ALIGNMENT, "fp32 arrays must be 4-byte and param_out 2-byte aligned");
+    if (n == 0) return ZERO_OK;
+    const zh::AdamScalars k{(float)hp->beta1, (float)hp->beta2, (float)(1.0 - hp->beta1),
+                            (float)(1.0 - hp->beta2), (float)hp->lr, (float)hp->eps,
+                            (float)(1.0 - hp->lr * hp->weight_decay), clip_coef,
+                            (float)(1.0 - std::pow(hp->beta1, (double)step_t)),
+                            (float)(1.0 - std::pow(hp->beta2, (double)step_t))};
+    const bool bf16 = param_dtype == ZERO_BF16;
+    uint16_t *out = static_cast<uint16_t *>(param_out);
+    const int want = n_threads > 0 ? n_threads : zh::available_cpus();
+    const int64_t chunks = (n + kHostChunk - 1) / kHostChunk;
+    const std::function<void(int64_t)> task = [&](int64_t c) {
+        const int64_t i0 = c * kHostChunk;
+        zh::adamw_cast_range(k, g + i0, master + i0, m + i0, v + i0, out + i0,
+                             std::min(kHostChunk, n - i0), bf16);
+    };
+    if (want <= 1 || chunks == 1) {
+        for (int64_t c = 0; c < chunks; ++c) task(c);
+        return ZERO_OK;
+    }
+    zh::Pool pool(std::min<int64_t>(want, chunks));
+    pool.run(chunks, task);
+    return ZERO_OK;
 }
 
 ZERO_API zero_status zero_flat_set_lr(zero_flat *h, double lr) {

@@ -36,7 +36,8 @@
  *     handle was created on; the caller owns every buffer it passes and keeps
  *     it alive until the work queued on `stream` has finished.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
- *   - The library needs the CUDA driver; it contains no CPU fallback.
+ *   - The library needs the CUDA driver; it contains no CPU fallback (the
+ *     host update of the offload mode is a mode the caller picks, below).
  *   - A handle is not thread-safe: calls on one handle must not overlap.
  */
 #ifndef ZERO_GB300_H
@@ -227,6 +228,54 @@ zero_status zero_shard_step_accumulated(zero_flat *h, const int32_t *ranks, int3
                                         const float *const *acc, float *const *master,
                                         float *const *m, float *const *v, void *flat_param_out,
                                         double extra_norm_sq, void *stream, zero_step_result *res);
+
+/* ZeRO-Offload shard step: the optimizer update runs on the host CPU cores
+ * ("DeepSpeed 与 FSDP" §ZeRO-Offload: the reduced gradients move to the CPU,
+ * the CPU updates the fp32 master weights with Adam, and the 16-bit weights
+ * move back to the GPU; ZeRO reading §4.1: optimizer states in CPU memory).
+ * On the GPU, as in zero_shard_step: the reduce, unscale, overflow check and
+ * norm partials, with the unscaled fp32 gradient rows written straight into a
+ * pinned host buffer that the handle owns; then the loss-scale decision, the
+ * clip coefficient and the bias corrections.  The call reads that decision
+ * back (one synchronization of `stream`).  If the step is applied,
+ * `n_threads` host threads (0: every CPU this process may run on) update
+ * master/m/v and write the 16-bit parameters into a pinned staging buffer;
+ * each finished segment is copied to flat_param_out[r * shard_size + ...] on
+ * `stream` at once.  The update is the same sequence of fp32 operations as
+ * zero_shard_step's, so the results are bit-identical to it.  This is the
+ * offload mode of the method, never a substitute for the GPU path: the
+ * reduce and the decision still need the GPU.
+ * master, m, v: HOST fp32 arrays (pageable or pinned), shard_size elements
+ * per stepped rank, 4-byte aligned; updated when the call returns.
+ * flat_param_out: device, as for zero_shard_step; its copies are queued on
+ * `stream` when the call returns.  grads and the rest: as zero_shard_step.
+ * Not capturable in a CUDA graph (host synchronization and host compute).
+ * Errors: as for zero_shard_step; INVALID_ARG for n_threads < 0; NO_MEMORY
+ * when the pinned buffers (6 bytes per stepped element) cannot be had. */
+zero_status zero_shard_step_offload(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                                    const void *grads, int64_t grad_ld,
+                                    int64_t grad_rank_offset_mul, float *const *master,
+                                    float *const *m, float *const *v, void *flat_param_out,
+                                    double extra_norm_sq, int32_t n_threads, void *stream,
+                                    zero_step_result *res);
+
+/* The host half of zero_shard_step_offload on its own, for a caller that
+ * reduces gradients elsewhere: for i < n, with gc = g[i] * clip_coef,
+ *     m = b1 m + (1-b1) gc;  v = b2 v + (1-b2) gc^2;
+ *     mh = m / (1 - b1^t);  vh = v / (1 - b2^t);
+ *     theta = theta (1 - lr wd) - (lr mh) / (sqrt(vh) + eps)
+ * ("DeepSpeed 与 FSDP" §ZeRO-Offload, with the decoupled decay of AdamW),
+ * each a single fp32 operation, the scalars rounded once to fp32 (1 - beta^t
+ * from fp64 pow, t = step_t, the count of applied steps including this one),
+ * then param_out[i] = the round-to-nearest-even 16-bit encoding of theta.
+ * All pointers are HOST memory: g, master, m, v fp32 (4-byte aligned),
+ * param_out 16-bit (2-byte aligned).  n_threads as above.  Needs no GPU.
+ * Errors: INVALID_ARG (NULL pointer with n > 0, n < 0, step_t < 1,
+ * n_threads < 0, bad hparams), UNSUPPORTED_DTYPE, ALIGNMENT. */
+zero_status zero_offload_adamw_host(const zero_hparams *hp, int64_t step_t, float clip_coef,
+                                    const float *g, float *master, float *m, float *v,
+                                    void *param_out, int64_t n, zero_dtype param_dtype,
+                                    int32_t n_threads);
 
 /* Change the learning rate for the steps launched after this call (a
  * schedule's warm-up or decay; the ZeRO reading §5.3 warns that warm-up must
