@@ -85,12 +85,15 @@ struct zero_flat {
     zg::DevState *h_state = nullptr;  // pinned staging for state reads
     uint64_t device_bytes = 0;
     // offload step: pinned host gradient rows and 16-bit staging, the host
-    // worker pool, and an event after the last parameter copy
+    // worker pool, the stream and per-segment events of the gradient copies
+    // to the host, and an event after the last parameter copy
     float *h_g = nullptr;
     int64_t h_g_rows = 0;
     uint16_t *h_out = nullptr;
     int64_t h_out_rows = 0;
     std::unique_ptr<zh::Pool> pool;
+    cudaStream_t copy_stream = nullptr;
+    std::vector<cudaEvent_t> seg_ev;
     cudaEvent_t out_done = nullptr;
     // per-kernel timing (zero_flat_profile_enable)
     bool profile = false;
@@ -220,6 +223,11 @@ void release(zero_flat *h) {
         cudaEventSynchronize(h->out_done);        // copies may still read h_out
         cudaEventDestroy(h->out_done);
     }
+    if (h->copy_stream) {
+        cudaStreamSynchronize(h->copy_stream);
+        cudaStreamDestroy(h->copy_stream);
+    }
+    for (cudaEvent_t e : h->seg_ev) cudaEventDestroy(e);
     if (h->h_g) cudaFreeHost(h->h_g);
     if (h->h_out) cudaFreeHost(h->h_out);
     for (cudaEvent_t e : h->ev) cudaEventDestroy(e);
@@ -462,21 +470,21 @@ int in_kind_of(const zero_flat *h) {
 
 // K1 as planned (contributions -> scratch rows, or an accumulator norm pass),
 // K2, K3 (from the scratch rows, or from the accumulators), with the timing
-// marks and the optional result read-back.  With host_g (the offload step)
-// K1 writes the gradient rows there and K3 and the last timing mark are left
-// to the caller.  Called on the handle's device.
+// marks and the optional result read-back.  With host_update (the offload
+// step) K3 and the last timing mark are left to the caller.  Called on the
+// handle's device.
 zero_status launch_step(zero_flat *h, zg::ReducePlan rp, zg::AdamPlan ap, double extra_norm_sq,
-                        cudaStream_t st, zero_step_result *res, float *host_g = nullptr) {
+                        cudaStream_t st, zero_step_result *res, bool host_update = false) {
     const int64_t S = h->shard;
     const int64_t batch = std::min<int64_t>(rp.n_ranks, zg::kMaxRanksPerLaunch);
     rp.grid_x = zg::grid_x_for(S, batch, h->sm_count, h->reduce_bps[rp.mode]);
     ap.grid_x = zg::grid_x_for(S, batch, h->sm_count,
                                ap.q8 ? zg::kAdamQ8BlocksPerSm : zg::kAdamBlocksPerSm);
     const int64_t parts = (int64_t)rp.grid_x * rp.n_ranks;
-    const int64_t rows = rp.mode == zg::kModeStep && !host_g ? rp.n_ranks : 0;
+    const int64_t rows = rp.mode == zg::kModeStep ? rp.n_ranks : 0;
     zero_status s = ensure_scratch(h, rows, parts);
     if (s) return s;
-    rp.g = host_g ? host_g : h->d_g;
+    rp.g = h->d_g;
     rp.g_stride = h->g_stride;
     rp.part_ss = h->d_part_ss;
     rp.part_of = h->d_part_of;
@@ -516,7 +524,7 @@ zero_status launch_step(zero_flat *h, zg::ReducePlan rp, zg::AdamPlan ap, double
     if ((e = mark(h, st))) return cuda_fail(e, "timing event");
     if ((e = zg::launch_finalize(f, st))) return cuda_fail(e, "finalize kernel launch");
     if ((e = mark(h, st))) return cuda_fail(e, "timing event");
-    if (host_g) return ZERO_OK;
+    if (host_update) return ZERO_OK;
     if ((e = zg::run_adamw(ap, st))) return cuda_fail(e, "adamw kernel launch");
     if ((e = mark(h, st))) return cuda_fail(e, "timing event");
     if (res) {
@@ -707,6 +715,10 @@ zero_status ensure_offload(zero_flat *h, int32_t n_ranks, int32_t n_threads) {
         cudaError_t e = cudaEventCreateWithFlags(&h->out_done, cudaEventDisableTiming);
         if (e) { h->out_done = nullptr; return cuda_fail(e, "cudaEventCreate"); }
     }
+    if (!h->copy_stream) {
+        cudaError_t e = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking);
+        if (e) { h->copy_stream = nullptr; return cuda_fail(e, "cudaStreamCreate"); }
+    }
     const int want = n_threads > 0 ? n_threads : zh::available_cpus();
     if (!h->pool || h->pool->size() != want) {
         h->pool.reset();
@@ -720,9 +732,11 @@ zero_status ensure_offload(zero_flat *h, int32_t n_ranks, int32_t n_threads) {
 constexpr int64_t kHostChunk = int64_t(1) << 16;
 constexpr int64_t kHostSegment = int64_t(1) << 24;
 
-// The host update of every stepped rank; each segment's 16-bit parameters are
-// copied to the device as soon as its last chunk is done.  Returns the first
-// copy error, if any.
+// The host update of every stepped rank.  The reduced gradient rows come
+// down from HBM segment by segment on the copy stream, and a host task waits
+// only for the segment it works on, so the copies overlap the update; each
+// segment's 16-bit parameters go back to the device on `st` as soon as its
+// last chunk is done.  Returns the first CUDA error, if any.
 cudaError_t host_update(zero_flat *h, const zh::AdamScalars &k, const int32_t *ranks,
                         int32_t n_ranks, float *const *master, float *const *m, float *const *v,
                         void *flat_param_out, cudaStream_t st) {
@@ -732,31 +746,56 @@ cudaError_t host_update(zero_flat *h, const zh::AdamScalars &k, const int32_t *r
     const int64_t chunks_per_seg = kHostSegment / kHostChunk;
     const int64_t segs = (S + kHostSegment - 1) / kHostSegment;
     const int64_t chunks = (S + kHostChunk - 1) / kHostChunk;
-    std::unique_ptr<std::atomic<int64_t>[]> left(new std::atomic<int64_t>[n_ranks * segs]);
+    const int64_t n_seg = n_ranks * segs;
+    cudaError_t e;
+    while ((int64_t)h->seg_ev.size() < n_seg) {
+        cudaEvent_t ev;
+        if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming))) return e;
+        h->seg_ev.push_back(ev);
+    }
     for (int64_t j = 0; j < n_ranks; ++j)
         for (int64_t q = 0; q < segs; ++q) {
-            const int64_t c0 = q * chunks_per_seg;
-            left[j * segs + q].store(std::min(chunks_per_seg, chunks - c0));
+            const int64_t s0 = q * kHostSegment, len = std::min(kHostSegment, S - s0);
+            const int64_t off = j * h->g_stride + s0;
+            if ((e = cudaMemcpyAsync(h->h_g + off, h->d_g + off, (size_t)len * 4,
+                                     cudaMemcpyDeviceToHost, h->copy_stream)))
+                return e;
+            if ((e = cudaEventRecord(h->seg_ev[j * segs + q], h->copy_stream))) return e;
+        }
+    std::unique_ptr<std::atomic<int64_t>[]> left(new std::atomic<int64_t>[n_seg]);
+    std::unique_ptr<std::atomic<int>[]> ready(new std::atomic<int>[n_seg]);
+    for (int64_t j = 0; j < n_ranks; ++j)
+        for (int64_t q = 0; q < segs; ++q) {
+            left[j * segs + q].store(std::min(chunks_per_seg, chunks - q * chunks_per_seg));
+            ready[j * segs + q].store(0);
         }
     std::atomic<int> err{0};
     const int dev = h->device;
     uint16_t *out16 = static_cast<uint16_t *>(flat_param_out);
+    auto note = [&](cudaError_t x) {
+        int none = 0;
+        if (x) err.compare_exchange_strong(none, (int)x);
+    };
     const std::function<void(int64_t)> task = [&](int64_t t) {
         const int64_t j = t / chunks, c = t % chunks;
+        const int64_t q = c / chunks_per_seg, sg = j * segs + q;
+        if (!ready[sg].load(std::memory_order_acquire)) {
+            const cudaError_t x = cudaEventSynchronize(h->seg_ev[sg]);
+            if (x) { note(x); return; }
+            ready[sg].store(1, std::memory_order_release);
+        }
         const int64_t i0 = c * kHostChunk;
         const int64_t n = std::min(kHostChunk, S - i0);
         uint16_t *stage = h->h_out + j * S;
         zh::adamw_cast_range(k, h->h_g + j * h->g_stride + i0, master[j] + i0, m[j] + i0,
                              v[j] + i0, stage + i0, n, bf16);
-        const int64_t q = c / chunks_per_seg;
-        if (left[j * segs + q].fetch_sub(1) == 1) {           // segment complete
+        if (left[sg].fetch_sub(1) == 1) {                      // segment complete
             const int64_t s0 = q * kHostSegment;
             const int64_t len = std::min(kHostSegment, S - s0);
-            cudaError_t e = cudaSetDevice(dev);
-            if (!e) e = cudaMemcpyAsync(out16 + (int64_t)ranks[j] * S + s0, stage + s0,
+            cudaError_t x = cudaSetDevice(dev);
+            if (!x) x = cudaMemcpyAsync(out16 + (int64_t)ranks[j] * S + s0, stage + s0,
                                         (size_t)len * 2, cudaMemcpyHostToDevice, st);
-            int none = 0;
-            if (e) err.compare_exchange_strong(none, (int)e);
+            note(x);
         }
     };
     h->pool->run(n_ranks * chunks, task);
@@ -792,7 +831,7 @@ ZERO_API zero_status zero_shard_step_offload(zero_flat *h, const int32_t *ranks,
     rp.ranks = ranks;
     rp.n_ranks = n_ranks;
     zg::AdamPlan ap;
-    if ((s = launch_step(h, rp, ap, extra_norm_sq, st, nullptr, h->h_g))) return s;
+    if ((s = launch_step(h, rp, ap, extra_norm_sq, st, nullptr, true))) return s;
     cudaError_t e = cudaMemcpyAsync(h->h_state, h->d_state, sizeof(zg::DevState),
                                     cudaMemcpyDeviceToHost, st);
     if (!e) e = cudaStreamSynchronize(st);

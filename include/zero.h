@@ -233,13 +233,14 @@ zero_status zero_shard_step_accumulated(zero_flat *h, const int32_t *ranks, int3
  * ("DeepSpeed 与 FSDP" §ZeRO-Offload: the reduced gradients move to the CPU,
  * the CPU updates the fp32 master weights with Adam, and the 16-bit weights
  * move back to the GPU; ZeRO reading §4.1: optimizer states in CPU memory).
- * On the GPU, as in zero_shard_step: the reduce, unscale, overflow check and
- * norm partials, with the unscaled fp32 gradient rows written straight into a
- * pinned host buffer that the handle owns; then the loss-scale decision, the
- * clip coefficient and the bias corrections.  The call reads that decision
- * back (one synchronization of `stream`).  If the step is applied,
- * `n_threads` host threads (0: every CPU this process may run on) update
- * master/m/v and write the 16-bit parameters into a pinned staging buffer;
+ * On the GPU, exactly as in zero_shard_step: the reduce, unscale, overflow
+ * check and norm partials into the handle's fp32 gradient rows, then the
+ * loss-scale decision, the clip coefficient and the bias corrections.  The
+ * call reads that decision back (one synchronization of `stream`).  If the
+ * step is applied, the gradient rows are copied to pinned host memory in
+ * segments on a stream of the handle, and `n_threads` host threads (0: every
+ * CPU this process may run on) update master/m/v segment by segment as the
+ * copies land, writing the 16-bit parameters into a pinned staging buffer;
  * each finished segment is copied to flat_param_out[r * shard_size + ...] on
  * `stream` at once.  The update is the same sequence of fp32 operations as
  * zero_shard_step's, so the results are bit-identical to it.  This is the
