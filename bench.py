@@ -597,16 +597,18 @@ def run_offload(args, w):
 
     N = w.world_size
     esize = 4 if w.grad_dtype == 2 else 2
-    # K1 reads the N contributions from HBM and writes the fp32 gradient rows
-    # (4 B/param) over the host link; the host update reads the gradient (4)
-    # and master/m/v (12), writes master/m/v (12) and the 16-bit param (2),
-    # whose copy to the device overlaps it.
+    # K1 reads the N contributions and writes the fp32 gradient rows in HBM.
+    # The host phase moves, in host memory: the DMA write of the gradient (4
+    # B/param), the CPU's reads of it (4) and of master/m/v (12), its writes
+    # of master/m/v (12) and of the 16-bit staging (2), and the DMA read of
+    # the staging (2) -- 36 B/param; over the link 4 B go down and 2 B up,
+    # overlapped with the update.
     kernels = {
-        "reduce_kernel": {"ms_mean": ms_red / max(nrec, 1), "bytes_per_param": N * esize + 4,
-                          "link_bytes_per_param": 4},
+        "reduce_kernel": {"ms_mean": ms_red / max(nrec, 1), "bytes_per_param": N * esize + 4},
         "finalize_kernel": {"ms_mean": ms_fin / max(nrec, 1), "bytes_per_param": 0},
-        "host_update": {"ms_mean": ms_host / max(nrec, 1), "bytes_per_param": 30,
-                        "link_bytes_per_param": 2},
+        "host_update": {"ms_mean": ms_host / max(nrec, 1), "bytes_per_param": 36,
+                        "cpu_bytes_per_param": 30, "dma_bytes_per_param": 6,
+                        "link_bytes_per_param": 6},
     }
     for k in kernels.values():
         k["achieved_gbs"] = (k["bytes_per_param"] * params / (k["ms_mean"] / 1e3) / 1e9
@@ -628,7 +630,7 @@ def run_offload(args, w):
                          "achieved": hu["achieved_gbs"], "peak": peak, "unit": "GB/s",
                          "frac": hu["achieved_gbs"] / peak if hu["achieved_gbs"] else None,
                          "peak_kind": "measured here: torch CPU copy on %d threads" % threads,
-                         "traffic": None, "bytes_per_launch": 30 * params},
+                         "traffic": None, "bytes_per_launch": 36 * params},
             "cpu_baseline": None, "e2e": None, "clocks": clocks,
             "gpu_launches": (n_batches + 1) * args.steps,
         }
