@@ -66,6 +66,7 @@ struct zero_flat {
     int device = 0;
     int sm_count = 0;
     int reduce_bps[4] = {1, 1, 1, 1}; // resident reduce blocks per SM, per ReduceMode
+    int staged_bps[3] = {1, 1, 1};    // the same for the staged reduce (no kModeNormOnly)
     int32_t world = 1;
     zero_dtype grad_dtype = ZERO_F16, param_dtype = ZERO_F16;
     zero_reduce_op op = ZERO_AVG;
@@ -341,7 +342,8 @@ ZERO_API zero_status zero_flat_init(const zero_param_info *infos, int32_t n_info
         const int kind = grad_dtype == ZERO_F32 ? zg::kInF32
                        : (grad_dtype == ZERO_BF16 ? zg::kInBF16 : zg::kInF16);
         for (int mode = 0; mode < 4; ++mode) {
-            e = zg::reduce_blocks_per_sm(kind, mode, &h->reduce_bps[mode]);
+            e = zg::reduce_blocks_per_sm(kind, mode, false, &h->reduce_bps[mode]);
+            if (!e && mode < 3) e = zg::reduce_blocks_per_sm(kind, mode, true, &h->staged_bps[mode]);
             if (e) { delete h; return cuda_fail(e, "occupancy query"); }
         }
     }
@@ -468,6 +470,14 @@ int in_kind_of(const zero_flat *h) {
     return h->grad_dtype == ZERO_F32 ? zg::kInF32 : (h->grad_dtype == ZERO_BF16 ? zg::kInBF16 : zg::kInF16);
 }
 
+// A kernel gave up a bounded wait (the step it belonged to was skipped):
+// clear the device error word and report it.
+zero_status take_device_error(zero_flat *h, cudaStream_t st) {
+    cudaMemsetAsync(&h->d_state->error, 0, sizeof(int32_t), st);
+    cudaStreamSynchronize(st);
+    return fail(ZERO_ERR_TIMEOUT, "a kernel gave up waiting for its bulk copies; the step was skipped");
+}
+
 // K1 as planned (contributions -> scratch rows, or an accumulator norm pass),
 // K2, K3 (from the scratch rows, or from the accumulators), with the timing
 // marks and the optional result read-back.  With host_update (the offload
@@ -477,7 +487,11 @@ zero_status launch_step(zero_flat *h, zg::ReducePlan rp, zg::AdamPlan ap, double
                         cudaStream_t st, zero_step_result *res, bool host_update = false) {
     const int64_t S = h->shard;
     const int64_t batch = std::min<int64_t>(rp.n_ranks, zg::kMaxRanksPerLaunch);
-    rp.grid_x = zg::grid_x_for(S, batch, h->sm_count, h->reduce_bps[rp.mode]);
+    rp.S = S;
+    rp.n_contrib = h->world;
+    rp.staged = zg::reduce_wants_staging(rp);
+    rp.grid_x = zg::grid_x_for(S, batch, h->sm_count,
+                               rp.staged ? h->staged_bps[rp.mode] : h->reduce_bps[rp.mode]);
     ap.grid_x = zg::grid_x_for(S, batch, h->sm_count,
                                ap.q8 ? zg::kAdamQ8BlocksPerSm : zg::kAdamBlocksPerSm);
     const int64_t parts = (int64_t)rp.grid_x * rp.n_ranks;
@@ -536,6 +550,7 @@ zero_status launch_step(zero_flat *h, zg::ReducePlan rp, zg::AdamPlan ap, double
         res->grad_norm = h->h_state->res.grad_norm;
         res->clip_coef = h->h_state->res.clip_coef;
         res->scale_used = h->h_state->res.scale_used;
+        if (h->h_state->error) return take_device_error(h, st);
     }
     return ZERO_OK;
 }
@@ -632,8 +647,10 @@ ZERO_API zero_status zero_grad_accumulate(zero_flat *h, const int32_t *ranks, in
     rp.n_contrib = h->world;
     rp.avg = h->op == ZERO_AVG;
     rp.st = h->d_state;
+    rp.staged = zg::reduce_wants_staging(rp);
     const int64_t batch = std::min<int64_t>(n_ranks, zg::kMaxRanksPerLaunch);
-    rp.grid_x = zg::grid_x_for(h->shard, batch, h->sm_count, h->reduce_bps[rp.mode]);
+    rp.grid_x = zg::grid_x_for(h->shard, batch, h->sm_count,
+                               rp.staged ? h->staged_bps[rp.mode] : h->reduce_bps[rp.mode]);
     const cudaError_t e = zg::run_reduce(rp, (cudaStream_t)stream);
     if (e) return cuda_fail(e, "accumulate kernel launch");
     return ZERO_OK;
@@ -837,6 +854,7 @@ ZERO_API zero_status zero_shard_step_offload(zero_flat *h, const int32_t *ranks,
     if (!e) e = cudaStreamSynchronize(st);
     if (e) return cuda_fail(e, "reading the step decision");
     const zg::DevState ds = *h->h_state;
+    if (ds.error) return take_device_error(h, st);
     if (!ds.res.skipped) {
         // the previous call's copies (perhaps on another stream) read h_out
         if ((e = cudaEventSynchronize(h->out_done))) return cuda_fail(e, "waiting for the last copies");

@@ -7,6 +7,9 @@
 //                       reduce-scatter: "PyTorch FSDP ... 深度解析" §3.3;
 //                       sum-then-split in the numpy demo of "DeepSpeed 与
 //                       FSDP"; fp32 reduce per its MixedPrecision example).
+//   K1 reduce_staged_kernel  the same for contributor rows that are not
+//                       64-byte aligned: TMA bulk copies of aligned spans into
+//                       shared memory, re-aligned there.
 //   K2 finalize_kernel  one block: fixed-order total of the partials, global
 //                       norm, clip coefficient, overflow skip and the dynamic
 //                       loss-scale state machine (ZeRO reading §5.1, §5.3).
@@ -403,6 +406,314 @@ reduce_kernel(const __grid_constant__ ReduceArgs a) {
     }
 }
 
+// ------------------------------------------------------------------ K1, staged
+// The reduce for contributor rows whose starts are not 64-byte aligned.  For
+// each block tile (kStageTile elements) and contributor row, one bulk copy
+// (TMA, cp.async.bulk) brings the 64-byte-aligned span of global memory that
+// covers the tile into a shared-memory slot, so DRAM sees only whole 64-byte
+// units.  A thread then re-aligns its 8 elements from the slot (one 16-byte
+// shared load when the row's offset is a multiple of 16 bytes, else two and a
+// funnel shift).  Rows come in groups of kRows per stage, two stages in
+// flight, completion tracked by one mbarrier per stage.  The arithmetic per
+// element is that of reduce_kernel: contributions added in contributor order.
+// Every mbarrier wait is bounded (one second); a block that gives up sets the
+// error word, counts as an overflow (so the step is skipped) and waits, again
+// bounded, for its copies before it exits.
+template <int kIn> struct StageTraits {
+    static constexpr int kE = kIn == kInF32 ? 4 : 2;          // bytes per element
+    static constexpr int kRows = kIn == kInF32 ? 4 : 8;       // rows per stage
+    static constexpr int kSlot = kStageTile * kE + 64;        // bytes per row slot
+    static constexpr int kStages = 2;
+    static constexpr int kHeader = 128;                       // the mbarriers
+    static constexpr int kSmem = kHeader + kStages * kRows * kSlot;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait for the phase of `parity` to complete, for at most one second.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_test(bar, parity))
+        if (global_ns() - t0 > 1000000000ull) return false;
+    return true;
+}
+// Order this thread's earlier generic-proxy accesses of shared memory before
+// later async-proxy (bulk copy) writes to it.
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Bytes [o, o + 16) of the 32 bytes lo:hi (o a multiple of 2, below 16).
+__device__ __forceinline__ uint4 bytes_at(const uint4 &lo, const uint4 &hi, uint32_t o) {
+    const uint32_t u[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    const uint32_t s = (o & 3u) * 8u;
+    uint4 r;
+    switch (o >> 2) {                  // uniform across the block for a given row
+        case 0:
+            r = make_uint4(__funnelshift_r(u[0], u[1], s), __funnelshift_r(u[1], u[2], s),
+                           __funnelshift_r(u[2], u[3], s), __funnelshift_r(u[3], u[4], s));
+            break;
+        case 1:
+            r = make_uint4(__funnelshift_r(u[1], u[2], s), __funnelshift_r(u[2], u[3], s),
+                           __funnelshift_r(u[3], u[4], s), __funnelshift_r(u[4], u[5], s));
+            break;
+        case 2:
+            r = make_uint4(__funnelshift_r(u[2], u[3], s), __funnelshift_r(u[3], u[4], s),
+                           __funnelshift_r(u[4], u[5], s), __funnelshift_r(u[5], u[6], s));
+            break;
+        default:
+            r = make_uint4(__funnelshift_r(u[3], u[4], s), __funnelshift_r(u[4], u[5], s),
+                           __funnelshift_r(u[5], u[6], s), __funnelshift_r(u[6], u[7], s));
+            break;
+    }
+    return r;
+}
+
+// This thread's 8 elements of one staged row, as fp32: the row's tile starts
+// d bytes into its slot (d < 64, a multiple of the element size).
+template <int kIn>
+__device__ __forceinline__ void staged_elems(const unsigned char *slot, uint32_t d, float f[kVec]) {
+    if constexpr (kIn == kInF32) {
+        const uint32_t off = d + threadIdx.x * 32u;
+        const uint32_t o = d & 15u;
+        uint4 w0, w1;
+        if (o == 0) {
+            w0 = *reinterpret_cast<const uint4 *>(slot + off);
+            w1 = *reinterpret_cast<const uint4 *>(slot + off + 16);
+        } else {
+            const unsigned char *p = slot + off - o;
+            const uint4 a0 = *reinterpret_cast<const uint4 *>(p);
+            const uint4 a1 = *reinterpret_cast<const uint4 *>(p + 16);
+            const uint4 a2 = *reinterpret_cast<const uint4 *>(p + 32);
+            w0 = bytes_at(a0, a1, o);
+            w1 = bytes_at(a1, a2, o);
+        }
+        const uint4 w[2] = {w0, w1};
+        words_to_f32<kInF32>(w, f);
+    } else {
+        const uint32_t off = d + threadIdx.x * 16u;
+        const uint32_t o = d & 15u;
+        uint4 w;
+        if (o == 0) {
+            w = *reinterpret_cast<const uint4 *>(slot + off);
+        } else {
+            const unsigned char *p = slot + off - o;
+            w = bytes_at(*reinterpret_cast<const uint4 *>(p),
+                         *reinterpret_cast<const uint4 *>(p + 16), o);
+        }
+        const uint4 ws[1] = {w};
+        words_to_f32<kIn>(ws, f);
+    }
+}
+
+template <int kIn, int kMode>
+__global__ void __launch_bounds__(kBlock, 3) reduce_staged_kernel(const __grid_constant__ ReduceArgs a) {
+    using T = typename InTraits<kIn>::T;
+    using ST = StageTraits<kIn>;
+    constexpr int kE = ST::kE, kR = ST::kRows, kSlot = ST::kSlot;
+    constexpr bool kNorm = kMode == kModeStep;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const uint32_t bar0 = smem_u32(smem);                     // stage s barrier at bar0 + 8*s
+    unsigned char *slots = smem + ST::kHeader;
+
+    const int j = blockIdx.y;
+    const int64_t S = a.S;
+    int64_t valid = a.full_numel - a.first[j];
+    valid = valid < 0 ? 0 : (valid > S ? S : valid);
+    const T *base = static_cast<const T *>(a.in[j]);
+    const unsigned char *bbase = static_cast<const unsigned char *>(a.in[j]);
+    float *g = a.g + (int64_t)j * a.g_stride;
+    float *acc_out = a.acc[j];
+    const int N = a.n_contrib;
+    const int64_t ld = a.ld;
+    const bool avg = a.avg != 0;
+    const Divisor dn = make_divisor((float)N);
+    const Divisor ds = make_divisor(kNorm ? a.st->scaler.scale : 1.0f);
+    auto finish = [&](float x) { return avg ? divide(x, dn) : x; };
+
+    const int groups = (N + kR - 1) / kR;
+    const int64_t n_tiles = valid / kStageTile;
+    const int64_t my_tiles =
+        (int64_t)blockIdx.x < n_tiles ? (n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int64_t n_jobs = my_tiles * groups;           // job = (tile of this block, row group)
+
+    // byte address of row c's element i (of this rank's slice)
+    auto row_addr = [&](int c, int64_t i) {
+        return bbase + ((int64_t)c * ld + i) * kE;
+    };
+    auto issue = [&](int64_t job, int stage) {          // thread 0
+        const int64_t q = job / groups;
+        const int gi = (int)(job - q * groups);
+        const int64_t i0 = (blockIdx.x + q * gridDim.x) * (int64_t)kStageTile;
+        const int c0 = gi * kR;
+        const int nr = N - c0 < kR ? N - c0 : kR;
+        uint32_t total = 0;
+        for (int r = 0; r < nr; ++r) {
+            const uintptr_t A = (uintptr_t)row_addr(c0 + r, i0);
+            const uintptr_t lo = A & ~(uintptr_t)63;
+            const uintptr_t hi = (A + (uintptr_t)kStageTile * kE + 63) & ~(uintptr_t)63;
+            total += (uint32_t)(hi - lo);
+        }
+        const uint32_t bar = bar0 + 8u * stage;
+        mbar_expect_tx(bar, total);
+        for (int r = 0; r < nr; ++r) {
+            const uintptr_t A = (uintptr_t)row_addr(c0 + r, i0);
+            const uintptr_t lo = A & ~(uintptr_t)63;
+            const uintptr_t hi = (A + (uintptr_t)kStageTile * kE + 63) & ~(uintptr_t)63;
+            bulk_g2s(smem_u32(slots + (stage * kR + r) * kSlot), reinterpret_cast<const void *>(lo),
+                     (uint32_t)(hi - lo), bar);
+        }
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar0, 1);
+        mbar_init(bar0 + 8, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (n_jobs > 0) issue(0, 0);
+        if (n_jobs > 1) issue(1, 1);
+    }
+
+    NormAcc na;
+    int of = 0;
+    float x[kVec];
+    uint32_t parity = 0u;                                       // bit s: stage s's wait parity
+    int64_t job = 0;
+    bool failed = false;
+    bool my_ok = true;                                          // this thread's last wait
+    for (; job < n_jobs; ++job) {
+        const int stage = (int)(job & 1);
+        my_ok = mbar_wait_bounded(bar0 + 8u * stage, (parity >> stage) & 1u);
+        if (my_ok) {
+            parity ^= 1u << stage;
+            const int64_t q = job / groups;
+            const int gi = (int)(job - q * groups);
+            const int64_t t0 = (blockIdx.x + q * gridDim.x) * (int64_t)kStageTile;
+            const int c0 = gi * kR;
+            if (gi == 0) {
+#pragma unroll
+                for (int e = 0; e < kVec; ++e) x[e] = 0.0f;
+            }
+#pragma unroll
+            for (int r = 0; r < kR; ++r) {
+                if (c0 + r < N) {                               // contributor order
+                    const uint32_t d = (uint32_t)((uintptr_t)row_addr(c0 + r, t0) & 63u);
+                    float f[kVec];
+                    staged_elems<kIn>(slots + (stage * kR + r) * kSlot, d, f);
+#pragma unroll
+                    for (int e = 0; e < kVec; ++e) x[e] = __fadd_rn(x[e], f[e]);
+                }
+            }
+            if (gi == groups - 1) {                             // the tile's elements are reduced
+                const int64_t i0 = t0 + (int64_t)threadIdx.x * kVec;
+#pragma unroll
+                for (int e = 0; e < kVec; ++e) x[e] = finish(x[e]);
+                if constexpr (kNorm) {
+#pragma unroll
+                    for (int e = 0; e < kVec; ++e) {
+                        x[e] = divide(x[e], ds);
+                        of |= !isfinite(x[e]);
+                    }
+                    na.add_chunk(x);
+                    st_f4(g + i0, make_float4(x[0], x[1], x[2], x[3]));
+                    st_f4(g + i0 + 4, make_float4(x[4], x[5], x[6], x[7]));
+                } else {
+                    if constexpr (kMode == kModeAccAdd) {
+                        const float4 o0 = ld_f4(acc_out + i0), o1 = ld_f4(acc_out + i0 + 4);
+                        const float o[kVec] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+#pragma unroll
+                        for (int e = 0; e < kVec; ++e) x[e] = __fadd_rn(o[e], x[e]);
+                    }
+                    st_f4(acc_out + i0, make_float4(x[0], x[1], x[2], x[3]));
+                    st_f4(acc_out + i0 + 4, make_float4(x[4], x[5], x[6], x[7]));
+                }
+            }
+        }
+        // one barrier per job: every read of the stage is done (it may be
+        // refilled) and a timed-out wait anywhere in the block is seen by all
+        if (__syncthreads_or(!my_ok)) { failed = true; break; }
+        if (threadIdx.x == 0 && job + 2 < n_jobs) {
+            fence_proxy_async();
+            issue(job + 2, stage);
+        }
+    }
+    if (failed) {
+        // give the copies still in flight a bounded chance to land before the
+        // block's shared memory goes away: this job's (unless thread 0 saw it
+        // complete) and the next one's
+        if (threadIdx.x == 0) {
+            for (int64_t k = my_ok ? job + 1 : job; k < job + 2 && k < n_jobs; ++k)
+                mbar_wait_bounded(bar0 + 8u * (uint32_t)(k & 1), (parity >> (k & 1)) & 1u);
+            atomicExch(a.err, 1);
+        }
+        of = 1;
+        __syncthreads();
+    }
+
+    // ragged tail (elements past the last full tile) and padding, as in reduce_kernel
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = n_tiles * kStageTile + tid; i < valid; i += nthreads) {
+        float y = 0.0f;
+        for (int c = 0; c < N; ++c) y = __fadd_rn(y, elem_to_f32<kIn>(base + (int64_t)c * ld + i));
+        y = finish(y);
+        if constexpr (kNorm) {
+            y = divide(y, ds);
+            of |= !isfinite(y);
+            na.add_exact(y);
+            g[i] = y;
+        }
+        if constexpr (kMode == kModeAccFirst) acc_out[i] = y;
+        if constexpr (kMode == kModeAccAdd) acc_out[i] = __fadd_rn(acc_out[i], y);
+    }
+    for (int64_t i = valid + tid; i < S; i += nthreads) {
+        if constexpr (kMode == kModeStep) g[i] = 0.0f;
+        if constexpr (kMode == kModeAccFirst) acc_out[i] = 0.0f;
+        if constexpr (kMode == kModeAccAdd) acc_out[i] = __fadd_rn(acc_out[i], 0.0f);
+    }
+    if constexpr (kNorm) {
+        const int64_t pidx = a.part_base + (int64_t)j * gridDim.x + blockIdx.x;
+        block_partial(na.total(), of, a.part_ss + pidx, a.part_of + pidx);
+    }
+}
+
 // ------------------------------------------------------------------ K2
 __global__ void __launch_bounds__(kFinalizeThreads) finalize_kernel(const __grid_constant__ FinalizeArgs a) {
     __shared__ double warp_ss[kFinalizeThreads / 32];
@@ -711,8 +1022,27 @@ __global__ void __launch_bounds__(kBlock) adamw_q8_kernel(const __grid_constant_
 
 }  // namespace
 
+template <int kIn, int kMode>
+static cudaError_t launch_staged(const ReduceArgs &a, dim3 grid, cudaStream_t s) {
+    constexpr int kSmem = StageTraits<kIn>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(reduce_staged_kernel<kIn, kMode>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    reduce_staged_kernel<kIn, kMode><<<grid, kBlock, kSmem, s>>>(a);
+    return cudaGetLastError();
+}
+
 template <int kIn>
-static cudaError_t launch_reduce_in(const ReduceArgs &a, dim3 grid, int mode, cudaStream_t s) {
+static cudaError_t launch_reduce_in(const ReduceArgs &a, dim3 grid, int mode, bool staged,
+                                    cudaStream_t s) {
+    if (staged) {
+        switch (mode) {
+            case kModeStep: return launch_staged<kIn, kModeStep>(a, grid, s);
+            case kModeAccFirst: return launch_staged<kIn, kModeAccFirst>(a, grid, s);
+            case kModeAccAdd: return launch_staged<kIn, kModeAccAdd>(a, grid, s);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (mode) {
         case kModeStep: reduce_kernel<kIn, kModeStep><<<grid, kBlock, 0, s>>>(a); break;
         case kModeAccFirst: reduce_kernel<kIn, kModeAccFirst><<<grid, kBlock, 0, s>>>(a); break;
@@ -722,18 +1052,34 @@ static cudaError_t launch_reduce_in(const ReduceArgs &a, dim3 grid, int mode, cu
     return cudaGetLastError();
 }
 
-cudaError_t launch_reduce(const ReduceArgs &a, int grid_x, int in_kind, int mode, cudaStream_t s) {
+cudaError_t launch_reduce(const ReduceArgs &a, int grid_x, int in_kind, int mode, bool staged,
+                          cudaStream_t s) {
     const dim3 grid((unsigned)grid_x, (unsigned)a.n_ranks);
     if (mode == kModeNormOnly) {
+        if (staged) return cudaErrorInvalidValue;
         reduce_kernel<kInF32, kModeNormOnly><<<grid, kBlock, 0, s>>>(a);
         return cudaGetLastError();
     }
     switch (in_kind) {
-        case kInF16: return launch_reduce_in<kInF16>(a, grid, mode, s);
-        case kInBF16: return launch_reduce_in<kInBF16>(a, grid, mode, s);
-        case kInF32: return launch_reduce_in<kInF32>(a, grid, mode, s);
+        case kInF16: return launch_reduce_in<kInF16>(a, grid, mode, staged, s);
+        case kInBF16: return launch_reduce_in<kInBF16>(a, grid, mode, staged, s);
+        case kInF32: return launch_reduce_in<kInF32>(a, grid, mode, staged, s);
     }
     return cudaErrorInvalidValue;
+}
+
+bool reduce_wants_staging(const ReducePlan &p) {
+    if (p.mode == kModeNormOnly || p.S < kStageTile || !p.grads) return false;
+    const size_t esize = p.in_kind == kInF32 ? 4 : 2;
+    const bool rows_vary = p.n_contrib > 1 && ((size_t)p.ld * esize) % 64 != 0;
+    bool any = false;
+    for (int32_t j = 0; j < p.n_ranks; ++j) {
+        const uintptr_t base = (uintptr_t)p.grads + (uintptr_t)(p.ranks[j] * p.rank_mul) * esize;
+        any = any || rows_vary || base % 64 != 0;
+        if ((p.mode == kModeAccFirst || p.mode == kModeAccAdd) && (uintptr_t)p.acc_out[j] % 16)
+            return false;
+    }
+    return any;
 }
 
 cudaError_t launch_finalize(const FinalizeArgs &a, cudaStream_t s) {
@@ -773,6 +1119,7 @@ cudaError_t run_reduce(const ReducePlan &p, cudaStream_t s) {
         a.avg = p.mode == kModeNormOnly ? 0 : p.avg;
         a.n_ranks = nb;
         a.st = p.st;
+        a.err = p.st ? const_cast<int32_t *>(&p.st->error) : nullptr;
         for (int32_t j = 0; j < nb; ++j) {
             const int64_t r = p.ranks[b0 + j];
             bool vec;
@@ -790,7 +1137,7 @@ cudaError_t run_reduce(const ReducePlan &p, cudaStream_t s) {
             a.first[j] = r * p.S;
             a.vec[j] = vec;
         }
-        const cudaError_t e = launch_reduce(a, p.grid_x, p.in_kind, p.mode, s);
+        const cudaError_t e = launch_reduce(a, p.grid_x, p.in_kind, p.mode, p.staged, s);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -842,21 +1189,32 @@ cudaError_t run_adamw(const AdamPlan &p, cudaStream_t s) {
 }
 
 template <int kIn, int kMode>
-static cudaError_t occ(int *bps) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, reduce_kernel<kIn, kMode>, kBlock, 0);
+static cudaError_t occ(bool staged, int *bps) {
+    if (!staged)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, reduce_kernel<kIn, kMode>, kBlock, 0);
+    if constexpr (kMode == kModeNormOnly) {
+        return cudaErrorInvalidValue;
+    } else {
+        constexpr int kSmem = StageTraits<kIn>::kSmem;
+        cudaError_t e = cudaFuncSetAttribute(reduce_staged_kernel<kIn, kMode>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e != cudaSuccess) return e;
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, reduce_staged_kernel<kIn, kMode>,
+                                                             kBlock, kSmem);
+    }
 }
 
-cudaError_t reduce_blocks_per_sm(int in_kind, int mode, int *bps) {
+cudaError_t reduce_blocks_per_sm(int in_kind, int mode, bool staged, int *bps) {
     cudaError_t e = cudaErrorInvalidValue;
     *bps = 1;
     if (mode == kModeNormOnly) {
-        e = occ<kInF32, kModeNormOnly>(bps);
+        e = occ<kInF32, kModeNormOnly>(staged, bps);
     } else {
-#define ZG_OCC(K)                                                    \
-        switch (mode) {                                              \
-            case kModeStep: e = occ<K, kModeStep>(bps); break;       \
-            case kModeAccFirst: e = occ<K, kModeAccFirst>(bps); break; \
-            case kModeAccAdd: e = occ<K, kModeAccAdd>(bps); break;   \
+#define ZG_OCC(K)                                                            \
+        switch (mode) {                                                      \
+            case kModeStep: e = occ<K, kModeStep>(staged, bps); break;       \
+            case kModeAccFirst: e = occ<K, kModeAccFirst>(staged, bps); break; \
+            case kModeAccAdd: e = occ<K, kModeAccAdd>(staged, bps); break;   \
         }
         if (in_kind == kInF16) { ZG_OCC(kInF16) }
         else if (in_kind == kInBF16) { ZG_OCC(kInBF16) }

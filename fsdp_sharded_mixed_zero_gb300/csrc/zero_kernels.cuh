@@ -37,7 +37,8 @@ struct DevState {
     ResultDev res;
     float bc1, bc2;                   // bias corrections of this step (1 - beta^t)
     int32_t bc_saturated;             // t ran past the table: both corrections are 1
-    int32_t pad;
+    int32_t error;                    // nonzero: a kernel gave up a bounded wait (the
+                                      // step is then skipped as if it had overflowed)
 };
 
 // Elements per int8 quantization block of the all-gather payload (one warp's
@@ -75,7 +76,11 @@ struct ReduceArgs {
     float *acc[kMaxRanksPerLaunch];       // kModeAccFirst / kModeAccAdd: rank j's accumulator
     int64_t first[kMaxRanksPerLaunch];    // r * S (flat index of the shard's element 0)
     uint8_t vec[kMaxRanksPerLaunch];      // 16-byte-aligned rows: vector path
+    int32_t *err;                         // staged kernel: set on a timed-out wait
 };
+
+// Elements per block tile of the staged reduce (one 8-element chunk per thread).
+constexpr int kStageTile = kBlock * kVec;
 
 // K2: one block; deterministic total of the partials, norm, clip, loss scale.
 struct FinalizeArgs {
@@ -116,8 +121,11 @@ struct AdamArgs {
 };
 
 // in_kind: InKind; mode: ReduceMode.  from_acc: g = acc / scale_used, with
-// padding elements (flat index >= full_numel) taken as zero.
-cudaError_t launch_reduce(const ReduceArgs &a, int grid_x, int in_kind, int mode, cudaStream_t s);
+// padding elements (flat index >= full_numel) taken as zero.  staged: the
+// TMA-staged reduce for rows that are not 64-byte aligned (modes Step,
+// AccFirst and AccAdd).
+cudaError_t launch_reduce(const ReduceArgs &a, int grid_x, int in_kind, int mode, bool staged,
+                          cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeArgs &a, cudaStream_t s);
 cudaError_t launch_adamw(const AdamArgs &a, int grid_x, bool bf16_out, bool from_acc,
                          cudaStream_t s);
@@ -146,8 +154,18 @@ struct ReducePlan {
     int32_t avg = 0;
     const DevState *st = nullptr;
     int grid_x = 1;
+    bool staged = false;              // reduce_wants_staging(*this), decided before grid_x
 };
 cudaError_t run_reduce(const ReducePlan &p, cudaStream_t s);
+
+// Whether a plan's contributions should go through the staged reduce: some
+// stepped rank has a contributor row whose start is not 64-byte aligned, and
+// the shard holds at least one full tile.  (A 16-byte vector load that
+// starts inside a 64-byte DRAM access unit makes the unit's other half a
+// separate request, which is fetched again: 7 % extra traffic with 32-byte
+// aligned rows; 2-byte aligned rows cannot use vector loads at all.)  Plans
+// whose accumulators are not 16-byte aligned stay on the plain kernel.
+bool reduce_wants_staging(const ReducePlan &p);
 
 struct AdamPlan {
     const float *g = nullptr;         // scratch rows (g_stride floats per stepped rank), or
@@ -179,7 +197,7 @@ constexpr int kAdamBlocksPerSm = 2;
 constexpr int kAdamQ8BlocksPerSm = 3;    // AdamW + int8 payload (72 registers): 6.10 ms vs 6.90 at two
 
 // Resident blocks per SM of one reduce-kernel instance (occupancy API).
-cudaError_t reduce_blocks_per_sm(int in_kind, int mode, int *bps);
+cudaError_t reduce_blocks_per_sm(int in_kind, int mode, bool staged, int *bps);
 
 inline int grid_x_for(int64_t S, int64_t ranks_in_launch, int sm_count, int blocks_per_sm) {
     const int64_t chunks = (S + kVec - 1) / kVec;

@@ -61,6 +61,7 @@ struct DeviceSetup {
     unsigned char *base;              // device address of g_noalloc_scratch
     int sm_count;
     int reduce_bps[3];                // per contribution encoding (InKind)
+    int staged_bps[3];                // the staged reduce, per encoding
 };
 DeviceSetup g_setup[kMaxDevices];
 std::mutex g_setup_mu;
@@ -90,7 +91,9 @@ zero_status setup_device(int dev, const DeviceSetup **out) {
         e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
         for (int kind = 0; kind < 3; ++kind) {
-            e = zg::reduce_blocks_per_sm(kind, zg::kModeStep, &d.reduce_bps[kind]);
+            e = zg::reduce_blocks_per_sm(kind, zg::kModeStep, false, &d.reduce_bps[kind]);
+            if (e == cudaSuccess)
+                e = zg::reduce_blocks_per_sm(kind, zg::kModeStep, true, &d.staged_bps[kind]);
             if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
         }
         d.base = static_cast<unsigned char *>(p);
@@ -259,7 +262,19 @@ ZERO_API zero_status zero_shard_step_noalloc(
     // ---- launch geometry (as zero_shard_step computes it)
     const int in_kind = grad_dtype == ZERO_F32 ? zg::kInF32
                       : (grad_dtype == ZERO_BF16 ? zg::kInBF16 : zg::kInF16);
-    const int gx1 = zg::grid_x_for(S, n_ranks, d->sm_count, d->reduce_bps[in_kind]);
+    zg::ReducePlan rp;
+    rp.mode = zg::kModeStep;
+    rp.grads = grads;
+    rp.in_kind = in_kind;
+    rp.ld = grad_ld;
+    rp.rank_mul = grad_rank_offset_mul;
+    rp.ranks = ranks;
+    rp.n_ranks = n_ranks;
+    rp.S = S;
+    rp.n_contrib = world_size;
+    rp.staged = zg::reduce_wants_staging(rp);
+    const int gx1 = zg::grid_x_for(S, n_ranks, d->sm_count,
+                                   rp.staged ? d->staged_bps[in_kind] : d->reduce_bps[in_kind]);
     const int gx3 = zg::grid_x_for(S, n_ranks, d->sm_count, zg::kAdamBlocksPerSm);
     const int64_t parts = (int64_t)gx1 * n_ranks;
     if (parts > kMaxParts) return fail(ZERO_ERR_INVALID_ARG, "too many norm partials");
@@ -281,21 +296,11 @@ ZERO_API zero_status zero_shard_step_noalloc(
     e = cudaMemcpyAsync(&dstate->scaler, &sc, sizeof(sc), cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return cuda_fail(e, "writing the loss-scale state");
 
-    zg::ReducePlan rp;
-    rp.mode = zg::kModeStep;
-    rp.grads = grads;
-    rp.in_kind = in_kind;
-    rp.ld = grad_ld;
-    rp.rank_mul = grad_rank_offset_mul;
     rp.g = gbuf;
     rp.g_stride = g_stride;
     rp.part_ss = part_ss;
     rp.part_of = part_of;
-    rp.ranks = ranks;
-    rp.n_ranks = n_ranks;
-    rp.S = S;
     rp.full_numel = full_numel;
-    rp.n_contrib = world_size;
     rp.avg = op == ZERO_AVG;
     rp.st = dstate;
     rp.grid_x = gx1;
@@ -352,6 +357,11 @@ ZERO_API zero_status zero_shard_step_noalloc(
         res->grad_norm = out_state.res.grad_norm;
         res->clip_coef = out_state.res.clip_coef;
         res->scale_used = out_state.res.scale_used;
+    }
+    if (out_state.error) {               // a bounded wait gave up: the step was skipped
+        cudaMemsetAsync(&dstate->error, 0, sizeof(int32_t), st);
+        cudaStreamSynchronize(st);
+        return fail(ZERO_ERR_TIMEOUT, "a kernel gave up waiting for its bulk copies; the step was skipped");
     }
     return ZERO_OK;
 }

@@ -164,6 +164,16 @@ FLAT_800M = Workload(
     shapes=[(800_000_000,)], world_size=8, ranks=[7], grad_dtype=F16, op=AVG, dynamic=True,
     steps=5, sigma_g=2e-4, sigma_n=2e-4, seed=5, grads_layout="slice")
 
+# The profiling case with an odd shard size in the full [N, padded] layout:
+# rank 7's slice of every contributor row starts 2-byte aligned, so the
+# reduce takes the staged (bulk-copy) kernel; ~3 GB resident.
+FLAT_800M_ODD = Workload(
+    name="flat800m_odd_rank7", description="800M + 8 params in one flat buffer, N=8, rank 7's "
+    "shard (100,000,001 params) in the full contributor layout (2-byte aligned slices), fp16 AVG "
+    "at loss scale 2^16 (profiling size of the staged reduce)",
+    shapes=[(800_000_008,)], world_size=8, ranks=[7], grad_dtype=F16, op=AVG, dynamic=True,
+    steps=5, sigma_g=2e-4, sigma_n=2e-4, seed=5, grads_layout="full")
+
 # The 10B rank-7 step with fp32 contributions (reduce_dtype=float32): 40 GB of
 # contributions, fp16 parameters.
 TEN_B_F32 = Workload(
@@ -173,5 +183,5 @@ TEN_B_F32 = Workload(
     dynamic=True, steps=5, sigma_g=2e-4, sigma_n=2e-4, seed=6, grads_layout="slice")
 
 ALL = [TINY, GPT2, GPT_1P5B, LLAMA_7B, TEN_B]
-EXTRA = [FLAT_800M, TEN_B_F32]
+EXTRA = [FLAT_800M, FLAT_800M_ODD, TEN_B_F32]
 BY_NAME = {w.name: w for w in ALL + EXTRA}
