@@ -414,8 +414,9 @@ def run_ours(args, w):
     kernels = {
         "reduce_kernel": {"ms_mean": ms_red / max(nrec, 1),
                           "bytes_per_param": N * esize + 4 if K == 1 else 4},
-        "adamw_kernel": {"ms_mean": ms_adam / max(nrec, 1),
-                         "bytes_per_param": 30 + (1 + 4 / 256 if args.q8 else 0)},
+        ("adamw_q8_kernel" if args.q8 else "adamw_kernel"): {
+            "ms_mean": ms_adam / max(nrec, 1),
+            "bytes_per_param": 30 + (1 + 4 / 256 if args.q8 else 0)},
         "finalize_kernel": {"ms_mean": ms_fin / max(nrec, 1), "bytes_per_param": 0},
     }
     if K > 1:

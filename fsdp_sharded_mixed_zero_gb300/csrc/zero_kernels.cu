@@ -789,6 +789,38 @@ __device__ __forceinline__ void adam_elem(float g, float &th, float &m, float &v
     th = __fsub_rn(th, __fdiv_rn(__fmul_rn(k.lr, mh), __fadd_rn(__fsqrt_rn(vh), k.eps)));
 }
 
+// One full warp stores its 32 x 16 consecutive output bytes (lane L's at
+// o + 16 L, o = this lane's address) where o is 2-byte but not 16-byte
+// aligned.  delta = o mod 16 is the same for every lane, and the aligned
+// 16-byte word that starts delta bytes before lane L's span holds lane L-1's
+// last delta bytes and lane L's first 16 - delta: lanes 1..31 write those
+// words whole (one shuffle-up of the neighbour's data, four funnel shifts);
+// lane 0 writes its first 16 - delta bytes and lane 31 its last delta bytes in
+// 2-byte pieces.  Every lane of the warp must call this.
+__device__ __forceinline__ void store_warp_realigned(uint16_t *o, const uint4 &w, int lane) {
+    const uint32_t delta = (uint32_t)((uintptr_t)o & 15u);
+    uint4 prev;
+    prev.x = __shfl_up_sync(0xFFFFFFFFu, w.x, 1);
+    prev.y = __shfl_up_sync(0xFFFFFFFFu, w.y, 1);
+    prev.z = __shfl_up_sync(0xFFFFFFFFu, w.z, 1);
+    prev.w = __shfl_up_sync(0xFFFFFFFFu, w.w, 1);
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+    const int head = (int)(16u - delta) / 2;            // this lane's halves in the next word
+    if (lane > 0)
+        *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(o) - delta) =
+            bytes_at(prev, w, 16u - delta);
+    if (lane == 0) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (e < head) o[e] = (uint16_t)(u[e >> 1] >> (16 * (e & 1)));
+    }
+    if (lane == 31) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (e >= head) o[e] = (uint16_t)(u[e >> 1] >> (16 * (e & 1)));
+    }
+}
+
 // kFromAcc: the gradient rows are micro-step accumulators that still carry
 // the loss scale: g = acc / scale_used (the same division the reduce kernel
 // applies), padding elements (flat index >= full_numel) are zero.
@@ -846,6 +878,8 @@ __global__ void __launch_bounds__(kBlock) adamw_kernel(const __grid_constant__ A
             uint16_t *o = out + i0;
             if (oal == 16) {
                 *reinterpret_cast<uint4 *>(o) = make_uint4(w0, w1, w2, w3);
+            } else if (ch - (threadIdx.x & 31) + 31 < nch) {   // a full warp: aligned stores
+                store_warp_realigned(o, make_uint4(w0, w1, w2, w3), threadIdx.x & 31);
             } else if (oal == 4) {
                 uint32_t *o32 = reinterpret_cast<uint32_t *>(o);
                 o32[0] = w0; o32[1] = w1; o32[2] = w2; o32[3] = w3;
@@ -915,6 +949,7 @@ __global__ void __launch_bounds__(kBlock) adamw_q8_kernel(const __grid_constant_
         const int64_t i0 = b * kQ8Block + (int64_t)lane * kVec;
         const int64_t rem = S - i0;
         const int cnt = rem <= 0 ? 0 : (rem >= kVec ? kVec : (int)rem);
+        const bool full_block = (b + 1) * kQ8Block <= S;          // warp-uniform
         float P[kVec];
         if (cnt == kVec && vec) {
             const float4 g0 = ld_nc_f4(g + i0), g1 = ld_nc_f4(g + i0 + 4);
@@ -939,6 +974,8 @@ __global__ void __launch_bounds__(kBlock) adamw_q8_kernel(const __grid_constant_
                 uint16_t *o = out + i0;
                 if (oal == 16) {
                     *reinterpret_cast<uint4 *>(o) = make_uint4(w0, w1, w2, w3);
+                } else if (full_block) {                       // every lane is here
+                    store_warp_realigned(o, make_uint4(w0, w1, w2, w3), lane);
                 } else if (oal == 4) {
                     uint32_t *o32 = reinterpret_cast<uint32_t *>(o);
                     o32[0] = w0; o32[1] = w1; o32[2] = w2; o32[3] = w3;
