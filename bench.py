@@ -321,7 +321,9 @@ def run_ours(args, w):
     params = dw.S * len(w.ranks)
     n_batches = -(-len(w.ranks) // 64)
     K = max(1, args.micro_steps)
-    launches_per_step = 2 * n_batches + 1 + (K * n_batches if K > 1 else 0)
+    # the reduce launches (the last block makes the decision), the AdamW launches,
+    # and with micro-steps the accumulate launches
+    launches_per_step = 2 * n_batches + (K * n_batches if K > 1 else 0)
     acc_events = []
     if K > 1:
         dw.alloc_acc()
@@ -633,7 +635,7 @@ def run_offload(args, w):
                          "peak_kind": "measured here: torch CPU copy on %d threads" % threads,
                          "traffic": None, "bytes_per_launch": 36 * params},
             "cpu_baseline": None, "e2e": None, "clocks": clocks,
-            "gpu_launches": (n_batches + 1) * args.steps,
+            "gpu_launches": n_batches * args.steps,
         }
         print(json.dumps(line), flush=True)
     dw.close()

@@ -75,6 +75,7 @@ struct zero_flat {
     // per-element fp32 scalars, each rounded once from fp64
     float b1 = 0, b2 = 0, omb1 = 0, omb2 = 0, lr = 0, eps = 0, decay = 0, min_scale = 0;
     zg::DevState *d_state = nullptr;
+    uint32_t *d_done = nullptr;       // blocks of the current reduce that have counted in
     float2 *d_bc = nullptr;
     int64_t bc_len = 0;
     float *d_g = nullptr;             // reduced-gradient rows
@@ -233,6 +234,7 @@ void release(zero_flat *h) {
     if (h->h_out) cudaFreeHost(h->h_out);
     for (cudaEvent_t e : h->ev) cudaEventDestroy(e);
     cudaFree(h->d_state);
+    cudaFree(h->d_done);
     cudaFree(h->d_bc);
     cudaFree(h->d_g);
     cudaFree(h->d_part_ss);
@@ -374,6 +376,10 @@ ZERO_API zero_status zero_flat_init(const zero_param_info *infos, int32_t n_info
     h->device_bytes += sizeof(zg::DevState);
     e = cudaMemcpy(h->d_state, &init, sizeof(init), cudaMemcpyHostToDevice);
     if (e) { release(h); return cuda_fail(e, "cudaMemcpy(state)"); }
+    e = cudaMalloc(&h->d_done, sizeof(uint32_t));
+    if (!e) e = cudaMemset(h->d_done, 0, sizeof(uint32_t));
+    if (e) { release(h); return cuda_fail(e, "cudaMalloc(block counter)"); }
+    h->device_bytes += sizeof(uint32_t);
     e = cudaMallocHost(&h->h_state, sizeof(zg::DevState));
     if (e) { h->h_state = nullptr; release(h); return cuda_fail(e, "cudaMallocHost(state)"); }
     s = build_bc_table(h);
@@ -520,9 +526,6 @@ zero_status launch_step(zero_flat *h, zg::ReducePlan rp, zg::AdamPlan ap, double
     ap.lr = h->lr; ap.eps = h->eps; ap.decay = h->decay;
     ap.st = h->d_state;
 
-    cudaError_t e;
-    if ((e = mark(h, st))) return cuda_fail(e, "timing event");
-    if ((e = zg::run_reduce(rp, st))) return cuda_fail(e, "reduce kernel launch");
     zg::FinalizeArgs f{};
     f.part_ss = h->d_part_ss;
     f.part_of = h->d_part_of;
@@ -535,8 +538,18 @@ zero_status launch_step(zero_flat *h, zg::ReducePlan rp, zg::AdamPlan ap, double
     f.bc_table = h->d_bc;
     f.bc_len = h->bc_len;
     f.st = h->d_state;
+    // the last reduce block makes the decision (no K2 launch) whenever there
+    // is a reduce to count in; an empty shard still needs K2
+    rp.fuse_finalize = S > 0;
+    rp.done = h->d_done;
+    rp.fin = f;
+
+    cudaError_t e;
     if ((e = mark(h, st))) return cuda_fail(e, "timing event");
-    if ((e = zg::launch_finalize(f, st))) return cuda_fail(e, "finalize kernel launch");
+    if ((e = zg::run_reduce(rp, st))) return cuda_fail(e, "reduce kernel launch");
+    if ((e = mark(h, st))) return cuda_fail(e, "timing event");
+    if (!rp.fuse_finalize && (e = zg::launch_finalize(f, st)))
+        return cuda_fail(e, "finalize kernel launch");
     if ((e = mark(h, st))) return cuda_fail(e, "timing event");
     if (host_update) return ZERO_OK;
     if ((e = zg::run_adamw(ap, st))) return cuda_fail(e, "adamw kernel launch");

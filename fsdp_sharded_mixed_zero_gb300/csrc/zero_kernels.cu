@@ -10,9 +10,11 @@
 //   K1 reduce_staged_kernel  the same for contributor rows that are not
 //                       64-byte aligned: TMA bulk copies of aligned spans into
 //                       shared memory, re-aligned there.
-//   K2 finalize_kernel  one block: fixed-order total of the partials, global
-//                       norm, clip coefficient, overflow skip and the dynamic
-//                       loss-scale state machine (ZeRO reading §5.1, §5.3).
+//   K2 the decision     fixed-order total of the partials, global norm, clip
+//                       coefficient, overflow skip and the dynamic loss-scale
+//                       state machine (ZeRO reading §5.1, §5.3): made by the
+//                       K1 block that finishes last (finalize_block), or by
+//                       finalize_kernel when there is no reduce to count in.
 //   K3 adamw_kernel     AdamW with bias correction and decoupled weight decay
 //                       on fp32 master/m/v ("DeepSpeed 与 FSDP" §ZeRO-Offload
 //                       equations, §ZeRO-1 step 2) and the round-to-nearest
@@ -202,6 +204,92 @@ __device__ __forceinline__ void block_partial(double ss, int of, double *out_ss,
         for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += warp_ss[w];
         *out_ss = t;
         *out_of = of;
+    }
+}
+
+// ------------------------------------------------------------------ decision
+// The step's decision from the norm partials, by one block of up to 1024
+// threads: fixed-order fp64 total of the partials (strided per thread, then
+// a warp tree, then the warps in order), global norm, clip coefficient,
+// overflow skip and the dynamic loss-scale state machine (ZeRO reading §5.1,
+// §5.3); the bias corrections of an applied step come from the table.
+// Partials are read through L2 (another block may have written them).
+__device__ void finalize_block(const FinalizeArgs &a) {
+    __shared__ double warp_ss[kFinalizeThreads / 32];
+    DevState *st = a.st;
+    ScalerDev sc{};
+    float2 bc = make_float2(1.0f, 1.0f);
+    if (threadIdx.x == 0) {               // independent of the partials: load early
+        sc = st->scaler;
+        const int64_t t1 = sc.step_t + 1;
+        if (t1 < a.bc_len) bc = a.bc_table[t1];
+    }
+    double s = 0.0;
+    int of = 0;
+    for (int i = threadIdx.x; i < a.n_parts; i += blockDim.x) {
+        s += __ldcg(a.part_ss + i);
+        of |= __ldcg(a.part_of + i);
+    }
+    of = __syncthreads_or(of);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xFFFFFFFFu, s, o);
+    if ((threadIdx.x & 31) == 0) warp_ss[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    double total = 0.0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) total += warp_ss[w];
+
+    ResultDev r;
+    r.overflow = of;
+    r.grad_norm = sqrt(total + a.extra_norm_sq);
+    r.scale_used = sc.scale;
+    if (of) {                              // skip the step, shrink the scale
+        r.skipped = 1;
+        r.clip_coef = 1.0f;
+        sc.overflow_count += 1;
+        if (a.dynamic) {
+            const float h = __fdiv_rn(sc.scale, 2.0f);
+            sc.scale = h < a.min_scale ? a.min_scale : h;
+            sc.good_steps = 0;
+        }
+    } else {
+        r.skipped = 0;
+        sc.step_t += 1;
+        float coef = 1.0f;
+        if (a.max_grad_norm > 0.0) {
+            const double q = a.max_grad_norm / (r.grad_norm + 1e-6);
+            if (q < 1.0) coef = (float)q;
+        }
+        r.clip_coef = coef;
+        if (a.dynamic) {                   // grow after `window` clean steps
+            sc.good_steps += 1;
+            if (sc.good_steps == a.window) {
+                sc.scale = __fmul_rn(sc.scale, 2.0f);
+                sc.good_steps = 0;
+            }
+        }
+        st->bc1 = bc.x;                    // entry t of the table (t = the new step_t)
+        st->bc2 = bc.y;
+    }
+    st->scaler = sc;
+    st->res = r;
+}
+
+// After this block's partial is written: count the block; the block that
+// completes the count (every block of every launch of the step has written
+// its partial by then) makes the step's decision and re-arms the counter.
+// No block waits for another.
+__device__ __forceinline__ void count_and_finalize(const ReduceArgs &a) {
+    __shared__ int last;
+    if (threadIdx.x == 0) {
+        __threadfence();                   // the partial before the count
+        last = atomicAdd(a.done, 1u) == a.total_blocks - 1u;
+    }
+    __syncthreads();
+    if (last) {
+        __threadfence();                   // every counted block's partial is visible
+        finalize_block(a.fin);
+        if (threadIdx.x == 0) *a.done = 0u;
     }
 }
 
@@ -403,6 +491,7 @@ reduce_kernel(const __grid_constant__ ReduceArgs a) {
     if constexpr (kNorm) {
         const int64_t pidx = a.part_base + (int64_t)j * gridDim.x + blockIdx.x;
         block_partial(na.total(), of, a.part_ss + pidx, a.part_of + pidx);
+        if (a.fuse_finalize) count_and_finalize(a);
     }
 }
 
@@ -711,64 +800,13 @@ __global__ void __launch_bounds__(kBlock, 3) reduce_staged_kernel(const __grid_c
     if constexpr (kNorm) {
         const int64_t pidx = a.part_base + (int64_t)j * gridDim.x + blockIdx.x;
         block_partial(na.total(), of, a.part_ss + pidx, a.part_of + pidx);
+        if (a.fuse_finalize) count_and_finalize(a);
     }
 }
 
 // ------------------------------------------------------------------ K2
 __global__ void __launch_bounds__(kFinalizeThreads) finalize_kernel(const __grid_constant__ FinalizeArgs a) {
-    __shared__ double warp_ss[kFinalizeThreads / 32];
-    double s = 0.0;
-    int of = 0;
-    for (int i = threadIdx.x; i < a.n_parts; i += blockDim.x) {
-        s += a.part_ss[i];
-        of |= a.part_of[i];
-    }
-    of = __syncthreads_or(of);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xFFFFFFFFu, s, o);
-    if ((threadIdx.x & 31) == 0) warp_ss[threadIdx.x >> 5] = s;
-    __syncthreads();
-    if (threadIdx.x != 0) return;
-    double total = 0.0;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) total += warp_ss[w];
-
-    DevState *st = a.st;
-    ScalerDev sc = st->scaler;
-    ResultDev r;
-    r.overflow = of;
-    r.grad_norm = sqrt(total + a.extra_norm_sq);
-    r.scale_used = sc.scale;
-    if (of) {                              // skip the step, shrink the scale
-        r.skipped = 1;
-        r.clip_coef = 1.0f;
-        sc.overflow_count += 1;
-        if (a.dynamic) {
-            const float h = __fdiv_rn(sc.scale, 2.0f);
-            sc.scale = h < a.min_scale ? a.min_scale : h;
-            sc.good_steps = 0;
-        }
-    } else {
-        r.skipped = 0;
-        sc.step_t += 1;
-        float coef = 1.0f;
-        if (a.max_grad_norm > 0.0) {
-            const double q = a.max_grad_norm / (r.grad_norm + 1e-6);
-            if (q < 1.0) coef = (float)q;
-        }
-        r.clip_coef = coef;
-        if (a.dynamic) {                   // grow after `window` clean steps
-            sc.good_steps += 1;
-            if (sc.good_steps == a.window) {
-                sc.scale = __fmul_rn(sc.scale, 2.0f);
-                sc.good_steps = 0;
-            }
-        }
-        const float2 bc = sc.step_t < a.bc_len ? a.bc_table[sc.step_t] : make_float2(1.0f, 1.0f);
-        st->bc1 = bc.x;
-        st->bc2 = bc.y;
-    }
-    st->scaler = sc;
-    st->res = r;
+    finalize_block(a);
 }
 
 // ------------------------------------------------------------------ K3
@@ -1157,6 +1195,10 @@ cudaError_t run_reduce(const ReducePlan &p, cudaStream_t s) {
         a.n_ranks = nb;
         a.st = p.st;
         a.err = p.st ? const_cast<int32_t *>(&p.st->error) : nullptr;
+        a.fuse_finalize = p.fuse_finalize;
+        a.total_blocks = (uint32_t)((int64_t)p.grid_x * p.n_ranks);
+        a.done = p.done;
+        a.fin = p.fin;
         for (int32_t j = 0; j < nb; ++j) {
             const int64_t r = p.ranks[b0 + j];
             bool vec;

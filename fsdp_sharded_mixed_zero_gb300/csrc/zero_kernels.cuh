@@ -57,6 +57,21 @@ enum InKind : int { kInF16 = 0, kInBF16 = 1, kInF32 = 2 };
 //                  norm only (the AdamW kernel re-derives g from acc)
 enum ReduceMode : int { kModeStep = 0, kModeAccFirst = 1, kModeAccAdd = 2, kModeNormOnly = 3 };
 
+// K2: one block; deterministic total of the partials, norm, clip, loss scale.
+struct FinalizeArgs {
+    const double *part_ss;
+    const int32_t *part_of;
+    int32_t n_parts;
+    int32_t dynamic;
+    int32_t window;
+    float min_scale;
+    double extra_norm_sq;
+    double max_grad_norm;
+    const float2 *bc_table;           // bc_table[t] = {1 - b1^t, 1 - b2^t} as fp32
+    int64_t bc_len;                   // entries t >= bc_len are {1, 1}
+    DevState *st;
+};
+
 // K1: reduce of the N contributions + AVG + unscale + overflow + norm partials.
 struct ReduceArgs {
     int64_t ld;                       // contributor row stride, elements
@@ -77,25 +92,18 @@ struct ReduceArgs {
     int64_t first[kMaxRanksPerLaunch];    // r * S (flat index of the shard's element 0)
     uint8_t vec[kMaxRanksPerLaunch];      // 16-byte-aligned rows: vector path
     int32_t *err;                         // staged kernel: set on a timed-out wait
+    // The step's decision made by the block that finishes last (norm modes):
+    // each block counts itself in *done after writing its partial; the one
+    // that brings the count to total_blocks (over every launch of the step)
+    // runs the finalize on all partials and resets the count.
+    int32_t fuse_finalize;
+    uint32_t total_blocks;
+    uint32_t *done;
+    FinalizeArgs fin;
 };
 
 // Elements per block tile of the staged reduce (one 8-element chunk per thread).
 constexpr int kStageTile = kBlock * kVec;
-
-// K2: one block; deterministic total of the partials, norm, clip, loss scale.
-struct FinalizeArgs {
-    const double *part_ss;
-    const int32_t *part_of;
-    int32_t n_parts;
-    int32_t dynamic;
-    int32_t window;
-    float min_scale;
-    double extra_norm_sq;
-    double max_grad_norm;
-    const float2 *bc_table;           // bc_table[t] = {1 - b1^t, 1 - b2^t} as fp32
-    int64_t bc_len;                   // entries t >= bc_len are {1, 1}
-    DevState *st;
-};
 
 // K3: AdamW + cast into the flat buffer.
 struct AdamArgs {
@@ -155,6 +163,11 @@ struct ReducePlan {
     const DevState *st = nullptr;
     int grid_x = 1;
     bool staged = false;              // reduce_wants_staging(*this), decided before grid_x
+    // kModeStep / kModeNormOnly: finalize in the last block (done: a zeroed
+    // device counter owned by the caller), else the caller launches K2
+    bool fuse_finalize = false;
+    uint32_t *done = nullptr;
+    FinalizeArgs fin{};
 };
 cudaError_t run_reduce(const ReducePlan &p, cudaStream_t s);
 

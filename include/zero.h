@@ -311,7 +311,9 @@ zero_status zero_flat_device_bytes(const zero_flat *h, uint64_t *bytes);
 
 /* Per-kernel timing, for measurement tools.  While enabled, every
  * zero_shard_step records CUDA events on its stream around its reduce,
- * finalize and AdamW launches (a few microseconds per step).
+ * finalize and AdamW launches (a few microseconds per step).  The step's
+ * decision is normally made inside the reduce launch (by its last block), so
+ * ms_finalize is then only the gap between two events.
  * zero_flat_profile_read waits for the recorded events, returns the summed
  * device milliseconds of each kernel class and the number of steps recorded,
  * and clears the record.  Any output may be NULL. */

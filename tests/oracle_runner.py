@@ -56,8 +56,12 @@ def norm_exact(arrays, acc=None, overflow=0):
 
 
 def shard_step(hp, st, world_size, full, S, ranks, grads, ld, mul, master, m, v, out,
-               avg=True, grad_is_bf16=False, param_is_bf16=False, extra_norm_sq=0.0):
-    """Equivalent of oracle.shard_step; returns (overflow, skipped, norm, coef, scale_used)."""
+               avg=True, grad_is_bf16=False, param_is_bf16=False, extra_norm_sq=0.0,
+               coef_override=None):
+    """Equivalent of oracle.shard_step; returns (overflow, skipped, norm, coef, scale_used).
+    coef_override: update with this clip coefficient instead of the oracle's own
+    (the decision is still the oracle's) -- separates the norm's summation error
+    from the elementwise arithmetic."""
     scale = st.scale
     gs = []
     for r in ranks:
@@ -69,11 +73,12 @@ def shard_step(hp, st, world_size, full, S, ranks, grads, ld, mul, master, m, v,
     coef, skip = oracle.scaler_decide(hp, st, of, norm)
     if not skip:
         t = st.step_t
+        c = coef if coef_override is None else float(coef_override)
 
         def job(args):
             j, a, b = args
             r = ranks[j]
-            oracle.adamw_cast(hp, t, coef, gs[j][a:b], master[j][a:b], m[j][a:b], v[j][a:b],
+            oracle.adamw_cast(hp, t, c, gs[j][a:b], master[j][a:b], m[j][a:b], v[j][a:b],
                               param_is_bf16=param_is_bf16, out=out[r * S + a:r * S + b])
 
         list(_pool().map(job, [(j, a, b) for j in range(len(ranks)) for a, b in _chunks(S)]))
