@@ -68,6 +68,8 @@ def parse_args():
                    help="time the ZeRO-Offload step (optimizer on the host cores)")
     p.add_argument("--offload-threads", type=int, default=0,
                    help="host threads of the offload update (0: every available CPU)")
+    p.add_argument("--offload-gpu-share", type=float, default=0.0,
+                   help="fraction of each shard the GPU updates over the host link")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -559,7 +561,7 @@ def run_offload(args, w):
     dw = DeviceWorkload(w, device=dev)
     dw.gen_grads(0, dw.scaler().scale)
     stream = torch.cuda.current_stream(dev)
-    hm, hmm, hv = ([t.cpu() for t in ts] for ts in (dw.master, dw.m, dw.v))
+    hm, hmm, hv = ([t.cpu().pin_memory() for t in ts] for ts in (dw.master, dw.m, dw.v))
     dw.master = dw.m = dw.v = None                       # the state lives on the host
     torch.cuda.empty_cache()
     params = dw.S * len(w.ranks)
@@ -568,7 +570,8 @@ def run_offload(args, w):
     def one_step():
         return dw.flat.step_offload(w.ranks, dw.grads, hm, hmm, hv, dw.out,
                                     grad_rank_offset_mul=w.grad_rank_mul,
-                                    n_threads=args.offload_threads, stream=stream)
+                                    n_threads=args.offload_threads,
+                                    gpu_share=args.offload_gpu_share, stream=stream)
 
     for _ in range(args.warmup):
         one_step()
@@ -601,17 +604,19 @@ def run_offload(args, w):
     N = w.world_size
     esize = 4 if w.grad_dtype == 2 else 2
     # K1 reads the N contributions and writes the fp32 gradient rows in HBM.
-    # The host phase moves, in host memory: the DMA write of the gradient (4
-    # B/param), the CPU's reads of it (4) and of master/m/v (12), its writes
-    # of master/m/v (12) and of the 16-bit staging (2), and the DMA read of
-    # the staging (2) -- 36 B/param; over the link 4 B go down and 2 B up,
-    # overlapped with the update.
+    # On the host threads' share the update moves, in host memory: the DMA
+    # write of the gradient (4 B/param), the CPU's reads of it (4) and of
+    # master/m/v (12), its writes of master/m/v (12) and of the 16-bit staging
+    # (2), and the DMA read of the staging (2) -- 36 B/param, 6 of them over
+    # the link.  On the GPU's share the AdamW kernel reads and writes
+    # master/m/v over the link: 24 B/param of host memory and of link traffic.
+    f = max(0.0, min(1.0, args.offload_gpu_share))
+    host_bpp = f * 24 + (1 - f) * 36
     kernels = {
         "reduce_kernel": {"ms_mean": ms_red / max(nrec, 1), "bytes_per_param": N * esize + 4},
         "finalize_kernel": {"ms_mean": ms_fin / max(nrec, 1), "bytes_per_param": 0},
-        "host_update": {"ms_mean": ms_host / max(nrec, 1), "bytes_per_param": 36,
-                        "cpu_bytes_per_param": 30, "dma_bytes_per_param": 6,
-                        "link_bytes_per_param": 6},
+        "host_update": {"ms_mean": ms_host / max(nrec, 1), "bytes_per_param": host_bpp,
+                        "link_bytes_per_param": f * 24 + (1 - f) * 6},
     }
     for k in kernels.values():
         k["achieved_gbs"] = (k["bytes_per_param"] * params / (k["ms_mean"] / 1e3) / 1e9
@@ -627,15 +632,16 @@ def run_offload(args, w):
                        "emulated_world_size": N, "stepped_ranks": w.ranks,
                        "offload": "AdamW on host cores, fp32 master/m/v in host memory",
                        "host_threads": args.offload_threads or len(os.sched_getaffinity(0)),
+                       "gpu_share": f,
                        "parallelism": "replicas%d" % world},
             "kernels": kernels,
             "roofline": {"bound": "host-memory", "kernel": "host_update",
                          "achieved": hu["achieved_gbs"], "peak": peak, "unit": "GB/s",
                          "frac": hu["achieved_gbs"] / peak if hu["achieved_gbs"] else None,
                          "peak_kind": "measured here: torch CPU copy on %d threads" % threads,
-                         "traffic": None, "bytes_per_launch": 36 * params},
+                         "traffic": None, "bytes_per_launch": host_bpp * params},
             "cpu_baseline": None, "e2e": None, "clocks": clocks,
-            "gpu_launches": n_batches * args.steps,
+            "gpu_launches": n_batches * (2 if f > 0 else 1) * args.steps,
         }
         print(json.dumps(line), flush=True)
     dw.close()

@@ -101,8 +101,8 @@ def _load():
                                               C.c_double, vp, C.POINTER(StepResult)]
     L.zero_flat_set_lr.argtypes = [vp, C.c_double]
     L.zero_shard_step_offload.argtypes = [vp, C.POINTER(i32), i32, vp, i64, i64, C.POINTER(vp),
-                                          C.POINTER(vp), C.POINTER(vp), vp, C.c_double, i32, vp,
-                                          C.POINTER(StepResult)]
+                                          C.POINTER(vp), C.POINTER(vp), vp, C.c_double, i32,
+                                          C.c_double, vp, C.POINTER(StepResult)]
     L.zero_offload_adamw_host.argtypes = [C.POINTER(Hparams), i64, C.c_float, vp, vp, vp, vp,
                                           vp, i64, i32, i32]
     L.zero_status_string.argtypes = [i32]
@@ -254,17 +254,19 @@ def zero_shard_step_accumulated(h, ranks, acc_ptrs, master_ptrs, m_ptrs, v_ptrs,
 
 
 def zero_shard_step_offload(h, ranks, grads_ptr, grad_ld, grad_rank_offset_mul, master_ptrs,
-                            m_ptrs, v_ptrs, out_ptr, extra_norm_sq=0.0, n_threads=0, stream=0,
-                            want_result=True):
-    """The offload step: master/m/v pointers are HOST memory; returns a
-    StepResult when want_result (the call synchronizes the stream either way)."""
+                            m_ptrs, v_ptrs, out_ptr, extra_norm_sq=0.0, n_threads=0,
+                            gpu_share=0.0, stream=0, want_result=True):
+    """The offload step: master/m/v pointers are HOST memory; the GPU updates
+    the first gpu_share of each shard over the host link, the host threads the
+    rest.  Returns a StepResult when want_result."""
     n = len(ranks)
     r = (C.c_int32 * n)(*ranks)
     arrs = [(C.c_void_p * n)(*p) for p in (master_ptrs, m_ptrs, v_ptrs)]
     res = StepResult() if want_result else None
     _check(_lib.zero_shard_step_offload(h, r, n, C.c_void_p(grads_ptr), grad_ld,
                                         grad_rank_offset_mul, *arrs, C.c_void_p(out_ptr),
-                                        float(extra_norm_sq), int(n_threads), C.c_void_p(stream),
+                                        float(extra_norm_sq), int(n_threads), float(gpu_share),
+                                        C.c_void_p(stream),
                                         C.byref(res) if res is not None else None),
            "zero_shard_step_offload")
     return res
@@ -409,9 +411,12 @@ class ZeroFlat:
                                            want_result)
 
     def step_offload(self, ranks, grads, master, m, v, out, grad_rank_offset_mul=None,
-                     extra_norm_sq=0.0, n_threads=0, stream=None, want_result=True):
-        """The ZeRO-Offload step: master, m, v are fp32 CPU tensors (pinned or
-        not); grads and out are CUDA tensors as for step()."""
+                     extra_norm_sq=0.0, n_threads=0, gpu_share=0.0, stream=None,
+                     want_result=True):
+        """The ZeRO-Offload step: master, m, v are fp32 CPU tensors (pinned,
+        or pageable when gpu_share is 0 or the device reads pageable memory);
+        grads and out are CUDA tensors as for step().  gpu_share: the fraction
+        of each shard the GPU updates over the host link."""
         import torch
         if stream is None:
             stream = torch.cuda.current_stream()
@@ -424,7 +429,7 @@ class ZeroFlat:
                                        grads.stride(0), grad_rank_offset_mul,
                                        [t.data_ptr() for t in master], [t.data_ptr() for t in m],
                                        [t.data_ptr() for t in v], out.data_ptr(), extra_norm_sq,
-                                       n_threads, stream.cuda_stream, want_result)
+                                       n_threads, gpu_share, stream.cuda_stream, want_result)
 
     def set_lr(self, lr):
         zero_flat_set_lr(self.handle, lr)

@@ -94,9 +94,13 @@ struct zero_flat {
     uint16_t *h_out = nullptr;
     int64_t h_out_rows = 0;
     std::unique_ptr<zh::Pool> pool;
-    cudaStream_t copy_stream = nullptr;
+    cudaStream_t copy_stream = nullptr;   // gradient rows HBM -> host
+    cudaStream_t up_stream = nullptr;     // 16-bit parameters host -> HBM
     std::vector<cudaEvent_t> seg_ev;
-    cudaEvent_t out_done = nullptr;
+    cudaEvent_t out_done = nullptr;       // after the last parameter copy (up_stream)
+    cudaEvent_t decided = nullptr;        // the decision read back (caller's stream)
+    cudaEvent_t gpu_part_done = nullptr;  // the GPU's share of the update
+    bool pageable_access = false;         // the device reads pageable host memory
     // per-kernel timing (zero_flat_profile_enable)
     bool profile = false;
     std::vector<cudaEvent_t> ev;      // 4 events per recorded step
@@ -225,10 +229,13 @@ void release(zero_flat *h) {
         cudaEventSynchronize(h->out_done);        // copies may still read h_out
         cudaEventDestroy(h->out_done);
     }
-    if (h->copy_stream) {
-        cudaStreamSynchronize(h->copy_stream);
-        cudaStreamDestroy(h->copy_stream);
-    }
+    for (cudaStream_t sx : {h->copy_stream, h->up_stream})
+        if (sx) {
+            cudaStreamSynchronize(sx);
+            cudaStreamDestroy(sx);
+        }
+    for (cudaEvent_t ex : {h->decided, h->gpu_part_done})
+        if (ex) cudaEventDestroy(ex);
     for (cudaEvent_t e : h->seg_ev) cudaEventDestroy(e);
     if (h->h_g) cudaFreeHost(h->h_g);
     if (h->h_out) cudaFreeHost(h->h_out);
@@ -348,6 +355,12 @@ ZERO_API zero_status zero_flat_init(const zero_param_info *infos, int32_t n_info
             if (!e && mode < 3) e = zg::reduce_blocks_per_sm(kind, mode, true, &h->staged_bps[mode]);
             if (e) { delete h; return cuda_fail(e, "occupancy query"); }
         }
+    }
+    {
+        int pageable = 0;
+        if (cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, h->device) == cudaSuccess)
+            h->pageable_access = pageable != 0;
+        cudaGetLastError();
     }
     h->world = world_size;
     h->grad_dtype = grad_dtype;
@@ -745,10 +758,16 @@ zero_status ensure_offload(zero_flat *h, int32_t n_ranks, int32_t n_threads) {
         cudaError_t e = cudaEventCreateWithFlags(&h->out_done, cudaEventDisableTiming);
         if (e) { h->out_done = nullptr; return cuda_fail(e, "cudaEventCreate"); }
     }
-    if (!h->copy_stream) {
-        cudaError_t e = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking);
-        if (e) { h->copy_stream = nullptr; return cuda_fail(e, "cudaStreamCreate"); }
-    }
+    for (cudaStream_t *sx : {&h->copy_stream, &h->up_stream})
+        if (!*sx) {
+            cudaError_t e = cudaStreamCreateWithFlags(sx, cudaStreamNonBlocking);
+            if (e) { *sx = nullptr; return cuda_fail(e, "cudaStreamCreate"); }
+        }
+    for (cudaEvent_t *ex : {&h->decided, &h->gpu_part_done})
+        if (!*ex) {
+            cudaError_t e = cudaEventCreateWithFlags(ex, cudaEventDisableTiming);
+            if (e) { *ex = nullptr; return cuda_fail(e, "cudaEventCreate"); }
+        }
     const int want = n_threads > 0 ? n_threads : zh::available_cpus();
     if (!h->pool || h->pool->size() != want) {
         h->pool.reset();
@@ -762,20 +781,22 @@ zero_status ensure_offload(zero_flat *h, int32_t n_ranks, int32_t n_threads) {
 constexpr int64_t kHostChunk = int64_t(1) << 16;
 constexpr int64_t kHostSegment = int64_t(1) << 24;
 
-// The host update of every stepped rank.  The reduced gradient rows come
-// down from HBM segment by segment on the copy stream, and a host task waits
-// only for the segment it works on, so the copies overlap the update; each
-// segment's 16-bit parameters go back to the device on `st` as soon as its
+// The host update of elements [i_begin, S) of every stepped rank (i_begin a
+// multiple of kHostChunk).  The reduced gradient rows come down from HBM
+// segment by segment on the copy stream, and a host task waits only for the
+// segment it works on, so the copies overlap the update; each segment's
+// 16-bit parameters go back to the device on the up stream as soon as its
 // last chunk is done.  Returns the first CUDA error, if any.
 cudaError_t host_update(zero_flat *h, const zh::AdamScalars &k, const int32_t *ranks,
                         int32_t n_ranks, float *const *master, float *const *m, float *const *v,
-                        void *flat_param_out, cudaStream_t st) {
+                        void *flat_param_out, int64_t i_begin) {
     const int64_t S = h->shard;
-    if (S == 0) return cudaSuccess;
+    const int64_t span = S - i_begin;
+    if (span <= 0) return cudaSuccess;
     const bool bf16 = h->param_dtype == ZERO_BF16;
     const int64_t chunks_per_seg = kHostSegment / kHostChunk;
-    const int64_t segs = (S + kHostSegment - 1) / kHostSegment;
-    const int64_t chunks = (S + kHostChunk - 1) / kHostChunk;
+    const int64_t segs = (span + kHostSegment - 1) / kHostSegment;
+    const int64_t chunks = (span + kHostChunk - 1) / kHostChunk;
     const int64_t n_seg = n_ranks * segs;
     cudaError_t e;
     while ((int64_t)h->seg_ev.size() < n_seg) {
@@ -785,7 +806,7 @@ cudaError_t host_update(zero_flat *h, const zh::AdamScalars &k, const int32_t *r
     }
     for (int64_t j = 0; j < n_ranks; ++j)
         for (int64_t q = 0; q < segs; ++q) {
-            const int64_t s0 = q * kHostSegment, len = std::min(kHostSegment, S - s0);
+            const int64_t s0 = i_begin + q * kHostSegment, len = std::min(kHostSegment, S - s0);
             const int64_t off = j * h->g_stride + s0;
             if ((e = cudaMemcpyAsync(h->h_g + off, h->d_g + off, (size_t)len * 4,
                                      cudaMemcpyDeviceToHost, h->copy_stream)))
@@ -814,22 +835,37 @@ cudaError_t host_update(zero_flat *h, const zh::AdamScalars &k, const int32_t *r
             if (x) { note(x); return; }
             ready[sg].store(1, std::memory_order_release);
         }
-        const int64_t i0 = c * kHostChunk;
+        const int64_t i0 = i_begin + c * kHostChunk;
         const int64_t n = std::min(kHostChunk, S - i0);
         uint16_t *stage = h->h_out + j * S;
         zh::adamw_cast_range(k, h->h_g + j * h->g_stride + i0, master[j] + i0, m[j] + i0,
                              v[j] + i0, stage + i0, n, bf16);
         if (left[sg].fetch_sub(1) == 1) {                      // segment complete
-            const int64_t s0 = q * kHostSegment;
+            const int64_t s0 = i_begin + q * kHostSegment;
             const int64_t len = std::min(kHostSegment, S - s0);
             cudaError_t x = cudaSetDevice(dev);
             if (!x) x = cudaMemcpyAsync(out16 + (int64_t)ranks[j] * S + s0, stage + s0,
-                                        (size_t)len * 2, cudaMemcpyHostToDevice, st);
+                                        (size_t)len * 2, cudaMemcpyHostToDevice, h->up_stream);
             note(x);
         }
     };
     h->pool->run(n_ranks * chunks, task);
     return (cudaError_t)err.load();
+}
+
+// Whether the GPU can read and write every stepped rank's host arrays.
+bool gpu_reaches(const zero_flat *h, int32_t n_ranks, float *const *const rows[3]) {
+    if (h->pageable_access) return true;
+    for (int a = 0; a < 3; ++a)
+        for (int32_t j = 0; j < n_ranks; ++j) {
+            cudaPointerAttributes at{};
+            if (cudaPointerGetAttributes(&at, rows[a][j]) != cudaSuccess) {
+                cudaGetLastError();
+                return false;
+            }
+            if (at.type != cudaMemoryTypeHost) return false;   // pinned / registered only
+        }
+    return true;
 }
 
 }  // namespace
@@ -839,7 +875,7 @@ ZERO_API zero_status zero_shard_step_offload(zero_flat *h, const int32_t *ranks,
                                              int64_t grad_rank_offset_mul, float *const *master,
                                              float *const *m, float *const *v,
                                              void *flat_param_out, double extra_norm_sq,
-                                             int32_t n_threads, void *stream,
+                                             int32_t n_threads, double gpu_share, void *stream,
                                              zero_step_result *res) {
     if (!h) return fail(ZERO_ERR_INVALID_ARG, "handle is NULL");
     int32_t max_rank = 0;
@@ -848,8 +884,18 @@ ZERO_API zero_status zero_shard_step_offload(zero_flat *h, const int32_t *ranks,
     if ((s = check_update(h, n_ranks, master, m, v, flat_param_out, extra_norm_sq))) return s;
     if ((s = check_grads(h, grads, grad_ld, grad_rank_offset_mul, max_rank))) return s;
     if (n_threads < 0) return fail(ZERO_ERR_INVALID_ARG, "n_threads must be >= 0");
+    if (!(gpu_share >= 0.0 && gpu_share <= 1.0))
+        return fail(ZERO_ERR_INVALID_ARG, "gpu_share must be in [0, 1]");
+    const int64_t S = h->shard;
+    // the GPU takes elements [0, split) of every rank, the host threads the rest
+    int64_t split = gpu_share >= 1.0 ? S : (int64_t)(gpu_share * (double)S) / kHostChunk * kHostChunk;
+    split = std::min(split, S);
     DeviceGuard guard(h->device);
     if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the handle's device");
+    float *const *const rows[3] = {master, m, v};
+    if (split > 0 && !gpu_reaches(h, n_ranks, rows))
+        return fail(ZERO_ERR_INVALID_ARG,
+                    "gpu_share > 0 needs host arrays the GPU can access (pinned or registered)");
     if ((s = ensure_offload(h, n_ranks, n_threads))) return s;
     const cudaStream_t st = (cudaStream_t)stream;
     zg::ReducePlan rp;
@@ -860,24 +906,50 @@ ZERO_API zero_status zero_shard_step_offload(zero_flat *h, const int32_t *ranks,
     rp.rank_mul = grad_rank_offset_mul;
     rp.ranks = ranks;
     rp.n_ranks = n_ranks;
-    zg::AdamPlan ap;
-    if ((s = launch_step(h, rp, ap, extra_norm_sq, st, nullptr, true))) return s;
+    zg::AdamPlan none;
+    if ((s = launch_step(h, rp, none, extra_norm_sq, st, nullptr, true))) return s;
     cudaError_t e = cudaMemcpyAsync(h->h_state, h->d_state, sizeof(zg::DevState),
                                     cudaMemcpyDeviceToHost, st);
-    if (!e) e = cudaStreamSynchronize(st);
+    if (!e) e = cudaEventRecord(h->decided, st);
     if (e) return cuda_fail(e, "reading the step decision");
+    if (split > 0) {                                  // the GPU's share, queued behind the decision
+        zg::AdamPlan ap;
+        ap.g = h->d_g;
+        ap.g_stride = h->g_stride;
+        ap.master = master;
+        ap.m = m;
+        ap.v = v;
+        ap.out = flat_param_out;
+        ap.bf16_out = h->param_dtype == ZERO_BF16;
+        ap.ranks = ranks;
+        ap.n_ranks = n_ranks;
+        ap.S = S;
+        ap.count = split;
+        ap.full_numel = h->full_numel;
+        ap.b1 = h->b1; ap.b2 = h->b2; ap.omb1 = h->omb1; ap.omb2 = h->omb2;
+        ap.lr = h->lr; ap.eps = h->eps; ap.decay = h->decay;
+        ap.st = h->d_state;
+        ap.grid_x = zg::grid_x_for(split, std::min<int64_t>(n_ranks, zg::kMaxRanksPerLaunch),
+                                   h->sm_count, zg::kAdamBlocksPerSm);
+        if ((e = zg::run_adamw(ap, st))) return cuda_fail(e, "adamw kernel launch");
+    }
+    if ((e = cudaEventRecord(h->gpu_part_done, st))) return cuda_fail(e, "cudaEventRecord");
+    if ((e = cudaEventSynchronize(h->decided))) return cuda_fail(e, "waiting for the step decision");
     const zg::DevState ds = *h->h_state;
     if (ds.error) return take_device_error(h, st);
-    if (!ds.res.skipped) {
-        // the previous call's copies (perhaps on another stream) read h_out
+    if (!ds.res.skipped && split < S) {
+        // the previous call's parameter copies read h_out
         if ((e = cudaEventSynchronize(h->out_done))) return cuda_fail(e, "waiting for the last copies");
         const zh::AdamScalars k{h->b1, h->b2, h->omb1, h->omb2, h->lr, h->eps, h->decay,
                                 ds.res.clip_coef, ds.bc1, ds.bc2};
-        if ((e = host_update(h, k, ranks, n_ranks, master, m, v, flat_param_out, st)))
+        if ((e = host_update(h, k, ranks, n_ranks, master, m, v, flat_param_out, split)))
             return cuda_fail(e, "copying parameters to the device");
         if ((e = cudaSetDevice(h->device))) return cuda_fail(e, "cudaSetDevice");
-        if ((e = cudaEventRecord(h->out_done, st))) return cuda_fail(e, "cudaEventRecord");
+        if ((e = cudaEventRecord(h->out_done, h->up_stream))) return cuda_fail(e, "cudaEventRecord");
+        if ((e = cudaStreamWaitEvent(st, h->out_done, 0))) return cuda_fail(e, "cudaStreamWaitEvent");
     }
+    // the GPU's share of the host arrays is written when the call returns too
+    if ((e = cudaEventSynchronize(h->gpu_part_done))) return cuda_fail(e, "waiting for the GPU share");
     if ((e = mark(h, st))) return cuda_fail(e, "timing event");
     if (res) {
         res->overflow = ds.res.overflow;

@@ -1230,12 +1230,14 @@ cudaError_t launch_adamw_q8(const AdamArgs &a, int grid_x, bool bf16_out, cudaSt
 }
 
 cudaError_t run_adamw(const AdamPlan &p, cudaStream_t s) {
-    if (p.S <= 0) return cudaSuccess;
-    if (p.q8 && p.acc) return cudaErrorInvalidValue;   // no quantizing variant reads accumulators
+    const int64_t count = p.count < 0 ? p.S : p.count;
+    if (count <= 0) return cudaSuccess;
+    if (count > p.S) return cudaErrorInvalidValue;
+    if (p.q8 && (p.acc || count != p.S)) return cudaErrorInvalidValue;  // whole shards only
     for (int32_t b0 = 0; b0 < p.n_ranks; b0 += kMaxRanksPerLaunch) {
         const int32_t nb = p.n_ranks - b0 < kMaxRanksPerLaunch ? p.n_ranks - b0 : kMaxRanksPerLaunch;
         AdamArgs a{};
-        a.S = p.S;
+        a.S = count;                                   // the kernels' element range per rank
         a.full_numel = p.full_numel;
         a.b1 = p.b1; a.b2 = p.b2; a.omb1 = p.omb1; a.omb2 = p.omb2;
         a.lr = p.lr; a.eps = p.eps; a.decay = p.decay;

@@ -195,6 +195,8 @@ struct AdamPlan {
     int8_t *q8 = nullptr;             // non-NULL: also write the int8 payload and its scales
     float *q8_scales = nullptr;
     int grid_x = 1;
+    int64_t count = -1;               // elements updated per rank from element 0 (< 0: S);
+                                      // the output slot of rank r still starts at r * S
 };
 cudaError_t run_adamw(const AdamPlan &p, cudaStream_t s);
 

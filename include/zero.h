@@ -236,29 +236,37 @@ zero_status zero_shard_step_accumulated(zero_flat *h, const int32_t *ranks, int3
  * On the GPU, exactly as in zero_shard_step: the reduce, unscale, overflow
  * check and norm partials into the handle's fp32 gradient rows, then the
  * loss-scale decision, the clip coefficient and the bias corrections.  The
- * call reads that decision back (one synchronization of `stream`).  If the
- * step is applied, the gradient rows are copied to pinned host memory in
- * segments on a stream of the handle, and `n_threads` host threads (0: every
- * CPU this process may run on) update master/m/v segment by segment as the
- * copies land, writing the 16-bit parameters into a pinned staging buffer;
- * each finished segment is copied to flat_param_out[r * shard_size + ...] on
- * `stream` at once.  The update is the same sequence of fp32 operations as
- * zero_shard_step's, so the results are bit-identical to it.  This is the
- * offload mode of the method, never a substitute for the GPU path: the
- * reduce and the decision still need the GPU.
- * master, m, v: HOST fp32 arrays (pageable or pinned), shard_size elements
- * per stepped rank, 4-byte aligned; updated when the call returns.
- * flat_param_out: device, as for zero_shard_step; its copies are queued on
- * `stream` when the call returns.  grads and the rest: as zero_shard_step.
+ * call waits for that decision (one event).  If the step is applied, the
+ * update of each stepped rank's state is split at element
+ * split = gpu_share * shard_size (rounded down to 65536 elements, or the
+ * whole shard for gpu_share = 1):
+ *   - elements [0, split): the GPU's AdamW kernel, reading and writing the
+ *     host-resident master/m/v over the host link (the host memory must be
+ *     pinned, or the device must access pageable memory);
+ *   - elements [split, shard_size): `n_threads` host threads (0: every CPU
+ *     this process may run on), while the gradient rows come down from HBM in
+ *     segments on a stream of the handle; the 16-bit parameters are staged in
+ *     pinned memory and each finished segment is copied to
+ *     flat_param_out[r * shard_size + ...] on a second stream of the handle.
+ * Both halves run at once and do the same sequence of fp32 operations as
+ * zero_shard_step, so the results are bit-identical to it for any split.
+ * This is the offload mode of the method, never a substitute for the GPU
+ * path: the reduce and the decision still need the GPU.
+ * master, m, v: HOST fp32 arrays, shard_size elements per stepped rank,
+ * 4-byte aligned; fully updated when the call returns.  flat_param_out:
+ * device, as for zero_shard_step; when the call returns, `stream` is ordered
+ * after every write to it.  grads and the rest: as zero_shard_step.
  * Not capturable in a CUDA graph (host synchronization and host compute).
- * Errors: as for zero_shard_step; INVALID_ARG for n_threads < 0; NO_MEMORY
- * when the pinned buffers (6 bytes per stepped element) cannot be had. */
+ * Errors: as for zero_shard_step; INVALID_ARG for n_threads < 0, gpu_share
+ * outside [0, 1], or gpu_share > 0 with host memory the GPU cannot access;
+ * NO_MEMORY when the pinned buffers (6 bytes per stepped element) cannot be
+ * had. */
 zero_status zero_shard_step_offload(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
                                     const void *grads, int64_t grad_ld,
                                     int64_t grad_rank_offset_mul, float *const *master,
                                     float *const *m, float *const *v, void *flat_param_out,
-                                    double extra_norm_sq, int32_t n_threads, void *stream,
-                                    zero_step_result *res);
+                                    double extra_norm_sq, int32_t n_threads, double gpu_share,
+                                    void *stream, zero_step_result *res);
 
 /* The host half of zero_shard_step_offload on its own, for a caller that
  * reduces gradients elsewhere: for i < n, with gc = g[i] * clip_coef,

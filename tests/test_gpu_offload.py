@@ -39,18 +39,20 @@ def _host_copies(ts, pin):
 
 CASES = [
     (_wl("tiny_inf_skip", [(512, 1024), (1024,), (1024, 512), (512,)], 4, [0, 1, 2, 3],
-         steps=4, inf_at=(2, 1, 9)), True, 0),
+         steps=4, inf_at=(2, 1, 9)), True, 0, 0.5),
     (_wl("bf16_sum_ragged", [(40_001,), (33,)], 8, list(range(8)), dtype=BF16, op=SUM,
-         dynamic=False), False, 3),
-    (_wl("slice_rank3", [(3_000_001,)], 8, [3], layout="slice"), True, 0),
-    (_wl("fp32_contrib", [(100_003,)], 2, [0, 1], dtype=F32), False, 1),
-    (_wl("n70_two_launches", [(70 * 33 + 5,)], 70, list(range(70)), steps=2), True, 0),
-    (_wl("multi_segment", [(2 * (1 << 24) + 12_345,)], 1, [0], steps=2), True, 0),
+         dynamic=False), False, 3, 0.0),
+    (_wl("slice_rank3", [(3_000_001,)], 8, [3], layout="slice"), True, 0, 0.4),
+    (_wl("fp32_contrib", [(100_003,)], 2, [0, 1], dtype=F32), False, 1, 0.0),
+    (_wl("n70_two_launches", [(70 * 33 + 5,)], 70, list(range(70)), steps=2), True, 0, 1.0),
+    (_wl("multi_segment", [(2 * (1 << 24) + 12_345,)], 1, [0], steps=2), True, 0, 0.3),
+    (_wl("gpu_only_pinned", [(1_000_003,)], 4, [0, 1, 2, 3], steps=3, inf_at=(1, 0, 5)),
+     True, 0, 1.0),
 ]
 
 
-@pytest.mark.parametrize("w,pin,n_threads", CASES, ids=[c[0].name for c in CASES])
-def test_offload_step_matches_oracle(ora, w, pin, n_threads):
+@pytest.mark.parametrize("w,pin,n_threads,gpu_share", CASES, ids=[c[0].name for c in CASES])
+def test_offload_step_matches_oracle(ora, w, pin, n_threads, gpu_share):
     _need_gpu()
     from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
     hp = ora.hparams(**w.hparams_kwargs())
@@ -71,7 +73,8 @@ def test_offload_step_matches_oracle(ora, w, pin, n_threads):
             g = host_grads(dw.grads)
             before = u16(dw.out).copy()
             res = dw.flat.step_offload(w.ranks, dw.grads, hm, hmm, hv, dw.out,
-                                       grad_rank_offset_mul=w.grad_rank_mul, n_threads=n_threads)
+                                       grad_rank_offset_mul=w.grad_rank_mul, n_threads=n_threads,
+                                       gpu_share=gpu_share)
             want = runner.shard_step(hp, st, w.world_size, dw.full, dw.S, w.ranks, g, w.grad_ld,
                                      w.grad_rank_mul, master, m, v, out, avg=w.op == AVG,
                                      grad_is_bf16=w.grad_dtype == BF16, param_is_bf16=pbf16)
@@ -91,12 +94,14 @@ def test_offload_step_matches_oracle(ora, w, pin, n_threads):
         dw.close()
 
 
-def test_offload_equals_device_step_bit_for_bit():
+@pytest.mark.parametrize("gpu_share", [0.0, 0.3, 0.7, 1.0])
+def test_offload_equals_device_step_bit_for_bit(gpu_share):
     """The same inputs through the all-GPU step and the offload step (two
-    handles): identical master, m, v, parameters and results."""
+    handles), for several splits of each shard between the GPU and the host
+    threads: identical master, m, v, parameters and results."""
     _need_gpu()
     from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
-    w = _wl("bits", [(250_007,), (99,)], 4, [0, 1, 2, 3], steps=3, inf_at=(1, 2, 5))
+    w = _wl("bits", [(1_000_007,), (99,)], 4, [0, 1, 2, 3], steps=3, inf_at=(1, 2, 5))
     a, b = DeviceWorkload(w), DeviceWorkload(w)
     try:
         hm, hmm, hv = (_host_copies(x, True) for x in (b.master, b.m, b.v))
@@ -105,7 +110,7 @@ def test_offload_equals_device_step_bit_for_bit():
             b.grads.copy_(a.grads)
             ra = a.step()
             rb = b.flat.step_offload(w.ranks, b.grads, hm, hmm, hv, b.out,
-                                     grad_rank_offset_mul=w.grad_rank_mul)
+                                     grad_rank_offset_mul=w.grad_rank_mul, gpu_share=gpu_share)
             assert (ra.overflow, ra.skipped, ra.grad_norm, ra.clip_coef, ra.scale_used) == \
                    (rb.overflow, rb.skipped, rb.grad_norm, rb.clip_coef, rb.scale_used)
         torch.cuda.synchronize()
@@ -136,4 +141,9 @@ def test_offload_argument_errors():
     assert e.value.status == 3
     with pytest.raises(Z.ZeroError):
         Z.zero_shard_step_offload(f.handle, [4], g.data_ptr(), 100, 0, p, p, p, out.data_ptr())
+    for bad in (-0.1, 1.5, float("nan")):
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_shard_step_offload(f.handle, [0], g.data_ptr(), 100, 0, p, p, p,
+                                      out.data_ptr(), gpu_share=bad)
+        assert e.value.status == 1
     f.close()
