@@ -3,7 +3,7 @@
 // the three launches of a step.  No arithmetic of the update happens here
 // beyond forming the per-step fp32 scalars from the fp64 hyper-parameters.
 #include "zero.h"
-#include "zero_kernels.cuh"
+#include "zero_plan.h"
 #include "host_adam.h"
 
 #include <algorithm>

@@ -27,7 +27,7 @@
 // (cudaGetSymbolAddress, with that device current) and the launch geometry,
 // and caches them; make that first call before any stream capture.
 #include "zero.h"
-#include "zero_kernels.cuh"
+#include "zero_plan.h"
 
 #include <cmath>
 #include <cstdarg>

@@ -1,0 +1,90 @@
+// zero_plan.h -- host-side planning of the step's kernels over any number of
+// stepped ranks (one launch per kMaxRanksPerLaunch ranks), shared by every
+// entry point: which reduce kernel a plan takes, the launch geometry, and the
+// per-launch argument blocks.
+#pragma once
+
+#include "zero_kernels.cuh"
+
+namespace zg {
+
+// Host-side planning of one kernel class over any number of stepped ranks
+// (one launch per kMaxRanksPerLaunch ranks), shared by every entry point.
+struct ReducePlan {
+    int mode = kModeStep;             // ReduceMode
+    const void *grads = nullptr;      // contributions: rank r, contributor c, element i at
+    int in_kind = kInF16;             //   grads[c*ld + r*rank_mul + i] (InKind encoding)
+    int64_t ld = 0;
+    int64_t rank_mul = 0;
+    const float *const *acc_in = nullptr;  // kModeNormOnly: per-rank accumulators
+    float *const *acc_out = nullptr;       // kModeAccFirst / kModeAccAdd
+    float *g = nullptr;               // kModeStep: rows of g_stride floats per stepped rank
+    int64_t g_stride = 0;
+    double *part_ss = nullptr;        // kModeStep / kModeNormOnly: grid_x partials per rank
+    int32_t *part_of = nullptr;
+    const int32_t *ranks = nullptr;
+    int32_t n_ranks = 0;
+    int64_t S = 0, full_numel = 0;
+    int32_t n_contrib = 1;
+    int32_t avg = 0;
+    const DevState *st = nullptr;
+    int grid_x = 1;
+    bool staged = false;              // reduce_wants_staging(*this), decided before grid_x
+    // kModeStep / kModeNormOnly: finalize in the last block (done: a zeroed
+    // device counter owned by the caller), else the caller launches K2
+    bool fuse_finalize = false;
+    uint32_t *done = nullptr;
+    FinalizeArgs fin{};
+};
+cudaError_t run_reduce(const ReducePlan &p, cudaStream_t s);
+
+// Whether a plan's contributions should go through the staged reduce: some
+// stepped rank has a contributor row whose start is not 64-byte aligned, and
+// the shard holds at least one full tile.  (A 16-byte vector load that
+// starts inside a 64-byte DRAM access unit makes the unit's other half a
+// separate request, which is fetched again: 7 % extra traffic with 32-byte
+// aligned rows; 2-byte aligned rows cannot use vector loads at all.)  Plans
+// whose accumulators are not 16-byte aligned stay on the plain kernel.
+bool reduce_wants_staging(const ReducePlan &p);
+
+struct AdamPlan {
+    const float *g = nullptr;         // scratch rows (g_stride floats per stepped rank), or
+    int64_t g_stride = 0;
+    const float *const *acc = nullptr;    // per-rank accumulators (then g = acc / scale)
+    float *const *master = nullptr, *const *m = nullptr, *const *v = nullptr;
+    void *out = nullptr;
+    bool bf16_out = false;
+    const int32_t *ranks = nullptr;
+    int32_t n_ranks = 0;
+    int64_t S = 0, full_numel = 0;
+    float b1 = 0, b2 = 0, omb1 = 0, omb2 = 0, lr = 0, eps = 0, decay = 0;
+    const DevState *st = nullptr;
+    int8_t *q8 = nullptr;             // non-NULL: also write the int8 payload and its scales
+    float *q8_scales = nullptr;
+    int grid_x = 1;
+    int64_t count = -1;               // elements updated per rank from element 0 (< 0: S);
+                                      // the output slot of rank r still starts at r * S
+};
+cudaError_t run_adamw(const AdamPlan &p, cudaStream_t s);
+
+// Launch geometry, measured on GB300 (152 SMs) on the 10B rank-7 step.  The
+// AdamW kernel streams four arrays in and four out and is fastest with exactly
+// two 256-thread blocks per SM (5.67 ms; 6.50 ms with four, 6.3 ms with three,
+// and grids between whole multiples of the SM count are worse).  The
+// read-dominated reduce is fastest with one full wave of resident blocks (its
+// 48 registers allow five per SM; a partial second wave costs ~15 %).  A
+// launch's blocks are split across the stepped ranks it handles and never
+// exceed the work there is.
+constexpr int kAdamBlocksPerSm = 2;
+constexpr int kAdamQ8BlocksPerSm = 3;    // AdamW + int8 payload (72 registers): 6.10 ms vs 6.90 at two
+
+inline int grid_x_for(int64_t S, int64_t ranks_in_launch, int sm_count, int blocks_per_sm) {
+    const int64_t chunks = (S + kVec - 1) / kVec;
+    const int64_t want = (chunks + kBlock - 1) / kBlock;
+    int64_t cap = (int64_t)sm_count * blocks_per_sm / (ranks_in_launch > 0 ? ranks_in_launch : 1);
+    if (cap < 1) cap = 1;
+    const int64_t g = want < cap ? want : cap;
+    return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace zg
