@@ -19,7 +19,7 @@ __all__ = [
     "zero_flat_free", "zero_flat_profile_enable", "zero_flat_profile_read",
     "zero_shard_step_noalloc", "zero_grad_accumulate", "zero_shard_step_accumulated",
     "zero_shard_step_q8", "ZERO_Q8_BLOCK", "zero_flat_set_lr", "zero_shard_step_offload",
-    "zero_offload_adamw_host",
+    "zero_offload_adamw_host", "zero_debug_set_stage_tx_pad",
     "zero_status_string", "zero_last_error", "ZeroFlat",
     "LIB_PATH",
 ]
@@ -100,6 +100,7 @@ def _load():
                                               C.POINTER(vp), C.POINTER(vp), C.POINTER(vp), vp,
                                               C.c_double, vp, C.POINTER(StepResult)]
     L.zero_flat_set_lr.argtypes = [vp, C.c_double]
+    L.zero_debug_set_stage_tx_pad.argtypes = [C.c_uint32]
     L.zero_shard_step_offload.argtypes = [vp, C.POINTER(i32), i32, vp, i64, i64, C.POINTER(vp),
                                           C.POINTER(vp), C.POINTER(vp), vp, C.c_double, i32,
                                           C.c_double, vp, C.POINTER(StepResult)]
@@ -114,7 +115,7 @@ def _load():
                  "zero_flat_device_bytes", "zero_flat_free", "zero_flat_profile_enable",
                  "zero_flat_profile_read", "zero_shard_step_noalloc", "zero_grad_accumulate",
                  "zero_shard_step_q8", "zero_flat_set_lr", "zero_shard_step_offload",
-                 "zero_offload_adamw_host",
+                 "zero_offload_adamw_host", "zero_debug_set_stage_tx_pad",
                  "zero_shard_step_accumulated"):
         getattr(L, name).restype = i32
     return L
@@ -281,6 +282,11 @@ def zero_offload_adamw_host(hp, step_t, clip_coef, g_ptr, master_ptr, m_ptr, v_p
                                         C.c_void_p(m_ptr), C.c_void_p(v_ptr), C.c_void_p(out_ptr),
                                         int(n), int(param_dtype), int(n_threads)),
            "zero_offload_adamw_host")
+
+
+def zero_debug_set_stage_tx_pad(nbytes):
+    """Test hook: the staged reduce's waits run out (see include/zero_debug.h)."""
+    _check(_lib.zero_debug_set_stage_tx_pad(int(nbytes)), "zero_debug_set_stage_tx_pad")
 
 
 def zero_flat_set_lr(h, lr):

@@ -16,7 +16,7 @@ SOURCES = ["zero_kernels.cu", "zero_plan.cu", "zero_api.cu", "zero_noalloc.cu"]
 HOST_SOURCES = ["host_adam.cc"]
 HEADERS = [os.path.join(CSRC, "zero_kernels.cuh"), os.path.join(CSRC, "zero_plan.h"),
            os.path.join(CSRC, "host_adam.h"),
-           os.path.join(ROOT, "include", "zero.h")]
+           os.path.join(ROOT, "include", "zero.h"), os.path.join(ROOT, "include", "zero_debug.h")]
 LIB = os.path.join(HERE, "libzero_gb300.so")
 BUILD = os.path.join(HERE, "_build")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

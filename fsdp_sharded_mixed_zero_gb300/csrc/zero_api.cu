@@ -3,6 +3,7 @@
 // the three launches of a step.  No arithmetic of the update happens here
 // beyond forming the per-step fp32 scalars from the fp64 hyper-parameters.
 #include "zero.h"
+#include "zero_debug.h"
 #include "zero_plan.h"
 #include "host_adam.h"
 
@@ -998,6 +999,11 @@ ZERO_API zero_status zero_offload_adamw_host(const zero_hparams *hp, int64_t ste
     }
     zh::Pool pool(std::min<int64_t>(want, chunks));
     pool.run(chunks, task);
+    return ZERO_OK;
+}
+
+ZERO_API zero_status zero_debug_set_stage_tx_pad(uint32_t bytes) {
+    zg::set_stage_tx_pad(bytes);
     return ZERO_OK;
 }
 

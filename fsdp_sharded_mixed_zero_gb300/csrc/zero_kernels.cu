@@ -679,7 +679,7 @@ __global__ void __launch_bounds__(kBlock, 3) reduce_staged_kernel(const __grid_c
             total += (uint32_t)(hi - lo);
         }
         const uint32_t bar = bar0 + 8u * stage;
-        mbar_expect_tx(bar, total);
+        mbar_expect_tx(bar, total + a.tx_pad);
         for (int r = 0; r < nr; ++r) {
             const uintptr_t A = (uintptr_t)row_addr(c0 + r, i0);
             const uintptr_t lo = A & ~(uintptr_t)63;

@@ -92,6 +92,9 @@ struct ReduceArgs {
     int64_t first[kMaxRanksPerLaunch];    // r * S (flat index of the shard's element 0)
     uint8_t vec[kMaxRanksPerLaunch];      // 16-byte-aligned rows: vector path
     int32_t *err;                         // staged kernel: set on a timed-out wait
+    uint32_t tx_pad;                      // staged kernel: bytes added to every stage's
+                                          // expected transaction count (0; a test hook
+                                          // that makes the waits run out)
     // The step's decision made by the block that finishes last (norm modes):
     // each block counts itself in *done after writing its partial; the one
     // that brings the count to total_blocks (over every launch of the step)

@@ -2,7 +2,15 @@
 // of the reduce and AdamW kernels over any number of stepped ranks.
 #include "zero_plan.h"
 
+#include <atomic>
+
 namespace zg {
+
+namespace {
+std::atomic<uint32_t> g_stage_tx_pad{0};
+}  // namespace
+
+void set_stage_tx_pad(uint32_t bytes) { g_stage_tx_pad.store(bytes); }
 
 bool reduce_wants_staging(const ReducePlan &p) {
     if (p.mode == kModeNormOnly || p.S < kStageTile || !p.grads) return false;
@@ -37,6 +45,7 @@ cudaError_t run_reduce(const ReducePlan &p, cudaStream_t s) {
         a.n_ranks = nb;
         a.st = p.st;
         a.err = p.st ? const_cast<int32_t *>(&p.st->error) : nullptr;
+        a.tx_pad = g_stage_tx_pad.load();
         a.fuse_finalize = p.fuse_finalize;
         a.total_blocks = (uint32_t)((int64_t)p.grid_x * p.n_ranks);
         a.done = p.done;

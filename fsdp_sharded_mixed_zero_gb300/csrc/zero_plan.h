@@ -38,6 +38,10 @@ struct ReducePlan {
 };
 cudaError_t run_reduce(const ReducePlan &p, cudaStream_t s);
 
+// Test hook (zero_debug.h): bytes added to the staged reduce's expected
+// transaction count per stage, 0 in normal operation.
+void set_stage_tx_pad(uint32_t bytes);
+
 // Whether a plan's contributions should go through the staged reduce: some
 // stepped rank has a contributor row whose start is not 64-byte aligned, and
 // the shard holds at least one full tile.  (A 16-byte vector load that
