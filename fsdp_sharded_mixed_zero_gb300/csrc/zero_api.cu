@@ -1,6 +1,7 @@
 // zero_api.cu -- host side of the C ABI declared in include/zero.h: argument
 // validation, the flat-parameter layout, device state, scratch management and
-// the three launches of a step.  No arithmetic of the update happens here
+// the launches of a step (the reduce, whose last block makes the step's
+// decision, and the AdamW), and the offload step's host half.  No arithmetic of the update happens here
 // beyond forming the per-step fp32 scalars from the fp64 hyper-parameters.
 #include "zero.h"
 #include "zero_debug.h"

@@ -1,4 +1,4 @@
-// zero_kernels.cu -- the three kernels of one ZeRO shard step on sm_103a.
+// zero_kernels.cu -- the kernels of one ZeRO shard step on sm_103a.
 //
 //   K1 reduce_kernel    N-way reduce of the fp16/bf16/fp32 gradient contributions of
 //                       each stepped shard, AVG, loss-scale division, inf/NaN
