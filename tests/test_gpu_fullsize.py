@@ -1,5 +1,6 @@
 """Full-size parity for the 7B (rank 0 of 8, 842,301,952 params) and 10B
-(rank 7 of 8, 1.25e9 params) shards, in the launch configuration the
+(rank 7 of 8, 1.25e9 params) shards, and for a 2.2e9-element shard (past the
+int32 index range), in the launch configuration the
 benchmark times.  Every step: the oracle reduces the whole gradient (chunks
 copied to the host, reduced by the oracle's own code on host threads, squared
 norm summed exactly), takes the loss-scale / clip decision, and
@@ -27,8 +28,19 @@ CHUNK = 1 << 26
 
 def sample_indices(S, k, seed):
     rng = np.random.default_rng(seed)
-    return np.unique(np.concatenate([np.arange(64), np.arange(S - 64, S),
-                                     rng.integers(0, S, k)])).astype(np.int64)
+    parts = [np.arange(64), np.arange(S - 64, S), rng.integers(0, S, k)]
+    for edge in (1 << 31, 1 << 32):                  # int32 / uint32 index boundaries
+        if S > edge + 64:
+            parts.append(np.arange(edge - 64, edge + 64))
+    return np.unique(np.concatenate(parts)).astype(np.int64)
+
+
+# A shard of more than 2^31 elements (rank 1 of 2, slot starting 4.4 GB into the
+# flat buffer; ~53 GB resident): 64-bit indexing in every kernel.
+HUGE = W.Workload(name="shard_2p2e9", description="2.2e9-element shard, N=2, rank 1",
+                  shapes=[(4_400_000_004,)], world_size=2, ranks=[1], grad_dtype=W.F16, op=AVG,
+                  dynamic=True, steps=2, sigma_g=2e-4, sigma_n=2e-4, seed=9,
+                  grads_layout="slice")
 
 
 def oracle_reduce(ora, dw, w, scale, idx):
@@ -49,7 +61,7 @@ def oracle_reduce(ora, dw, w, scale, idx):
     return ora.norm_sum(acc), of, g_s
 
 
-@pytest.mark.parametrize("w", [W.LLAMA_7B, W.TEN_B, W.TEN_B_F32], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [W.LLAMA_7B, W.TEN_B, W.TEN_B_F32, HUGE], ids=lambda w: w.name)
 def test_fullsize_sampled(ora, w):
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
