@@ -19,7 +19,8 @@ __all__ = [
     "zero_flat_free", "zero_flat_profile_enable", "zero_flat_profile_read",
     "zero_shard_step_noalloc", "zero_grad_accumulate", "zero_shard_step_accumulated",
     "zero_shard_step_q8", "ZERO_Q8_BLOCK", "zero_flat_set_lr", "zero_shard_step_offload",
-    "zero_offload_adamw_host", "zero_debug_set_stage_tx_pad",
+    "zero_offload_adamw_host", "zero_debug_set_stage_tx_pad", "zero_shard_reduce",
+    "zero_shard_apply",
     "zero_status_string", "zero_last_error", "ZeroFlat",
     "LIB_PATH",
 ]
@@ -101,6 +102,9 @@ def _load():
                                               C.c_double, vp, C.POINTER(StepResult)]
     L.zero_flat_set_lr.argtypes = [vp, C.c_double]
     L.zero_debug_set_stage_tx_pad.argtypes = [C.c_uint32]
+    L.zero_shard_reduce.argtypes = [vp, C.POINTER(i32), i32, vp, i64, i64, vp, vp, vp]
+    L.zero_shard_apply.argtypes = [vp, C.POINTER(i32), i32, C.POINTER(vp), C.POINTER(vp),
+                                   C.POINTER(vp), vp, vp, vp, vp, C.POINTER(StepResult)]
     L.zero_shard_step_offload.argtypes = [vp, C.POINTER(i32), i32, vp, i64, i64, C.POINTER(vp),
                                           C.POINTER(vp), C.POINTER(vp), vp, C.c_double, i32,
                                           C.c_double, vp, C.POINTER(StepResult)]
@@ -116,6 +120,7 @@ def _load():
                  "zero_flat_profile_read", "zero_shard_step_noalloc", "zero_grad_accumulate",
                  "zero_shard_step_q8", "zero_flat_set_lr", "zero_shard_step_offload",
                  "zero_offload_adamw_host", "zero_debug_set_stage_tx_pad",
+                 "zero_shard_reduce", "zero_shard_apply",
                  "zero_shard_step_accumulated"):
         getattr(L, name).restype = i32
     return L
@@ -284,6 +289,30 @@ def zero_offload_adamw_host(hp, step_t, clip_coef, g_ptr, master_ptr, m_ptr, v_p
            "zero_offload_adamw_host")
 
 
+def zero_shard_reduce(h, ranks, grads_ptr, grad_ld, grad_rank_offset_mul, norm_sq_ptr,
+                      overflow_ptr, stream=0):
+    """First half of a split step: device totals of this handle's norm^2 and
+    overflow flag."""
+    n = len(ranks)
+    r = (C.c_int32 * n)(*ranks)
+    _check(_lib.zero_shard_reduce(h, r, n, C.c_void_p(grads_ptr), grad_ld, grad_rank_offset_mul,
+                                  C.c_void_p(norm_sq_ptr), C.c_void_p(overflow_ptr),
+                                  C.c_void_p(stream)), "zero_shard_reduce")
+
+
+def zero_shard_apply(h, ranks, master_ptrs, m_ptrs, v_ptrs, out_ptr, norm_sq_ptr, overflow_ptr,
+                     stream=0, want_result=True):
+    """Second half: the decision from the summed device totals, then AdamW."""
+    n = len(ranks)
+    r = (C.c_int32 * n)(*ranks)
+    arrs = [(C.c_void_p * n)(*p) for p in (master_ptrs, m_ptrs, v_ptrs)]
+    res = StepResult() if want_result else None
+    _check(_lib.zero_shard_apply(h, r, n, *arrs, C.c_void_p(out_ptr), C.c_void_p(norm_sq_ptr),
+                                 C.c_void_p(overflow_ptr), C.c_void_p(stream),
+                                 C.byref(res) if res is not None else None), "zero_shard_apply")
+    return res
+
+
 def zero_debug_set_stage_tx_pad(nbytes):
     """Test hook: the staged reduce's waits run out (see include/zero_debug.h)."""
     _check(_lib.zero_debug_set_stage_tx_pad(int(nbytes)), "zero_debug_set_stage_tx_pad")
@@ -436,6 +465,29 @@ class ZeroFlat:
                                        [t.data_ptr() for t in master], [t.data_ptr() for t in m],
                                        [t.data_ptr() for t in v], out.data_ptr(), extra_norm_sq,
                                        n_threads, gpu_share, stream.cuda_stream, want_result)
+
+    def reduce(self, ranks, grads, norm_sq, overflow, grad_rank_offset_mul=None, stream=None):
+        """First half of a split step; norm_sq: float64 CUDA scalar tensor,
+        overflow: int32 CUDA scalar tensor (both written)."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        assert grads.dim() == 2 and grads.stride(1) == 1
+        if grad_rank_offset_mul is None:
+            grad_rank_offset_mul = self.shard_size if len(ranks) > 1 else 0
+        zero_shard_reduce(self.handle, list(ranks), grads.data_ptr(), grads.stride(0),
+                          grad_rank_offset_mul, norm_sq.data_ptr(), overflow.data_ptr(),
+                          stream.cuda_stream)
+
+    def apply(self, ranks, master, m, v, out, norm_sq, overflow, stream=None, want_result=True):
+        """Second half: the decision from the (summed) totals, then AdamW."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        return zero_shard_apply(self.handle, list(ranks), [t.data_ptr() for t in master],
+                                [t.data_ptr() for t in m], [t.data_ptr() for t in v],
+                                out.data_ptr(), norm_sq.data_ptr(), overflow.data_ptr(),
+                                stream.cuda_stream, want_result)
 
     def set_lr(self, lr):
         zero_flat_set_lr(self.handle, lr)

@@ -103,6 +103,9 @@ struct zero_flat {
     cudaEvent_t decided = nullptr;        // the decision read back (caller's stream)
     cudaEvent_t gpu_part_done = nullptr;  // the GPU's share of the update
     bool pageable_access = false;         // the device reads pageable host memory
+    // split step: the ranks whose gradient rows zero_shard_reduce left in the
+    // scratch, waiting for zero_shard_apply
+    std::vector<int32_t> reduced_ranks;
     // per-kernel timing (zero_flat_profile_enable)
     bool profile = false;
     std::vector<cudaEvent_t> ev;      // 4 events per recorded step
@@ -504,8 +507,9 @@ zero_status take_device_error(zero_flat *h, cudaStream_t st) {
 // marks and the optional result read-back.  With host_update (the offload
 // step) K3 and the last timing mark are left to the caller.  Called on the
 // handle's device.
-zero_status launch_step(zero_flat *h, zg::ReducePlan rp, zg::AdamPlan ap, double extra_norm_sq,
-                        cudaStream_t st, zero_step_result *res, bool host_update = false) {
+// Geometry, scratch and the handle's buffers for a reduce plan whose mode,
+// contributions and ranks the caller has set; *parts = norm partials.
+zero_status plan_reduce(zero_flat *h, zg::ReducePlan &rp, int64_t *parts) {
     const int64_t S = h->shard;
     const int64_t batch = std::min<int64_t>(rp.n_ranks, zg::kMaxRanksPerLaunch);
     rp.S = S;
@@ -513,38 +517,49 @@ zero_status launch_step(zero_flat *h, zg::ReducePlan rp, zg::AdamPlan ap, double
     rp.staged = zg::reduce_wants_staging(rp);
     rp.grid_x = zg::grid_x_for(S, batch, h->sm_count,
                                rp.staged ? h->staged_bps[rp.mode] : h->reduce_bps[rp.mode]);
-    ap.grid_x = zg::grid_x_for(S, batch, h->sm_count,
-                               ap.q8 ? zg::kAdamQ8BlocksPerSm : zg::kAdamBlocksPerSm);
-    const int64_t parts = (int64_t)rp.grid_x * rp.n_ranks;
+    *parts = (int64_t)rp.grid_x * rp.n_ranks;
     const int64_t rows = rp.mode == zg::kModeStep ? rp.n_ranks : 0;
-    zero_status s = ensure_scratch(h, rows, parts);
+    zero_status s = ensure_scratch(h, rows, *parts);
     if (s) return s;
     rp.g = h->d_g;
     rp.g_stride = h->g_stride;
     rp.part_ss = h->d_part_ss;
     rp.part_of = h->d_part_of;
-    rp.S = S;
     rp.full_numel = h->full_numel;
-    rp.n_contrib = h->world;
     rp.avg = h->op == ZERO_AVG;
     rp.st = h->d_state;
+    rp.done = h->d_done;
+    return ZERO_OK;
+}
+
+// The handle's scalars, buffers and geometry for an AdamW plan whose state
+// pointers (and accumulators, or int8 outputs) the caller has set.
+void plan_adamw(zero_flat *h, zg::AdamPlan &ap, const int32_t *ranks, int32_t n_ranks) {
+    const int64_t S = h->shard;
+    const int64_t batch = std::min<int64_t>(n_ranks, zg::kMaxRanksPerLaunch);
+    ap.grid_x = zg::grid_x_for(S, batch, h->sm_count,
+                               ap.q8 ? zg::kAdamQ8BlocksPerSm : zg::kAdamBlocksPerSm);
     if (!ap.acc) {
         ap.g = h->d_g;
         ap.g_stride = h->g_stride;
     }
     ap.bf16_out = h->param_dtype == ZERO_BF16;
-    ap.ranks = rp.ranks;
-    ap.n_ranks = rp.n_ranks;
+    ap.ranks = ranks;
+    ap.n_ranks = n_ranks;
     ap.S = S;
     ap.full_numel = h->full_numel;
     ap.b1 = h->b1; ap.b2 = h->b2; ap.omb1 = h->omb1; ap.omb2 = h->omb2;
     ap.lr = h->lr; ap.eps = h->eps; ap.decay = h->decay;
     ap.st = h->d_state;
+}
 
+// The decision's arguments over n_parts partials (or one pair of totals).
+zg::FinalizeArgs decision_args(zero_flat *h, const double *part_ss, const int32_t *part_of,
+                               int32_t n_parts, double extra_norm_sq) {
     zg::FinalizeArgs f{};
-    f.part_ss = h->d_part_ss;
-    f.part_of = h->d_part_of;
-    f.n_parts = S > 0 ? (int32_t)parts : 0;
+    f.part_ss = part_ss;
+    f.part_of = part_of;
+    f.n_parts = n_parts;
     f.dynamic = h->hp.dynamic_loss_scale;
     f.window = h->hp.loss_scale_window;
     f.min_scale = h->min_scale;
@@ -553,10 +568,37 @@ zero_status launch_step(zero_flat *h, zg::ReducePlan rp, zg::AdamPlan ap, double
     f.bc_table = h->d_bc;
     f.bc_len = h->bc_len;
     f.st = h->d_state;
+    return f;
+}
+
+// Copy the step's result to the host (synchronizes `st`).
+zero_status read_result(zero_flat *h, cudaStream_t st, zero_step_result *res) {
+    cudaError_t e = cudaMemcpyAsync(h->h_state, h->d_state, sizeof(zg::DevState),
+                                    cudaMemcpyDeviceToHost, st);
+    if (!e) e = cudaStreamSynchronize(st);
+    if (e) return cuda_fail(e, "reading the step result");
+    res->overflow = h->h_state->res.overflow;
+    res->skipped = h->h_state->res.skipped;
+    res->grad_norm = h->h_state->res.grad_norm;
+    res->clip_coef = h->h_state->res.clip_coef;
+    res->scale_used = h->h_state->res.scale_used;
+    if (h->h_state->error) return take_device_error(h, st);
+    return ZERO_OK;
+}
+
+zero_status launch_step(zero_flat *h, zg::ReducePlan rp, zg::AdamPlan ap, double extra_norm_sq,
+                        cudaStream_t st, zero_step_result *res, bool host_update = false) {
+    const int64_t S = h->shard;
+    h->reduced_ranks.clear();             // this step overwrites a split step's gradient rows
+    int64_t parts = 0;
+    zero_status s = plan_reduce(h, rp, &parts);
+    if (s) return s;
+    plan_adamw(h, ap, rp.ranks, rp.n_ranks);
+    const zg::FinalizeArgs f =
+        decision_args(h, h->d_part_ss, h->d_part_of, S > 0 ? (int32_t)parts : 0, extra_norm_sq);
     // the last reduce block makes the decision (no K2 launch) whenever there
     // is a reduce to count in; an empty shard still needs K2
     rp.fuse_finalize = S > 0;
-    rp.done = h->d_done;
     rp.fin = f;
 
     cudaError_t e;
@@ -569,18 +611,7 @@ zero_status launch_step(zero_flat *h, zg::ReducePlan rp, zg::AdamPlan ap, double
     if (host_update) return ZERO_OK;
     if ((e = zg::run_adamw(ap, st))) return cuda_fail(e, "adamw kernel launch");
     if ((e = mark(h, st))) return cuda_fail(e, "timing event");
-    if (res) {
-        e = cudaMemcpyAsync(h->h_state, h->d_state, sizeof(zg::DevState), cudaMemcpyDeviceToHost, st);
-        if (!e) e = cudaStreamSynchronize(st);
-        if (e) return cuda_fail(e, "reading the step result");
-        res->overflow = h->h_state->res.overflow;
-        res->skipped = h->h_state->res.skipped;
-        res->grad_norm = h->h_state->res.grad_norm;
-        res->clip_coef = h->h_state->res.clip_coef;
-        res->scale_used = h->h_state->res.scale_used;
-        if (h->h_state->error) return take_device_error(h, st);
-    }
-    return ZERO_OK;
+    return res ? read_result(h, st, res) : ZERO_OK;
 }
 
 }  // namespace
@@ -612,6 +643,83 @@ ZERO_API zero_status zero_shard_step(zero_flat *h, const int32_t *ranks, int32_t
     ap.v = v;
     ap.out = flat_param_out;
     return launch_step(h, rp, ap, extra_norm_sq, (cudaStream_t)stream, res);
+}
+
+ZERO_API zero_status zero_shard_reduce(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                                       const void *grads, int64_t grad_ld,
+                                       int64_t grad_rank_offset_mul, double *norm_sq_out,
+                                       int32_t *overflow_out, void *stream) {
+    if (!h) return fail(ZERO_ERR_INVALID_ARG, "handle is NULL");
+    int32_t max_rank = 0;
+    zero_status s;
+    if ((s = check_ranks(h, ranks, n_ranks, &max_rank))) return s;
+    if ((s = check_grads(h, grads, grad_ld, grad_rank_offset_mul, max_rank))) return s;
+    if (!norm_sq_out || !overflow_out) return fail(ZERO_ERR_INVALID_ARG, "NULL output");
+    if ((uintptr_t)norm_sq_out % 8 || (uintptr_t)overflow_out % 4)
+        return fail(ZERO_ERR_ALIGNMENT, "norm_sq_out must be 8-byte, overflow_out 4-byte aligned");
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the handle's device");
+    const cudaStream_t st = (cudaStream_t)stream;
+    zg::ReducePlan rp;
+    rp.mode = zg::kModeStep;
+    rp.grads = grads;
+    rp.in_kind = in_kind_of(h);
+    rp.ld = grad_ld;
+    rp.rank_mul = grad_rank_offset_mul;
+    rp.ranks = ranks;
+    rp.n_ranks = n_ranks;
+    int64_t parts = 0;
+    if ((s = plan_reduce(h, rp, &parts))) return s;
+    cudaError_t e;
+    if (h->shard > 0) {                   // the last block totals the partials
+        zg::FinalizeArgs f = decision_args(h, h->d_part_ss, h->d_part_of, (int32_t)parts, 0.0);
+        f.sum_out = norm_sq_out;
+        f.of_out = overflow_out;
+        rp.fuse_finalize = true;
+        rp.fin = f;
+        e = zg::run_reduce(rp, st);
+    } else {
+        e = cudaMemsetAsync(norm_sq_out, 0, sizeof(double), st);
+        if (!e) e = cudaMemsetAsync(overflow_out, 0, sizeof(int32_t), st);
+    }
+    if (e) return cuda_fail(e, "reduce kernel launch");
+    h->reduced_ranks.assign(ranks, ranks + n_ranks);
+    return ZERO_OK;
+}
+
+ZERO_API zero_status zero_shard_apply(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                                      float *const *master, float *const *m, float *const *v,
+                                      void *flat_param_out, const double *norm_sq,
+                                      const int32_t *overflow, void *stream,
+                                      zero_step_result *res) {
+    if (!h) return fail(ZERO_ERR_INVALID_ARG, "handle is NULL");
+    int32_t max_rank = 0;
+    zero_status s;
+    if ((s = check_ranks(h, ranks, n_ranks, &max_rank))) return s;
+    if ((s = check_update(h, n_ranks, master, m, v, flat_param_out, 0.0))) return s;
+    if (!norm_sq || !overflow) return fail(ZERO_ERR_INVALID_ARG, "NULL total");
+    if ((uintptr_t)norm_sq % 8 || (uintptr_t)overflow % 4)
+        return fail(ZERO_ERR_ALIGNMENT, "norm_sq must be 8-byte, overflow 4-byte aligned");
+    if (h->reduced_ranks.size() != (size_t)n_ranks ||
+        !std::equal(ranks, ranks + n_ranks, h->reduced_ranks.begin()))
+        return fail(ZERO_ERR_INVALID_ARG,
+                    "zero_shard_apply needs the ranks of the preceding zero_shard_reduce");
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the handle's device");
+    const cudaStream_t st = (cudaStream_t)stream;
+    zg::AdamPlan ap;
+    ap.master = master;
+    ap.m = m;
+    ap.v = v;
+    ap.out = flat_param_out;
+    plan_adamw(h, ap, ranks, n_ranks);
+    // the decision from the caller's totals: one "partial" holding them
+    const zg::FinalizeArgs f = decision_args(h, norm_sq, overflow, 1, 0.0);
+    cudaError_t e;
+    if ((e = zg::launch_finalize(f, st))) return cuda_fail(e, "finalize kernel launch");
+    if ((e = zg::run_adamw(ap, st))) return cuda_fail(e, "adamw kernel launch");
+    h->reduced_ranks.clear();
+    return res ? read_result(h, st, res) : ZERO_OK;
 }
 
 ZERO_API zero_status zero_shard_step_q8(zero_flat *h, const int32_t *ranks, int32_t n_ranks,

@@ -238,6 +238,11 @@ __device__ void finalize_block(const FinalizeArgs &a) {
     if (threadIdx.x != 0) return;
     double total = 0.0;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) total += warp_ss[w];
+    if (a.sum_out) {                       // first half of a split step
+        *a.sum_out = total;
+        *a.of_out = of;
+        return;
+    }
 
     ResultDev r;
     r.overflow = of;

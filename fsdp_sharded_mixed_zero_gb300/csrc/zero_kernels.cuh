@@ -70,6 +70,10 @@ struct FinalizeArgs {
     const float2 *bc_table;           // bc_table[t] = {1 - b1^t, 1 - b2^t} as fp32
     int64_t bc_len;                   // entries t >= bc_len are {1, 1}
     DevState *st;
+    // non-NULL: only total the partials into *sum_out and *of_out (the first
+    // half of a split step); no decision, no state change
+    double *sum_out;
+    int32_t *of_out;
 };
 
 // K1: reduce of the N contributions + AVG + unscale + overflow + norm partials.

@@ -56,7 +56,7 @@ typedef enum {
     ZERO_ERR_ALIGNMENT = 3,         /* pointer not aligned to its element size */
     ZERO_ERR_CUDA = 4,              /* a CUDA runtime call failed (see zero_last_error) */
     ZERO_ERR_OVERFLOW_SIZE = 5,     /* a size or offset does not fit in int64 */
-    ZERO_ERR_TIMEOUT = 6,           /* reserved for bounded device waits */
+    ZERO_ERR_TIMEOUT = 6,           /* a bounded device wait gave up; the step was skipped */
     ZERO_ERR_NO_MEMORY = 7          /* host or device allocation failed */
 } zero_status;
 
@@ -228,6 +228,45 @@ zero_status zero_shard_step_accumulated(zero_flat *h, const int32_t *ranks, int3
                                         const float *const *acc, float *const *master,
                                         float *const *m, float *const *v, void *flat_param_out,
                                         double extra_norm_sq, void *stream, zero_step_result *res);
+
+/* The step split at its global decision ("overflow detection and clipping are
+ * one global decision", ZeRO reading §5.3): for a rank that steps several
+ * FlatParameters (one handle each, "PyTorch FSDP ... 深度解析" §3.1: one
+ * FlatParameter per wrapped module) with one clip norm and one loss-scale
+ * decision, and the point where a multi-GPU caller would all-reduce the two
+ * scalars across ranks.
+ *
+ * zero_shard_reduce: K1 exactly as in zero_shard_step -- the reduce, unscale
+ * (by the handle's current loss scale), overflow check and norm partials,
+ * the unscaled gradient rows kept in the handle's scratch -- and its last
+ * block writes this handle's totals to DEVICE memory:
+ *     *norm_sq_out = sum of g^2 over the stepped shards (fp64),
+ *     *overflow_out = 1 if any g is inf/NaN, else 0.
+ * No decision, no state change.  norm_sq_out 8-byte and overflow_out 4-byte
+ * aligned device pointers.  Asynchronous on `stream`.
+ *
+ * zero_shard_apply: the decision from the caller's totals -- *norm_sq (the
+ * SUM of the norm_sq_out of every FlatParameter the decision covers, and of
+ * every rank's) and *overflow (their MAX), both device memory -- through the
+ * handle's loss-scale state machine exactly as zero_shard_step decides, then
+ * AdamW and the cast on the gradient rows the preceding zero_shard_reduce
+ * left.  Each handle of a group applies the same totals, so all take the
+ * same skip / clip / scale decision.  `ranks` must equal those of the
+ * preceding zero_shard_reduce on this handle, with no other step on the
+ * handle in between, and `stream` must be ordered after that reduce and after
+ * the writes of the totals.  res: as for zero_shard_step.
+ *
+ * zero_shard_reduce followed by zero_shard_apply with its own totals is
+ * bit-identical to zero_shard_step.  Errors: as for zero_shard_step;
+ * INVALID_ARG for NULL totals or ranks that differ from the reduce's (or no
+ * pending reduce); ALIGNMENT for misaligned totals. */
+zero_status zero_shard_reduce(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                              const void *grads, int64_t grad_ld, int64_t grad_rank_offset_mul,
+                              double *norm_sq_out, int32_t *overflow_out, void *stream);
+zero_status zero_shard_apply(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                             float *const *master, float *const *m, float *const *v,
+                             void *flat_param_out, const double *norm_sq,
+                             const int32_t *overflow, void *stream, zero_step_result *res);
 
 /* ZeRO-Offload shard step: the optimizer update runs on the host CPU cores
  * ("DeepSpeed 与 FSDP" §ZeRO-Offload: the reduced gradients move to the CPU,
