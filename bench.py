@@ -70,6 +70,11 @@ def parse_args():
                    help="host threads of the offload update (0: every available CPU)")
     p.add_argument("--offload-gpu-share", type=float, default=0.0,
                    help="fraction of each shard the GPU updates over the host link")
+    p.add_argument("--group", type=int, default=0,
+                   help="time a group of this many FlatParameters (one rank's shard each) "
+                        "stepped with one global decision, against per-FlatParameter steps")
+    p.add_argument("--group-params", type=int, default=1_000_000,
+                   help="params in each group member's shard")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -648,6 +653,101 @@ def run_offload(args, w):
     group.close()
 
 
+def run_group(args):
+    """M FlatParameters (N=8, rank 7's shard of group_params each, fp16 AVG,
+    dynamic loss scale) stepped three ways: one zero_group_step (one global
+    decision, two launches per 64 members); the split step per member with
+    the totals summed on the device (the same global decision, two launches
+    per member plus the decision); and one zero_shard_step per member (a
+    decision per member -- a timing baseline only)."""
+    import torch
+    import fsdp_sharded_mixed_zero_gb300 as Z
+    from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
+    from synth.workloads import AVG, F16, Workload
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    group = RankGroup(backend="nccl", device=dev)
+    M, P = args.group, args.group_params
+    ws = [Workload(name="member%d" % k, description="", shapes=[(8 * P,)], world_size=8,
+                   ranks=[7], grad_dtype=F16, op=AVG, dynamic=True, steps=1, sigma_g=1e-3,
+                   sigma_n=1e-3, grads_layout="slice", seed=k) for k in range(M)]
+    ds = [DeviceWorkload(w, device=dev) for w in ws]
+    for d in ds:
+        d.gen_grads(0, d.scaler().scale)
+    grp = Z.ZeroGroup([d.flat for d in ds])
+    margs = [dict(ranks=w.ranks, grads=d.grads, master=d.master, m=d.m, v=d.v, out=d.out,
+                  grad_rank_offset_mul=0) for w, d in zip(ws, ds)]
+    ss = [torch.zeros((), dtype=torch.float64, device=dev) for _ in ds]
+    of = [torch.zeros((), dtype=torch.int32, device=dev) for _ in ds]
+    stream = torch.cuda.current_stream(dev)
+
+    def grouped():
+        grp.step(margs, stream=stream, want_result=False)
+
+    def split():
+        for w, d, a, b in zip(ws, ds, ss, of):
+            d.flat.reduce(w.ranks, d.grads, a, b, grad_rank_offset_mul=0, stream=stream)
+        tot, mx = torch.stack(ss).sum(), torch.stack(of).max()
+        for w, d in zip(ws, ds):
+            d.flat.apply(w.ranks, d.master, d.m, d.v, d.out, tot, mx, stream=stream,
+                         want_result=False)
+
+    def per_member():
+        for d in ds:
+            d.step(want_result=False, stream=stream)
+
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = str(local)
+    times = {}
+    clocks = None
+    for name, fn in (("group", grouped), ("split", split), ("per_flat_parameter", per_member)):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        sampler = ClockSampler(uuid) if name == "group" else None
+        if sampler:
+            sampler.start()
+        group.barrier()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        group.barrier()
+        if sampler:
+            clocks = sampler.stop()
+        times[name] = group.max(e0.elapsed_time(e1))
+    res = grp.step(margs, stream=stream)
+    assert res.skipped == 0 and res.overflow == 0, "benchmark inputs overflowed"
+    params = M * ds[0].S
+    n_batches = -(-M // 64)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": whole_job_value(params, args.steps, world, times["group"]),
+            "unit": "Gparams/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": times["group"] / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "group%dx%d" % (M, ds[0].S), "flat_parameters": M,
+                       "params_per_flat_parameter_shard": ds[0].S, "emulated_world_size": 8,
+                       "stepped_ranks": [7], "parallelism": "replicas%d" % world},
+            "compare_ms_per_step": {k: v / args.steps for k, v in times.items()},
+            "clocks": clocks,
+            "gpu_launches": 2 * n_batches * args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    grp.close()
+    for d in ds:
+        d.close()
+    group.close()
+
+
 def main():
     args = parse_args()
     from synth.workloads import BY_NAME
@@ -656,6 +756,8 @@ def main():
         run_reference(args, w)
     elif args.offload:
         run_offload(args, w)
+    elif args.group:
+        run_group(args)
     else:
         run_ours(args, w)
 

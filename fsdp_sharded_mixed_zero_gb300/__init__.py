@@ -20,7 +20,7 @@ __all__ = [
     "zero_shard_step_noalloc", "zero_grad_accumulate", "zero_shard_step_accumulated",
     "zero_shard_step_q8", "ZERO_Q8_BLOCK", "zero_flat_set_lr", "zero_shard_step_offload",
     "zero_offload_adamw_host", "zero_debug_set_stage_tx_pad", "zero_shard_reduce",
-    "zero_shard_apply",
+    "zero_shard_apply", "GroupMember", "ZeroGroup",
     "zero_status_string", "zero_last_error", "ZeroFlat",
     "LIB_PATH",
 ]
@@ -69,6 +69,13 @@ class StepResult(C.Structure):
                 ("clip_coef", C.c_float), ("scale_used", C.c_float)]
 
 
+class GroupMember(C.Structure):
+    _fields_ = [("ranks", C.POINTER(C.c_int32)), ("n_ranks", C.c_int32), ("grads", C.c_void_p),
+                ("grad_ld", C.c_int64), ("grad_rank_offset_mul", C.c_int64),
+                ("master", C.POINTER(C.c_void_p)), ("m", C.POINTER(C.c_void_p)),
+                ("v", C.POINTER(C.c_void_p)), ("flat_param_out", C.c_void_p)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError("libzero_gb300.so is not built (expected at %s); run "
@@ -103,6 +110,13 @@ def _load():
     L.zero_flat_set_lr.argtypes = [vp, C.c_double]
     L.zero_debug_set_stage_tx_pad.argtypes = [C.c_uint32]
     L.zero_shard_reduce.argtypes = [vp, C.POINTER(i32), i32, vp, i64, i64, vp, vp, vp]
+    L.zero_group_init.argtypes = [C.POINTER(vp), i32, C.POINTER(vp)]
+    L.zero_group_step.argtypes = [vp, C.POINTER(GroupMember), C.c_double, vp,
+                                  C.POINTER(StepResult)]
+    L.zero_group_loss_scaler_state.argtypes = [vp, C.POINTER(ScalerState), vp]
+    L.zero_group_set_loss_scaler_state.argtypes = [vp, C.POINTER(ScalerState), vp]
+    L.zero_group_set_lr.argtypes = [vp, C.c_double]
+    L.zero_group_free.argtypes = [vp]
     L.zero_shard_apply.argtypes = [vp, C.POINTER(i32), i32, C.POINTER(vp), C.POINTER(vp),
                                    C.POINTER(vp), vp, vp, vp, vp, C.POINTER(StepResult)]
     L.zero_shard_step_offload.argtypes = [vp, C.POINTER(i32), i32, vp, i64, i64, C.POINTER(vp),
@@ -120,7 +134,9 @@ def _load():
                  "zero_flat_profile_read", "zero_shard_step_noalloc", "zero_grad_accumulate",
                  "zero_shard_step_q8", "zero_flat_set_lr", "zero_shard_step_offload",
                  "zero_offload_adamw_host", "zero_debug_set_stage_tx_pad",
-                 "zero_shard_reduce", "zero_shard_apply",
+                 "zero_shard_reduce", "zero_shard_apply", "zero_group_init", "zero_group_step",
+                 "zero_group_loss_scaler_state", "zero_group_set_loss_scaler_state",
+                 "zero_group_set_lr", "zero_group_free",
                  "zero_shard_step_accumulated"):
         getattr(L, name).restype = i32
     return L
@@ -311,6 +327,70 @@ def zero_shard_apply(h, ranks, master_ptrs, m_ptrs, v_ptrs, out_ptr, norm_sq_ptr
                                  C.c_void_p(overflow_ptr), C.c_void_p(stream),
                                  C.byref(res) if res is not None else None), "zero_shard_apply")
     return res
+
+
+class ZeroGroup:
+    """FlatParameters of one rank stepped together with one global decision.
+
+    members: ZeroFlat objects sharing world size, dtypes, op and hparams.
+    step(args): args[k] = dict(ranks, grads, master, m, v, out[, grad_rank_offset_mul])
+    for member k, torch CUDA tensors as for ZeroFlat.step."""
+
+    def __init__(self, members):
+        self.members = list(members)
+        arr = (C.c_void_p * len(self.members))(*[f.handle for f in self.members])
+        h = C.c_void_p()
+        _check(_lib.zero_group_init(arr, len(self.members), C.byref(h)), "zero_group_init")
+        self.handle = h.value
+
+    def step(self, args, extra_norm_sq=0.0, stream=None, want_result=True):
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        keep = []                                   # ctypes arrays alive for the call
+        ms = (GroupMember * len(args))()
+        for k, (f, a) in enumerate(zip(self.members, args)):
+            ranks = list(a["ranks"])
+            mul = a.get("grad_rank_offset_mul")
+            if mul is None:
+                mul = f.shard_size if len(ranks) > 1 else 0
+            g = a["grads"]
+            assert g.dim() == 2 and g.stride(1) == 1
+            r = (C.c_int32 * len(ranks))(*ranks)
+            arrs = [(C.c_void_p * len(ranks))(*[t.data_ptr() for t in a[name]])
+                    for name in ("master", "m", "v")]
+            keep += [r] + arrs
+            ms[k] = GroupMember(r, len(ranks), g.data_ptr(), g.stride(0), mul, arrs[0], arrs[1],
+                                arrs[2], a["out"].data_ptr())
+        res = StepResult() if want_result else None
+        _check(_lib.zero_group_step(self.handle, ms, float(extra_norm_sq),
+                                    C.c_void_p(stream.cuda_stream),
+                                    C.byref(res) if res is not None else None), "zero_group_step")
+        return res
+
+    def scaler_state(self, stream=None):
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        st = ScalerState()
+        _check(_lib.zero_group_loss_scaler_state(self.handle, C.byref(st),
+                                                 C.c_void_p(stream.cuda_stream)),
+               "zero_group_loss_scaler_state")
+        return st
+
+    def set_lr(self, lr):
+        _check(_lib.zero_group_set_lr(self.handle, float(lr)), "zero_group_set_lr")
+
+    def close(self):
+        if getattr(self, "handle", None):
+            _lib.zero_group_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def zero_debug_set_stage_tx_pad(nbytes):

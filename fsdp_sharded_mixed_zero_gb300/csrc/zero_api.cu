@@ -140,6 +140,28 @@ zero_status build_bc_table(zero_flat *h) {
     return ZERO_OK;
 }
 
+// The loss-scale state of a new handle (scale from the hyper-parameters), the
+// block counter, the pinned read-back block and the bias-correction table.
+zero_status init_device_state(zero_flat *h) {
+    zg::DevState init{};
+    init.scaler.scale = h->hp.dynamic_loss_scale ? (float)std::ldexp(1.0, h->hp.initial_scale_power)
+                                                 : (float)h->hp.static_loss_scale;
+    init.bc1 = init.bc2 = 1.0f;
+    cudaError_t e = cudaMalloc(&h->d_state, sizeof(zg::DevState));
+    if (e) { h->d_state = nullptr; return cuda_fail(e, "cudaMalloc(state)"); }
+    h->device_bytes += sizeof(zg::DevState);
+    e = cudaMemcpy(h->d_state, &init, sizeof(init), cudaMemcpyHostToDevice);
+    if (e) return cuda_fail(e, "cudaMemcpy(state)");
+    e = cudaMalloc(&h->d_done, sizeof(uint32_t));
+    if (e) { h->d_done = nullptr; return cuda_fail(e, "cudaMalloc(block counter)"); }
+    e = cudaMemset(h->d_done, 0, sizeof(uint32_t));
+    if (e) return cuda_fail(e, "cudaMemset(block counter)");
+    h->device_bytes += sizeof(uint32_t);
+    e = cudaMallocHost(&h->h_state, sizeof(zg::DevState));
+    if (e) { h->h_state = nullptr; return cuda_fail(e, "cudaMallocHost(state)"); }
+    return build_bc_table(h);
+}
+
 zero_status validate_hparams(const zero_hparams *hp) {
     if (!hp) return fail(ZERO_ERR_INVALID_ARG, "hparams is NULL");
     auto finite = [](double x) { return std::isfinite(x); };
@@ -385,22 +407,7 @@ ZERO_API zero_status zero_flat_init(const zero_param_info *infos, int32_t n_info
     h->decay = (float)(1.0 - hp->lr * hp->weight_decay);
     h->min_scale = (float)hp->min_loss_scale;
 
-    zg::DevState init{};
-    init.scaler.scale = hp->dynamic_loss_scale ? (float)std::ldexp(1.0, hp->initial_scale_power)
-                                               : (float)hp->static_loss_scale;
-    init.bc1 = init.bc2 = 1.0f;
-    e = cudaMalloc(&h->d_state, sizeof(zg::DevState));
-    if (e) { release(h); return cuda_fail(e, "cudaMalloc(state)"); }
-    h->device_bytes += sizeof(zg::DevState);
-    e = cudaMemcpy(h->d_state, &init, sizeof(init), cudaMemcpyHostToDevice);
-    if (e) { release(h); return cuda_fail(e, "cudaMemcpy(state)"); }
-    e = cudaMalloc(&h->d_done, sizeof(uint32_t));
-    if (!e) e = cudaMemset(h->d_done, 0, sizeof(uint32_t));
-    if (e) { release(h); return cuda_fail(e, "cudaMalloc(block counter)"); }
-    h->device_bytes += sizeof(uint32_t);
-    e = cudaMallocHost(&h->h_state, sizeof(zg::DevState));
-    if (e) { h->h_state = nullptr; release(h); return cuda_fail(e, "cudaMallocHost(state)"); }
-    s = build_bc_table(h);
+    s = init_device_state(h);
     if (s) { release(h); return s; }
     *out = h;
     return ZERO_OK;
@@ -1159,6 +1166,183 @@ ZERO_API zero_status zero_set_loss_scaler_state(zero_flat *h, const zero_scaler_
                         cudaMemcpyHostToDevice, st);
     if (!e) e = cudaStreamSynchronize(st);
     if (e) return cuda_fail(e, "writing the loss-scale state");
+    return ZERO_OK;
+}
+
+// ------------------------------------------------------------------ groups
+struct zero_group {
+    zero_flat *core = nullptr;            // the group's state, table, counter and partials
+    std::vector<zero_flat *> members;
+};
+
+namespace {
+
+bool same_hparams(const zero_hparams &a, const zero_hparams &b) {
+    return a.lr == b.lr && a.beta1 == b.beta1 && a.beta2 == b.beta2 && a.eps == b.eps &&
+           a.weight_decay == b.weight_decay && a.max_grad_norm == b.max_grad_norm &&
+           a.dynamic_loss_scale == b.dynamic_loss_scale &&
+           a.initial_scale_power == b.initial_scale_power &&
+           a.loss_scale_window == b.loss_scale_window && a.reserved == b.reserved &&
+           a.static_loss_scale == b.static_loss_scale && a.min_loss_scale == b.min_loss_scale;
+}
+
+}  // namespace
+
+ZERO_API zero_status zero_group_init(zero_flat *const *members, int32_t n_members,
+                                     zero_group **out) {
+    if (!out) return fail(ZERO_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!members || n_members < 1) return fail(ZERO_ERR_INVALID_ARG, "need at least one member");
+    const zero_flat *a = members[0];
+    for (int32_t k = 0; k < n_members; ++k) {
+        const zero_flat *b = members[k];
+        if (!b) return fail(ZERO_ERR_INVALID_ARG, "member %d is NULL", k);
+        for (int32_t q = 0; q < k; ++q)
+            if (members[q] == b) return fail(ZERO_ERR_INVALID_ARG, "member %d listed twice", k);
+        if (b->device != a->device || b->world != a->world || b->grad_dtype != a->grad_dtype ||
+            b->param_dtype != a->param_dtype || b->op != a->op || !same_hparams(b->hp, a->hp))
+            return fail(ZERO_ERR_INVALID_ARG,
+                        "member %d differs from member 0 (device, world size, dtypes, op or "
+                        "hyper-parameters)", k);
+    }
+    DeviceGuard guard(a->device);
+    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the members' device");
+    zero_group *g = new (std::nothrow) zero_group;
+    zero_flat *c = g ? new (std::nothrow) zero_flat : nullptr;
+    if (!c) { delete g; return fail(ZERO_ERR_NO_MEMORY, "host allocation failed"); }
+    g->core = c;
+    c->device = a->device;
+    c->sm_count = a->sm_count;
+    for (int k = 0; k < 4; ++k) c->reduce_bps[k] = a->reduce_bps[k];
+    for (int k = 0; k < 3; ++k) c->staged_bps[k] = a->staged_bps[k];
+    c->world = a->world;
+    c->grad_dtype = a->grad_dtype;
+    c->param_dtype = a->param_dtype;
+    c->op = a->op;
+    c->hp = a->hp;
+    c->b1 = a->b1; c->b2 = a->b2; c->omb1 = a->omb1; c->omb2 = a->omb2;
+    c->lr = a->lr; c->eps = a->eps; c->decay = a->decay; c->min_scale = a->min_scale;
+    zero_status s = init_device_state(c);
+    if (s) { release(c); delete g; return s; }
+    g->members.assign(members, members + n_members);
+    *out = g;
+    return ZERO_OK;
+}
+
+ZERO_API zero_status zero_group_step(zero_group *g, const zero_group_member *args,
+                                     double extra_norm_sq, void *stream, zero_step_result *res) {
+    if (!g || !args) return fail(ZERO_ERR_INVALID_ARG, "NULL argument");
+    if (!std::isfinite(extra_norm_sq) || extra_norm_sq < 0)
+        return fail(ZERO_ERR_INVALID_ARG, "extra_norm_sq must be finite and >= 0");
+    zero_flat *c = g->core;
+    zero_status s;
+    for (size_t k = 0; k < g->members.size(); ++k) {
+        const zero_flat *mk = g->members[k];
+        const zero_group_member &x = args[k];
+        int32_t max_rank = 0;
+        if ((s = check_ranks(mk, x.ranks, x.n_ranks, &max_rank)) ||
+            (s = check_update(mk, x.n_ranks, x.master, x.m, x.v, x.flat_param_out, 0.0)) ||
+            (s = check_grads(mk, x.grads, x.grad_ld, x.grad_rank_offset_mul, max_rank))) {
+            char msg[512];
+            snprintf(msg, sizeof(msg), "member %zu: %s", k, g_last_error);
+            return fail(s, "%s", msg);
+        }
+    }
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the group's device");
+    const cudaStream_t st = (cudaStream_t)stream;
+    // every (member, stepped rank) row, in member order
+    std::vector<zg::ReduceRow> rrows, part;
+    std::vector<zg::AdamRow> arows;
+    int64_t max_s = 0;
+    for (size_t k = 0; k < g->members.size(); ++k) {
+        zero_flat *mk = g->members[k];
+        const zero_group_member &x = args[k];
+        if ((s = ensure_scratch(mk, x.n_ranks, 0))) return s;
+        mk->reduced_ranks.clear();        // this step overwrites the member's scratch
+        zg::ReducePlan p;
+        p.mode = zg::kModeStep;
+        p.grads = x.grads;
+        p.in_kind = in_kind_of(mk);
+        p.ld = x.grad_ld;
+        p.rank_mul = x.grad_rank_offset_mul;
+        p.ranks = x.ranks;
+        p.n_ranks = x.n_ranks;
+        p.S = mk->shard;
+        p.full_numel = mk->full_numel;
+        p.g = mk->d_g;
+        p.g_stride = mk->g_stride;
+        zg::reduce_rows_of(p, part);
+        rrows.insert(rrows.end(), part.begin(), part.end());
+        for (int32_t j = 0; j < x.n_ranks; ++j) {
+            const int64_t r = x.ranks[j];
+            zg::AdamRow w;
+            w.g = mk->d_g + (int64_t)j * mk->g_stride;
+            w.master = x.master[j];
+            w.m = x.m[j];
+            w.v = x.v[j];
+            w.out = static_cast<uint16_t *>(x.flat_param_out) + r * mk->shard;
+            w.S = mk->shard;
+            w.valid = part[j].valid;
+            arows.push_back(w);
+        }
+        max_s = std::max(max_s, mk->shard);
+    }
+    const int32_t n_rows = (int32_t)rrows.size();
+    const int64_t batch = std::min<int64_t>(n_rows, zg::kMaxRanksPerLaunch);
+    zg::ReducePlan rp;
+    rp.mode = zg::kModeStep;
+    rp.in_kind = in_kind_of(c);
+    rp.n_contrib = c->world;
+    rp.avg = c->op == ZERO_AVG;
+    rp.st = c->d_state;
+    rp.done = c->d_done;
+    rp.staged = zg::rows_want_staging(rp.mode, rp.in_kind, rp.n_contrib, rrows.data(), n_rows);
+    rp.grid_x = zg::grid_x_for(max_s, batch, c->sm_count,
+                               rp.staged ? c->staged_bps[rp.mode] : c->reduce_bps[rp.mode]);
+    const int64_t parts = (int64_t)rp.grid_x * n_rows;
+    if ((s = ensure_scratch(c, 0, parts))) return s;
+    rp.part_ss = c->d_part_ss;
+    rp.part_of = c->d_part_of;
+    const zg::FinalizeArgs f =
+        decision_args(c, c->d_part_ss, c->d_part_of, max_s > 0 ? (int32_t)parts : 0, extra_norm_sq);
+    rp.fuse_finalize = max_s > 0;
+    rp.fin = f;
+    zg::AdamPlan ap;
+    ap.bf16_out = c->param_dtype == ZERO_BF16;
+    ap.b1 = c->b1; ap.b2 = c->b2; ap.omb1 = c->omb1; ap.omb2 = c->omb2;
+    ap.lr = c->lr; ap.eps = c->eps; ap.decay = c->decay;
+    ap.st = c->d_state;
+    ap.grid_x = zg::grid_x_for(max_s, batch, c->sm_count, zg::kAdamBlocksPerSm);
+    cudaError_t e;
+    if ((e = zg::run_reduce_rows(rp, rrows.data(), n_rows, st))) return cuda_fail(e, "reduce kernel launch");
+    if (!rp.fuse_finalize && (e = zg::launch_finalize(f, st)))
+        return cuda_fail(e, "finalize kernel launch");
+    if ((e = zg::run_adamw_rows(ap, arows.data(), n_rows, st))) return cuda_fail(e, "adamw kernel launch");
+    return res ? read_result(c, st, res) : ZERO_OK;
+}
+
+ZERO_API zero_status zero_group_loss_scaler_state(zero_group *g, zero_scaler_state *out,
+                                                  void *stream) {
+    if (!g) return fail(ZERO_ERR_INVALID_ARG, "group is NULL");
+    return zero_loss_scaler_state(g->core, out, stream);
+}
+
+ZERO_API zero_status zero_group_set_loss_scaler_state(zero_group *g, const zero_scaler_state *in,
+                                                      void *stream) {
+    if (!g) return fail(ZERO_ERR_INVALID_ARG, "group is NULL");
+    return zero_set_loss_scaler_state(g->core, in, stream);
+}
+
+ZERO_API zero_status zero_group_set_lr(zero_group *g, double lr) {
+    if (!g) return fail(ZERO_ERR_INVALID_ARG, "group is NULL");
+    return zero_flat_set_lr(g->core, lr);
+}
+
+ZERO_API zero_status zero_group_free(zero_group *g) {
+    if (!g) return ZERO_OK;
+    release(g->core);
+    delete g;
     return ZERO_OK;
 }
 

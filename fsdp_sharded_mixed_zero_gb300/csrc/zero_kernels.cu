@@ -343,7 +343,10 @@ __device__ __forceinline__ float elem_to_f32(const typename InTraits<kIn>::T *p)
     else return to_f32<kIn == kInBF16>(*p);
 }
 
-template <int kIn, int kMode>
+// kOneShape: every row of the launch has the same contributor row stride and
+// shard size (one FlatParameter), read as ld[0] and S[0] -- constant operands
+// rather than registers held across the loops.
+template <int kIn, int kMode, bool kOneShape = true>
 __global__ void __launch_bounds__(kBlock, (reduce_min_blocks<kIn, kMode>()))
 reduce_kernel(const __grid_constant__ ReduceArgs a) {
     using T = typename InTraits<kIn>::T;
@@ -351,14 +354,13 @@ reduce_kernel(const __grid_constant__ ReduceArgs a) {
     constexpr int kB = InTraits<kIn>::kBatch;
     constexpr bool kNorm = kMode == kModeStep || kMode == kModeNormOnly;
     const int j = blockIdx.y;
-    const int64_t S = a.S;
-    int64_t valid = a.full_numel - a.first[j];   // elements [valid, S) are padding
-    valid = valid < 0 ? 0 : (valid > S ? S : valid);
+    const int64_t S = kOneShape ? a.S[0] : a.S[j];
+    const int64_t valid = a.valid[j];             // elements [valid, S) are padding
     const T *base = static_cast<const T *>(a.in[j]);
-    float *g = a.g + (int64_t)j * a.g_stride;
+    float *g = a.g[j];
     float *acc_out = a.acc[j];
     const int N = a.n_contrib;
-    const int64_t ld = a.ld;
+    const int64_t ld = kOneShape ? a.ld[0] : a.ld[j];
     const bool avg = a.avg != 0;
     const Divisor dn = make_divisor((float)N);
     const Divisor ds = make_divisor(kNorm ? a.st->scaler.scale : 1.0f);
@@ -646,15 +648,14 @@ __global__ void __launch_bounds__(kBlock, 3) reduce_staged_kernel(const __grid_c
     unsigned char *slots = smem + ST::kHeader;
 
     const int j = blockIdx.y;
-    const int64_t S = a.S;
-    int64_t valid = a.full_numel - a.first[j];
-    valid = valid < 0 ? 0 : (valid > S ? S : valid);
+    const int64_t S = a.S[j];
+    const int64_t valid = a.valid[j];
     const T *base = static_cast<const T *>(a.in[j]);
     const unsigned char *bbase = static_cast<const unsigned char *>(a.in[j]);
-    float *g = a.g + (int64_t)j * a.g_stride;
+    float *g = a.g[j];
     float *acc_out = a.acc[j];
     const int N = a.n_contrib;
-    const int64_t ld = a.ld;
+    const int64_t ld = a.ld[j];
     const bool avg = a.avg != 0;
     const Divisor dn = make_divisor((float)N);
     const Divisor ds = make_divisor(kNorm ? a.st->scaler.scale : 1.0f);
@@ -883,11 +884,10 @@ __global__ void __launch_bounds__(kBlock) adamw_kernel(const __grid_constant__ A
     float *mm = a.m[j];
     float *vv = a.v[j];
     const float *g = a.g[j];
-    uint16_t *out = reinterpret_cast<uint16_t *>(a.out) + a.out_off[j];
-    const int64_t S = a.S;
+    uint16_t *out = a.out[j];
+    const int64_t S = a.S[j];
     const Divisor ds = make_divisor(kFromAcc ? st->res.scale_used : 1.0f);
-    int64_t valid = a.full_numel - a.out_off[j];
-    valid = valid < 0 ? 0 : (valid > S ? S : valid);
+    const int64_t valid = a.valid[j];
     auto grad = [&](float x, int64_t i) {
         if constexpr (kFromAcc) return i < valid ? divide(x, ds) : 0.0f;
         else return x;
@@ -976,10 +976,10 @@ __global__ void __launch_bounds__(kBlock) adamw_q8_kernel(const __grid_constant_
     float *mm = a.m[j];
     float *vv = a.v[j];
     const float *g = a.g[j];
-    uint16_t *out = a.out ? reinterpret_cast<uint16_t *>(a.out) + a.out_off[j] : nullptr;
-    int8_t *q8 = a.q8 + a.out_off[j];
-    float *scales = a.q8_scales + a.q8_scale_off[j];
-    const int64_t S = a.S;
+    uint16_t *out = a.out[j];
+    int8_t *q8 = a.q8[j];
+    float *scales = a.q8_scales[j];
+    const int64_t S = a.S[j];
     const bool vec = a.vec[j] != 0;
     const int oal = a.out_align[j];
     const bool q8vec = a.q8_align[j] == 8;
@@ -1112,6 +1112,17 @@ static cudaError_t launch_staged(const ReduceArgs &a, dim3 grid, cudaStream_t s)
     return cudaGetLastError();
 }
 
+template <int kIn, bool kOneShape>
+static cudaError_t launch_plain(const ReduceArgs &a, dim3 grid, int mode, cudaStream_t s) {
+    switch (mode) {
+        case kModeStep: reduce_kernel<kIn, kModeStep, kOneShape><<<grid, kBlock, 0, s>>>(a); break;
+        case kModeAccFirst: reduce_kernel<kIn, kModeAccFirst, kOneShape><<<grid, kBlock, 0, s>>>(a); break;
+        case kModeAccAdd: reduce_kernel<kIn, kModeAccAdd, kOneShape><<<grid, kBlock, 0, s>>>(a); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
 template <int kIn>
 static cudaError_t launch_reduce_in(const ReduceArgs &a, dim3 grid, int mode, bool staged,
                                     cudaStream_t s) {
@@ -1123,13 +1134,11 @@ static cudaError_t launch_reduce_in(const ReduceArgs &a, dim3 grid, int mode, bo
             default: return cudaErrorInvalidValue;
         }
     }
-    switch (mode) {
-        case kModeStep: reduce_kernel<kIn, kModeStep><<<grid, kBlock, 0, s>>>(a); break;
-        case kModeAccFirst: reduce_kernel<kIn, kModeAccFirst><<<grid, kBlock, 0, s>>>(a); break;
-        case kModeAccAdd: reduce_kernel<kIn, kModeAccAdd><<<grid, kBlock, 0, s>>>(a); break;
-        default: return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
+    bool one_shape = true;
+    for (int32_t j = 1; j < a.n_ranks; ++j)
+        one_shape = one_shape && a.ld[j] == a.ld[0] && a.S[j] == a.S[0];
+    return one_shape ? launch_plain<kIn, true>(a, grid, mode, s)
+                     : launch_plain<kIn, false>(a, grid, mode, s);
 }
 
 cudaError_t launch_reduce(const ReduceArgs &a, int grid_x, int in_kind, int mode, bool staged,

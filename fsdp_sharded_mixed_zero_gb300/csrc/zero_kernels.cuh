@@ -77,23 +77,24 @@ struct FinalizeArgs {
 };
 
 // K1: reduce of the N contributions + AVG + unscale + overflow + norm partials.
+// Row j of a launch (blockIdx.y) is one stepped rank's shard of one
+// FlatParameter; rows may come from different FlatParameters that share the
+// contributor count, the op and the contribution encoding.
 struct ReduceArgs {
-    int64_t ld;                       // contributor row stride, elements
-    int64_t S;                        // shard size
-    int64_t full_numel;
-    float *g;                         // kModeStep: reduced gradient rows, row j at g + j*g_stride
-    int64_t g_stride;
     double *part_ss;                  // per-block partial sums of squares
     int32_t *part_of;                 // per-block overflow flags
     int32_t part_base;                // partial index = part_base + j*gridDim.x + blockIdx.x
     int32_t n_contrib;
     int32_t avg;
-    int32_t n_ranks;
+    int32_t n_ranks;                  // rows in this launch
     const DevState *st;
-    const void *in[kMaxRanksPerLaunch];   // contributor 0's element 0 of rank j's slice
-                                          // (kModeNormOnly: the rank's accumulator)
-    float *acc[kMaxRanksPerLaunch];       // kModeAccFirst / kModeAccAdd: rank j's accumulator
-    int64_t first[kMaxRanksPerLaunch];    // r * S (flat index of the shard's element 0)
+    const void *in[kMaxRanksPerLaunch];   // contributor 0's element 0 of row j's slice
+                                          // (kModeNormOnly: the row's accumulator)
+    float *g[kMaxRanksPerLaunch];         // kModeStep: row j's reduced-gradient output
+    float *acc[kMaxRanksPerLaunch];       // kModeAccFirst / kModeAccAdd: row j's accumulator
+    int64_t S[kMaxRanksPerLaunch];        // row j's shard size
+    int64_t valid[kMaxRanksPerLaunch];    // elements [valid, S) are padding
+    int64_t ld[kMaxRanksPerLaunch];       // contributor row stride of row j, elements
     uint8_t vec[kMaxRanksPerLaunch];      // 16-byte-aligned rows: vector path
     int32_t *err;                         // staged kernel: set on a timed-out wait
     uint32_t tx_pad;                      // staged kernel: bytes added to every stage's
@@ -112,26 +113,25 @@ struct ReduceArgs {
 // Elements per block tile of the staged reduce (one 8-element chunk per thread).
 constexpr int kStageTile = kBlock * kVec;
 
-// K3: AdamW + cast into the flat buffer.
+// K3: AdamW + cast into the flat buffer; row j (blockIdx.y) as for K1.
 struct AdamArgs {
-    int64_t S;
-    int64_t full_numel;
     float b1, b2, omb1, omb2, lr, eps, decay;
-    int32_t n_ranks;
+    int32_t n_ranks;                  // rows in this launch
     const DevState *st;
-    void *out;                        // flat 16-bit buffer
-    const float *g[kMaxRanksPerLaunch];   // reduced gradient row of rank j (or its accumulator)
+    const float *g[kMaxRanksPerLaunch];   // reduced gradient row j (or its accumulator)
     float *master[kMaxRanksPerLaunch];
     float *m[kMaxRanksPerLaunch];
     float *v[kMaxRanksPerLaunch];
-    int64_t out_off[kMaxRanksPerLaunch];  // r * S
+    uint16_t *out[kMaxRanksPerLaunch];    // row j's slot in its flat 16-bit buffer
+                                          // (adamw_q8_kernel: may be NULL)
+    int64_t S[kMaxRanksPerLaunch];        // elements updated in row j
+    int64_t valid[kMaxRanksPerLaunch];    // from accumulators: [valid, S) is padding
     uint8_t vec[kMaxRanksPerLaunch];      // g/master/m/v 16-byte aligned
     uint8_t out_align[kMaxRanksPerLaunch];// byte alignment of the output slot: 16, 4 or 2
-    // int8 all-gather payload (adamw_q8_kernel only): codes in the flat int8
-    // buffer at out_off, one fp32 scale per kQ8Block elements of the shard
-    int8_t *q8;
-    float *q8_scales;
-    int64_t q8_scale_off[kMaxRanksPerLaunch];  // r * ceil(S / kQ8Block)
+    // int8 all-gather payload (adamw_q8_kernel only): row j's codes and its
+    // one fp32 scale per kQ8Block elements
+    int8_t *q8[kMaxRanksPerLaunch];
+    float *q8_scales[kMaxRanksPerLaunch];
     uint8_t q8_align[kMaxRanksPerLaunch];      // 8: 8-byte code stores, else byte stores
 };
 

@@ -12,31 +12,59 @@ std::atomic<uint32_t> g_stage_tx_pad{0};
 
 void set_stage_tx_pad(uint32_t bytes) { g_stage_tx_pad.store(bytes); }
 
-bool reduce_wants_staging(const ReducePlan &p) {
-    if (p.mode == kModeNormOnly || p.S < kStageTile || !p.grads) return false;
+void reduce_rows_of(const ReducePlan &p, std::vector<ReduceRow> &rows) {
     const size_t esize = p.in_kind == kInF32 ? 4 : 2;
-    const bool rows_vary = p.n_contrib > 1 && ((size_t)p.ld * esize) % 64 != 0;
-    bool any = false;
+    rows.resize(p.n_ranks);
     for (int32_t j = 0; j < p.n_ranks; ++j) {
-        const uintptr_t base = (uintptr_t)p.grads + (uintptr_t)(p.ranks[j] * p.rank_mul) * esize;
-        any = any || rows_vary || base % 64 != 0;
-        if ((p.mode == kModeAccFirst || p.mode == kModeAccAdd) && (uintptr_t)p.acc_out[j] % 16)
-            return false;
+        const int64_t r = p.ranks[j];
+        ReduceRow &w = rows[j];
+        if (p.mode == kModeNormOnly) {
+            w.in = p.acc_in[j];
+            w.ld = 0;
+        } else {
+            w.in = static_cast<const char *>(p.grads) + (size_t)(r * p.rank_mul) * esize;
+            w.ld = p.ld;
+        }
+        w.S = p.S;
+        int64_t valid = p.full_numel - r * p.S;
+        w.valid = valid < 0 ? 0 : (valid > p.S ? p.S : valid);
+        w.g = p.g ? p.g + (int64_t)j * p.g_stride : nullptr;
+        w.acc = (p.mode == kModeAccFirst || p.mode == kModeAccAdd) ? p.acc_out[j] : nullptr;
     }
-    return any;
 }
 
-cudaError_t run_reduce(const ReducePlan &p, cudaStream_t s) {
-    if (p.S <= 0) return cudaSuccess;
+bool rows_want_staging(int mode, int in_kind, int32_t n_contrib, const ReduceRow *rows,
+                       int32_t n_rows) {
+    if (mode == kModeNormOnly) return false;
+    const size_t esize = in_kind == kInF32 ? 4 : 2;
+    bool any = false, tile = false;
+    for (int32_t j = 0; j < n_rows; ++j) {
+        const ReduceRow &w = rows[j];
+        if (!w.in) return false;
+        if ((mode == kModeAccFirst || mode == kModeAccAdd) && (uintptr_t)w.acc % 16) return false;
+        const bool rows_vary = n_contrib > 1 && ((size_t)w.ld * esize) % 64 != 0;
+        any = any || rows_vary || (uintptr_t)w.in % 64 != 0;
+        tile = tile || w.S >= kStageTile;
+    }
+    return any && tile;
+}
+
+bool reduce_wants_staging(const ReducePlan &p) {
+    if (p.mode == kModeNormOnly || !p.grads) return false;
+    std::vector<ReduceRow> rows;
+    reduce_rows_of(p, rows);
+    return rows_want_staging(p.mode, p.in_kind, p.n_contrib, rows.data(), p.n_ranks);
+}
+
+cudaError_t run_reduce_rows(const ReducePlan &p, const ReduceRow *rows, int32_t n_rows,
+                            cudaStream_t s) {
     const size_t esize = p.in_kind == kInF32 ? 4 : 2;
-    for (int32_t b0 = 0; b0 < p.n_ranks; b0 += kMaxRanksPerLaunch) {
-        const int32_t nb = p.n_ranks - b0 < kMaxRanksPerLaunch ? p.n_ranks - b0 : kMaxRanksPerLaunch;
+    int64_t max_s = 0;
+    for (int32_t j = 0; j < n_rows; ++j) max_s = rows[j].S > max_s ? rows[j].S : max_s;
+    if (max_s <= 0) return cudaSuccess;
+    for (int32_t b0 = 0; b0 < n_rows; b0 += kMaxRanksPerLaunch) {
+        const int32_t nb = n_rows - b0 < kMaxRanksPerLaunch ? n_rows - b0 : kMaxRanksPerLaunch;
         ReduceArgs a{};
-        a.ld = p.ld;
-        a.S = p.S;
-        a.full_numel = p.full_numel;
-        a.g = p.g ? p.g + (int64_t)b0 * p.g_stride : nullptr;
-        a.g_stride = p.g_stride;
         a.part_ss = p.part_ss;
         a.part_of = p.part_of;
         a.part_base = b0 * p.grid_x;
@@ -47,27 +75,67 @@ cudaError_t run_reduce(const ReducePlan &p, cudaStream_t s) {
         a.err = p.st ? const_cast<int32_t *>(&p.st->error) : nullptr;
         a.tx_pad = g_stage_tx_pad.load();
         a.fuse_finalize = p.fuse_finalize;
-        a.total_blocks = (uint32_t)((int64_t)p.grid_x * p.n_ranks);
+        a.total_blocks = (uint32_t)((int64_t)p.grid_x * n_rows);
         a.done = p.done;
         a.fin = p.fin;
         for (int32_t j = 0; j < nb; ++j) {
-            const int64_t r = p.ranks[b0 + j];
-            bool vec;
-            if (p.mode == kModeNormOnly) {
-                a.in[j] = p.acc_in[b0 + j];
-                vec = (uintptr_t)a.in[j] % 16 == 0;
-            } else {
-                a.in[j] = static_cast<const char *>(p.grads) + (size_t)(r * p.rank_mul) * esize;
-                vec = (uintptr_t)a.in[j] % 16 == 0 && ((size_t)p.ld * esize) % 16 == 0;
-            }
-            if (p.mode == kModeAccFirst || p.mode == kModeAccAdd) {
-                a.acc[j] = p.acc_out[b0 + j];
-                vec = vec && (uintptr_t)a.acc[j] % 16 == 0;
-            }
-            a.first[j] = r * p.S;
+            const ReduceRow &w = rows[b0 + j];
+            a.in[j] = w.in;
+            a.g[j] = w.g;
+            a.acc[j] = w.acc;
+            a.S[j] = w.S;
+            a.valid[j] = w.valid;
+            a.ld[j] = w.ld;
+            bool vec = (uintptr_t)w.in % 16 == 0;
+            if (p.mode != kModeNormOnly) vec = vec && ((size_t)w.ld * esize) % 16 == 0;
+            if (p.mode == kModeAccFirst || p.mode == kModeAccAdd)
+                vec = vec && (uintptr_t)w.acc % 16 == 0;
             a.vec[j] = vec;
         }
         const cudaError_t e = launch_reduce(a, p.grid_x, p.in_kind, p.mode, p.staged, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t run_reduce(const ReducePlan &p, cudaStream_t s) {
+    if (p.S <= 0) return cudaSuccess;
+    std::vector<ReduceRow> rows;
+    reduce_rows_of(p, rows);
+    return run_reduce_rows(p, rows.data(), p.n_ranks, s);
+}
+
+cudaError_t run_adamw_rows(const AdamPlan &p, const AdamRow *rows, int32_t n_rows,
+                           cudaStream_t s) {
+    int64_t max_s = 0;
+    for (int32_t j = 0; j < n_rows; ++j) max_s = rows[j].S > max_s ? rows[j].S : max_s;
+    if (max_s <= 0) return cudaSuccess;
+    for (int32_t b0 = 0; b0 < n_rows; b0 += kMaxRanksPerLaunch) {
+        const int32_t nb = n_rows - b0 < kMaxRanksPerLaunch ? n_rows - b0 : kMaxRanksPerLaunch;
+        AdamArgs a{};
+        a.b1 = p.b1; a.b2 = p.b2; a.omb1 = p.omb1; a.omb2 = p.omb2;
+        a.lr = p.lr; a.eps = p.eps; a.decay = p.decay;
+        a.n_ranks = nb;
+        a.st = p.st;
+        for (int32_t j = 0; j < nb; ++j) {
+            const AdamRow &w = rows[b0 + j];
+            a.g[j] = w.g;
+            a.master[j] = w.master;
+            a.m[j] = w.m;
+            a.v[j] = w.v;
+            a.out[j] = w.out;
+            a.S[j] = w.S;
+            a.valid[j] = w.valid;
+            a.vec[j] = (uintptr_t)w.g % 16 == 0 && (uintptr_t)w.master % 16 == 0 &&
+                       (uintptr_t)w.m % 16 == 0 && (uintptr_t)w.v % 16 == 0;
+            const uintptr_t addr = (uintptr_t)w.out;
+            a.out_align[j] = addr % 16 == 0 ? 16 : (addr % 4 == 0 ? 4 : 2);
+            a.q8[j] = w.q8;
+            a.q8_scales[j] = w.q8_scales;
+            a.q8_align[j] = (uintptr_t)w.q8 % 8 == 0 ? 8 : 1;
+        }
+        const cudaError_t e = p.q8 ? launch_adamw_q8(a, p.grid_x, p.bf16_out, s)
+                                   : launch_adamw(a, p.grid_x, p.bf16_out, p.acc != nullptr, s);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -78,39 +146,24 @@ cudaError_t run_adamw(const AdamPlan &p, cudaStream_t s) {
     if (count <= 0) return cudaSuccess;
     if (count > p.S) return cudaErrorInvalidValue;
     if (p.q8 && (p.acc || count != p.S)) return cudaErrorInvalidValue;  // whole shards only
-    for (int32_t b0 = 0; b0 < p.n_ranks; b0 += kMaxRanksPerLaunch) {
-        const int32_t nb = p.n_ranks - b0 < kMaxRanksPerLaunch ? p.n_ranks - b0 : kMaxRanksPerLaunch;
-        AdamArgs a{};
-        a.S = count;                                   // the kernels' element range per rank
-        a.full_numel = p.full_numel;
-        a.b1 = p.b1; a.b2 = p.b2; a.omb1 = p.omb1; a.omb2 = p.omb2;
-        a.lr = p.lr; a.eps = p.eps; a.decay = p.decay;
-        a.n_ranks = nb;
-        a.st = p.st;
-        a.out = p.out;
-        for (int32_t j = 0; j < nb; ++j) {
-            const int64_t r = p.ranks[b0 + j];
-            a.g[j] = p.acc ? p.acc[b0 + j] : p.g + (int64_t)(b0 + j) * p.g_stride;
-            a.master[j] = p.master[b0 + j];
-            a.m[j] = p.m[b0 + j];
-            a.v[j] = p.v[b0 + j];
-            a.out_off[j] = r * p.S;
-            a.vec[j] = (uintptr_t)a.g[j] % 16 == 0 && (uintptr_t)a.master[j] % 16 == 0 &&
-                       (uintptr_t)a.m[j] % 16 == 0 && (uintptr_t)a.v[j] % 16 == 0;
-            const uintptr_t addr = (uintptr_t)p.out + (uintptr_t)(r * p.S) * 2;
-            a.out_align[j] = addr % 16 == 0 ? 16 : (addr % 4 == 0 ? 4 : 2);
-            if (p.q8) {
-                a.q8_scale_off[j] = r * ((p.S + kQ8Block - 1) / kQ8Block);
-                a.q8_align[j] = ((uintptr_t)(p.q8 + r * p.S)) % 8 == 0 ? 8 : 1;
-            }
+    std::vector<AdamRow> rows(p.n_ranks);
+    for (int32_t j = 0; j < p.n_ranks; ++j) {
+        const int64_t r = p.ranks[j];
+        AdamRow &w = rows[j];
+        w.g = p.acc ? p.acc[j] : p.g + (int64_t)j * p.g_stride;
+        w.master = p.master[j];
+        w.m = p.m[j];
+        w.v = p.v[j];
+        w.out = p.out ? static_cast<uint16_t *>(p.out) + r * p.S : nullptr;
+        w.S = count;                                   // the kernels' element range per rank
+        int64_t valid = p.full_numel - r * p.S;
+        w.valid = valid < 0 ? 0 : (valid > count ? count : valid);
+        if (p.q8) {
+            w.q8 = p.q8 + r * p.S;
+            w.q8_scales = p.q8_scales + r * ((p.S + kQ8Block - 1) / kQ8Block);
         }
-        a.q8 = p.q8;
-        a.q8_scales = p.q8_scales;
-        const cudaError_t e = p.q8 ? launch_adamw_q8(a, p.grid_x, p.bf16_out, s)
-                                   : launch_adamw(a, p.grid_x, p.bf16_out, p.acc != nullptr, s);
-        if (e != cudaSuccess) return e;
     }
-    return cudaSuccess;
+    return run_adamw_rows(p, rows.data(), p.n_ranks, s);
 }
 
 }  // namespace zg

@@ -6,6 +6,8 @@
 
 #include "zero_kernels.cuh"
 
+#include <vector>
+
 namespace zg {
 
 // Host-side planning of one kernel class over any number of stepped ranks
@@ -37,6 +39,28 @@ struct ReducePlan {
     FinalizeArgs fin{};
 };
 cudaError_t run_reduce(const ReducePlan &p, cudaStream_t s);
+
+// One row of a reduce launch: a stepped rank's shard of one FlatParameter.
+struct ReduceRow {
+    const void *in = nullptr;         // contributor 0's element 0 of the slice
+                                      // (kModeNormOnly: the accumulator)
+    int64_t ld = 0;                   // contributor row stride, elements
+    int64_t S = 0;                    // shard size
+    int64_t valid = 0;                // elements [valid, S) are padding
+    float *g = nullptr;               // kModeStep: reduced-gradient output row
+    float *acc = nullptr;             // kModeAccFirst / kModeAccAdd: accumulator
+};
+// The rows of a single-FlatParameter plan (its ranks, in order).
+void reduce_rows_of(const ReducePlan &p, std::vector<ReduceRow> &rows);
+// Whether rows should take the staged reduce (a row start off a 64-byte
+// boundary, a row with a full tile, and every accumulator 16-byte aligned).
+bool rows_want_staging(int mode, int in_kind, int32_t n_contrib, const ReduceRow *rows,
+                       int32_t n_rows);
+// The launches of a reduce over any rows: p supplies the launch-wide settings
+// (mode, encoding, contributor count, op, state, partials, grid, staging,
+// decision); total_blocks of the decision counts every row.
+cudaError_t run_reduce_rows(const ReducePlan &p, const ReduceRow *rows, int32_t n_rows,
+                            cudaStream_t s);
 
 // Test hook (zero_debug.h): bytes added to the staged reduce's expected
 // transaction count per stage, 0 in normal operation.
@@ -70,6 +94,22 @@ struct AdamPlan {
                                       // the output slot of rank r still starts at r * S
 };
 cudaError_t run_adamw(const AdamPlan &p, cudaStream_t s);
+
+// One row of an AdamW launch.
+struct AdamRow {
+    const float *g = nullptr;         // reduced gradient (or accumulator) row
+    float *master = nullptr, *m = nullptr, *v = nullptr;
+    uint16_t *out = nullptr;          // the row's slot in its flat 16-bit buffer
+    int64_t S = 0;                    // elements updated
+    int64_t valid = 0;                // from accumulators: [valid, S) is padding
+    int8_t *q8 = nullptr;             // int8 payload of the slot, and its scales
+    float *q8_scales = nullptr;
+};
+// The launches of AdamW over any rows: p supplies the scalars, state, output
+// encoding, accumulator mode (p.acc non-NULL), int8 mode (p.q8 non-NULL) and
+// grid.
+cudaError_t run_adamw_rows(const AdamPlan &p, const AdamRow *rows, int32_t n_rows,
+                           cudaStream_t s);
 
 // Launch geometry, measured on GB300 (152 SMs) on the 10B rank-7 step.  The
 // AdamW kernel streams four arrays in and four out and is fastest with exactly

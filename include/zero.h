@@ -268,6 +268,53 @@ zero_status zero_shard_apply(zero_flat *h, const int32_t *ranks, int32_t n_ranks
                              void *flat_param_out, const double *norm_sq,
                              const int32_t *overflow, void *stream, zero_step_result *res);
 
+/* A group: the FlatParameters one rank steps together ("PyTorch FSDP ...
+ * 深度解析" §3.1: one FlatParameter per wrapped module) with one clip norm and
+ * one loss-scale decision (ZeRO reading §5.3), in one reduce launch and one
+ * AdamW launch per 64 (member, stepped rank) rows instead of two launches per
+ * FlatParameter.  The members are existing handles that share world_size,
+ * grad and param dtypes, op and every zero_hparams field; the group takes
+ * its hyper-parameters from the first member and owns its own loss-scale
+ * state (initialised as a new handle's), bias-correction table and norm
+ * partials; the members' own loss-scale states are not used by group steps.
+ * A member's handle supplies its layout and its reduced-gradient scratch, so
+ * a handle should be stepped either alone or in groups, not both in one
+ * step.  Errors: INVALID_ARG (no members, NULL, members that differ, a
+ * member listed twice, members on another device), NO_MEMORY, CUDA. */
+typedef struct zero_group zero_group;
+zero_status zero_group_init(zero_flat *const *members, int32_t n_members, zero_group **out);
+
+/* The arguments of one member in a group step, exactly those of
+ * zero_shard_step for that member's handle. */
+typedef struct {
+    const int32_t *ranks;
+    int32_t n_ranks;
+    const void *grads;
+    int64_t grad_ld;
+    int64_t grad_rank_offset_mul;
+    float *const *master;
+    float *const *m;
+    float *const *v;
+    void *flat_param_out;
+} zero_group_member;
+
+/* One step of every member (args[k] for the group's member k): the reduce
+ * of every member's stepped shards with the group's loss scale, one global
+ * norm over all of them plus extra_norm_sq, one overflow decision and loss-
+ * scale update, then AdamW and the cast into every member's slot -- the same
+ * per-element arithmetic as zero_shard_step.  Asynchronous on `stream` when
+ * res is NULL.  Errors: as for zero_shard_step, per member. */
+zero_status zero_group_step(zero_group *g, const zero_group_member *args, double extra_norm_sq,
+                            void *stream, zero_step_result *res);
+
+/* The group's loss-scale state (synchronizes `stream`), its restore, and its
+ * learning rate (as zero_flat_set_lr). */
+zero_status zero_group_loss_scaler_state(zero_group *g, zero_scaler_state *out, void *stream);
+zero_status zero_group_set_loss_scaler_state(zero_group *g, const zero_scaler_state *in,
+                                             void *stream);
+zero_status zero_group_set_lr(zero_group *g, double lr);
+zero_status zero_group_free(zero_group *g);
+
 /* ZeRO-Offload shard step: the optimizer update runs on the host CPU cores
  * ("DeepSpeed 与 FSDP" §ZeRO-Offload: the reduced gradients move to the CPU,
  * the CPU updates the fp32 master weights with Adam, and the 16-bit weights

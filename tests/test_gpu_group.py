@@ -1,0 +1,173 @@
+"""Group steps (zero_group_step): the FlatParameters of one rank -- one
+handle each, different shapes, layouts and shard sizes -- stepped with one
+clip norm and one loss-scale decision in one reduce launch and one AdamW
+launch per 64 (member, rank) rows.  Compared with the oracle's single global
+decision over all members (exact norm of the union, one ora_scaler_decide,
+AdamW per member), a one-member group with zero_shard_step bit for bit, and
+the launch count checked with the CUDA profiler."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from synth.workloads import AVG, F16, Workload  # noqa: E402
+
+import tests.oracle_runner as runner  # noqa: E402
+from tests.gpu_helpers import (NORM_RTOL, assert_params_close, assert_state, f32,  # noqa: E402
+                               host_grads, u16)
+
+pytestmark = pytest.mark.gpu
+
+
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+
+
+def _wl(name, shapes, N, ranks, layout="full", inf_at=None, seed=1, steps=3):
+    return Workload(name=name, description=name, shapes=shapes, world_size=N, ranks=ranks,
+                    grad_dtype=F16, op=AVG, dynamic=True, steps=steps, sigma_g=1e-3,
+                    sigma_n=1e-3, inf_at=inf_at, grads_layout=layout, seed=seed)
+
+
+def _args(w, d):
+    return dict(ranks=w.ranks, grads=d.grads, master=d.master, m=d.m, v=d.v, out=d.out,
+                grad_rank_offset_mul=w.grad_rank_mul)
+
+
+def run_group_parity(ora, ws, steps=3):
+    """Step the members ws as one group on the GPU and in the oracle."""
+    import fsdp_sharded_mixed_zero_gb300 as Z
+    from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
+    hp = ora.hparams(**ws[0].hparams_kwargs())
+    ds = [DeviceWorkload(w, out_fill=0x5A5A) for w in ws]
+    group = Z.ZeroGroup([d.flat for d in ds])
+    try:
+        state = [([f32(t).copy() for t in d.master], [f32(t).copy() for t in d.m],
+                  [f32(t).copy() for t in d.v], u16(d.out).copy()) for d in ds]
+        st = ora.scaler_init(hp)
+        skipped = []
+        for step in range(steps):
+            assert group.scaler_state().as_tuple() == st.as_tuple()
+            scale = st.scale
+            grads = []
+            for d in ds:
+                d.gen_grads(step, scale)
+                grads.append(host_grads(d.grads))
+            res = group.step([_args(w, d) for w, d in zip(ws, ds)])
+            gs = []
+            for w, d, g in zip(ws, ds, grads):
+                for r in w.ranks:
+                    x = np.empty(max(d.S, 1), np.float32)[:d.S]
+                    runner.reduce_rank(g, w.grad_ld, r * w.grad_rank_mul, w.world_size, d.S,
+                                       r * d.S, d.full, True, scale, False, x)
+                    gs.append(x)
+            acc, of = runner.norm_exact(gs)
+            norm = float(np.sqrt(ora.norm_sum(acc)))
+            coef, skip = ora.scaler_decide(hp, st, of, norm)
+            assert (res.overflow, res.skipped, res.scale_used) == (of, skip, scale)
+            if not of:
+                assert abs(res.grad_norm - norm) <= NORM_RTOL * norm
+                assert abs(res.clip_coef - coef) <= NORM_RTOL * coef
+            k = 0
+            for w, d, (master, m, v, out) in zip(ws, ds, state):
+                for j, r in enumerate(w.ranks):
+                    if not skip:
+                        ora.adamw_cast(hp, st.step_t, coef, gs[k], master[j], m[j], v[j],
+                                       out=out[r * d.S:(r + 1) * d.S])
+                    k += 1
+                    assert_state(f32(d.master[j]), f32(d.m[j]), f32(d.v[j]), master[j], m[j],
+                                 v[j], tag=" (%s, step %d, rank %d)" % (w.name, step, r))
+                assert_params_close(u16(d.out), out, False, "%s params (step %d)" % (w.name, step))
+            skipped.append(skip)
+        assert group.scaler_state().as_tuple() == st.as_tuple()
+        return skipped
+    finally:
+        group.close()
+        for d in ds:
+            d.close()
+
+
+def test_group_of_four_flat_parameters(ora):
+    _need_gpu()
+    ws = [
+        _wl("attn_all_shards", [(256, 768), (768,)], 8, list(range(8)), seed=21),
+        _wl("mlp_slice_rank5", [(768, 3072), (3072,)], 8, [5], layout="slice", seed=22,
+            inf_at=(1, 6, 1000)),
+        _wl("odd_all_shards", [(80_001,)], 8, list(range(8)), seed=23),     # staged rows
+        _wl("norm_small", [(768,), (768,)], 8, [0, 3], seed=24),            # below one tile
+    ]
+    assert run_group_parity(ora, ws) == [0, 1, 0]
+
+
+def test_group_of_seventy_members_in_two_launches_each(ora):
+    _need_gpu()
+    ws = [_wl("m%02d" % k, [(2_000 + 37 * k,)], 4, [k % 4], layout="slice", seed=100 + k,
+              steps=2) for k in range(70)]
+    assert run_group_parity(ora, ws, steps=2) == [0, 0]
+    # launch count: 70 rows -> 2 reduce launches and 2 AdamW launches
+    import fsdp_sharded_mixed_zero_gb300 as Z
+    from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
+    from torch.profiler import ProfilerActivity, profile
+    ds = [DeviceWorkload(w) for w in ws]
+    group = Z.ZeroGroup([d.flat for d in ds])
+    try:
+        for d in ds:
+            d.gen_grads(0, group.scaler_state().scale)
+        args = [_args(w, d) for w, d in zip(ws, ds)]
+        names = []
+        for _ in range(2):                   # the profiler's first session may be empty
+            with profile(activities=[ProfilerActivity.CUDA]) as prof:
+                group.step(args, want_result=False)
+                torch.cuda.synchronize()
+            names = [e.name for e in prof.events() if "zg::" in e.name or "kernel" in e.name]
+            if names:
+                break
+        if names:
+            assert sum("reduce" in n for n in names) == 2, names
+            assert sum("adamw" in n for n in names) == 2, names
+    finally:
+        group.close()
+        for d in ds:
+            d.close()
+
+
+def test_one_member_group_equals_the_shard_step():
+    _need_gpu()
+    import fsdp_sharded_mixed_zero_gb300 as Z
+    from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
+    w = _wl("solo", [(300_007,)], 4, [0, 1, 2, 3], inf_at=(1, 3, 9), steps=4)
+    a, b = DeviceWorkload(w), DeviceWorkload(w)
+    group = Z.ZeroGroup([b.flat])
+    try:
+        for step in range(w.steps):
+            a.gen_grads(step, a.scaler().scale)
+            b.grads.copy_(a.grads)
+            ra = a.step()
+            rb = group.step([_args(w, b)])
+            assert (ra.overflow, ra.skipped, ra.grad_norm, ra.clip_coef, ra.scale_used) == \
+                   (rb.overflow, rb.skipped, rb.grad_norm, rb.clip_coef, rb.scale_used)
+        for x, y in zip(a.master + a.m + a.v, b.master + b.m + b.v):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+        assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+        assert a.scaler().as_tuple() == group.scaler_state().as_tuple()
+    finally:
+        group.close()
+        a.close()
+        b.close()
+
+
+def test_group_rejects_mismatched_members():
+    _need_gpu()
+    import fsdp_sharded_mixed_zero_gb300 as Z
+    f4 = Z.ZeroFlat([(1000,)], 4)
+    f8 = Z.ZeroFlat([(1000,)], 8)
+    f4b = Z.ZeroFlat([(1000,)], 4, hp=Z.hparams(lr=1e-4))
+    try:
+        for members in ([f4, f8], [f4, f4b], [f4, f4]):
+            with pytest.raises(Z.ZeroError) as e:
+                Z.ZeroGroup(members)
+            assert e.value.status == 1
+    finally:
+        for f in (f4, f8, f4b):
+            f.close()
