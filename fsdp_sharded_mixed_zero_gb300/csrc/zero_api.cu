@@ -1244,7 +1244,7 @@ ZERO_API zero_status zero_group_step(zero_group *g, const zero_group_member *arg
             (s = check_update(mk, x.n_ranks, x.master, x.m, x.v, x.flat_param_out, 0.0)) ||
             (s = check_grads(mk, x.grads, x.grad_ld, x.grad_rank_offset_mul, max_rank))) {
             char msg[512];
-            snprintf(msg, sizeof(msg), "member %zu: %s", k, g_last_error);
+            snprintf(msg, sizeof(msg), "member %zu: %.480s", k, g_last_error);
             return fail(s, "%s", msg);
         }
     }

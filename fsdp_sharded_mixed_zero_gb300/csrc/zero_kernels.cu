@@ -343,9 +343,10 @@ __device__ __forceinline__ float elem_to_f32(const typename InTraits<kIn>::T *p)
     else return to_f32<kIn == kInBF16>(*p);
 }
 
-// kOneShape: every row of the launch has the same contributor row stride and
-// shard size (one FlatParameter), read as ld[0] and S[0] -- constant operands
-// rather than registers held across the loops.
+// kOneShape: the rows of the launch are one FlatParameter's -- the same
+// contributor row stride and shard size, read as ld[0] and S[0], and evenly
+// spaced gradient rows, g[0] + j * g_stride -- constant operands rather than
+// registers held across the loops.
 template <int kIn, int kMode, bool kOneShape = true>
 __global__ void __launch_bounds__(kBlock, (reduce_min_blocks<kIn, kMode>()))
 reduce_kernel(const __grid_constant__ ReduceArgs a) {
@@ -355,9 +356,15 @@ reduce_kernel(const __grid_constant__ ReduceArgs a) {
     constexpr bool kNorm = kMode == kModeStep || kMode == kModeNormOnly;
     const int j = blockIdx.y;
     const int64_t S = kOneShape ? a.S[0] : a.S[j];
-    const int64_t valid = a.valid[j];             // elements [valid, S) are padding
+    int64_t valid;                                // elements [valid, S) are padding
+    if constexpr (kOneShape) {
+        valid = a.full_numel - a.first[j];
+        valid = valid < 0 ? 0 : (valid > S ? S : valid);
+    } else {
+        valid = a.valid[j];
+    }
     const T *base = static_cast<const T *>(a.in[j]);
-    float *g = a.g[j];
+    float *g = kOneShape ? a.g[0] + (int64_t)j * a.g_stride : a.g[j];
     float *acc_out = a.acc[j];
     const int N = a.n_contrib;
     const int64_t ld = kOneShape ? a.ld[0] : a.ld[j];
@@ -1136,7 +1143,9 @@ static cudaError_t launch_reduce_in(const ReduceArgs &a, dim3 grid, int mode, bo
     }
     bool one_shape = true;
     for (int32_t j = 1; j < a.n_ranks; ++j)
-        one_shape = one_shape && a.ld[j] == a.ld[0] && a.S[j] == a.S[0];
+        one_shape = one_shape && a.ld[j] == a.ld[0] && a.S[j] == a.S[0] &&
+                    (mode != kModeStep || a.g[j] == a.g[0] + (int64_t)j * a.g_stride);
+    if (a.full_numel < 0) one_shape = false;      // rows of several FlatParameters
     return one_shape ? launch_plain<kIn, true>(a, grid, mode, s)
                      : launch_plain<kIn, false>(a, grid, mode, s);
 }

@@ -91,9 +91,13 @@ struct ReduceArgs {
     const void *in[kMaxRanksPerLaunch];   // contributor 0's element 0 of row j's slice
                                           // (kModeNormOnly: the row's accumulator)
     float *g[kMaxRanksPerLaunch];         // kModeStep: row j's reduced-gradient output
+    int64_t g_stride;                     // g[j] == g[0] + j * g_stride when the rows are
+                                          // one FlatParameter's (0: not evenly spaced)
     float *acc[kMaxRanksPerLaunch];       // kModeAccFirst / kModeAccAdd: row j's accumulator
     int64_t S[kMaxRanksPerLaunch];        // row j's shard size
     int64_t valid[kMaxRanksPerLaunch];    // elements [valid, S) are padding
+    int64_t full_numel;                   // one-FlatParameter launches: valid is
+    int64_t first[kMaxRanksPerLaunch];    // clamp(full_numel - first[j], 0, S)
     int64_t ld[kMaxRanksPerLaunch];       // contributor row stride of row j, elements
     uint8_t vec[kMaxRanksPerLaunch];      // 16-byte-aligned rows: vector path
     int32_t *err;                         // staged kernel: set on a timed-out wait

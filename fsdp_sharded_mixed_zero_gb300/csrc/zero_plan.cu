@@ -28,6 +28,7 @@ void reduce_rows_of(const ReducePlan &p, std::vector<ReduceRow> &rows) {
         w.S = p.S;
         int64_t valid = p.full_numel - r * p.S;
         w.valid = valid < 0 ? 0 : (valid > p.S ? p.S : valid);
+        w.first = r * p.S;
         w.g = p.g ? p.g + (int64_t)j * p.g_stride : nullptr;
         w.acc = (p.mode == kModeAccFirst || p.mode == kModeAccAdd) ? p.acc_out[j] : nullptr;
     }
@@ -57,7 +58,7 @@ bool reduce_wants_staging(const ReducePlan &p) {
 }
 
 cudaError_t run_reduce_rows(const ReducePlan &p, const ReduceRow *rows, int32_t n_rows,
-                            cudaStream_t s) {
+                            cudaStream_t s, bool one_flat_parameter) {
     const size_t esize = p.in_kind == kInF32 ? 4 : 2;
     int64_t max_s = 0;
     for (int32_t j = 0; j < n_rows; ++j) max_s = rows[j].S > max_s ? rows[j].S : max_s;
@@ -68,6 +69,8 @@ cudaError_t run_reduce_rows(const ReducePlan &p, const ReduceRow *rows, int32_t 
         a.part_ss = p.part_ss;
         a.part_of = p.part_of;
         a.part_base = b0 * p.grid_x;
+        a.g_stride = p.g_stride;
+        a.full_numel = one_flat_parameter ? p.full_numel : -1;
         a.n_contrib = p.mode == kModeNormOnly ? 1 : p.n_contrib;
         a.avg = p.mode == kModeNormOnly ? 0 : p.avg;
         a.n_ranks = nb;
@@ -85,6 +88,7 @@ cudaError_t run_reduce_rows(const ReducePlan &p, const ReduceRow *rows, int32_t 
             a.acc[j] = w.acc;
             a.S[j] = w.S;
             a.valid[j] = w.valid;
+            a.first[j] = w.first;
             a.ld[j] = w.ld;
             bool vec = (uintptr_t)w.in % 16 == 0;
             if (p.mode != kModeNormOnly) vec = vec && ((size_t)w.ld * esize) % 16 == 0;
@@ -102,7 +106,7 @@ cudaError_t run_reduce(const ReducePlan &p, cudaStream_t s) {
     if (p.S <= 0) return cudaSuccess;
     std::vector<ReduceRow> rows;
     reduce_rows_of(p, rows);
-    return run_reduce_rows(p, rows.data(), p.n_ranks, s);
+    return run_reduce_rows(p, rows.data(), p.n_ranks, s, true);
 }
 
 cudaError_t run_adamw_rows(const AdamPlan &p, const AdamRow *rows, int32_t n_rows,

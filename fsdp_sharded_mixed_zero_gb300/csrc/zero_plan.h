@@ -49,6 +49,7 @@ struct ReduceRow {
     int64_t valid = 0;                // elements [valid, S) are padding
     float *g = nullptr;               // kModeStep: reduced-gradient output row
     float *acc = nullptr;             // kModeAccFirst / kModeAccAdd: accumulator
+    int64_t first = 0;                // flat index of the shard's element 0
 };
 // The rows of a single-FlatParameter plan (its ranks, in order).
 void reduce_rows_of(const ReducePlan &p, std::vector<ReduceRow> &rows);
@@ -60,7 +61,9 @@ bool rows_want_staging(int mode, int in_kind, int32_t n_contrib, const ReduceRow
 // (mode, encoding, contributor count, op, state, partials, grid, staging,
 // decision); total_blocks of the decision counts every row.
 cudaError_t run_reduce_rows(const ReducePlan &p, const ReduceRow *rows, int32_t n_rows,
-                            cudaStream_t s);
+                            cudaStream_t s, bool one_flat_parameter = false);
+// (p.g_stride: the spacing of the rows' gradient outputs when they are one
+// FlatParameter's scratch rows, else 0.)
 
 // Test hook (zero_debug.h): bytes added to the staged reduce's expected
 // transaction count per stage, 0 in normal operation.
