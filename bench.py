@@ -659,7 +659,9 @@ def run_group(args):
     decision, two launches per 64 members); the split step per member with
     the totals summed on the device (the same global decision, two launches
     per member plus the decision); and one zero_shard_step per member (a
-    decision per member -- a timing baseline only)."""
+    decision per member -- a timing baseline only).  With --micro-steps K a
+    step is K accumulations and the step from the accumulators, grouped
+    (K + 1 launches per 64 members) or per member."""
     import torch
     import fsdp_sharded_mixed_zero_gb300 as Z
     from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
@@ -683,8 +685,22 @@ def run_group(args):
     of = [torch.zeros((), dtype=torch.int32, device=dev) for _ in ds]
     stream = torch.cuda.current_stream(dev)
 
+    micro = max(1, args.micro_steps)
+    if micro > 1:                           # accumulation: micro-steps, then the step
+        for d in ds:
+            d.alloc_acc()
+        aargs = [dict(ranks=w.ranks, grads=d.grads, acc=d.acc, grad_rank_offset_mul=0)
+                 for w, d in zip(ws, ds)]
+        sargs = [dict(ranks=w.ranks, acc=d.acc, master=d.master, m=d.m, v=d.v, out=d.out)
+                 for w, d in zip(ws, ds)]
+
     def grouped():
-        grp.step(margs, stream=stream, want_result=False)
+        if micro == 1:
+            grp.step(margs, stream=stream, want_result=False)
+            return
+        for k in range(micro):
+            grp.accumulate(aargs, first_micro_step=(k == 0), stream=stream)
+        grp.step_accumulated(sargs, stream=stream, want_result=False)
 
     def split():
         for w, d, a, b in zip(ws, ds, ss, of):
@@ -696,7 +712,12 @@ def run_group(args):
 
     def per_member():
         for d in ds:
-            d.step(want_result=False, stream=stream)
+            if micro == 1:
+                d.step(want_result=False, stream=stream)
+                continue
+            for k in range(micro):
+                d.accumulate(first=(k == 0), stream=stream)
+            d.step_accumulated(want_result=False, stream=stream)
 
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -704,7 +725,10 @@ def run_group(args):
         uuid = str(local)
     times = {}
     clocks = None
-    for name, fn in (("group", grouped), ("split", split), ("per_flat_parameter", per_member)):
+    arms = [("group", grouped), ("split", split), ("per_flat_parameter", per_member)]
+    if micro > 1:
+        arms = [arms[0], arms[2]]           # the split step has no accumulation form
+    for name, fn in arms:
         for _ in range(args.warmup):
             fn()
         torch.cuda.synchronize(dev)
@@ -724,7 +748,12 @@ def run_group(args):
         if sampler:
             clocks = sampler.stop()
         times[name] = group.max(e0.elapsed_time(e1))
-    res = grp.step(margs, stream=stream)
+    if micro == 1:
+        res = grp.step(margs, stream=stream)
+    else:
+        for k in range(micro):
+            grp.accumulate(aargs, first_micro_step=(k == 0), stream=stream)
+        res = grp.step_accumulated(sargs, stream=stream)
     assert res.skipped == 0 and res.overflow == 0, "benchmark inputs overflowed"
     params = M * ds[0].S
     n_batches = -(-M // 64)
@@ -734,12 +763,14 @@ def run_group(args):
             "unit": "Gparams/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": times["group"] / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": "group%dx%d" % (M, ds[0].S), "flat_parameters": M,
+            "config": {"workload": "group%dx%d" % (M, ds[0].S)
+                       + ("_micro%d" % micro if micro > 1 else ""), "flat_parameters": M,
+                       "micro_steps": micro,
                        "params_per_flat_parameter_shard": ds[0].S, "emulated_world_size": 8,
                        "stepped_ranks": [7], "parallelism": "replicas%d" % world},
             "compare_ms_per_step": {k: v / args.steps for k, v in times.items()},
             "clocks": clocks,
-            "gpu_launches": 2 * n_batches * args.steps,
+            "gpu_launches": (micro + 1) * n_batches * args.steps,
         }
         print(json.dumps(line), flush=True)
     grp.close()

@@ -73,7 +73,8 @@ class GroupMember(C.Structure):
     _fields_ = [("ranks", C.POINTER(C.c_int32)), ("n_ranks", C.c_int32), ("grads", C.c_void_p),
                 ("grad_ld", C.c_int64), ("grad_rank_offset_mul", C.c_int64),
                 ("master", C.POINTER(C.c_void_p)), ("m", C.POINTER(C.c_void_p)),
-                ("v", C.POINTER(C.c_void_p)), ("flat_param_out", C.c_void_p)]
+                ("v", C.POINTER(C.c_void_p)), ("flat_param_out", C.c_void_p),
+                ("acc", C.POINTER(C.c_void_p))]
 
 
 def _load():
@@ -113,6 +114,9 @@ def _load():
     L.zero_group_init.argtypes = [C.POINTER(vp), i32, C.POINTER(vp)]
     L.zero_group_step.argtypes = [vp, C.POINTER(GroupMember), C.c_double, vp,
                                   C.POINTER(StepResult)]
+    L.zero_group_accumulate.argtypes = [vp, C.POINTER(GroupMember), i32, vp]
+    L.zero_group_step_accumulated.argtypes = [vp, C.POINTER(GroupMember), C.c_double, vp,
+                                              C.POINTER(StepResult)]
     L.zero_group_loss_scaler_state.argtypes = [vp, C.POINTER(ScalerState), vp]
     L.zero_group_set_loss_scaler_state.argtypes = [vp, C.POINTER(ScalerState), vp]
     L.zero_group_set_lr.argtypes = [vp, C.c_double]
@@ -136,7 +140,8 @@ def _load():
                  "zero_offload_adamw_host", "zero_debug_set_stage_tx_pad",
                  "zero_shard_reduce", "zero_shard_apply", "zero_group_init", "zero_group_step",
                  "zero_group_loss_scaler_state", "zero_group_set_loss_scaler_state",
-                 "zero_group_set_lr", "zero_group_free",
+                 "zero_group_set_lr", "zero_group_free", "zero_group_accumulate",
+                 "zero_group_step_accumulated",
                  "zero_shard_step_accumulated"):
         getattr(L, name).restype = i32
     return L
@@ -334,7 +339,9 @@ class ZeroGroup:
 
     members: ZeroFlat objects sharing world size, dtypes, op and hparams.
     step(args): args[k] = dict(ranks, grads, master, m, v, out[, grad_rank_offset_mul])
-    for member k, torch CUDA tensors as for ZeroFlat.step."""
+    for member k, torch CUDA tensors as for ZeroFlat.step; accumulate() and
+    step_accumulated() take acc (fp32 rows, one per stepped rank) as for
+    ZeroFlat.accumulate and ZeroFlat.step_accumulated."""
 
     def __init__(self, members):
         self.members = list(members)
@@ -343,29 +350,70 @@ class ZeroGroup:
         _check(_lib.zero_group_init(arr, len(self.members), C.byref(h)), "zero_group_init")
         self.handle = h.value
 
+    def _members(self, args, keep):
+        """The GroupMember array of args (ctypes arrays appended to keep)."""
+        ms = (GroupMember * len(args))()
+        for k, (f, a) in enumerate(zip(self.members, args)):
+            ranks = list(a["ranks"])
+            r = (C.c_int32 * len(ranks))(*ranks)
+            keep.append(r)
+            x = GroupMember()
+            x.ranks, x.n_ranks = r, len(ranks)
+            g = a.get("grads")
+            if g is not None:
+                assert g.dim() == 2 and g.stride(1) == 1
+                mul = a.get("grad_rank_offset_mul")
+                if mul is None:
+                    mul = f.shard_size if len(ranks) > 1 else 0
+                x.grads, x.grad_ld, x.grad_rank_offset_mul = g.data_ptr(), g.stride(0), mul
+            for name in ("master", "m", "v", "acc"):
+                if a.get(name) is not None:
+                    arr = (C.c_void_p * len(ranks))(*[t.data_ptr() for t in a[name]])
+                    keep.append(arr)
+                    setattr(x, name, arr)
+            if a.get("out") is not None:
+                x.flat_param_out = a["out"].data_ptr()
+            ms[k] = x
+        return ms
+
     def step(self, args, extra_norm_sq=0.0, stream=None, want_result=True):
         import torch
         if stream is None:
             stream = torch.cuda.current_stream()
         keep = []                                   # ctypes arrays alive for the call
-        ms = (GroupMember * len(args))()
-        for k, (f, a) in enumerate(zip(self.members, args)):
-            ranks = list(a["ranks"])
-            mul = a.get("grad_rank_offset_mul")
-            if mul is None:
-                mul = f.shard_size if len(ranks) > 1 else 0
-            g = a["grads"]
-            assert g.dim() == 2 and g.stride(1) == 1
-            r = (C.c_int32 * len(ranks))(*ranks)
-            arrs = [(C.c_void_p * len(ranks))(*[t.data_ptr() for t in a[name]])
-                    for name in ("master", "m", "v")]
-            keep += [r] + arrs
-            ms[k] = GroupMember(r, len(ranks), g.data_ptr(), g.stride(0), mul, arrs[0], arrs[1],
-                                arrs[2], a["out"].data_ptr())
+        ms = self._members(args, keep)
         res = StepResult() if want_result else None
         _check(_lib.zero_group_step(self.handle, ms, float(extra_norm_sq),
                                     C.c_void_p(stream.cuda_stream),
                                     C.byref(res) if res is not None else None), "zero_group_step")
+        return res
+
+    def accumulate(self, args, first_micro_step, stream=None):
+        """One micro-step: args[k] = dict(ranks, grads, acc[, grad_rank_offset_mul]);
+        each member's reduced micro-step gradient (loss scale not divided out)
+        written (first) or added into its fp32 accumulator rows acc[j], one per
+        stepped rank.  One launch per 64 rows of all members."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        keep = []
+        ms = self._members(args, keep)
+        _check(_lib.zero_group_accumulate(self.handle, ms, 1 if first_micro_step else 0,
+                                          C.c_void_p(stream.cuda_stream)),
+               "zero_group_accumulate")
+
+    def step_accumulated(self, args, extra_norm_sq=0.0, stream=None, want_result=True):
+        """The group step from accumulators: args[k] = dict(ranks, acc, master, m, v, out)."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        keep = []
+        ms = self._members(args, keep)
+        res = StepResult() if want_result else None
+        _check(_lib.zero_group_step_accumulated(self.handle, ms, float(extra_norm_sq),
+                                                C.c_void_p(stream.cuda_stream),
+                                                C.byref(res) if res is not None else None),
+               "zero_group_step_accumulated")
         return res
 
     def scaler_state(self, stream=None):

@@ -1177,9 +1177,11 @@ struct zero_group {
 
 namespace {
 
+// Every field but lr and weight_decay, which each member keeps as its own
+// parameter group's.
 bool same_hparams(const zero_hparams &a, const zero_hparams &b) {
-    return a.lr == b.lr && a.beta1 == b.beta1 && a.beta2 == b.beta2 && a.eps == b.eps &&
-           a.weight_decay == b.weight_decay && a.max_grad_norm == b.max_grad_norm &&
+    return a.beta1 == b.beta1 && a.beta2 == b.beta2 && a.eps == b.eps &&
+           a.max_grad_norm == b.max_grad_norm &&
            a.dynamic_loss_scale == b.dynamic_loss_scale &&
            a.initial_scale_power == b.initial_scale_power &&
            a.loss_scale_window == b.loss_scale_window && a.reserved == b.reserved &&
@@ -1203,7 +1205,7 @@ ZERO_API zero_status zero_group_init(zero_flat *const *members, int32_t n_member
             b->param_dtype != a->param_dtype || b->op != a->op || !same_hparams(b->hp, a->hp))
             return fail(ZERO_ERR_INVALID_ARG,
                         "member %d differs from member 0 (device, world size, dtypes, op or "
-                        "hyper-parameters)", k);
+                        "hyper-parameters other than lr and weight_decay)", k);
     }
     DeviceGuard guard(a->device);
     if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the members' device");
@@ -1229,70 +1231,111 @@ ZERO_API zero_status zero_group_init(zero_flat *const *members, int32_t n_member
     return ZERO_OK;
 }
 
-ZERO_API zero_status zero_group_step(zero_group *g, const zero_group_member *args,
-                                     double extra_norm_sq, void *stream, zero_step_result *res) {
-    if (!g || !args) return fail(ZERO_ERR_INVALID_ARG, "NULL argument");
-    if (!std::isfinite(extra_norm_sq) || extra_norm_sq < 0)
-        return fail(ZERO_ERR_INVALID_ARG, "extra_norm_sq must be finite and >= 0");
-    zero_flat *c = g->core;
-    zero_status s;
+namespace {
+
+enum GroupCall { kGroupStep, kGroupAccumulate, kGroupStepAccumulated };
+
+// Validate every member's arguments for `call`; on an error the message names
+// the member.
+zero_status check_group_args(const zero_group *g, const zero_group_member *args, GroupCall call) {
     for (size_t k = 0; k < g->members.size(); ++k) {
         const zero_flat *mk = g->members[k];
         const zero_group_member &x = args[k];
         int32_t max_rank = 0;
-        if ((s = check_ranks(mk, x.ranks, x.n_ranks, &max_rank)) ||
-            (s = check_update(mk, x.n_ranks, x.master, x.m, x.v, x.flat_param_out, 0.0)) ||
-            (s = check_grads(mk, x.grads, x.grad_ld, x.grad_rank_offset_mul, max_rank))) {
+        zero_status s = check_ranks(mk, x.ranks, x.n_ranks, &max_rank);
+        if (!s && call != kGroupStep) s = check_rows(mk, x.acc, x.n_ranks, "acc");
+        if (!s && call != kGroupAccumulate)
+            s = check_update(mk, x.n_ranks, x.master, x.m, x.v, x.flat_param_out, 0.0);
+        if (!s && call != kGroupStepAccumulated)
+            s = check_grads(mk, x.grads, x.grad_ld, x.grad_rank_offset_mul, max_rank);
+        if (s) {
             char msg[512];
             snprintf(msg, sizeof(msg), "member %zu: %.480s", k, g_last_error);
             return fail(s, "%s", msg);
         }
     }
-    DeviceGuard guard(c->device);
-    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the group's device");
-    const cudaStream_t st = (cudaStream_t)stream;
-    // every (member, stepped rank) row, in member order
-    std::vector<zg::ReduceRow> rrows, part;
-    std::vector<zg::AdamRow> arows;
-    int64_t max_s = 0;
+    return ZERO_OK;
+}
+
+// The reduce rows (and, for the steps, the AdamW rows) of every member, in
+// member order; *max_s = the largest shard.
+zero_status group_rows(zero_group *g, const zero_group_member *args, int mode,
+                       std::vector<zg::ReduceRow> &rrows, std::vector<zg::AdamRow> *arows,
+                       int64_t *max_s) {
+    std::vector<zg::ReduceRow> part;
+    *max_s = 0;
     for (size_t k = 0; k < g->members.size(); ++k) {
         zero_flat *mk = g->members[k];
         const zero_group_member &x = args[k];
-        if ((s = ensure_scratch(mk, x.n_ranks, 0))) return s;
-        mk->reduced_ranks.clear();        // this step overwrites the member's scratch
         zg::ReducePlan p;
-        p.mode = zg::kModeStep;
-        p.grads = x.grads;
-        p.in_kind = in_kind_of(mk);
-        p.ld = x.grad_ld;
-        p.rank_mul = x.grad_rank_offset_mul;
+        p.mode = mode;
         p.ranks = x.ranks;
         p.n_ranks = x.n_ranks;
         p.S = mk->shard;
         p.full_numel = mk->full_numel;
-        p.g = mk->d_g;
-        p.g_stride = mk->g_stride;
+        if (mode == zg::kModeNormOnly) {
+            p.in_kind = zg::kInF32;
+            p.acc_in = const_cast<const float *const *>(x.acc);
+        } else {
+            p.grads = x.grads;
+            p.in_kind = in_kind_of(mk);
+            p.ld = x.grad_ld;
+            p.rank_mul = x.grad_rank_offset_mul;
+            p.acc_out = x.acc;
+        }
+        if (mode == zg::kModeStep) {
+            zero_status s = ensure_scratch(mk, x.n_ranks, 0);
+            if (s) return s;
+            mk->reduced_ranks.clear();    // this step overwrites the member's scratch
+            p.g = mk->d_g;
+            p.g_stride = mk->g_stride;
+        }
         zg::reduce_rows_of(p, part);
         rrows.insert(rrows.end(), part.begin(), part.end());
-        for (int32_t j = 0; j < x.n_ranks; ++j) {
-            const int64_t r = x.ranks[j];
-            zg::AdamRow w;
-            w.g = mk->d_g + (int64_t)j * mk->g_stride;
-            w.master = x.master[j];
-            w.m = x.m[j];
-            w.v = x.v[j];
-            w.out = static_cast<uint16_t *>(x.flat_param_out) + r * mk->shard;
-            w.S = mk->shard;
-            w.valid = part[j].valid;
-            arows.push_back(w);
+        if (arows) {
+            for (int32_t j = 0; j < x.n_ranks; ++j) {
+                const int64_t r = x.ranks[j];
+                zg::AdamRow w;
+                w.g = mode == zg::kModeNormOnly ? x.acc[j] : mk->d_g + (int64_t)j * mk->g_stride;
+                w.master = x.master[j];
+                w.m = x.m[j];
+                w.v = x.v[j];
+                w.out = static_cast<uint16_t *>(x.flat_param_out) + r * mk->shard;
+                w.S = mk->shard;
+                w.valid = part[j].valid;
+                w.lr = mk->lr;                // the member's parameter-group rates
+                w.decay = mk->decay;
+                arows->push_back(w);
+            }
         }
-        max_s = std::max(max_s, mk->shard);
+        *max_s = std::max(*max_s, mk->shard);
     }
+    return ZERO_OK;
+}
+
+// The plain or accumulated group step: the reduce (or norm pass) over every
+// row with the decision in its last block, then one AdamW over every row.
+zero_status group_step(zero_group *g, const zero_group_member *args, double extra_norm_sq,
+                       void *stream, zero_step_result *res, bool from_acc) {
+    if (!g || !args) return fail(ZERO_ERR_INVALID_ARG, "NULL argument");
+    if (!std::isfinite(extra_norm_sq) || extra_norm_sq < 0)
+        return fail(ZERO_ERR_INVALID_ARG, "extra_norm_sq must be finite and >= 0");
+    zero_status s = check_group_args(g, args, from_acc ? kGroupStepAccumulated : kGroupStep);
+    if (s) return s;
+    zero_flat *c = g->core;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the group's device");
+    const cudaStream_t st = (cudaStream_t)stream;
+    const int mode = from_acc ? zg::kModeNormOnly : zg::kModeStep;
+    std::vector<zg::ReduceRow> rrows;
+    std::vector<zg::AdamRow> arows;
+    int64_t max_s = 0;
+    if ((s = group_rows(g, args, mode, rrows, &arows, &max_s))) return s;
     const int32_t n_rows = (int32_t)rrows.size();
     const int64_t batch = std::min<int64_t>(n_rows, zg::kMaxRanksPerLaunch);
     zg::ReducePlan rp;
-    rp.mode = zg::kModeStep;
-    rp.in_kind = in_kind_of(c);
+    rp.mode = mode;
+    rp.in_kind = from_acc ? zg::kInF32 : in_kind_of(c);
     rp.n_contrib = c->world;
     rp.avg = c->op == ZERO_AVG;
     rp.st = c->d_state;
@@ -1314,12 +1357,54 @@ ZERO_API zero_status zero_group_step(zero_group *g, const zero_group_member *arg
     ap.lr = c->lr; ap.eps = c->eps; ap.decay = c->decay;
     ap.st = c->d_state;
     ap.grid_x = zg::grid_x_for(max_s, batch, c->sm_count, zg::kAdamBlocksPerSm);
+    if (from_acc) ap.acc = args[0].acc;   // marks the rows' gradients as accumulators
     cudaError_t e;
     if ((e = zg::run_reduce_rows(rp, rrows.data(), n_rows, st))) return cuda_fail(e, "reduce kernel launch");
     if (!rp.fuse_finalize && (e = zg::launch_finalize(f, st)))
         return cuda_fail(e, "finalize kernel launch");
     if ((e = zg::run_adamw_rows(ap, arows.data(), n_rows, st))) return cuda_fail(e, "adamw kernel launch");
     return res ? read_result(c, st, res) : ZERO_OK;
+}
+
+}  // namespace
+
+ZERO_API zero_status zero_group_step(zero_group *g, const zero_group_member *args,
+                                     double extra_norm_sq, void *stream, zero_step_result *res) {
+    return group_step(g, args, extra_norm_sq, stream, res, false);
+}
+
+ZERO_API zero_status zero_group_step_accumulated(zero_group *g, const zero_group_member *args,
+                                                 double extra_norm_sq, void *stream,
+                                                 zero_step_result *res) {
+    return group_step(g, args, extra_norm_sq, stream, res, true);
+}
+
+ZERO_API zero_status zero_group_accumulate(zero_group *g, const zero_group_member *args,
+                                          int32_t first_micro_step, void *stream) {
+    if (!g || !args) return fail(ZERO_ERR_INVALID_ARG, "NULL argument");
+    zero_status s = check_group_args(g, args, kGroupAccumulate);
+    if (s) return s;
+    zero_flat *c = g->core;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the group's device");
+    const int mode = first_micro_step ? zg::kModeAccFirst : zg::kModeAccAdd;
+    std::vector<zg::ReduceRow> rrows;
+    int64_t max_s = 0;
+    if ((s = group_rows(g, args, mode, rrows, nullptr, &max_s))) return s;
+    const int32_t n_rows = (int32_t)rrows.size();
+    zg::ReducePlan rp;
+    rp.mode = mode;
+    rp.in_kind = in_kind_of(c);
+    rp.n_contrib = c->world;
+    rp.avg = c->op == ZERO_AVG;
+    rp.st = c->d_state;
+    rp.staged = zg::rows_want_staging(rp.mode, rp.in_kind, rp.n_contrib, rrows.data(), n_rows);
+    rp.grid_x = zg::grid_x_for(max_s, std::min<int64_t>(n_rows, zg::kMaxRanksPerLaunch),
+                               c->sm_count,
+                               rp.staged ? c->staged_bps[rp.mode] : c->reduce_bps[rp.mode]);
+    const cudaError_t e = zg::run_reduce_rows(rp, rrows.data(), n_rows, (cudaStream_t)stream);
+    if (e) return cuda_fail(e, "accumulate kernel launch");
+    return ZERO_OK;
 }
 
 ZERO_API zero_status zero_group_loss_scaler_state(zero_group *g, zero_scaler_state *out,
@@ -1336,7 +1421,9 @@ ZERO_API zero_status zero_group_set_loss_scaler_state(zero_group *g, const zero_
 
 ZERO_API zero_status zero_group_set_lr(zero_group *g, double lr) {
     if (!g) return fail(ZERO_ERR_INVALID_ARG, "group is NULL");
-    return zero_flat_set_lr(g->core, lr);
+    zero_status s = zero_flat_set_lr(g->core, lr);
+    for (size_t k = 0; k < g->members.size() && !s; ++k) s = zero_flat_set_lr(g->members[k], lr);
+    return s;
 }
 
 ZERO_API zero_status zero_group_free(zero_group *g) {

@@ -875,18 +875,20 @@ __device__ __forceinline__ void store_warp_realigned(uint16_t *o, const uint4 &w
 // kFromAcc: the gradient rows are micro-step accumulators that still carry
 // the loss scale: g = acc / scale_used (the same division the reduce kernel
 // applies), padding elements (flat index >= full_numel) are zero.
-template <bool kBf16, bool kFromAcc>
+// kOneRate: every row of the launch has row 0's lr and decay (read as
+// constant operands rather than per-row values held in registers).
+template <bool kBf16, bool kFromAcc, bool kOneRate>
 __global__ void __launch_bounds__(kBlock) adamw_kernel(const __grid_constant__ AdamArgs a) {
     const DevState *st = a.st;
     if (st->res.skipped) return;
     AdamConst k;
     k.b1 = a.b1; k.b2 = a.b2; k.omb1 = a.omb1; k.omb2 = a.omb2;
-    k.lr = a.lr; k.eps = a.eps; k.decay = a.decay;
+    const int j = blockIdx.y;
+    k.lr = a.lr[kOneRate ? 0 : j]; k.eps = a.eps; k.decay = a.decay[kOneRate ? 0 : j];
     k.coef = st->res.clip_coef;
     k.bc1 = st->bc1;
     k.bc2 = st->bc2;
 
-    const int j = blockIdx.y;
     float *th = a.master[j];
     float *mm = a.m[j];
     float *vv = a.v[j];
@@ -967,18 +969,18 @@ __device__ __forceinline__ float decode16(float x) {
     else return __half2float(__float2half_rn(x));
 }
 
-template <bool kBf16>
+template <bool kBf16, bool kOneRate>
 __global__ void __launch_bounds__(kBlock) adamw_q8_kernel(const __grid_constant__ AdamArgs a) {
     const DevState *st = a.st;
     if (st->res.skipped) return;
     AdamConst k;
     k.b1 = a.b1; k.b2 = a.b2; k.omb1 = a.omb1; k.omb2 = a.omb2;
-    k.lr = a.lr; k.eps = a.eps; k.decay = a.decay;
+    const int j = blockIdx.y;
+    k.lr = a.lr[kOneRate ? 0 : j]; k.eps = a.eps; k.decay = a.decay[kOneRate ? 0 : j];
     k.coef = st->res.clip_coef;
     k.bc1 = st->bc1;
     k.bc2 = st->bc2;
 
-    const int j = blockIdx.y;
     float *th = a.master[j];
     float *mm = a.m[j];
     float *vv = a.v[j];
@@ -1155,7 +1157,10 @@ cudaError_t launch_reduce(const ReduceArgs &a, int grid_x, int in_kind, int mode
     const dim3 grid((unsigned)grid_x, (unsigned)a.n_ranks);
     if (mode == kModeNormOnly) {
         if (staged) return cudaErrorInvalidValue;
-        reduce_kernel<kInF32, kModeNormOnly><<<grid, kBlock, 0, s>>>(a);
+        if (a.full_numel >= 0)                    // the rows of one FlatParameter
+            reduce_kernel<kInF32, kModeNormOnly, true><<<grid, kBlock, 0, s>>>(a);
+        else
+            reduce_kernel<kInF32, kModeNormOnly, false><<<grid, kBlock, 0, s>>>(a);
         return cudaGetLastError();
     }
     switch (in_kind) {
@@ -1171,24 +1176,42 @@ cudaError_t launch_finalize(const FinalizeArgs &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+static bool one_rate(const AdamArgs &a) {
+    for (int32_t j = 1; j < a.n_ranks; ++j)
+        if (a.lr[j] != a.lr[0] || a.decay[j] != a.decay[0]) return false;
+    return true;
+}
+
+template <bool kOneRate>
+static void launch_adamw_rate(const AdamArgs &a, dim3 grid, bool bf16_out, bool from_acc,
+                              cudaStream_t s) {
+    if (from_acc) {
+        if (bf16_out) adamw_kernel<true, true, kOneRate><<<grid, kBlock, 0, s>>>(a);
+        else adamw_kernel<false, true, kOneRate><<<grid, kBlock, 0, s>>>(a);
+    } else {
+        if (bf16_out) adamw_kernel<true, false, kOneRate><<<grid, kBlock, 0, s>>>(a);
+        else adamw_kernel<false, false, kOneRate><<<grid, kBlock, 0, s>>>(a);
+    }
+}
+
 cudaError_t launch_adamw(const AdamArgs &a, int grid_x, bool bf16_out, bool from_acc,
                          cudaStream_t s) {
     const dim3 grid((unsigned)grid_x, (unsigned)a.n_ranks);
-    if (from_acc) {
-        if (bf16_out) adamw_kernel<true, true><<<grid, kBlock, 0, s>>>(a);
-        else adamw_kernel<false, true><<<grid, kBlock, 0, s>>>(a);
-    } else {
-        if (bf16_out) adamw_kernel<true, false><<<grid, kBlock, 0, s>>>(a);
-        else adamw_kernel<false, false><<<grid, kBlock, 0, s>>>(a);
-    }
+    if (one_rate(a)) launch_adamw_rate<true>(a, grid, bf16_out, from_acc, s);
+    else launch_adamw_rate<false>(a, grid, bf16_out, from_acc, s);
     return cudaGetLastError();
 }
 
-
 cudaError_t launch_adamw_q8(const AdamArgs &a, int grid_x, bool bf16_out, cudaStream_t s) {
     const dim3 grid((unsigned)grid_x, (unsigned)a.n_ranks);
-    if (bf16_out) adamw_q8_kernel<true><<<grid, kBlock, 0, s>>>(a);
-    else adamw_q8_kernel<false><<<grid, kBlock, 0, s>>>(a);
+    const bool one = one_rate(a);
+    if (bf16_out) {
+        if (one) adamw_q8_kernel<true, true><<<grid, kBlock, 0, s>>>(a);
+        else adamw_q8_kernel<true, false><<<grid, kBlock, 0, s>>>(a);
+    } else {
+        if (one) adamw_q8_kernel<false, true><<<grid, kBlock, 0, s>>>(a);
+        else adamw_q8_kernel<false, false><<<grid, kBlock, 0, s>>>(a);
+    }
     return cudaGetLastError();
 }
 

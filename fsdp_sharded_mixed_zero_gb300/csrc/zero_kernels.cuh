@@ -119,7 +119,7 @@ constexpr int kStageTile = kBlock * kVec;
 
 // K3: AdamW + cast into the flat buffer; row j (blockIdx.y) as for K1.
 struct AdamArgs {
-    float b1, b2, omb1, omb2, lr, eps, decay;
+    float b1, b2, omb1, omb2, eps;
     int32_t n_ranks;                  // rows in this launch
     const DevState *st;
     const float *g[kMaxRanksPerLaunch];   // reduced gradient row j (or its accumulator)
@@ -137,6 +137,10 @@ struct AdamArgs {
     int8_t *q8[kMaxRanksPerLaunch];
     float *q8_scales[kMaxRanksPerLaunch];
     uint8_t q8_align[kMaxRanksPerLaunch];      // 8: 8-byte code stores, else byte stores
+    // row j's learning rate and decay factor (float)(1 - lr*wd): the rows of a
+    // group may belong to parameter groups with their own rates
+    float lr[kMaxRanksPerLaunch];
+    float decay[kMaxRanksPerLaunch];
 };
 
 // in_kind: InKind; mode: ReduceMode.  from_acc: g = acc / scale_used, with

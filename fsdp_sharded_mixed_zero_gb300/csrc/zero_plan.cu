@@ -118,7 +118,7 @@ cudaError_t run_adamw_rows(const AdamPlan &p, const AdamRow *rows, int32_t n_row
         const int32_t nb = n_rows - b0 < kMaxRanksPerLaunch ? n_rows - b0 : kMaxRanksPerLaunch;
         AdamArgs a{};
         a.b1 = p.b1; a.b2 = p.b2; a.omb1 = p.omb1; a.omb2 = p.omb2;
-        a.lr = p.lr; a.eps = p.eps; a.decay = p.decay;
+        a.eps = p.eps;
         a.n_ranks = nb;
         a.st = p.st;
         for (int32_t j = 0; j < nb; ++j) {
@@ -137,6 +137,8 @@ cudaError_t run_adamw_rows(const AdamPlan &p, const AdamRow *rows, int32_t n_row
             a.q8[j] = w.q8;
             a.q8_scales[j] = w.q8_scales;
             a.q8_align[j] = (uintptr_t)w.q8 % 8 == 0 ? 8 : 1;
+            a.lr[j] = w.lr;
+            a.decay[j] = w.decay;
         }
         const cudaError_t e = p.q8 ? launch_adamw_q8(a, p.grid_x, p.bf16_out, s)
                                    : launch_adamw(a, p.grid_x, p.bf16_out, p.acc != nullptr, s);
@@ -162,6 +164,8 @@ cudaError_t run_adamw(const AdamPlan &p, cudaStream_t s) {
         w.S = count;                                   // the kernels' element range per rank
         int64_t valid = p.full_numel - r * p.S;
         w.valid = valid < 0 ? 0 : (valid > count ? count : valid);
+        w.lr = p.lr;
+        w.decay = p.decay;
         if (p.q8) {
             w.q8 = p.q8 + r * p.S;
             w.q8_scales = p.q8_scales + r * ((p.S + kQ8Block - 1) / kQ8Block);

@@ -107,10 +107,11 @@ struct AdamRow {
     int64_t valid = 0;                // from accumulators: [valid, S) is padding
     int8_t *q8 = nullptr;             // int8 payload of the slot, and its scales
     float *q8_scales = nullptr;
+    float lr = 0, decay = 0;          // the row's learning rate and (float)(1 - lr*wd)
 };
-// The launches of AdamW over any rows: p supplies the scalars, state, output
-// encoding, accumulator mode (p.acc non-NULL), int8 mode (p.q8 non-NULL) and
-// grid.
+// The launches of AdamW over any rows: p supplies the shared scalars (betas,
+// eps), state, output encoding, accumulator mode (p.acc non-NULL), int8 mode
+// (p.q8 non-NULL) and grid; each row its own lr and decay.
 cudaError_t run_adamw_rows(const AdamPlan &p, const AdamRow *rows, int32_t n_rows,
                            cudaStream_t s);
 

@@ -273,10 +273,14 @@ zero_status zero_shard_apply(zero_flat *h, const int32_t *ranks, int32_t n_ranks
  * one loss-scale decision (ZeRO reading §5.3), in one reduce launch and one
  * AdamW launch per 64 (member, stepped rank) rows instead of two launches per
  * FlatParameter.  The members are existing handles that share world_size,
- * grad and param dtypes, op and every zero_hparams field; the group takes
- * its hyper-parameters from the first member and owns its own loss-scale
- * state (initialised as a new handle's), bias-correction table and norm
- * partials; the members' own loss-scale states are not used by group steps.
+ * grad and param dtypes, op and every zero_hparams field but lr and
+ * weight_decay: each member keeps its own two, as a parameter group does
+ * ("PyTorch FSDP ... 深度解析" §8, the comparison table: DeepSpeed shards by
+ * parameter group), so e.g. biases and norms can step without decay in the
+ * same launches.  The rest comes from the first member.  The group owns its
+ * own loss-scale state (initialised as a new handle's), bias-correction
+ * table and norm partials; the members' own loss-scale states are not used
+ * by group steps.
  * A member's handle supplies its layout and its reduced-gradient scratch, so
  * a handle should be stepped either alone or in groups, not both in one
  * step.  Errors: INVALID_ARG (no members, NULL, members that differ, a
@@ -284,8 +288,10 @@ zero_status zero_shard_apply(zero_flat *h, const int32_t *ranks, int32_t n_ranks
 typedef struct zero_group zero_group;
 zero_status zero_group_init(zero_flat *const *members, int32_t n_members, zero_group **out);
 
-/* The arguments of one member in a group step, exactly those of
- * zero_shard_step for that member's handle. */
+/* The arguments of one member in a group call, those of zero_shard_step /
+ * zero_grad_accumulate / zero_shard_step_accumulated for that member's
+ * handle; each call reads the fields it needs (acc: the member's per-rank
+ * fp32 accumulators, used by the accumulation calls only). */
 typedef struct {
     const int32_t *ranks;
     int32_t n_ranks;
@@ -296,6 +302,7 @@ typedef struct {
     float *const *m;
     float *const *v;
     void *flat_param_out;
+    float *const *acc;
 } zero_group_member;
 
 /* One step of every member (args[k] for the group's member k): the reduce
@@ -307,8 +314,27 @@ typedef struct {
 zero_status zero_group_step(zero_group *g, const zero_group_member *args, double extra_norm_sq,
                             void *stream, zero_step_result *res);
 
-/* The group's loss-scale state (synchronizes `stream`), its restore, and its
- * learning rate (as zero_flat_set_lr). */
+/* Micro-step accumulation for every member in one launch per 64 rows, as
+ * zero_grad_accumulate does per member (acc = r on the first micro-step,
+ * acc += r after; the loss scale not divided out).  Reads ranks, grads,
+ * grad_ld, grad_rank_offset_mul and acc of each member.  Asynchronous.
+ * Errors: as for zero_grad_accumulate, per member. */
+zero_status zero_group_accumulate(zero_group *g, const zero_group_member *args,
+                                  int32_t first_micro_step, void *stream);
+
+/* The step from every member's accumulators: g = acc / scale (padding zero),
+ * one global norm, overflow decision and loss-scale update over all members,
+ * then AdamW and the cast -- as zero_shard_step_accumulated does per member,
+ * in one norm launch and one AdamW launch per 64 rows.  Reads ranks, acc,
+ * master, m, v and flat_param_out of each member.  res: as for
+ * zero_shard_step.  Errors: as for zero_shard_step_accumulated, per member. */
+zero_status zero_group_step_accumulated(zero_group *g, const zero_group_member *args,
+                                        double extra_norm_sq, void *stream,
+                                        zero_step_result *res);
+
+/* The group's loss-scale state (synchronizes `stream`), its restore, and a
+ * learning rate set on every member at once (as zero_flat_set_lr on each;
+ * zero_flat_set_lr on one member changes that member's rate alone). */
 zero_status zero_group_loss_scaler_state(zero_group *g, zero_scaler_state *out, void *stream);
 zero_status zero_group_set_loss_scaler_state(zero_group *g, const zero_scaler_state *in,
                                              void *stream);

@@ -24,10 +24,10 @@ def _need_gpu():
         pytest.skip("no GPU")
 
 
-def _wl(name, shapes, N, ranks, layout="full", inf_at=None, seed=1, steps=3):
+def _wl(name, shapes, N, ranks, layout="full", inf_at=None, seed=1, steps=3, hp=None):
     return Workload(name=name, description=name, shapes=shapes, world_size=N, ranks=ranks,
                     grad_dtype=F16, op=AVG, dynamic=True, steps=steps, sigma_g=1e-3,
-                    sigma_n=1e-3, inf_at=inf_at, grads_layout=layout, seed=seed)
+                    sigma_n=1e-3, inf_at=inf_at, grads_layout=layout, seed=seed, hp=hp or {})
 
 
 def _args(w, d):
@@ -35,11 +35,14 @@ def _args(w, d):
                 grad_rank_offset_mul=w.grad_rank_mul)
 
 
-def run_group_parity(ora, ws, steps=3):
-    """Step the members ws as one group on the GPU and in the oracle."""
+def run_group_parity(ora, ws, steps=3, lr_at=None):
+    """Step the members ws as one group on the GPU and in the oracle, each
+    member with its own parameter group's lr and weight decay; lr_at: {step:
+    lr} set on the whole group before that step."""
     import fsdp_sharded_mixed_zero_gb300 as Z
     from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
-    hp = ora.hparams(**ws[0].hparams_kwargs())
+    kws = [dict(w.hparams_kwargs()) for w in ws]
+    hp = ora.hparams(**kws[0])
     ds = [DeviceWorkload(w, out_fill=0x5A5A) for w in ws]
     group = Z.ZeroGroup([d.flat for d in ds])
     try:
@@ -48,6 +51,11 @@ def run_group_parity(ora, ws, steps=3):
         st = ora.scaler_init(hp)
         skipped = []
         for step in range(steps):
+            if lr_at and step in lr_at:
+                group.set_lr(lr_at[step])
+                for kw in kws:
+                    kw["lr"] = lr_at[step]
+            hps = [ora.hparams(**kw) for kw in kws]
             assert group.scaler_state().as_tuple() == st.as_tuple()
             scale = st.scale
             grads = []
@@ -70,10 +78,10 @@ def run_group_parity(ora, ws, steps=3):
                 assert abs(res.grad_norm - norm) <= NORM_RTOL * norm
                 assert abs(res.clip_coef - coef) <= NORM_RTOL * coef
             k = 0
-            for w, d, (master, m, v, out) in zip(ws, ds, state):
+            for w, d, hpk, (master, m, v, out) in zip(ws, ds, hps, state):
                 for j, r in enumerate(w.ranks):
                     if not skip:
-                        ora.adamw_cast(hp, st.step_t, coef, gs[k], master[j], m[j], v[j],
+                        ora.adamw_cast(hpk, st.step_t, coef, gs[k], master[j], m[j], v[j],
                                        out=out[r * d.S:(r + 1) * d.S])
                     k += 1
                     assert_state(f32(d.master[j]), f32(d.m[j]), f32(d.v[j]), master[j], m[j],
@@ -86,6 +94,22 @@ def run_group_parity(ora, ws, steps=3):
         group.close()
         for d in ds:
             d.close()
+
+
+def test_group_members_keep_their_own_rates(ora):
+    """Parameter groups in one group: weights with decay, biases and norms
+    without, a head with its own learning rate; then one learning rate set on
+    the whole group (each member keeps its weight decay)."""
+    _need_gpu()
+    ws = [
+        _wl("weights_decay", [(768, 3072)], 8, [1, 6], seed=41, steps=4,
+            hp=dict(lr=3e-5, weight_decay=0.01)),
+        _wl("bias_norm_no_decay", [(3072,), (768,), (768,)], 8, list(range(8)), seed=42,
+            steps=4, hp=dict(lr=3e-5, weight_decay=0.0)),
+        _wl("head_own_lr", [(80_032,)], 8, list(range(8)), seed=43, steps=4,
+            hp=dict(lr=1e-3, weight_decay=0.1)),
+    ]
+    assert run_group_parity(ora, ws, steps=4, lr_at={2: 2e-5}) == [0, 0, 0, 0]
 
 
 def test_group_of_four_flat_parameters(ora):
@@ -162,12 +186,140 @@ def test_group_rejects_mismatched_members():
     import fsdp_sharded_mixed_zero_gb300 as Z
     f4 = Z.ZeroFlat([(1000,)], 4)
     f8 = Z.ZeroFlat([(1000,)], 8)
-    f4b = Z.ZeroFlat([(1000,)], 4, hp=Z.hparams(lr=1e-4))
+    f4b = Z.ZeroFlat([(1000,)], 4, hp=Z.hparams(eps=1e-6))
     try:
-        for members in ([f4, f8], [f4, f4b], [f4, f4]):
+        for members in ([f4, f8], [f4, f4b], [f4, f4]):     # world, eps, listed twice
             with pytest.raises(Z.ZeroError) as e:
                 Z.ZeroGroup(members)
             assert e.value.status == 1
     finally:
         for f in (f4, f8, f4b):
             f.close()
+
+
+def _wl_micro(name, shapes, N, ranks, micro, layout="full", inf_at=None, seed=1, steps=3,
+              hp=None):
+    w = _wl(name, shapes, N, ranks, layout=layout, inf_at=inf_at, seed=seed, steps=steps, hp=hp)
+    w.micro_steps = micro
+    return w
+
+
+def run_group_accum_parity(ora, ws, micro, steps=3):
+    """steps group steps of `micro` micro-steps each: zero_group_accumulate
+    against the oracle's per-member accumulation (bit for bit), then
+    zero_group_step_accumulated against one global decision over every
+    member's g = acc / scale (padding zero)."""
+    import fsdp_sharded_mixed_zero_gb300 as Z
+    from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
+    hps = [ora.hparams(**w.hparams_kwargs()) for w in ws]
+    hp = hps[0]
+    ds = [DeviceWorkload(w, out_fill=0x5A5A) for w in ws]
+    for d in ds:
+        d.alloc_acc()
+    group = Z.ZeroGroup([d.flat for d in ds])
+    try:
+        state = [([f32(t).copy() for t in d.master], [f32(t).copy() for t in d.m],
+                  [f32(t).copy() for t in d.v], u16(d.out).copy()) for d in ds]
+        accs = [[np.zeros(d.S, np.float32) for _ in w.ranks] for w, d in zip(ws, ds)]
+        st = ora.scaler_init(hp)
+        skipped = []
+        for step in range(steps):
+            assert group.scaler_state().as_tuple() == st.as_tuple()
+            scale = st.scale
+            for k in range(micro):
+                for w, d, acc in zip(ws, ds, accs):
+                    d.gen_grads(step * micro + k, scale)
+                    ora.grad_accumulate(w.world_size, d.full, d.S, w.ranks, host_grads(d.grads),
+                                        w.grad_ld, w.grad_rank_mul, acc, first=(k == 0),
+                                        avg=w.op == AVG)
+                group.accumulate([dict(ranks=w.ranks, grads=d.grads, acc=d.acc,
+                                       grad_rank_offset_mul=w.grad_rank_mul)
+                                  for w, d in zip(ws, ds)], first_micro_step=(k == 0))
+                for w, d, acc in zip(ws, ds, accs):
+                    for j, r in enumerate(w.ranks):
+                        got = f32(d.acc[j])
+                        same = (got.view(np.uint32) == acc[j].view(np.uint32)) | \
+                               (np.isnan(got) & np.isnan(acc[j]))
+                        assert same.all(), "%s acc rank %d micro %d" % (w.name, r, k)
+            res = group.step_accumulated([dict(ranks=w.ranks, acc=d.acc, master=d.master,
+                                               m=d.m, v=d.v, out=d.out)
+                                          for w, d in zip(ws, ds)])
+            gs = []
+            for w, d, acc in zip(ws, ds, accs):
+                for j, r in enumerate(w.ranks):
+                    g = acc[j] / np.float32(scale)
+                    g[max(d.full - r * d.S, 0):] = 0.0
+                    gs.append(g)
+            nacc, of = runner.norm_exact(gs)
+            norm = float(np.sqrt(ora.norm_sum(nacc)))
+            coef, skip = ora.scaler_decide(hp, st, of, norm)
+            assert (res.overflow, res.skipped, res.scale_used) == (of, skip, scale)
+            if not of:
+                assert abs(res.grad_norm - norm) <= NORM_RTOL * norm
+                assert abs(res.clip_coef - coef) <= NORM_RTOL * coef
+            k = 0
+            for w, d, hpk, (master, m, v, out) in zip(ws, ds, hps, state):
+                for j, r in enumerate(w.ranks):
+                    if not skip:
+                        ora.adamw_cast(hpk, st.step_t, coef, gs[k], master[j], m[j], v[j],
+                                       out=out[r * d.S:(r + 1) * d.S])
+                    k += 1
+                    assert_state(f32(d.master[j]), f32(d.m[j]), f32(d.v[j]), master[j], m[j],
+                                 v[j], tag=" (%s, step %d, rank %d)" % (w.name, step, r))
+                assert_params_close(u16(d.out), out, False, "%s params (step %d)" % (w.name, step))
+            skipped.append(skip)
+        assert group.scaler_state().as_tuple() == st.as_tuple()
+        return skipped
+    finally:
+        group.close()
+        for d in ds:
+            d.close()
+
+
+def test_group_accumulation_staged_rows(ora):
+    """Aligned accumulators, one member whose rows start off 64 bytes (the
+    staged reduce), an overflow in micro-step 4 (step 1) of another member."""
+    _need_gpu()
+    ws = [
+        _wl_micro("attn_all_shards", [(256, 768), (768,)], 8, list(range(8)), 3, seed=31),
+        _wl_micro("odd_rows_all_shards", [(80_032,)], 8, list(range(8)), 3, seed=32),
+        _wl_micro("mlp_slice_rank2", [(768, 3072)], 8, [2], 3, layout="slice", seed=33,
+                  inf_at=(4, 2, 500), hp=dict(lr=1e-4, weight_decay=0.0)),
+    ]
+    assert run_group_accum_parity(ora, ws, micro=3) == [0, 1, 0]
+    # the accumulate launch of this group is the staged reduce
+    import fsdp_sharded_mixed_zero_gb300 as Z
+    from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
+    from torch.profiler import ProfilerActivity, profile
+    ds = [DeviceWorkload(w) for w in ws]
+    for d in ds:
+        d.alloc_acc()
+        d.gen_grads(0, 1.0)
+    group = Z.ZeroGroup([d.flat for d in ds])
+    try:
+        args = [dict(ranks=w.ranks, grads=d.grads, acc=d.acc, grad_rank_offset_mul=w.grad_rank_mul)
+                for w, d in zip(ws, ds)]
+        names = []
+        for _ in range(2):                   # the profiler's first session may be empty
+            with profile(activities=[ProfilerActivity.CUDA]) as prof:
+                group.accumulate(args, first_micro_step=True)
+                torch.cuda.synchronize()
+            names = [e.name for e in prof.events() if "kernel" in e.name]
+            if names:
+                break
+        if names:
+            assert any("reduce_staged_kernel" in n for n in names), names
+    finally:
+        group.close()
+        for d in ds:
+            d.close()
+
+
+def test_group_accumulation_plain_rows_and_many_members(ora):
+    """An odd shard size (accumulators off 16 bytes: the plain reduce for the
+    whole group) and 70 members (two launches per call)."""
+    _need_gpu()
+    ws = [_wl_micro("m%02d" % k, [(1_001 + 37 * k,)], 4, [k % 4], 2, layout="slice",
+                    seed=200 + k, steps=2) for k in range(69)]
+    ws.append(_wl_micro("odd_s", [(4 * 2_501,)], 4, [0, 1, 2, 3], 2, seed=300, steps=2))
+    assert run_group_accum_parity(ora, ws, micro=2, steps=2) == [0, 0]
