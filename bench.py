@@ -661,7 +661,8 @@ def run_group(args):
     per member plus the decision); and one zero_shard_step per member (a
     decision per member -- a timing baseline only).  With --micro-steps K a
     step is K accumulations and the step from the accumulators, grouped
-    (K + 1 launches per 64 members) or per member."""
+    (K + 1 launches per 64 members) or per member; with --q8 the steps also
+    write the int8 all-gather payload (zero_group_step_q8 / zero_shard_step_q8)."""
     import torch
     import fsdp_sharded_mixed_zero_gb300 as Z
     from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
@@ -686,6 +687,13 @@ def run_group(args):
     stream = torch.cuda.current_stream(dev)
 
     micro = max(1, args.micro_steps)
+    q8 = bool(args.q8)
+    if q8 and micro > 1:
+        raise SystemExit("--group takes --q8 or --micro-steps, not both")
+    if q8:                                  # the int8 all-gather payload as well
+        for a, d in zip(margs, ds):
+            a["q8"] = torch.empty(d.padded, dtype=torch.int8, device=dev)
+            a["q8_scales"] = torch.empty(8 * -(-d.S // 256), dtype=torch.float32, device=dev)
     if micro > 1:                           # accumulation: micro-steps, then the step
         for d in ds:
             d.alloc_acc()
@@ -695,6 +703,9 @@ def run_group(args):
                  for w, d in zip(ws, ds)]
 
     def grouped():
+        if q8:
+            grp.step_q8(margs, stream=stream, want_result=False)
+            return
         if micro == 1:
             grp.step(margs, stream=stream, want_result=False)
             return
@@ -711,7 +722,12 @@ def run_group(args):
                          want_result=False)
 
     def per_member():
-        for d in ds:
+        for w, d, a in zip(ws, ds, margs):
+            if q8:
+                d.flat.step_q8(w.ranks, d.grads, d.master, d.m, d.v, d.out, a["q8"],
+                               a["q8_scales"], grad_rank_offset_mul=0, stream=stream,
+                               want_result=False)
+                continue
             if micro == 1:
                 d.step(want_result=False, stream=stream)
                 continue
@@ -726,8 +742,8 @@ def run_group(args):
     times = {}
     clocks = None
     arms = [("group", grouped), ("split", split), ("per_flat_parameter", per_member)]
-    if micro > 1:
-        arms = [arms[0], arms[2]]           # the split step has no accumulation form
+    if micro > 1 or q8:
+        arms = [arms[0], arms[2]]           # the split step has no accumulation or int8 form
     for name, fn in arms:
         for _ in range(args.warmup):
             fn()
@@ -748,7 +764,9 @@ def run_group(args):
         if sampler:
             clocks = sampler.stop()
         times[name] = group.max(e0.elapsed_time(e1))
-    if micro == 1:
+    if q8:
+        res = grp.step_q8(margs, stream=stream)
+    elif micro == 1:
         res = grp.step(margs, stream=stream)
     else:
         for k in range(micro):
@@ -764,8 +782,8 @@ def run_group(args):
             "ms_per_step": times["group"] / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": "group%dx%d" % (M, ds[0].S)
-                       + ("_micro%d" % micro if micro > 1 else ""), "flat_parameters": M,
-                       "micro_steps": micro,
+                       + ("_micro%d" % micro if micro > 1 else "") + ("_q8" if q8 else ""),
+                       "flat_parameters": M, "micro_steps": micro, "q8_payload": q8,
                        "params_per_flat_parameter_shard": ds[0].S, "emulated_world_size": 8,
                        "stepped_ranks": [7], "parallelism": "replicas%d" % world},
             "compare_ms_per_step": {k: v / args.steps for k, v in times.items()},

@@ -74,7 +74,8 @@ class GroupMember(C.Structure):
                 ("grad_ld", C.c_int64), ("grad_rank_offset_mul", C.c_int64),
                 ("master", C.POINTER(C.c_void_p)), ("m", C.POINTER(C.c_void_p)),
                 ("v", C.POINTER(C.c_void_p)), ("flat_param_out", C.c_void_p),
-                ("acc", C.POINTER(C.c_void_p))]
+                ("acc", C.POINTER(C.c_void_p)), ("flat_q8_out", C.c_void_p),
+                ("q8_scales", C.c_void_p)]
 
 
 def _load():
@@ -114,6 +115,8 @@ def _load():
     L.zero_group_init.argtypes = [C.POINTER(vp), i32, C.POINTER(vp)]
     L.zero_group_step.argtypes = [vp, C.POINTER(GroupMember), C.c_double, vp,
                                   C.POINTER(StepResult)]
+    L.zero_group_step_q8.argtypes = [vp, C.POINTER(GroupMember), C.c_double, vp,
+                                     C.POINTER(StepResult)]
     L.zero_group_accumulate.argtypes = [vp, C.POINTER(GroupMember), i32, vp]
     L.zero_group_step_accumulated.argtypes = [vp, C.POINTER(GroupMember), C.c_double, vp,
                                               C.POINTER(StepResult)]
@@ -141,7 +144,7 @@ def _load():
                  "zero_shard_reduce", "zero_shard_apply", "zero_group_init", "zero_group_step",
                  "zero_group_loss_scaler_state", "zero_group_set_loss_scaler_state",
                  "zero_group_set_lr", "zero_group_free", "zero_group_accumulate",
-                 "zero_group_step_accumulated",
+                 "zero_group_step_accumulated", "zero_group_step_q8",
                  "zero_shard_step_accumulated"):
         getattr(L, name).restype = i32
     return L
@@ -373,6 +376,10 @@ class ZeroGroup:
                     setattr(x, name, arr)
             if a.get("out") is not None:
                 x.flat_param_out = a["out"].data_ptr()
+            if a.get("q8") is not None:
+                x.flat_q8_out = a["q8"].data_ptr()
+            if a.get("q8_scales") is not None:
+                x.q8_scales = a["q8_scales"].data_ptr()
             ms[k] = x
         return ms
 
@@ -386,6 +393,22 @@ class ZeroGroup:
         _check(_lib.zero_group_step(self.handle, ms, float(extra_norm_sq),
                                     C.c_void_p(stream.cuda_stream),
                                     C.byref(res) if res is not None else None), "zero_group_step")
+        return res
+
+    def step_q8(self, args, extra_norm_sq=0.0, stream=None, want_result=True):
+        """The group step that also writes every member's int8 payload: args[k]
+        as for step() plus q8 and q8_scales (as for ZeroFlat.step_q8; out may
+        be None)."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        keep = []
+        ms = self._members(args, keep)
+        res = StepResult() if want_result else None
+        _check(_lib.zero_group_step_q8(self.handle, ms, float(extra_norm_sq),
+                                       C.c_void_p(stream.cuda_stream),
+                                       C.byref(res) if res is not None else None),
+               "zero_group_step_q8")
         return res
 
     def accumulate(self, args, first_micro_step, stream=None):

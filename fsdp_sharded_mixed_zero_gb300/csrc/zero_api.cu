@@ -1233,7 +1233,7 @@ ZERO_API zero_status zero_group_init(zero_flat *const *members, int32_t n_member
 
 namespace {
 
-enum GroupCall { kGroupStep, kGroupAccumulate, kGroupStepAccumulated };
+enum GroupCall { kGroupStep, kGroupAccumulate, kGroupStepAccumulated, kGroupStepQ8 };
 
 // Validate every member's arguments for `call`; on an error the message names
 // the member.
@@ -1243,9 +1243,17 @@ zero_status check_group_args(const zero_group *g, const zero_group_member *args,
         const zero_group_member &x = args[k];
         int32_t max_rank = 0;
         zero_status s = check_ranks(mk, x.ranks, x.n_ranks, &max_rank);
-        if (!s && call != kGroupStep) s = check_rows(mk, x.acc, x.n_ranks, "acc");
+        if (!s && (call == kGroupAccumulate || call == kGroupStepAccumulated))
+            s = check_rows(mk, x.acc, x.n_ranks, "acc");
         if (!s && call != kGroupAccumulate)
-            s = check_update(mk, x.n_ranks, x.master, x.m, x.v, x.flat_param_out, 0.0);
+            s = check_update(mk, x.n_ranks, x.master, x.m, x.v, x.flat_param_out, 0.0,
+                             call == kGroupStepQ8);
+        if (!s && call == kGroupStepQ8) {
+            if (!x.flat_q8_out || !x.q8_scales)
+                s = fail(ZERO_ERR_INVALID_ARG, "int8 outputs are NULL");
+            else if ((uintptr_t)x.q8_scales % 4)
+                s = fail(ZERO_ERR_ALIGNMENT, "q8_scales must be 4-byte aligned");
+        }
         if (!s && call != kGroupStepAccumulated)
             s = check_grads(mk, x.grads, x.grad_ld, x.grad_rank_offset_mul, max_rank);
         if (s) {
@@ -1259,7 +1267,7 @@ zero_status check_group_args(const zero_group *g, const zero_group_member *args,
 
 // The reduce rows (and, for the steps, the AdamW rows) of every member, in
 // member order; *max_s = the largest shard.
-zero_status group_rows(zero_group *g, const zero_group_member *args, int mode,
+zero_status group_rows(zero_group *g, const zero_group_member *args, int mode, bool q8,
                        std::vector<zg::ReduceRow> &rrows, std::vector<zg::AdamRow> *arows,
                        int64_t *max_s) {
     std::vector<zg::ReduceRow> part;
@@ -1300,7 +1308,12 @@ zero_status group_rows(zero_group *g, const zero_group_member *args, int mode,
                 w.master = x.master[j];
                 w.m = x.m[j];
                 w.v = x.v[j];
-                w.out = static_cast<uint16_t *>(x.flat_param_out) + r * mk->shard;
+                w.out = x.flat_param_out ? static_cast<uint16_t *>(x.flat_param_out) + r * mk->shard
+                                         : nullptr;
+                if (q8) {
+                    w.q8 = x.flat_q8_out + r * mk->shard;
+                    w.q8_scales = x.q8_scales + r * ((mk->shard + zg::kQ8Block - 1) / zg::kQ8Block);
+                }
                 w.S = mk->shard;
                 w.valid = part[j].valid;
                 w.lr = mk->lr;                // the member's parameter-group rates
@@ -1316,11 +1329,12 @@ zero_status group_rows(zero_group *g, const zero_group_member *args, int mode,
 // The plain or accumulated group step: the reduce (or norm pass) over every
 // row with the decision in its last block, then one AdamW over every row.
 zero_status group_step(zero_group *g, const zero_group_member *args, double extra_norm_sq,
-                       void *stream, zero_step_result *res, bool from_acc) {
+                       void *stream, zero_step_result *res, GroupCall call) {
     if (!g || !args) return fail(ZERO_ERR_INVALID_ARG, "NULL argument");
     if (!std::isfinite(extra_norm_sq) || extra_norm_sq < 0)
         return fail(ZERO_ERR_INVALID_ARG, "extra_norm_sq must be finite and >= 0");
-    zero_status s = check_group_args(g, args, from_acc ? kGroupStepAccumulated : kGroupStep);
+    const bool from_acc = call == kGroupStepAccumulated, q8 = call == kGroupStepQ8;
+    zero_status s = check_group_args(g, args, call);
     if (s) return s;
     zero_flat *c = g->core;
     DeviceGuard guard(c->device);
@@ -1330,7 +1344,7 @@ zero_status group_step(zero_group *g, const zero_group_member *args, double extr
     std::vector<zg::ReduceRow> rrows;
     std::vector<zg::AdamRow> arows;
     int64_t max_s = 0;
-    if ((s = group_rows(g, args, mode, rrows, &arows, &max_s))) return s;
+    if ((s = group_rows(g, args, mode, q8, rrows, &arows, &max_s))) return s;
     const int32_t n_rows = (int32_t)rrows.size();
     const int64_t batch = std::min<int64_t>(n_rows, zg::kMaxRanksPerLaunch);
     zg::ReducePlan rp;
@@ -1356,8 +1370,10 @@ zero_status group_step(zero_group *g, const zero_group_member *args, double extr
     ap.b1 = c->b1; ap.b2 = c->b2; ap.omb1 = c->omb1; ap.omb2 = c->omb2;
     ap.lr = c->lr; ap.eps = c->eps; ap.decay = c->decay;
     ap.st = c->d_state;
-    ap.grid_x = zg::grid_x_for(max_s, batch, c->sm_count, zg::kAdamBlocksPerSm);
+    ap.grid_x = zg::grid_x_for(max_s, batch, c->sm_count,
+                               q8 ? zg::kAdamQ8BlocksPerSm : zg::kAdamBlocksPerSm);
     if (from_acc) ap.acc = args[0].acc;   // marks the rows' gradients as accumulators
+    if (q8) ap.q8 = args[0].flat_q8_out;  // selects the int8-payload kernel
     cudaError_t e;
     if ((e = zg::run_reduce_rows(rp, rrows.data(), n_rows, st))) return cuda_fail(e, "reduce kernel launch");
     if (!rp.fuse_finalize && (e = zg::launch_finalize(f, st)))
@@ -1370,13 +1386,19 @@ zero_status group_step(zero_group *g, const zero_group_member *args, double extr
 
 ZERO_API zero_status zero_group_step(zero_group *g, const zero_group_member *args,
                                      double extra_norm_sq, void *stream, zero_step_result *res) {
-    return group_step(g, args, extra_norm_sq, stream, res, false);
+    return group_step(g, args, extra_norm_sq, stream, res, kGroupStep);
+}
+
+ZERO_API zero_status zero_group_step_q8(zero_group *g, const zero_group_member *args,
+                                        double extra_norm_sq, void *stream,
+                                        zero_step_result *res) {
+    return group_step(g, args, extra_norm_sq, stream, res, kGroupStepQ8);
 }
 
 ZERO_API zero_status zero_group_step_accumulated(zero_group *g, const zero_group_member *args,
                                                  double extra_norm_sq, void *stream,
                                                  zero_step_result *res) {
-    return group_step(g, args, extra_norm_sq, stream, res, true);
+    return group_step(g, args, extra_norm_sq, stream, res, kGroupStepAccumulated);
 }
 
 ZERO_API zero_status zero_group_accumulate(zero_group *g, const zero_group_member *args,
@@ -1390,7 +1412,7 @@ ZERO_API zero_status zero_group_accumulate(zero_group *g, const zero_group_membe
     const int mode = first_micro_step ? zg::kModeAccFirst : zg::kModeAccAdd;
     std::vector<zg::ReduceRow> rrows;
     int64_t max_s = 0;
-    if ((s = group_rows(g, args, mode, rrows, nullptr, &max_s))) return s;
+    if ((s = group_rows(g, args, mode, false, rrows, nullptr, &max_s))) return s;
     const int32_t n_rows = (int32_t)rrows.size();
     zg::ReducePlan rp;
     rp.mode = mode;

@@ -289,9 +289,11 @@ typedef struct zero_group zero_group;
 zero_status zero_group_init(zero_flat *const *members, int32_t n_members, zero_group **out);
 
 /* The arguments of one member in a group call, those of zero_shard_step /
- * zero_grad_accumulate / zero_shard_step_accumulated for that member's
- * handle; each call reads the fields it needs (acc: the member's per-rank
- * fp32 accumulators, used by the accumulation calls only). */
+ * zero_grad_accumulate / zero_shard_step_accumulated / zero_shard_step_q8
+ * for that member's handle; each call reads the fields it needs (acc: the
+ * member's per-rank fp32 accumulators, used by the accumulation calls only;
+ * flat_q8_out and q8_scales: the member's int8 payload, zero_group_step_q8
+ * only). */
 typedef struct {
     const int32_t *ranks;
     int32_t n_ranks;
@@ -303,6 +305,8 @@ typedef struct {
     float *const *v;
     void *flat_param_out;
     float *const *acc;
+    int8_t *flat_q8_out;
+    float *q8_scales;
 } zero_group_member;
 
 /* One step of every member (args[k] for the group's member k): the reduce
@@ -313,6 +317,14 @@ typedef struct {
  * res is NULL.  Errors: as for zero_shard_step, per member. */
 zero_status zero_group_step(zero_group *g, const zero_group_member *args, double extra_norm_sq,
                             void *stream, zero_step_result *res);
+
+/* zero_group_step that also writes every member's int8 all-gather payload
+ * and its block scales, as zero_shard_step_q8 does per member (the same
+ * quantization of the same 16-bit values; flat_param_out may be NULL).
+ * One reduce launch and one int8-payload AdamW launch per 64 rows.  Errors:
+ * as for zero_shard_step_q8, per member. */
+zero_status zero_group_step_q8(zero_group *g, const zero_group_member *args, double extra_norm_sq,
+                               void *stream, zero_step_result *res);
 
 /* Micro-step accumulation for every member in one launch per 64 rows, as
  * zero_grad_accumulate does per member (acc = r on the first micro-step,

@@ -35,10 +35,16 @@ def _args(w, d):
                 grad_rank_offset_mul=w.grad_rank_mul)
 
 
-def run_group_parity(ora, ws, steps=3, lr_at=None):
+def _decode(u):
+    return u.view(np.float16).astype(np.float32)
+
+
+def run_group_parity(ora, ws, steps=3, lr_at=None, q8=False, q8_only=()):
     """Step the members ws as one group on the GPU and in the oracle, each
     member with its own parameter group's lr and weight decay; lr_at: {step:
-    lr} set on the whole group before that step."""
+    lr} set on the whole group before that step.  q8: zero_group_step_q8, the
+    int8 payload checked bit for bit against the oracle's quantizer of every
+    member's parameters; members in q8_only pass no 16-bit output."""
     import fsdp_sharded_mixed_zero_gb300 as Z
     from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
     kws = [dict(w.hparams_kwargs()) for w in ws]
@@ -50,6 +56,13 @@ def run_group_parity(ora, ws, steps=3, lr_at=None):
                   [f32(t).copy() for t in d.v], u16(d.out).copy()) for d in ds]
         st = ora.scaler_init(hp)
         skipped = []
+        if q8:
+            nbs = [-(-d.S // 256) for d in ds]
+            q8s = [torch.full((d.padded,), 0x55, dtype=torch.int8, device="cuda") for d in ds]
+            scs = [torch.full((w.world_size * nb,), -1.0, device="cuda")
+                   for w, nb in zip(ws, nbs)]
+            want_q = [np.full(d.padded, 0x55, np.int8) for d in ds]
+            want_s = [np.full(w.world_size * nb, -1.0, np.float32) for w, nb in zip(ws, nbs)]
         for step in range(steps):
             if lr_at and step in lr_at:
                 group.set_lr(lr_at[step])
@@ -62,7 +75,15 @@ def run_group_parity(ora, ws, steps=3, lr_at=None):
             for d in ds:
                 d.gen_grads(step, scale)
                 grads.append(host_grads(d.grads))
-            res = group.step([_args(w, d) for w, d in zip(ws, ds)])
+            if q8:
+                margs = [_args(w, d) for w, d in zip(ws, ds)]
+                for k, a in enumerate(margs):
+                    a.update(q8=q8s[k], q8_scales=scs[k])
+                    if k in q8_only:
+                        a["out"] = None
+                res = group.step_q8(margs)
+            else:
+                res = group.step([_args(w, d) for w, d in zip(ws, ds)])
             gs = []
             for w, d, g in zip(ws, ds, grads):
                 for r in w.ranks:
@@ -86,7 +107,25 @@ def run_group_parity(ora, ws, steps=3, lr_at=None):
                     k += 1
                     assert_state(f32(d.master[j]), f32(d.m[j]), f32(d.v[j]), master[j], m[j],
                                  v[j], tag=" (%s, step %d, rank %d)" % (w.name, step, r))
-                assert_params_close(u16(d.out), out, False, "%s params (step %d)" % (w.name, step))
+                if q8 and ws.index(w) in q8_only:
+                    assert bool((d.out.view(torch.int16) == 0x5A5A).all())
+                else:
+                    assert_params_close(u16(d.out), out, False,
+                                        "%s params (step %d)" % (w.name, step))
+            if q8:
+                for i, (w, d, (_, _, _, out)) in enumerate(zip(ws, ds, state)):
+                    S, nb = d.S, nbs[i]
+                    if not skip:
+                        for r in w.ranks:
+                            qq, ss = ora.quantize_q8(
+                                np.ascontiguousarray(_decode(out[r * S:(r + 1) * S])), 256)
+                            want_q[i][r * S:(r + 1) * S] = qq
+                            want_s[i][r * nb:(r + 1) * nb] = ss
+                    assert np.array_equal(q8s[i].cpu().numpy(), want_q[i]), \
+                        "%s codes (step %d)" % (w.name, step)
+                    assert np.array_equal(scs[i].cpu().numpy().view(np.uint32),
+                                          want_s[i].view(np.uint32)), \
+                        "%s scales (step %d)" % (w.name, step)
             skipped.append(skip)
         assert group.scaler_state().as_tuple() == st.as_tuple()
         return skipped
@@ -94,6 +133,22 @@ def run_group_parity(ora, ws, steps=3, lr_at=None):
         group.close()
         for d in ds:
             d.close()
+
+
+def test_group_step_with_int8_payload(ora):
+    """zero_group_step_q8: four members (one slice, one staged, one q8-only
+    without the 16-bit output, one with its own rates), an overflow skipping
+    every member and leaving every payload as it was."""
+    _need_gpu()
+    ws = [
+        _wl("attn_all_shards", [(256, 768), (768,)], 8, list(range(8)), seed=51),
+        _wl("mlp_slice_rank5", [(768, 3072), (3072,)], 8, [5], layout="slice", seed=52,
+            inf_at=(1, 6, 1000)),
+        _wl("odd_all_shards", [(80_001,)], 8, list(range(8)), seed=53),
+        _wl("norms_q8_only", [(768,), (768,), (777,)], 8, [0, 3, 7], seed=54,
+            hp=dict(lr=1e-4, weight_decay=0.0)),
+    ]
+    assert run_group_parity(ora, ws, q8=True, q8_only=(3,)) == [0, 1, 0]
 
 
 def test_group_members_keep_their_own_rates(ora):
