@@ -662,7 +662,9 @@ def run_group(args):
     decision per member -- a timing baseline only).  With --micro-steps K a
     step is K accumulations and the step from the accumulators, grouped
     (K + 1 launches per 64 members) or per member; with --q8 the steps also
-    write the int8 all-gather payload (zero_group_step_q8 / zero_shard_step_q8)."""
+    write the int8 all-gather payload (zero_group_step_q8 / zero_shard_step_q8);
+    with --offload the fp32 state lives in pinned host memory and the update
+    runs on the host threads (zero_group_step_offload / zero_shard_step_offload)."""
     import torch
     import fsdp_sharded_mixed_zero_gb300 as Z
     from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
@@ -688,8 +690,16 @@ def run_group(args):
 
     micro = max(1, args.micro_steps)
     q8 = bool(args.q8)
-    if q8 and micro > 1:
-        raise SystemExit("--group takes --q8 or --micro-steps, not both")
+    off = bool(args.offload)
+    if (q8 + (micro > 1) + off) > 1:
+        raise SystemExit("--group takes one of --q8, --micro-steps, --offload")
+    if off:                                 # fp32 state in pinned host memory
+        hargs = []
+        for a in margs:
+            h = dict(a)
+            for name in ("master", "m", "v"):
+                h[name] = [t.detach().cpu().pin_memory() for t in a[name]]
+            hargs.append(h)
     if q8:                                  # the int8 all-gather payload as well
         for a, d in zip(margs, ds):
             a["q8"] = torch.empty(d.padded, dtype=torch.int8, device=dev)
@@ -703,6 +713,10 @@ def run_group(args):
                  for w, d in zip(ws, ds)]
 
     def grouped():
+        if off:
+            grp.step_offload(hargs, n_threads=args.offload_threads,
+                             gpu_share=args.offload_gpu_share, stream=stream)
+            return
         if q8:
             grp.step_q8(margs, stream=stream, want_result=False)
             return
@@ -722,7 +736,12 @@ def run_group(args):
                          want_result=False)
 
     def per_member():
-        for w, d, a in zip(ws, ds, margs):
+        for w, d, a, h in zip(ws, ds, margs, hargs if off else margs):
+            if off:
+                d.flat.step_offload(w.ranks, d.grads, h["master"], h["m"], h["v"], d.out,
+                                    grad_rank_offset_mul=0, n_threads=args.offload_threads,
+                                    gpu_share=args.offload_gpu_share, stream=stream)
+                continue
             if q8:
                 d.flat.step_q8(w.ranks, d.grads, d.master, d.m, d.v, d.out, a["q8"],
                                a["q8_scales"], grad_rank_offset_mul=0, stream=stream,
@@ -742,8 +761,8 @@ def run_group(args):
     times = {}
     clocks = None
     arms = [("group", grouped), ("split", split), ("per_flat_parameter", per_member)]
-    if micro > 1 or q8:
-        arms = [arms[0], arms[2]]           # the split step has no accumulation or int8 form
+    if micro > 1 or q8 or off:
+        arms = [arms[0], arms[2]]           # the split step has no accumulation, int8 or offload form
     for name, fn in arms:
         for _ in range(args.warmup):
             fn()
@@ -764,7 +783,10 @@ def run_group(args):
         if sampler:
             clocks = sampler.stop()
         times[name] = group.max(e0.elapsed_time(e1))
-    if q8:
+    if off:
+        res = grp.step_offload(hargs, n_threads=args.offload_threads,
+                               gpu_share=args.offload_gpu_share, stream=stream)
+    elif q8:
         res = grp.step_q8(margs, stream=stream)
     elif micro == 1:
         res = grp.step(margs, stream=stream)
@@ -782,13 +804,16 @@ def run_group(args):
             "ms_per_step": times["group"] / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": "group%dx%d" % (M, ds[0].S)
-                       + ("_micro%d" % micro if micro > 1 else "") + ("_q8" if q8 else ""),
+                       + ("_micro%d" % micro if micro > 1 else "") + ("_q8" if q8 else "")
+                       + ("_offload" if off else ""),
                        "flat_parameters": M, "micro_steps": micro, "q8_payload": q8,
+                       "offload": off,
                        "params_per_flat_parameter_shard": ds[0].S, "emulated_world_size": 8,
                        "stepped_ranks": [7], "parallelism": "replicas%d" % world},
             "compare_ms_per_step": {k: v / args.steps for k, v in times.items()},
             "clocks": clocks,
-            "gpu_launches": (micro + 1) * n_batches * args.steps,
+            "gpu_launches": ((micro + 1) * n_batches if not off
+                             else n_batches * (1 + (args.offload_gpu_share > 0))) * args.steps,
         }
         print(json.dumps(line), flush=True)
     grp.close()
@@ -803,10 +828,10 @@ def main():
     w = BY_NAME[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
-    elif args.offload:
-        run_offload(args, w)
     elif args.group:
         run_group(args)
+    elif args.offload:
+        run_offload(args, w)
     else:
         run_ours(args, w)
 

@@ -117,6 +117,8 @@ def _load():
                                   C.POINTER(StepResult)]
     L.zero_group_step_q8.argtypes = [vp, C.POINTER(GroupMember), C.c_double, vp,
                                      C.POINTER(StepResult)]
+    L.zero_group_step_offload.argtypes = [vp, C.POINTER(GroupMember), C.c_double, i32,
+                                          C.c_double, vp, C.POINTER(StepResult)]
     L.zero_group_accumulate.argtypes = [vp, C.POINTER(GroupMember), i32, vp]
     L.zero_group_step_accumulated.argtypes = [vp, C.POINTER(GroupMember), C.c_double, vp,
                                               C.POINTER(StepResult)]
@@ -145,6 +147,7 @@ def _load():
                  "zero_group_loss_scaler_state", "zero_group_set_loss_scaler_state",
                  "zero_group_set_lr", "zero_group_free", "zero_group_accumulate",
                  "zero_group_step_accumulated", "zero_group_step_q8",
+                 "zero_group_step_offload",
                  "zero_shard_step_accumulated"):
         getattr(L, name).restype = i32
     return L
@@ -409,6 +412,21 @@ class ZeroGroup:
                                        C.c_void_p(stream.cuda_stream),
                                        C.byref(res) if res is not None else None),
                "zero_group_step_q8")
+        return res
+
+    def step_offload(self, args, extra_norm_sq=0.0, n_threads=0, gpu_share=0.0, stream=None):
+        """The ZeRO-Offload group step: args[k] as for step() with master, m, v
+        host (CPU, pinned for gpu_share > 0) fp32 tensors.  Returns the step
+        result; the host arrays are updated when it returns."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        keep = []
+        ms = self._members(args, keep)
+        res = StepResult()
+        _check(_lib.zero_group_step_offload(self.handle, ms, float(extra_norm_sq), int(n_threads),
+                                            float(gpu_share), C.c_void_p(stream.cuda_stream),
+                                            C.byref(res)), "zero_group_step_offload")
         return res
 
     def accumulate(self, args, first_micro_step, stream=None):

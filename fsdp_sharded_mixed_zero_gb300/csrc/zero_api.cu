@@ -831,10 +831,17 @@ ZERO_API zero_status zero_shard_step_accumulated(zero_flat *h, const int32_t *ra
 namespace {
 
 // Pinned host buffers and worker threads of the offload step, grown on demand.
-zero_status ensure_offload(zero_flat *h, int32_t n_ranks, int32_t n_threads) {
+// Pinned host rows of the handle's offload updates (reduced-gradient copies
+// and 16-bit parameter staging) for n_ranks stepped ranks.  busy: an event
+// whose copies may still read the staging (besides the handle's own), waited
+// for before a buffer is replaced.
+zero_status ensure_host_rows(zero_flat *h, int32_t n_ranks, cudaEvent_t busy) {
     const int64_t S = h->shard;
-    if (n_ranks > h->h_g_rows) {
+    if (n_ranks > h->h_g_rows || n_ranks > h->h_out_rows) {
         if (h->out_done) cudaEventSynchronize(h->out_done);
+        if (busy) cudaEventSynchronize(busy);
+    }
+    if (n_ranks > h->h_g_rows) {
         if (h->h_g) cudaFreeHost(h->h_g);
         h->h_g = nullptr;
         h->h_g_rows = 0;
@@ -853,7 +860,6 @@ zero_status ensure_offload(zero_flat *h, int32_t n_ranks, int32_t n_threads) {
         h->h_g_rows = n_ranks;
     }
     if (n_ranks > h->h_out_rows) {
-        if (h->out_done) cudaEventSynchronize(h->out_done);
         if (h->h_out) cudaFreeHost(h->h_out);
         h->h_out = nullptr;
         h->h_out_rows = 0;
@@ -871,6 +877,11 @@ zero_status ensure_offload(zero_flat *h, int32_t n_ranks, int32_t n_threads) {
         }
         h->h_out_rows = n_ranks;
     }
+    return ZERO_OK;
+}
+
+// The streams, events and worker threads that run offload updates.
+zero_status ensure_host_runtime(zero_flat *h, int32_t n_threads) {
     if (!h->out_done) {
         cudaError_t e = cudaEventCreateWithFlags(&h->out_done, cudaEventDisableTiming);
         if (e) { h->out_done = nullptr; return cuda_fail(e, "cudaEventCreate"); }
@@ -894,80 +905,109 @@ zero_status ensure_offload(zero_flat *h, int32_t n_ranks, int32_t n_threads) {
     return ZERO_OK;
 }
 
+zero_status ensure_offload(zero_flat *h, int32_t n_ranks, int32_t n_threads) {
+    zero_status s = ensure_host_runtime(h, n_threads);
+    return s ? s : ensure_host_rows(h, n_ranks, nullptr);
+}
+
 // Elements per host task, and per parameter copy back to the device.
 constexpr int64_t kHostChunk = int64_t(1) << 16;
 constexpr int64_t kHostSegment = int64_t(1) << 24;
 
-// The host update of elements [i_begin, S) of every stepped rank (i_begin a
-// multiple of kHostChunk).  The reduced gradient rows come down from HBM
-// segment by segment on the copy stream, and a host task waits only for the
-// segment it works on, so the copies overlap the update; each segment's
+// One row of a host update: a stepped rank's shard of one FlatParameter,
+// updated on the host over elements [i_begin, S) (i_begin a multiple of
+// kHostChunk).
+struct HostRow {
+    const float *d_g;                 // the reduced gradient row in HBM
+    float *h_g;                       // its pinned host copy
+    float *master, *m, *v;            // fp32 state in host memory
+    uint16_t *stage;                  // pinned 16-bit staging of the row
+    uint16_t *d_out;                  // the row's slot in the device flat buffer
+    int64_t S, i_begin;
+    zh::AdamScalars k;                // the row's scalars (its parameter group's lr, decay)
+};
+
+// The host update of every row.  The reduced gradient rows come down from
+// HBM segment by segment on rt's copy stream, and a host task waits only for
+// the segment it works on, so the copies overlap the update; each segment's
 // 16-bit parameters go back to the device on the up stream as soon as its
-// last chunk is done.  Returns the first CUDA error, if any.
-cudaError_t host_update(zero_flat *h, const zh::AdamScalars &k, const int32_t *ranks,
-                        int32_t n_ranks, float *const *master, float *const *m, float *const *v,
-                        void *flat_param_out, int64_t i_begin) {
-    const int64_t S = h->shard;
-    const int64_t span = S - i_begin;
-    if (span <= 0) return cudaSuccess;
-    const bool bf16 = h->param_dtype == ZERO_BF16;
+// last chunk is done.  rt supplies the streams, the pool, the segment events
+// and the device.  Returns the first CUDA error, if any.
+cudaError_t host_update_rows(zero_flat *rt, const HostRow *rows, int64_t n_rows, bool bf16) {
     const int64_t chunks_per_seg = kHostSegment / kHostChunk;
-    const int64_t segs = (span + kHostSegment - 1) / kHostSegment;
-    const int64_t chunks = (span + kHostChunk - 1) / kHostChunk;
-    const int64_t n_seg = n_ranks * segs;
+    // per row: its first segment and its first task, in row order
+    std::vector<int64_t> seg0(n_rows + 1, 0), task0(n_rows + 1, 0);
+    for (int64_t j = 0; j < n_rows; ++j) {
+        const int64_t span = std::max<int64_t>(rows[j].S - rows[j].i_begin, 0);
+        seg0[j + 1] = seg0[j] + (span + kHostSegment - 1) / kHostSegment;
+        task0[j + 1] = task0[j] + (span + kHostChunk - 1) / kHostChunk;
+    }
+    const int64_t n_seg = seg0[n_rows], n_tasks = task0[n_rows];
+    if (n_tasks == 0) return cudaSuccess;
     cudaError_t e;
-    while ((int64_t)h->seg_ev.size() < n_seg) {
+    while ((int64_t)rt->seg_ev.size() < n_seg) {
         cudaEvent_t ev;
         if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming))) return e;
-        h->seg_ev.push_back(ev);
+        rt->seg_ev.push_back(ev);
     }
-    for (int64_t j = 0; j < n_ranks; ++j)
-        for (int64_t q = 0; q < segs; ++q) {
-            const int64_t s0 = i_begin + q * kHostSegment, len = std::min(kHostSegment, S - s0);
-            const int64_t off = j * h->g_stride + s0;
-            if ((e = cudaMemcpyAsync(h->h_g + off, h->d_g + off, (size_t)len * 4,
-                                     cudaMemcpyDeviceToHost, h->copy_stream)))
-                return e;
-            if ((e = cudaEventRecord(h->seg_ev[j * segs + q], h->copy_stream))) return e;
-        }
     std::unique_ptr<std::atomic<int64_t>[]> left(new std::atomic<int64_t>[n_seg]);
     std::unique_ptr<std::atomic<int>[]> ready(new std::atomic<int>[n_seg]);
-    for (int64_t j = 0; j < n_ranks; ++j)
-        for (int64_t q = 0; q < segs; ++q) {
-            left[j * segs + q].store(std::min(chunks_per_seg, chunks - q * chunks_per_seg));
-            ready[j * segs + q].store(0);
+    for (int64_t j = 0; j < n_rows; ++j) {
+        const HostRow &w = rows[j];
+        const int64_t chunks = task0[j + 1] - task0[j];
+        for (int64_t q = 0; q < seg0[j + 1] - seg0[j]; ++q) {
+            const int64_t s0 = w.i_begin + q * kHostSegment, len = std::min(kHostSegment, w.S - s0);
+            if ((e = cudaMemcpyAsync(w.h_g + s0, w.d_g + s0, (size_t)len * 4,
+                                     cudaMemcpyDeviceToHost, rt->copy_stream)))
+                return e;
+            if ((e = cudaEventRecord(rt->seg_ev[seg0[j] + q], rt->copy_stream))) return e;
+            left[seg0[j] + q].store(std::min(chunks_per_seg, chunks - q * chunks_per_seg));
+            ready[seg0[j] + q].store(0);
         }
+    }
     std::atomic<int> err{0};
-    const int dev = h->device;
-    uint16_t *out16 = static_cast<uint16_t *>(flat_param_out);
+    const int dev = rt->device;
     auto note = [&](cudaError_t x) {
         int none = 0;
         if (x) err.compare_exchange_strong(none, (int)x);
     };
     const std::function<void(int64_t)> task = [&](int64_t t) {
-        const int64_t j = t / chunks, c = t % chunks;
-        const int64_t q = c / chunks_per_seg, sg = j * segs + q;
+        const int64_t j = std::upper_bound(task0.begin(), task0.end(), t) - task0.begin() - 1;
+        const HostRow &w = rows[j];
+        const int64_t c = t - task0[j];
+        const int64_t q = c / chunks_per_seg, sg = seg0[j] + q;
         if (!ready[sg].load(std::memory_order_acquire)) {
-            const cudaError_t x = cudaEventSynchronize(h->seg_ev[sg]);
+            const cudaError_t x = cudaEventSynchronize(rt->seg_ev[sg]);
             if (x) { note(x); return; }
             ready[sg].store(1, std::memory_order_release);
         }
-        const int64_t i0 = i_begin + c * kHostChunk;
-        const int64_t n = std::min(kHostChunk, S - i0);
-        uint16_t *stage = h->h_out + j * S;
-        zh::adamw_cast_range(k, h->h_g + j * h->g_stride + i0, master[j] + i0, m[j] + i0,
-                             v[j] + i0, stage + i0, n, bf16);
+        const int64_t i0 = w.i_begin + c * kHostChunk;
+        const int64_t n = std::min(kHostChunk, w.S - i0);
+        zh::adamw_cast_range(w.k, w.h_g + i0, w.master + i0, w.m + i0, w.v + i0, w.stage + i0, n,
+                             bf16);
         if (left[sg].fetch_sub(1) == 1) {                      // segment complete
-            const int64_t s0 = i_begin + q * kHostSegment;
-            const int64_t len = std::min(kHostSegment, S - s0);
+            const int64_t s0 = w.i_begin + q * kHostSegment;
+            const int64_t len = std::min(kHostSegment, w.S - s0);
             cudaError_t x = cudaSetDevice(dev);
-            if (!x) x = cudaMemcpyAsync(out16 + (int64_t)ranks[j] * S + s0, stage + s0,
-                                        (size_t)len * 2, cudaMemcpyHostToDevice, h->up_stream);
+            if (!x) x = cudaMemcpyAsync(w.d_out + s0, w.stage + s0, (size_t)len * 2,
+                                        cudaMemcpyHostToDevice, rt->up_stream);
             note(x);
         }
     };
-    h->pool->run(n_ranks * chunks, task);
+    rt->pool->run(n_tasks, task);
     return (cudaError_t)err.load();
+}
+
+// The rows of one handle's offload update (its pinned buffers, its ranks).
+void host_rows_of(zero_flat *h, const zh::AdamScalars &k, const int32_t *ranks, int32_t n_ranks,
+                  float *const *master, float *const *m, float *const *v, void *flat_param_out,
+                  int64_t i_begin, std::vector<HostRow> &rows) {
+    const int64_t S = h->shard;
+    uint16_t *out16 = static_cast<uint16_t *>(flat_param_out);
+    for (int32_t j = 0; j < n_ranks; ++j)
+        rows.push_back(HostRow{h->d_g + (int64_t)j * h->g_stride, h->h_g + (int64_t)j * h->g_stride,
+                               master[j], m[j], v[j], h->h_out + (int64_t)j * S,
+                               out16 + (int64_t)ranks[j] * S, S, i_begin, k});
 }
 
 // Whether the GPU can read and write every stepped rank's host arrays.
@@ -1059,7 +1099,10 @@ ZERO_API zero_status zero_shard_step_offload(zero_flat *h, const int32_t *ranks,
         if ((e = cudaEventSynchronize(h->out_done))) return cuda_fail(e, "waiting for the last copies");
         const zh::AdamScalars k{h->b1, h->b2, h->omb1, h->omb2, h->lr, h->eps, h->decay,
                                 ds.res.clip_coef, ds.bc1, ds.bc2};
-        if ((e = host_update(h, k, ranks, n_ranks, master, m, v, flat_param_out, split)))
+        std::vector<HostRow> rows;
+        host_rows_of(h, k, ranks, n_ranks, master, m, v, flat_param_out, split, rows);
+        if ((e = host_update_rows(h, rows.data(), (int64_t)rows.size(),
+                                  h->param_dtype == ZERO_BF16)))
             return cuda_fail(e, "copying parameters to the device");
         if ((e = cudaSetDevice(h->device))) return cuda_fail(e, "cudaSetDevice");
         if ((e = cudaEventRecord(h->out_done, h->up_stream))) return cuda_fail(e, "cudaEventRecord");
@@ -1328,25 +1371,19 @@ zero_status group_rows(zero_group *g, const zero_group_member *args, int mode, b
 
 // The plain or accumulated group step: the reduce (or norm pass) over every
 // row with the decision in its last block, then one AdamW over every row.
-zero_status group_step(zero_group *g, const zero_group_member *args, double extra_norm_sq,
-                       void *stream, zero_step_result *res, GroupCall call) {
-    if (!g || !args) return fail(ZERO_ERR_INVALID_ARG, "NULL argument");
-    if (!std::isfinite(extra_norm_sq) || extra_norm_sq < 0)
-        return fail(ZERO_ERR_INVALID_ARG, "extra_norm_sq must be finite and >= 0");
+// The reduce (or the norm pass) of a group step over every row, with the
+// decision in its last block, queued on st; *arows: the rows of the update
+// that follows, *max_s: the largest shard.
+zero_status group_reduce(zero_group *g, const zero_group_member *args, double extra_norm_sq,
+                         cudaStream_t st, GroupCall call, std::vector<zg::AdamRow> *arows,
+                         int64_t *max_s) {
     const bool from_acc = call == kGroupStepAccumulated, q8 = call == kGroupStepQ8;
-    zero_status s = check_group_args(g, args, call);
-    if (s) return s;
     zero_flat *c = g->core;
-    DeviceGuard guard(c->device);
-    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the group's device");
-    const cudaStream_t st = (cudaStream_t)stream;
     const int mode = from_acc ? zg::kModeNormOnly : zg::kModeStep;
     std::vector<zg::ReduceRow> rrows;
-    std::vector<zg::AdamRow> arows;
-    int64_t max_s = 0;
-    if ((s = group_rows(g, args, mode, q8, rrows, &arows, &max_s))) return s;
+    zero_status s = group_rows(g, args, mode, q8, rrows, arows, max_s);
+    if (s) return s;
     const int32_t n_rows = (int32_t)rrows.size();
-    const int64_t batch = std::min<int64_t>(n_rows, zg::kMaxRanksPerLaunch);
     zg::ReducePlan rp;
     rp.mode = mode;
     rp.in_kind = from_acc ? zg::kInF32 : in_kind_of(c);
@@ -1355,30 +1392,59 @@ zero_status group_step(zero_group *g, const zero_group_member *args, double extr
     rp.st = c->d_state;
     rp.done = c->d_done;
     rp.staged = zg::rows_want_staging(rp.mode, rp.in_kind, rp.n_contrib, rrows.data(), n_rows);
-    rp.grid_x = zg::grid_x_for(max_s, batch, c->sm_count,
+    rp.grid_x = zg::grid_x_for(*max_s, std::min<int64_t>(n_rows, zg::kMaxRanksPerLaunch),
+                               c->sm_count,
                                rp.staged ? c->staged_bps[rp.mode] : c->reduce_bps[rp.mode]);
     const int64_t parts = (int64_t)rp.grid_x * n_rows;
     if ((s = ensure_scratch(c, 0, parts))) return s;
     rp.part_ss = c->d_part_ss;
     rp.part_of = c->d_part_of;
-    const zg::FinalizeArgs f =
-        decision_args(c, c->d_part_ss, c->d_part_of, max_s > 0 ? (int32_t)parts : 0, extra_norm_sq);
-    rp.fuse_finalize = max_s > 0;
+    const zg::FinalizeArgs f = decision_args(c, c->d_part_ss, c->d_part_of,
+                                             *max_s > 0 ? (int32_t)parts : 0, extra_norm_sq);
+    rp.fuse_finalize = *max_s > 0;
     rp.fin = f;
-    zg::AdamPlan ap;
-    ap.bf16_out = c->param_dtype == ZERO_BF16;
-    ap.b1 = c->b1; ap.b2 = c->b2; ap.omb1 = c->omb1; ap.omb2 = c->omb2;
-    ap.lr = c->lr; ap.eps = c->eps; ap.decay = c->decay;
-    ap.st = c->d_state;
-    ap.grid_x = zg::grid_x_for(max_s, batch, c->sm_count,
-                               q8 ? zg::kAdamQ8BlocksPerSm : zg::kAdamBlocksPerSm);
-    if (from_acc) ap.acc = args[0].acc;   // marks the rows' gradients as accumulators
-    if (q8) ap.q8 = args[0].flat_q8_out;  // selects the int8-payload kernel
     cudaError_t e;
     if ((e = zg::run_reduce_rows(rp, rrows.data(), n_rows, st))) return cuda_fail(e, "reduce kernel launch");
     if (!rp.fuse_finalize && (e = zg::launch_finalize(f, st)))
         return cuda_fail(e, "finalize kernel launch");
-    if ((e = zg::run_adamw_rows(ap, arows.data(), n_rows, st))) return cuda_fail(e, "adamw kernel launch");
+    return ZERO_OK;
+}
+
+// The group's AdamW plan (shared scalars, state, output encoding, grid).
+zg::AdamPlan group_adam_plan(const zero_flat *c, int64_t max_s, int32_t n_rows, bool q8) {
+    zg::AdamPlan ap;
+    ap.bf16_out = c->param_dtype == ZERO_BF16;
+    ap.b1 = c->b1; ap.b2 = c->b2; ap.omb1 = c->omb1; ap.omb2 = c->omb2;
+    ap.eps = c->eps;
+    ap.st = c->d_state;
+    ap.grid_x = zg::grid_x_for(max_s, std::min<int32_t>(n_rows, zg::kMaxRanksPerLaunch),
+                               c->sm_count, q8 ? zg::kAdamQ8BlocksPerSm : zg::kAdamBlocksPerSm);
+    return ap;
+}
+
+// The plain, int8-payload or accumulated group step: the reduce (or norm
+// pass) over every row with the decision in its last block, then one AdamW
+// over every row.
+zero_status group_step(zero_group *g, const zero_group_member *args, double extra_norm_sq,
+                       void *stream, zero_step_result *res, GroupCall call) {
+    if (!g || !args) return fail(ZERO_ERR_INVALID_ARG, "NULL argument");
+    if (!std::isfinite(extra_norm_sq) || extra_norm_sq < 0)
+        return fail(ZERO_ERR_INVALID_ARG, "extra_norm_sq must be finite and >= 0");
+    zero_status s = check_group_args(g, args, call);
+    if (s) return s;
+    zero_flat *c = g->core;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the group's device");
+    const cudaStream_t st = (cudaStream_t)stream;
+    std::vector<zg::AdamRow> arows;
+    int64_t max_s = 0;
+    if ((s = group_reduce(g, args, extra_norm_sq, st, call, &arows, &max_s))) return s;
+    const bool q8 = call == kGroupStepQ8;
+    zg::AdamPlan ap = group_adam_plan(c, max_s, (int32_t)arows.size(), q8);
+    if (call == kGroupStepAccumulated) ap.acc = args[0].acc;   // the rows' g are accumulators
+    if (q8) ap.q8 = args[0].flat_q8_out;                       // the int8-payload kernel
+    const cudaError_t e = zg::run_adamw_rows(ap, arows.data(), (int32_t)arows.size(), st);
+    if (e) return cuda_fail(e, "adamw kernel launch");
     return res ? read_result(c, st, res) : ZERO_OK;
 }
 
@@ -1399,6 +1465,95 @@ ZERO_API zero_status zero_group_step_accumulated(zero_group *g, const zero_group
                                                  double extra_norm_sq, void *stream,
                                                  zero_step_result *res) {
     return group_step(g, args, extra_norm_sq, stream, res, kGroupStepAccumulated);
+}
+
+ZERO_API zero_status zero_group_step_offload(zero_group *g, const zero_group_member *args,
+                                             double extra_norm_sq, int32_t n_threads,
+                                             double gpu_share, void *stream,
+                                             zero_step_result *res) {
+    if (!g || !args) return fail(ZERO_ERR_INVALID_ARG, "NULL argument");
+    if (!std::isfinite(extra_norm_sq) || extra_norm_sq < 0)
+        return fail(ZERO_ERR_INVALID_ARG, "extra_norm_sq must be finite and >= 0");
+    if (n_threads < 0) return fail(ZERO_ERR_INVALID_ARG, "n_threads must be >= 0");
+    if (!(gpu_share >= 0.0 && gpu_share <= 1.0))
+        return fail(ZERO_ERR_INVALID_ARG, "gpu_share must be in [0, 1]");
+    zero_status s = check_group_args(g, args, kGroupStep);
+    if (s) return s;
+    zero_flat *c = g->core;
+    DeviceGuard guard(c->device);
+    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the group's device");
+    const size_t n_members = g->members.size();
+    // member k's GPU share: elements [0, split[k]) of each of its rows
+    std::vector<int64_t> split(n_members);
+    for (size_t k = 0; k < n_members; ++k) {
+        const zero_flat *mk = g->members[k];
+        const int64_t S = mk->shard;
+        split[k] = std::min(S, gpu_share >= 1.0
+                                   ? S
+                                   : (int64_t)(gpu_share * (double)S) / kHostChunk * kHostChunk);
+        float *const *const rows[3] = {args[k].master, args[k].m, args[k].v};
+        if (split[k] > 0 && !gpu_reaches(mk, args[k].n_ranks, rows))
+            return fail(ZERO_ERR_INVALID_ARG, "member %zu: gpu_share > 0 needs host arrays the "
+                        "GPU can access (pinned or registered)", k);
+    }
+    if ((s = ensure_host_runtime(c, n_threads))) return s;
+    for (size_t k = 0; k < n_members; ++k)
+        if ((s = ensure_host_rows(g->members[k], args[k].n_ranks, c->out_done))) return s;
+    const cudaStream_t st = (cudaStream_t)stream;
+    std::vector<zg::AdamRow> arows;
+    int64_t max_s = 0;
+    if ((s = group_reduce(g, args, extra_norm_sq, st, kGroupStep, &arows, &max_s))) return s;
+    cudaError_t e = cudaMemcpyAsync(c->h_state, c->d_state, sizeof(zg::DevState),
+                                    cudaMemcpyDeviceToHost, st);
+    if (!e) e = cudaEventRecord(c->decided, st);
+    if (e) return cuda_fail(e, "reading the step decision");
+    // the GPU's share of every row, queued behind the decision
+    std::vector<zg::AdamRow> gpu_rows;
+    int64_t max_split = 0;
+    for (size_t k = 0, i = 0; k < n_members; ++k)
+        for (int32_t j = 0; j < args[k].n_ranks; ++j, ++i)
+            if (split[k] > 0) {
+                gpu_rows.push_back(arows[i]);
+                gpu_rows.back().S = split[k];
+                max_split = std::max(max_split, split[k]);
+            }
+    if (!gpu_rows.empty()) {
+        const zg::AdamPlan ap = group_adam_plan(c, max_split, (int32_t)gpu_rows.size(), false);
+        if ((e = zg::run_adamw_rows(ap, gpu_rows.data(), (int32_t)gpu_rows.size(), st)))
+            return cuda_fail(e, "adamw kernel launch");
+    }
+    if ((e = cudaEventRecord(c->gpu_part_done, st))) return cuda_fail(e, "cudaEventRecord");
+    if ((e = cudaEventSynchronize(c->decided))) return cuda_fail(e, "waiting for the step decision");
+    const zg::DevState ds = *c->h_state;
+    if (ds.error) return take_device_error(c, st);
+    if (!ds.res.skipped) {
+        // the previous call's parameter copies read the members' staging
+        if ((e = cudaEventSynchronize(c->out_done))) return cuda_fail(e, "waiting for the last copies");
+        std::vector<HostRow> rows;
+        for (size_t k = 0; k < n_members; ++k) {
+            zero_flat *mk = g->members[k];
+            const zh::AdamScalars sk{c->b1, c->b2, c->omb1, c->omb2, mk->lr, c->eps, mk->decay,
+                                     ds.res.clip_coef, ds.bc1, ds.bc2};
+            host_rows_of(mk, sk, args[k].ranks, args[k].n_ranks, args[k].master, args[k].m,
+                         args[k].v, args[k].flat_param_out, split[k], rows);
+        }
+        if ((e = host_update_rows(c, rows.data(), (int64_t)rows.size(),
+                                  c->param_dtype == ZERO_BF16)))
+            return cuda_fail(e, "copying parameters to the device");
+        if ((e = cudaSetDevice(c->device))) return cuda_fail(e, "cudaSetDevice");
+        if ((e = cudaEventRecord(c->out_done, c->up_stream))) return cuda_fail(e, "cudaEventRecord");
+        if ((e = cudaStreamWaitEvent(st, c->out_done, 0))) return cuda_fail(e, "cudaStreamWaitEvent");
+    }
+    // the GPU's share of the host arrays is written when the call returns too
+    if ((e = cudaEventSynchronize(c->gpu_part_done))) return cuda_fail(e, "waiting for the GPU share");
+    if (res) {
+        res->overflow = ds.res.overflow;
+        res->skipped = ds.res.skipped;
+        res->grad_norm = ds.res.grad_norm;
+        res->clip_coef = ds.res.clip_coef;
+        res->scale_used = ds.res.scale_used;
+    }
+    return ZERO_OK;
 }
 
 ZERO_API zero_status zero_group_accumulate(zero_group *g, const zero_group_member *args,

@@ -344,6 +344,25 @@ zero_status zero_group_step_accumulated(zero_group *g, const zero_group_member *
                                         double extra_norm_sq, void *stream,
                                         zero_step_result *res);
 
+/* The ZeRO-Offload form of zero_group_step, as zero_shard_step_offload does
+ * per member: one reduce launch per 64 rows with the group's decision, then
+ * every member's update split at split_k = gpu_share * shard_size_k (rounded
+ * down to 65536 elements, or the whole shard for gpu_share = 1): elements
+ * [0, split_k) of every row by one GPU AdamW launch per 64 rows over the
+ * host-resident state, the rest by `n_threads` host threads of the group
+ * (0: every CPU this process may run on) working through all members' rows
+ * at once, the gradient rows coming down in segments and the 16-bit
+ * parameters going back segment by segment, as for one handle.  Each member
+ * keeps its own lr and weight decay.  Bit-identical to zero_group_step for
+ * any split.  master, m, v: HOST fp32 arrays, as for zero_shard_step_offload;
+ * flat_param_out: device; the other fields as for zero_group_step.  The
+ * group owns the streams and threads; each member's handle owns its pinned
+ * buffers (6 bytes per stepped element).  Not capturable in a CUDA graph.
+ * Errors: as for zero_shard_step_offload, per member. */
+zero_status zero_group_step_offload(zero_group *g, const zero_group_member *args,
+                                    double extra_norm_sq, int32_t n_threads, double gpu_share,
+                                    void *stream, zero_step_result *res);
+
 /* The group's loss-scale state (synchronizes `stream`), its restore, and a
  * learning rate set on every member at once (as zero_flat_set_lr on each;
  * zero_flat_set_lr on one member changes that member's rate alone). */

@@ -378,3 +378,54 @@ def test_group_accumulation_plain_rows_and_many_members(ora):
                     seed=200 + k, steps=2) for k in range(69)]
     ws.append(_wl_micro("odd_s", [(4 * 2_501,)], 4, [0, 1, 2, 3], 2, seed=300, steps=2))
     assert run_group_accum_parity(ora, ws, micro=2, steps=2) == [0, 0]
+
+
+@pytest.mark.parametrize("gpu_share", [0.0, 0.5, 1.0])
+def test_group_offload_equals_group_step(gpu_share):
+    """zero_group_step_offload (state in pinned host memory, the update split
+    between the GPU and the host threads) against zero_group_step on twin
+    handles: identical state, parameters and results every step, a skipped
+    step included; members with their own rates and one misaligned (staged)."""
+    _need_gpu()
+    import fsdp_sharded_mixed_zero_gb300 as Z
+    from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
+    ws = [
+        _wl("two_segments", [(8 * ((1 << 24) + 12_345),)], 8, [0], layout="slice", seed=61,
+            steps=4, inf_at=(2, 3, 99)),
+        _wl("mid_slice", [(3 * (1 << 20) + 12_345,)], 8, [2], layout="slice", seed=64, steps=4),
+        _wl("odd_all", [(80_001,)], 8, list(range(8)), seed=62, steps=4,
+            hp=dict(lr=1e-4, weight_decay=0.0)),
+        _wl("small_two", [(5_000,), (77,)], 8, [0, 3], seed=63, steps=4),
+    ]
+    da = [DeviceWorkload(w) for w in ws]
+    db = [DeviceWorkload(w) for w in ws]
+    ga = Z.ZeroGroup([d.flat for d in da])
+    gb = Z.ZeroGroup([d.flat for d in db])
+    try:
+        host = [[[t.detach().cpu().pin_memory() for t in getattr(d, name)]
+                 for name in ("master", "m", "v")] for d in db]
+        for step in range(4):
+            for a, b in zip(da, db):
+                a.gen_grads(step, ga.scaler_state().scale)
+                b.grads.copy_(a.grads)
+            ra = ga.step([_args(w, d) for w, d in zip(ws, da)])
+            bargs = []
+            for w, d, (hm, hmm, hv) in zip(ws, db, host):
+                x = _args(w, d)
+                x.update(master=hm, m=hmm, v=hv)
+                bargs.append(x)
+            rb = gb.step_offload(bargs, gpu_share=gpu_share)
+            assert (ra.overflow, ra.skipped, ra.grad_norm, ra.clip_coef, ra.scale_used) == \
+                   (rb.overflow, rb.skipped, rb.grad_norm, rb.clip_coef, rb.scale_used)
+            assert rb.skipped == (step == 2)
+        torch.cuda.synchronize()
+        for a, b, (hm, hmm, hv) in zip(da, db, host):
+            for x, y in zip(a.master + a.m + a.v, hm + hmm + hv):
+                assert torch.equal(x.cpu().view(torch.int32), y.view(torch.int32))
+            assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+        assert ga.scaler_state().as_tuple() == gb.scaler_state().as_tuple()
+    finally:
+        ga.close()
+        gb.close()
+        for d in da + db:
+            d.close()
