@@ -12,7 +12,7 @@ from concurrent.futures import ThreadPoolExecutor
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
-SOURCES = ["zero_kernels.cu", "zero_plan.cu", "zero_api.cu", "zero_noalloc.cu"]
+SOURCES = ["zero_kernels.cu", "zero_plan.cu", "zero_api.cu", "zero_group.cu", "zero_noalloc.cu"]
 HOST_SOURCES = ["host_adam.cc"]
 HEADERS = [os.path.join(CSRC, "zero_kernels.cuh"), os.path.join(CSRC, "zero_plan.h"),
            os.path.join(CSRC, "host_adam.h"),
