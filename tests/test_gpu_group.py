@@ -429,3 +429,54 @@ def test_group_offload_equals_group_step(gpu_share):
         gb.close()
         for d in da + db:
             d.close()
+
+
+def test_group_argument_errors_name_the_member():
+    """Every group entry point validates every member before launching: a bad
+    argument of member 1 is refused with the member named, and nothing runs
+    (the group's loss-scale state is unchanged)."""
+    _need_gpu()
+    import fsdp_sharded_mixed_zero_gb300 as Z
+    from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
+    ws = [_wl("a", [(4_000,)], 4, [0, 1, 2, 3], seed=71), _wl("b", [(1_000,)], 4, [1], seed=72,
+                                                              layout="slice")]
+    ds = [DeviceWorkload(w) for w in ws]
+    for d in ds:
+        d.alloc_acc()
+        d.gen_grads(0, 65536.0)
+    group = Z.ZeroGroup([d.flat for d in ds])
+    try:
+        before = group.scaler_state().as_tuple()
+
+        q8s = [torch.zeros(d.padded, dtype=torch.int8, device="cuda") for d in ds]
+        scs = [torch.zeros(4 * -(-d.S // 256), device="cuda") for d in ds]
+
+        def refused(call, status, **bad):
+            args = [_args(w, d) for w, d in zip(ws, ds)]
+            for a, d, q, c in zip(args, ds, q8s, scs):
+                a.update(acc=d.acc, q8=q, q8_scales=c)
+            args[1].update(bad)
+            with pytest.raises(Z.ZeroError) as e:
+                call(args)
+            assert e.value.status == status, str(e.value)
+            assert "member 1" in str(e.value), str(e.value)
+
+        bad_rank = dict(ranks=[4])                                  # rank >= world size
+        refused(group.step, 1, **bad_rank)
+        refused(lambda a: group.step_q8(a), 1, q8=None)             # no int8 outputs
+        sc = torch.zeros(64, dtype=torch.uint8, device="cuda")
+        refused(lambda a: group.step_q8(a), 3, q8_scales=sc[1:])    # misaligned scales
+        refused(lambda a: group.accumulate(a, True), 1, **bad_rank)
+        refused(lambda a: group.step_accumulated(a), 3,
+                acc=[ds[1].acc[0].view(torch.uint8)[2:].view(torch.uint8)])  # misaligned acc
+        refused(lambda a: group.step_offload(a), 1, **bad_rank)
+        for bad in (-0.5, 2.0):
+            with pytest.raises(Z.ZeroError) as e:
+                group.step_offload([_args(w, d) for w, d in zip(ws, ds)], gpu_share=bad)
+            assert e.value.status == 1
+        torch.cuda.synchronize()
+        assert group.scaler_state().as_tuple() == before
+    finally:
+        group.close()
+        for d in ds:
+            d.close()
