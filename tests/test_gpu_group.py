@@ -10,7 +10,7 @@ import pytest
 
 torch = pytest.importorskip("torch")
 
-from synth.workloads import AVG, F16, Workload  # noqa: E402
+from synth.workloads import AVG, BF16, F16, F32, SUM, Workload  # noqa: E402
 
 import tests.oracle_runner as runner  # noqa: E402
 from tests.gpu_helpers import (NORM_RTOL, assert_params_close, assert_state, f32,  # noqa: E402
@@ -24,9 +24,10 @@ def _need_gpu():
         pytest.skip("no GPU")
 
 
-def _wl(name, shapes, N, ranks, layout="full", inf_at=None, seed=1, steps=3, hp=None):
+def _wl(name, shapes, N, ranks, layout="full", inf_at=None, seed=1, steps=3, hp=None,
+        dtype=F16, op=AVG, dynamic=True):
     return Workload(name=name, description=name, shapes=shapes, world_size=N, ranks=ranks,
-                    grad_dtype=F16, op=AVG, dynamic=True, steps=steps, sigma_g=1e-3,
+                    grad_dtype=dtype, op=op, dynamic=dynamic, steps=steps, sigma_g=1e-3,
                     sigma_n=1e-3, inf_at=inf_at, grads_layout=layout, seed=seed, hp=hp or {})
 
 
@@ -89,7 +90,8 @@ def run_group_parity(ora, ws, steps=3, lr_at=None, q8=False, q8_only=()):
                 for r in w.ranks:
                     x = np.empty(max(d.S, 1), np.float32)[:d.S]
                     runner.reduce_rank(g, w.grad_ld, r * w.grad_rank_mul, w.world_size, d.S,
-                                       r * d.S, d.full, True, scale, False, x)
+                                       r * d.S, d.full, w.op == AVG, scale,
+                                       w.grad_dtype == BF16, x)
                     gs.append(x)
             acc, of = runner.norm_exact(gs)
             norm = float(np.sqrt(ora.norm_sum(acc)))
@@ -103,6 +105,7 @@ def run_group_parity(ora, ws, steps=3, lr_at=None, q8=False, q8_only=()):
                 for j, r in enumerate(w.ranks):
                     if not skip:
                         ora.adamw_cast(hpk, st.step_t, coef, gs[k], master[j], m[j], v[j],
+                                       param_is_bf16=w.param_dtype == BF16,
                                        out=out[r * d.S:(r + 1) * d.S])
                     k += 1
                     assert_state(f32(d.master[j]), f32(d.m[j]), f32(d.v[j]), master[j], m[j],
@@ -110,7 +113,7 @@ def run_group_parity(ora, ws, steps=3, lr_at=None, q8=False, q8_only=()):
                 if q8 and ws.index(w) in q8_only:
                     assert bool((d.out.view(torch.int16) == 0x5A5A).all())
                 else:
-                    assert_params_close(u16(d.out), out, False,
+                    assert_params_close(u16(d.out), out, w.param_dtype == BF16,
                                         "%s params (step %d)" % (w.name, step))
             if q8:
                 for i, (w, d, (_, _, _, out)) in enumerate(zip(ws, ds, state)):
@@ -149,6 +152,23 @@ def test_group_step_with_int8_payload(ora):
             hp=dict(lr=1e-4, weight_decay=0.0)),
     ]
     assert run_group_parity(ora, ws, q8=True, q8_only=(3,)) == [0, 1, 0]
+
+
+@pytest.mark.parametrize("dtype,op,dynamic", [(BF16, SUM, False), (F32, AVG, True)],
+                         ids=["bf16_sum_static", "fp32_contributions"])
+def test_group_other_dtypes(ora, dtype, op, dynamic):
+    """Groups whose members take bf16 contributions summed at a static scale
+    (bf16 parameters), or fp32 contributions (fp16 parameters): one staged
+    member (rows off 64 bytes), one slice, one all-shards; own rates in one."""
+    _need_gpu()
+    kw = dict(dtype=dtype, op=op, dynamic=dynamic)
+    ws = [
+        _wl("all_shards", [(512, 768), (768,)], 8, list(range(8)), seed=81, **kw),
+        _wl("odd_rows", [(80_001,)], 8, list(range(8)), seed=82, **kw),
+        _wl("slice_rank4", [(768, 3072)], 8, [4], layout="slice", seed=83,
+            hp=dict(lr=1e-4, weight_decay=0.0), **kw),
+    ]
+    assert run_group_parity(ora, ws) == [0, 0, 0]
 
 
 def test_group_members_keep_their_own_rates(ora):
@@ -317,6 +337,7 @@ def run_group_accum_parity(ora, ws, micro, steps=3):
                 for j, r in enumerate(w.ranks):
                     if not skip:
                         ora.adamw_cast(hpk, st.step_t, coef, gs[k], master[j], m[j], v[j],
+                                       param_is_bf16=w.param_dtype == BF16,
                                        out=out[r * d.S:(r + 1) * d.S])
                     k += 1
                     assert_state(f32(d.master[j]), f32(d.m[j]), f32(d.v[j]), master[j], m[j],
