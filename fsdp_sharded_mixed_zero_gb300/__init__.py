@@ -467,6 +467,15 @@ class ZeroGroup:
                "zero_group_loss_scaler_state")
         return st
 
+    def set_scaler_state(self, state, stream=None):
+        """Restore the group's loss-scale state (scale, counter, step)."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        _check(_lib.zero_group_set_loss_scaler_state(self.handle, C.byref(state),
+                                                     C.c_void_p(stream.cuda_stream)),
+               "zero_group_set_loss_scaler_state")
+
     def set_lr(self, lr):
         _check(_lib.zero_group_set_lr(self.handle, float(lr)), "zero_group_set_lr")
 

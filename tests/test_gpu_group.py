@@ -501,3 +501,52 @@ def test_group_argument_errors_name_the_member():
         group.close()
         for d in ds:
             d.close()
+
+
+def test_group_resume_from_saved_state():
+    """Checkpoint a group mid-run (every member's master/m/v/flat buffer and
+    the group's loss-scale state), build a new group over the same handles,
+    restore, continue: the same bits as the uninterrupted group (the scale
+    grows inside the window on the way)."""
+    _need_gpu()
+    import fsdp_sharded_mixed_zero_gb300 as Z
+    from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
+    hp = dict(initial_scale_power=5, window=2)
+    ws = [_wl("r0", [(30_000,)], 4, [0, 1, 2, 3], seed=91, steps=6, hp=hp),
+          _wl("r1", [(9_001,), (17,)], 4, [2], layout="slice", seed=92, steps=6,
+              hp=dict(hp, weight_decay=0.0))]
+    ds = [DeviceWorkload(w) for w in ws]
+
+    def tensors():
+        return [t for d in ds for t in d.master + d.m + d.v + [d.out]]
+
+    group = Z.ZeroGroup([d.flat for d in ds])
+    try:
+        for step in range(3):
+            for d in ds:
+                d.gen_grads(step, group.scaler_state().scale)
+            group.step([_args(w, d) for w, d in zip(ws, ds)])
+        saved = [t.clone() for t in tensors()]
+        saved_sc = group.scaler_state()
+        runs = []
+        for _ in range(2):
+            group.close()
+            group = Z.ZeroGroup([d.flat for d in ds])          # a new group object
+            for t, x in zip(tensors(), saved):
+                t.copy_(x)
+            group.set_scaler_state(saved_sc)
+            norms = []
+            for step in range(3, 6):
+                for d in ds:
+                    d.gen_grads(step, group.scaler_state().scale)
+                norms.append(group.step([_args(w, d) for w, d in zip(ws, ds)]).grad_norm)
+            runs.append((norms, group.scaler_state().as_tuple(), [t.clone() for t in tensors()]))
+        assert runs[0][0] == runs[1][0] and runs[0][1] == runs[1][1]
+        assert runs[0][1][0] != saved_sc.scale                    # the scale moved
+        for a, b in zip(runs[0][2], runs[1][2]):
+            assert torch.equal(a.view(torch.int16) if a.element_size() == 2 else a,
+                               b.view(torch.int16) if b.element_size() == 2 else b)
+    finally:
+        group.close()
+        for d in ds:
+            d.close()
