@@ -238,6 +238,9 @@ __device__ void finalize_block(const FinalizeArgs &a) {
     if (threadIdx.x != 0) return;
     double total = 0.0;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) total += warp_ss[w];
+    // a kernel that gave up a bounded wait since the error word was last
+    // read (e.g. an accumulation launch, which has no partials) voids the step
+    if (__ldcg(&st->error)) of = 1;
     if (a.sum_out) {                       // first half of a split step
         *a.sum_out = total;
         *a.of_out = of;

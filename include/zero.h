@@ -56,7 +56,9 @@ typedef enum {
     ZERO_ERR_ALIGNMENT = 3,         /* pointer not aligned to its element size */
     ZERO_ERR_CUDA = 4,              /* a CUDA runtime call failed (see zero_last_error) */
     ZERO_ERR_OVERFLOW_SIZE = 5,     /* a size or offset does not fit in int64 */
-    ZERO_ERR_TIMEOUT = 6,           /* a bounded device wait gave up; the step was skipped */
+    ZERO_ERR_TIMEOUT = 6,           /* a bounded device wait gave up (in this step, or in an
+                                       accumulation since the last step): the step was
+                                       skipped; reading it clears the condition */
     ZERO_ERR_NO_MEMORY = 7          /* host or device allocation failed */
 } zero_status;
 
