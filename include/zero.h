@@ -58,7 +58,9 @@ typedef enum {
     ZERO_ERR_OVERFLOW_SIZE = 5,     /* a size or offset does not fit in int64 */
     ZERO_ERR_TIMEOUT = 6,           /* a bounded device wait gave up (in this step, or in an
                                        accumulation since the last step): the step was
-                                       skipped; reading it clears the condition */
+                                       skipped.  Fail-stop: every later step is skipped too
+                                       until a call that reads a step result reports this
+                                       status, which clears the condition */
     ZERO_ERR_NO_MEMORY = 7          /* host or device allocation failed */
 } zero_status;
 
