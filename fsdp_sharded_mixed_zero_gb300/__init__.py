@@ -20,7 +20,10 @@ __all__ = [
     "zero_shard_step_noalloc", "zero_grad_accumulate", "zero_shard_step_accumulated",
     "zero_shard_step_q8", "ZERO_Q8_BLOCK", "zero_flat_set_lr", "zero_shard_step_offload",
     "zero_offload_adamw_host", "zero_debug_set_stage_tx_pad", "zero_shard_reduce",
-    "zero_shard_apply", "GroupMember", "ZeroGroup",
+    "zero_shard_apply", "GroupMember", "ZeroGroup", "zero_group_init", "zero_group_step",
+    "zero_group_step_q8", "zero_group_step_accumulated", "zero_group_step_offload",
+    "zero_group_accumulate", "zero_group_loss_scaler_state", "zero_group_set_loss_scaler_state",
+    "zero_group_set_lr", "zero_group_free",
     "zero_status_string", "zero_last_error", "ZeroFlat",
     "LIB_PATH",
 ]
@@ -340,21 +343,81 @@ def zero_shard_apply(h, ranks, master_ptrs, m_ptrs, v_ptrs, out_ptr, norm_sq_ptr
     return res
 
 
+def zero_group_init(handles):
+    """A group over the given handles (raw zero_flat pointers)."""
+    arr = (C.c_void_p * len(handles))(*handles)
+    g = C.c_void_p()
+    _check(_lib.zero_group_init(arr, len(handles), C.byref(g)), "zero_group_init")
+    return g.value
+
+
+def _group_call(name, g, members, *args, want_result=True):
+    res = StepResult() if want_result else None
+    _check(getattr(_lib, name)(g, members, *args, C.byref(res) if res is not None else None), name)
+    return res
+
+
+def zero_group_step(g, members, extra_norm_sq=0.0, stream=0, want_result=True):
+    """members: a GroupMember array, one entry per member of the group."""
+    return _group_call("zero_group_step", g, members, float(extra_norm_sq), C.c_void_p(stream),
+                       want_result=want_result)
+
+
+def zero_group_step_q8(g, members, extra_norm_sq=0.0, stream=0, want_result=True):
+    return _group_call("zero_group_step_q8", g, members, float(extra_norm_sq),
+                       C.c_void_p(stream), want_result=want_result)
+
+
+def zero_group_step_accumulated(g, members, extra_norm_sq=0.0, stream=0, want_result=True):
+    return _group_call("zero_group_step_accumulated", g, members, float(extra_norm_sq),
+                       C.c_void_p(stream), want_result=want_result)
+
+
+def zero_group_step_offload(g, members, extra_norm_sq=0.0, n_threads=0, gpu_share=0.0,
+                            stream=0):
+    return _group_call("zero_group_step_offload", g, members, float(extra_norm_sq),
+                       int(n_threads), float(gpu_share), C.c_void_p(stream))
+
+
+def zero_group_accumulate(g, members, first_micro_step, stream=0):
+    _check(_lib.zero_group_accumulate(g, members, 1 if first_micro_step else 0,
+                                      C.c_void_p(stream)), "zero_group_accumulate")
+
+
+def zero_group_loss_scaler_state(g, stream=0):
+    st = ScalerState()
+    _check(_lib.zero_group_loss_scaler_state(g, C.byref(st), C.c_void_p(stream)),
+           "zero_group_loss_scaler_state")
+    return st
+
+
+def zero_group_set_loss_scaler_state(g, state, stream=0):
+    _check(_lib.zero_group_set_loss_scaler_state(g, C.byref(state), C.c_void_p(stream)),
+           "zero_group_set_loss_scaler_state")
+
+
+def zero_group_set_lr(g, lr):
+    _check(_lib.zero_group_set_lr(g, float(lr)), "zero_group_set_lr")
+
+
+def zero_group_free(g):
+    _check(_lib.zero_group_free(g), "zero_group_free")
+
+
 class ZeroGroup:
     """FlatParameters of one rank stepped together with one global decision.
 
-    members: ZeroFlat objects sharing world size, dtypes, op and hparams.
+    members: ZeroFlat objects sharing world size, dtypes, op and every
+    hyper-parameter but lr and weight_decay (each member keeps its own).
     step(args): args[k] = dict(ranks, grads, master, m, v, out[, grad_rank_offset_mul])
     for member k, torch CUDA tensors as for ZeroFlat.step; accumulate() and
     step_accumulated() take acc (fp32 rows, one per stepped rank) as for
-    ZeroFlat.accumulate and ZeroFlat.step_accumulated."""
+    ZeroFlat.accumulate and ZeroFlat.step_accumulated; step_q8() takes q8 and
+    q8_scales as ZeroFlat.step_q8; step_offload() takes host master/m/v."""
 
     def __init__(self, members):
         self.members = list(members)
-        arr = (C.c_void_p * len(self.members))(*[f.handle for f in self.members])
-        h = C.c_void_p()
-        _check(_lib.zero_group_init(arr, len(self.members), C.byref(h)), "zero_group_init")
-        self.handle = h.value
+        self.handle = zero_group_init([f.handle for f in self.members])
 
     def _members(self, args, keep):
         """The GroupMember array of args (ctypes arrays appended to keep)."""
@@ -386,102 +449,59 @@ class ZeroGroup:
             ms[k] = x
         return ms
 
-    def step(self, args, extra_norm_sq=0.0, stream=None, want_result=True):
+    @staticmethod
+    def _stream(stream):
         import torch
-        if stream is None:
-            stream = torch.cuda.current_stream()
+        return (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+
+    def step(self, args, extra_norm_sq=0.0, stream=None, want_result=True):
         keep = []                                   # ctypes arrays alive for the call
-        ms = self._members(args, keep)
-        res = StepResult() if want_result else None
-        _check(_lib.zero_group_step(self.handle, ms, float(extra_norm_sq),
-                                    C.c_void_p(stream.cuda_stream),
-                                    C.byref(res) if res is not None else None), "zero_group_step")
-        return res
+        return zero_group_step(self.handle, self._members(args, keep), extra_norm_sq,
+                               self._stream(stream), want_result)
 
     def step_q8(self, args, extra_norm_sq=0.0, stream=None, want_result=True):
-        """The group step that also writes every member's int8 payload: args[k]
-        as for step() plus q8 and q8_scales (as for ZeroFlat.step_q8; out may
+        """The group step that also writes every member's int8 payload (out may
         be None)."""
-        import torch
-        if stream is None:
-            stream = torch.cuda.current_stream()
         keep = []
-        ms = self._members(args, keep)
-        res = StepResult() if want_result else None
-        _check(_lib.zero_group_step_q8(self.handle, ms, float(extra_norm_sq),
-                                       C.c_void_p(stream.cuda_stream),
-                                       C.byref(res) if res is not None else None),
-               "zero_group_step_q8")
-        return res
+        return zero_group_step_q8(self.handle, self._members(args, keep), extra_norm_sq,
+                                  self._stream(stream), want_result)
 
     def step_offload(self, args, extra_norm_sq=0.0, n_threads=0, gpu_share=0.0, stream=None):
-        """The ZeRO-Offload group step: args[k] as for step() with master, m, v
-        host (CPU, pinned for gpu_share > 0) fp32 tensors.  Returns the step
-        result; the host arrays are updated when it returns."""
-        import torch
-        if stream is None:
-            stream = torch.cuda.current_stream()
+        """The ZeRO-Offload group step: master, m, v host (CPU, pinned for
+        gpu_share > 0) fp32 tensors, updated when it returns."""
         keep = []
-        ms = self._members(args, keep)
-        res = StepResult()
-        _check(_lib.zero_group_step_offload(self.handle, ms, float(extra_norm_sq), int(n_threads),
-                                            float(gpu_share), C.c_void_p(stream.cuda_stream),
-                                            C.byref(res)), "zero_group_step_offload")
-        return res
+        return zero_group_step_offload(self.handle, self._members(args, keep), extra_norm_sq,
+                                       n_threads, gpu_share, self._stream(stream))
 
     def accumulate(self, args, first_micro_step, stream=None):
         """One micro-step: args[k] = dict(ranks, grads, acc[, grad_rank_offset_mul]);
         each member's reduced micro-step gradient (loss scale not divided out)
         written (first) or added into its fp32 accumulator rows acc[j], one per
         stepped rank.  One launch per 64 rows of all members."""
-        import torch
-        if stream is None:
-            stream = torch.cuda.current_stream()
         keep = []
-        ms = self._members(args, keep)
-        _check(_lib.zero_group_accumulate(self.handle, ms, 1 if first_micro_step else 0,
-                                          C.c_void_p(stream.cuda_stream)),
-               "zero_group_accumulate")
+        zero_group_accumulate(self.handle, self._members(args, keep), first_micro_step,
+                              self._stream(stream))
 
     def step_accumulated(self, args, extra_norm_sq=0.0, stream=None, want_result=True):
         """The group step from accumulators: args[k] = dict(ranks, acc, master, m, v, out)."""
-        import torch
-        if stream is None:
-            stream = torch.cuda.current_stream()
         keep = []
-        ms = self._members(args, keep)
-        res = StepResult() if want_result else None
-        _check(_lib.zero_group_step_accumulated(self.handle, ms, float(extra_norm_sq),
-                                                C.c_void_p(stream.cuda_stream),
-                                                C.byref(res) if res is not None else None),
-               "zero_group_step_accumulated")
-        return res
+        return zero_group_step_accumulated(self.handle, self._members(args, keep),
+                                           extra_norm_sq, self._stream(stream), want_result)
 
     def scaler_state(self, stream=None):
-        import torch
-        if stream is None:
-            stream = torch.cuda.current_stream()
-        st = ScalerState()
-        _check(_lib.zero_group_loss_scaler_state(self.handle, C.byref(st),
-                                                 C.c_void_p(stream.cuda_stream)),
-               "zero_group_loss_scaler_state")
-        return st
+        return zero_group_loss_scaler_state(self.handle, self._stream(stream))
 
     def set_scaler_state(self, state, stream=None):
         """Restore the group's loss-scale state (scale, counter, step)."""
-        import torch
-        if stream is None:
-            stream = torch.cuda.current_stream()
-        _check(_lib.zero_group_set_loss_scaler_state(self.handle, C.byref(state),
-                                                     C.c_void_p(stream.cuda_stream)),
-               "zero_group_set_loss_scaler_state")
+        zero_group_set_loss_scaler_state(self.handle, state, self._stream(stream))
 
     def set_lr(self, lr):
-        _check(_lib.zero_group_set_lr(self.handle, float(lr)), "zero_group_set_lr")
+        """Set lr on every member (each keeps its weight decay)."""
+        zero_group_set_lr(self.handle, lr)
 
     def close(self):
         if getattr(self, "handle", None):
-            _lib.zero_group_free(self.handle)
+            zero_group_free(self.handle)
             self.handle = None
 
     def __del__(self):
