@@ -287,8 +287,10 @@ zero_status zero_shard_apply(zero_flat *h, const int32_t *ranks, int32_t n_ranks
  * by group steps.
  * A member's handle supplies its layout and its reduced-gradient scratch, so
  * a handle should be stepped either alone or in groups, not both in one
- * step.  Errors: INVALID_ARG (no members, NULL, members that differ, a
- * member listed twice, members on another device), NO_MEMORY, CUDA. */
+ * step.  The group does not own its members: they must outlive every group
+ * call, and zero_group_free leaves them open.  Errors: INVALID_ARG (no
+ * members, NULL, members that differ, a member listed twice, members on
+ * another device), NO_MEMORY, CUDA. */
 typedef struct zero_group zero_group;
 zero_status zero_group_init(zero_flat *const *members, int32_t n_members, zero_group **out);
 
