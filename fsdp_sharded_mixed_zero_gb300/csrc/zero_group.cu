@@ -406,6 +406,10 @@ ZERO_API zero_status zero_group_set_lr(zero_group *g, double lr) {
 
 ZERO_API zero_status zero_group_free(zero_group *g) {
     if (!g) return ZERO_OK;
+    {
+        DeviceGuard guard(g->core->device);
+        cudaDeviceSynchronize();          // no group launch may still use the core's buffers
+    }
     release(g->core);
     delete g;
     return ZERO_OK;
