@@ -48,7 +48,7 @@ FALLBACK_HBM_GBS = 6800.0
 RESULT_D2H_BYTES = 64            # the device state block read back with the result
 
 
-def parse_args():
+def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=100)
@@ -81,7 +81,10 @@ def parse_args():
                    help="target length of the oracle's timed sample")
     p.add_argument("--ref-seconds", type=float, default=120.0,
                    help="target length of the whole --impl reference run")
-    return p.parse_args()
+    args = p.parse_args(argv)
+    if bool(args.q8) + (args.micro_steps > 1) + bool(args.offload) > 1:
+        p.error("--q8, --micro-steps K > 1 and --offload exclude one another")
+    return args
 
 
 # ---------------------------------------------------------------- plumbing
@@ -336,7 +339,6 @@ def run_ours(args, w):
         dw.alloc_acc()
     q8 = q8_scales = None
     if args.q8:
-        assert K == 1, "--q8 applies to the plain step"
         q8 = torch.empty(dw.padded, dtype=torch.int8, device=dev)
         q8_scales = torch.empty(w.world_size * -(-dw.S // 256), device=dev)
 
@@ -691,8 +693,6 @@ def run_group(args):
     micro = max(1, args.micro_steps)
     q8 = bool(args.q8)
     off = bool(args.offload)
-    if (q8 + (micro > 1) + off) > 1:
-        raise SystemExit("--group takes one of --q8, --micro-steps, --offload")
     if off:                                 # fp32 state in pinned host memory
         hargs = []
         for a in margs:

@@ -77,3 +77,19 @@ def test_torchrun_reference_arm_two_ranks():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+@pytest.mark.parametrize("argv", [["--q8", "--micro-steps", "2"], ["--offload", "--q8"],
+                                  ["--group", "4", "--offload", "--micro-steps", "3"]])
+def test_bench_rejects_step_forms_that_exclude_one_another(argv):
+    """The step forms are refused at argument parsing, before any device work."""
+    import bench
+    with pytest.raises(SystemExit) as e:
+        bench.parse_args(argv)
+    assert e.value.code == 2
+
+
+def test_bench_accepts_each_step_form_alone():
+    import bench
+    for argv in ([], ["--q8"], ["--micro-steps", "4"], ["--offload"], ["--group", "8", "--q8"]):
+        bench.parse_args(argv)
