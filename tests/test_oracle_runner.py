@@ -40,3 +40,51 @@ def test_threaded_matches_shard_step(ora, monkeypatch, N, n, bf16, avg, ranks):
         assert sa.as_tuple() == sb.as_tuple()
         for x, y in zip(ma + m_a + v_a + [oa], mb + m_b + v_b + [ob]):
             assert np.array_equal(x, y)
+
+
+def test_group_composition_equals_the_concatenated_step(ora):
+    """The composition the group parity tests use -- each member's reduced
+    gradient, one exact norm over all members, one decision, AdamW per
+    member -- equals the oracle's own step over the members' concatenation
+    (one FlatParameter, N=1: no padding, the same elements in the same
+    places), bit for bit, overflow step included."""
+    rng = np.random.default_rng(7)
+    sizes = [1_003, 40_000, 7]
+    total = sum(sizes)
+    hp = ora.hparams(lr=1e-3, max_grad_norm=1.0, window=2, initial_scale_power=4)
+    st_cat, st_grp = ora.scaler_init(hp), ora.scaler_init(hp)
+    theta = (rng.standard_normal(total) * 0.02).astype(np.float32)
+    cat = [theta.copy(), np.zeros(total, np.float32), np.zeros(total, np.float32)]
+    out_cat = np.zeros(total, np.uint16)
+    offs = np.cumsum([0] + sizes)
+    grp = [[theta[a:b].copy(), np.zeros(b - a, np.float32), np.zeros(b - a, np.float32)]
+           for a, b in zip(offs[:-1], offs[1:])]
+    out_grp = [np.zeros(n, np.uint16) for n in sizes]
+    for step in range(4):
+        g = (rng.standard_normal((1, total)) * 8).astype(np.float16).view(np.uint16)
+        if step == 2:
+            g[0, offs[1] + 5] = 0x7C00                    # +inf in member 1
+        r = ora.shard_step(hp, st_cat, 1, total, total, [0], g, total, 0, [cat[0]], [cat[1]],
+                           [cat[2]], out_cat)
+        scale = st_grp.scale
+        gs = []
+        for k, (a, b) in enumerate(zip(offs[:-1], offs[1:])):
+            x = np.empty(b - a, np.float32)
+            member = np.ascontiguousarray(g[:, a:b])
+            runner.reduce_rank(member, b - a, 0, 1, b - a, 0, b - a, True, scale, False, x)
+            gs.append(x)
+        acc, of = runner.norm_exact(gs)
+        norm = float(np.sqrt(ora.norm_sum(acc)))
+        coef, skip = ora.scaler_decide(hp, st_grp, of, norm)
+        if not skip:
+            for k, x in enumerate(gs):
+                ora.adamw_cast(hp, st_grp.step_t, coef, x, grp[k][0], grp[k][1], grp[k][2],
+                               out=out_grp[k])
+        assert (r.overflow, r.skipped, r.clip_coef) == (of, skip, coef)
+        if not of:
+            assert r.grad_norm == norm
+        assert st_cat.as_tuple() == st_grp.as_tuple()
+        for i in range(3):
+            assert np.array_equal(cat[i], np.concatenate([m[i] for m in grp]))
+        assert np.array_equal(out_cat, np.concatenate(out_grp))
+    assert st_cat.overflow_count == 1
