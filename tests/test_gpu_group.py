@@ -550,3 +550,51 @@ def test_group_resume_from_saved_state():
         group.close()
         for d in ds:
             d.close()
+
+
+def test_group_step_captured_in_a_cuda_graph_equals_eager():
+    """A group step (staged and plain rows, per-member rates) captured once in
+    a CUDA graph and replayed: the same bits and loss-scale state as the same
+    group stepped eagerly on twin handles."""
+    _need_gpu()
+    import fsdp_sharded_mixed_zero_gb300 as Z
+    from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
+    ws = [_wl("g0", [(512, 1024), (1024,)], 4, [0, 1, 2, 3], seed=101),
+          _wl("g1", [(40_001,)], 4, [0, 1, 2, 3], seed=102, hp=dict(weight_decay=0.0)),
+          _wl("g2", [(3_000,)], 4, [3], layout="slice", seed=103)]
+    da = [DeviceWorkload(w) for w in ws]
+    db = [DeviceWorkload(w) for w in ws]
+    ga = Z.ZeroGroup([d.flat for d in da])
+    gb = Z.ZeroGroup([d.flat for d in db])
+    try:
+        for a, b in zip(da, db):
+            a.gen_grads(0, ga.scaler_state().scale)
+            b.grads.copy_(a.grads)
+        args_a = [_args(w, d) for w, d in zip(ws, da)]
+        args_b = [_args(w, d) for w, d in zip(ws, db)]
+        # first step eagerly: the members' scratch and the group's partials are
+        # allocated here, not during capture
+        ga.step(args_a, want_result=False)
+        gb.step(args_b, want_result=False)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            gb.step(args_b, stream=s, want_result=False)
+        torch.cuda.current_stream().wait_stream(s)
+        for _ in range(3):
+            ga.step(args_a, want_result=False)
+            graph.replay()
+        torch.cuda.synchronize()
+        assert ga.scaler_state().as_tuple() == gb.scaler_state().as_tuple()
+        assert gb.scaler_state().step_t == 4
+        for a, b in zip(da, db):
+            for x, y in zip(a.master + a.m + a.v + [a.out], b.master + b.m + b.v + [b.out]):
+                if x.element_size() == 2:
+                    x, y = x.view(torch.int16), y.view(torch.int16)
+                assert torch.equal(x, y)
+    finally:
+        ga.close()
+        gb.close()
+        for d in da + db:
+            d.close()
