@@ -144,14 +144,23 @@ zero_status zero_flat_init(const zero_param_info *infos, int32_t n_infos, int32_
                            zero_dtype grad_dtype, zero_dtype param_dtype, zero_reduce_op op,
                            const zero_hparams *hp, zero_flat **out);
 
-/* full_numel, shard_size and padded_numel of the handle (any may be NULL). */
+/* full_numel, shard_size and padded_numel of the handle (any may be NULL):
+ * the layout zero_flat_init computed ("PyTorch FSDP ... 深度解析" §3.3,
+ * shard_size from the flat parameter's numel and world_size, padded so every
+ * rank's chunk is equal; "DeepSpeed 与 FSDP" §FSDP 的分片粒度与 FlatParameter,
+ * one flat buffer cut into world_size chunks).  Host only.
+ * Errors: INVALID_ARG (NULL handle). */
 zero_status zero_flat_layout(const zero_flat *h, int64_t *full_numel, int64_t *shard_size,
                              int64_t *padded_numel);
 
 /* One optimizer step on the stepped ranks ranks[0..n_ranks) (distinct, each
  * in [0, world_size); one rank for a real rank's step, or all N to emulate
  * the whole group on one GPU -- the norm and the overflow flag are then
- * global over every stepped shard).
+ * global over every stepped shard).  The step of "DeepSpeed 与 FSDP" §ZeRO-1
+ * steps 1-3 (each rank updates its own slice of the optimizer state and
+ * writes its slice of the parameters for the all-gather) with the reduce of
+ * "PyTorch FSDP ... 深度解析" §3.3 and the mixed-precision, loss-scale and
+ * clipping settings of the ZeRO reading §5.1 and §5.3.
  *
  * grads: device, grad_dtype (aligned to its element size); contributor c's
  * gradient for flat element
@@ -224,9 +233,11 @@ zero_status zero_grad_accumulate(zero_flat *h, const int32_t *ranks, int32_t n_r
                                  const void *grads, int64_t grad_ld, int64_t grad_rank_offset_mul,
                                  float *const *acc, int32_t first_micro_step, void *stream);
 
-/* The optimizer step on accumulated shards: g = acc[j] / scale (padding
- * elements count as zero), then the overflow check, global norm, loss-scale
- * decision, AdamW and cast exactly as in zero_shard_step.  acc is only read.
+/* The optimizer step on accumulated shards ("DeepSpeed 与 FSDP" §实践要点,
+ * gradient accumulation: one optimizer step after the micro-steps' gradients
+ * have been summed): g = acc[j] / scale (padding elements count as zero),
+ * then the overflow check, global norm, loss-scale decision, AdamW and cast
+ * exactly as in zero_shard_step.  acc is only read.
  * Other arguments and errors as for zero_shard_step. */
 zero_status zero_shard_step_accumulated(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
                                         const float *const *acc, float *const *master,
@@ -318,21 +329,24 @@ typedef struct {
 /* One step of every member (args[k] for the group's member k): the reduce
  * of every member's stepped shards with the group's loss scale, one global
  * norm over all of them plus extra_norm_sq, one overflow decision and loss-
- * scale update, then AdamW and the cast into every member's slot -- the same
+ * scale update (ZeRO reading §5.3: one decision for everything the rank
+ * steps), then AdamW and the cast into every member's slot -- the same
  * per-element arithmetic as zero_shard_step.  Asynchronous on `stream` when
  * res is NULL.  Errors: as for zero_shard_step, per member. */
 zero_status zero_group_step(zero_group *g, const zero_group_member *args, double extra_norm_sq,
                             void *stream, zero_step_result *res);
 
 /* zero_group_step that also writes every member's int8 all-gather payload
- * and its block scales, as zero_shard_step_q8 does per member (the same
+ * ("DeepSpeed 与 FSDP" §ZeRO++; ZeRO reading §4.2) and its block scales, as
+ * zero_shard_step_q8 does per member (the same
  * quantization of the same 16-bit values; flat_param_out may be NULL).
  * One reduce launch and one int8-payload AdamW launch per 64 rows.  Errors:
  * as for zero_shard_step_q8, per member. */
 zero_status zero_group_step_q8(zero_group *g, const zero_group_member *args, double extra_norm_sq,
                                void *stream, zero_step_result *res);
 
-/* Micro-step accumulation for every member in one launch per 64 rows, as
+/* Micro-step accumulation for every member in one launch per 64 rows
+ * ("DeepSpeed 与 FSDP" §实践要点, gradient accumulation), as
  * zero_grad_accumulate does per member (acc = r on the first micro-step,
  * acc += r after; the loss scale not divided out).  Reads ranks, grads,
  * grad_ld, grad_rank_offset_mul and acc of each member.  Asynchronous.
@@ -340,8 +354,10 @@ zero_status zero_group_step_q8(zero_group *g, const zero_group_member *args, dou
 zero_status zero_group_accumulate(zero_group *g, const zero_group_member *args,
                                   int32_t first_micro_step, void *stream);
 
-/* The step from every member's accumulators: g = acc / scale (padding zero),
- * one global norm, overflow decision and loss-scale update over all members,
+/* The step from every member's accumulators ("DeepSpeed 与 FSDP" §实践要点,
+ * gradient accumulation): g = acc / scale (padding zero),
+ * one global norm, overflow decision and loss-scale update over all members
+ * (ZeRO reading §5.3),
  * then AdamW and the cast -- as zero_shard_step_accumulated does per member,
  * in one norm launch and one AdamW launch per 64 rows.  Reads ranks, acc,
  * master, m, v and flat_param_out of each member.  res: as for
@@ -350,7 +366,8 @@ zero_status zero_group_step_accumulated(zero_group *g, const zero_group_member *
                                         double extra_norm_sq, void *stream,
                                         zero_step_result *res);
 
-/* The ZeRO-Offload form of zero_group_step, as zero_shard_step_offload does
+/* The ZeRO-Offload form of zero_group_step ("DeepSpeed 与 FSDP"
+ * §ZeRO-Offload; ZeRO reading §4.1), as zero_shard_step_offload does
  * per member: one reduce launch per 64 rows with the group's decision, then
  * every member's update split at split_k = gpu_share * shard_size_k (rounded
  * down to 65536 elements, or the whole shard for gpu_share = 1): elements
@@ -369,9 +386,12 @@ zero_status zero_group_step_offload(zero_group *g, const zero_group_member *args
                                     double extra_norm_sq, int32_t n_threads, double gpu_share,
                                     void *stream, zero_step_result *res);
 
-/* The group's loss-scale state (synchronizes `stream`), its restore, and a
- * learning rate set on every member at once (as zero_flat_set_lr on each;
- * zero_flat_set_lr on one member changes that member's rate alone). */
+/* The group's loss-scale state (synchronizes `stream`) and its restore, as
+ * zero_loss_scaler_state / zero_set_loss_scaler_state for a handle (the
+ * dynamic loss scale of the ZeRO reading §5.1 and §5.3), and a learning rate
+ * set on every member at once (as zero_flat_set_lr on each; zero_flat_set_lr
+ * on one member changes that member's rate alone; the `lr` of §5.1's
+ * optimizer settings). */
 zero_status zero_group_loss_scaler_state(zero_group *g, zero_scaler_state *out, void *stream);
 zero_status zero_group_set_loss_scaler_state(zero_group *g, const zero_scaler_state *in,
                                              void *stream);
@@ -443,12 +463,21 @@ zero_status zero_offload_adamw_host(const zero_hparams *hp, int64_t step_t, floa
  * with.  Errors: INVALID_ARG (NULL handle, lr negative or not finite). */
 zero_status zero_flat_set_lr(zero_flat *h, double lr);
 
-/* Copy the loss-scale state to the host; synchronizes `stream`. */
+/* Copy the loss-scale state to the host; synchronizes `stream`.  The state
+ * is that of the dynamic loss scale of the ZeRO reading §5.1 (fp16
+ * "loss_scale": 0 = dynamic, "initial_scale_power", "loss_scale_window",
+ * "min_loss_scale") and §5.3 (an overflow skips the step and shrinks the
+ * scale; clean steps grow it back): the scale the next step's gradients
+ * carry, the clean-step counter, Adam's t (applied steps) and the number of
+ * skipped steps.  out: host memory.  Errors: INVALID_ARG (NULL), CUDA. */
 zero_status zero_loss_scaler_state(zero_flat *h, zero_scaler_state *out, void *stream);
 
-/* Overwrite the loss-scale state (resume from a checkpoint): stream-ordered
- * before later steps on `stream`.  scale > 0, good_steps >= 0, step_t >= 0,
- * overflow_count >= 0, else INVALID_ARG. */
+/* Overwrite the loss-scale state (resume from a checkpoint): the state of
+ * the dynamic loss scale of the ZeRO reading §5.1 and §5.3, as
+ * zero_loss_scaler_state returns it.  Synchronizes `stream` before and after
+ * the copy, so later steps on any stream see it; `in` is host memory.
+ * scale > 0, good_steps >= 0, step_t >= 0, overflow_count >= 0, else
+ * INVALID_ARG; CUDA if the copy cannot be queued. */
 zero_status zero_set_loss_scaler_state(zero_flat *h, const zero_scaler_state *in, void *stream);
 
 /* Model-state bytes per GPU for Psi parameters and N ranks in mixed
