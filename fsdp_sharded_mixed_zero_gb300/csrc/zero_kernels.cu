@@ -212,7 +212,8 @@ __device__ __forceinline__ void block_partial(double ss, int of, double *out_ss,
 // threads: fixed-order fp64 total of the partials (strided per thread, then
 // a warp tree, then the warps in order), global norm, clip coefficient,
 // overflow skip and the dynamic loss-scale state machine (ZeRO reading §5.1,
-// §5.3); the bias corrections of an applied step come from the table.
+// §5.3); the bias corrections of an applied step come from the table, or by
+// value when there is none.
 // Partials are read through L2 (another block may have written them).
 __device__ void finalize_block(const FinalizeArgs &a) {
     __shared__ double warp_ss[kFinalizeThreads / 32];
@@ -222,7 +223,8 @@ __device__ void finalize_block(const FinalizeArgs &a) {
     if (threadIdx.x == 0) {               // independent of the partials: load early
         sc = st->scaler;
         const int64_t t1 = sc.step_t + 1;
-        if (t1 < a.bc_len) bc = a.bc_table[t1];
+        if (!a.bc_table) bc = a.bc_given;
+        else if (t1 < a.bc_len) bc = a.bc_table[t1];
     }
     double s = 0.0;
     int of = 0;

@@ -69,6 +69,8 @@ struct FinalizeArgs {
     double max_grad_norm;
     const float2 *bc_table;           // bc_table[t] = {1 - b1^t, 1 - b2^t} as fp32
     int64_t bc_len;                   // entries t >= bc_len are {1, 1}
+    float2 bc_given;                  // bc_table == NULL: the bias corrections of the
+                                      // step this decision would apply, by value
     DevState *st;
     // non-NULL: only total the partials into *sum_out and *of_out (the first
     // half of a split step); no decision, no state change

@@ -16,12 +16,15 @@
 // keeps until the process exits.  The loss-scale state stays with the caller
 // in host memory and is passed in and returned on every call.
 //
-// Sharing: every call on a device uses the same array.  Nothing in it has to
-// start at zero: each call first writes the loss-scale state, the reduce
-// kernel writes every gradient element and every partial it later reads, and
-// the finalize kernel writes the step's scalars.  Calls whose GPU work
-// overlaps (several host threads, or several streams without ordering) race
-// on the array and give wrong results; callers must order them.
+// Sharing: every call on a device uses the same array, which keeps whatever
+// the last call left in it.  Each call therefore starts by overwriting the
+// whole state block with the caller's loss-scale state and zeros -- among
+// them the error word, which a staged reduce sets when one of its bounded
+// waits gives up and which the decision reads (a set word skips the step).
+// The reduce kernel then writes every gradient element and every partial
+// that the later kernels read.  Calls whose GPU work overlaps (several host
+// threads, or several streams without ordering) race on the array and give
+// wrong results; callers must order them.
 //
 // Set-up: the first call on a device looks up the array's device address
 // (cudaGetSymbolAddress, with that device current) and the launch geometry,
@@ -101,79 +104,6 @@ zero_status setup_device(int dev, const DeviceSetup **out) {
     }
     *out = &d;
     return ZERO_OK;
-}
-
-// The finalize kernel of zero_shard_step with the bias corrections of the
-// step passed by value (the host knows t, since the caller passes the
-// loss-scale state): fixed-order total of the norm partials from the static
-// scratch, global norm, clip coefficient, overflow skip, loss-scale update.
-struct FinalizeGivenArgs {
-    const double *part_ss;
-    const int32_t *part_of;
-    int32_t n_parts;
-    int32_t dynamic;
-    int32_t window;
-    float min_scale;
-    double extra_norm_sq;
-    double max_grad_norm;
-    float bc1, bc2;                   // 1 - beta^(t+1) as fp32
-    zg::DevState *st;
-};
-
-__global__ void __launch_bounds__(zg::kFinalizeThreads)
-finalize_given_bc_kernel(const __grid_constant__ FinalizeGivenArgs a) {
-    __shared__ double warp_ss[zg::kFinalizeThreads / 32];
-    double s = 0.0;
-    int of = 0;
-    for (int i = threadIdx.x; i < a.n_parts; i += blockDim.x) {
-        s += a.part_ss[i];
-        of |= a.part_of[i];
-    }
-    of = __syncthreads_or(of);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xFFFFFFFFu, s, o);
-    if ((threadIdx.x & 31) == 0) warp_ss[threadIdx.x >> 5] = s;
-    __syncthreads();
-    if (threadIdx.x != 0) return;
-    double total = 0.0;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) total += warp_ss[w];
-
-    zg::DevState *st = a.st;
-    zg::ScalerDev sc = st->scaler;
-    zg::ResultDev r;
-    r.overflow = of;
-    r.grad_norm = sqrt(total + a.extra_norm_sq);
-    r.scale_used = sc.scale;
-    if (of) {
-        r.skipped = 1;
-        r.clip_coef = 1.0f;
-        sc.overflow_count += 1;
-        if (a.dynamic) {
-            const float h = __fdiv_rn(sc.scale, 2.0f);
-            sc.scale = h < a.min_scale ? a.min_scale : h;
-            sc.good_steps = 0;
-        }
-    } else {
-        r.skipped = 0;
-        sc.step_t += 1;
-        float coef = 1.0f;
-        if (a.max_grad_norm > 0.0) {
-            const double q = a.max_grad_norm / (r.grad_norm + 1e-6);
-            if (q < 1.0) coef = (float)q;
-        }
-        r.clip_coef = coef;
-        if (a.dynamic) {
-            sc.good_steps += 1;
-            if (sc.good_steps == a.window) {
-                sc.scale = __fmul_rn(sc.scale, 2.0f);
-                sc.good_steps = 0;
-            }
-        }
-        st->bc1 = a.bc1;
-        st->bc2 = a.bc2;
-    }
-    st->scaler = sc;
-    st->res = r;
 }
 
 bool hparams_ok(const zero_hparams *hp) {
@@ -292,8 +222,12 @@ ZERO_API zero_status zero_shard_step_noalloc(
     const float bc1 = (float)(1.0 - std::pow(hp->beta1, t1));
     const float bc2 = (float)(1.0 - std::pow(hp->beta2, t1));
 
-    zg::ScalerDev sc{state->scale, state->good_steps, state->step_t, state->overflow_count};
-    e = cudaMemcpyAsync(&dstate->scaler, &sc, sizeof(sc), cudaMemcpyHostToDevice, st);
+    // the whole state block: the caller's loss-scale state, everything else
+    // zero (the error word included, whatever an earlier call left there)
+    zg::DevState init{};
+    init.scaler = zg::ScalerDev{state->scale, state->good_steps, state->step_t,
+                                state->overflow_count};
+    e = cudaMemcpyAsync(dstate, &init, sizeof(init), cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return cuda_fail(e, "writing the loss-scale state");
 
     rp.g = gbuf;
@@ -305,7 +239,9 @@ ZERO_API zero_status zero_shard_step_noalloc(
     rp.st = dstate;
     rp.grid_x = gx1;
     if ((e = zg::run_reduce(rp, st)) != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
-    FinalizeGivenArgs f{};
+    // the decision kernel of zero_shard_step, with this step's bias
+    // corrections by value instead of from a table
+    zg::FinalizeArgs f{};
     f.part_ss = part_ss;
     f.part_of = part_of;
     f.n_parts = S > 0 ? (int32_t)parts : 0;
@@ -314,11 +250,10 @@ ZERO_API zero_status zero_shard_step_noalloc(
     f.min_scale = (float)hp->min_loss_scale;
     f.extra_norm_sq = extra_norm_sq;
     f.max_grad_norm = hp->max_grad_norm;
-    f.bc1 = bc1;
-    f.bc2 = bc2;
+    f.bc_table = nullptr;
+    f.bc_given = make_float2(bc1, bc2);
     f.st = dstate;
-    finalize_given_bc_kernel<<<1, zg::kFinalizeThreads, 0, st>>>(f);
-    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "finalize kernel launch");
+    if ((e = zg::launch_finalize(f, st)) != cudaSuccess) return cuda_fail(e, "finalize kernel launch");
     zg::AdamPlan ap;
     ap.g = gbuf;
     ap.g_stride = g_stride;
@@ -358,10 +293,7 @@ ZERO_API zero_status zero_shard_step_noalloc(
         res->clip_coef = out_state.res.clip_coef;
         res->scale_used = out_state.res.scale_used;
     }
-    if (out_state.error) {               // a bounded wait gave up: the step was skipped
-        cudaMemsetAsync(&dstate->error, 0, sizeof(int32_t), st);
-        cudaStreamSynchronize(st);
+    if (out_state.error)                 // a bounded wait gave up: the step was skipped
         return fail(ZERO_ERR_TIMEOUT, "a kernel gave up waiting for its bulk copies; the step was skipped");
-    }
     return ZERO_OK;
 }

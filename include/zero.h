@@ -529,9 +529,12 @@ zero_status zero_flat_profile_read(zero_flat *h, double *ms_reduce, double *ms_f
  * which loads this library holds until the process exits; stepped shards
  * needing more than about 8.3M fp32 scratch elements in total
  * (n_ranks * roundup(shard_size, 4)) are rejected with ZERO_ERR_INVALID_ARG
- * and a message in zero_last_error().  Every call shares that array (it keeps
- * the last call's contents; nothing in it needs to start at zero), so calls
- * whose GPU work overlaps race: order them.  The call is synchronous: it
+ * and a message in zero_last_error().  Every call shares that array, which
+ * keeps the last call's contents: each call begins by overwriting its state
+ * block (the caller's loss-scale state, and zeros for the step's scalars and
+ * the error word a timed-out bulk-copy wait sets), and its reduce writes
+ * every gradient element and partial the later kernels read.  Calls whose
+ * GPU work overlaps race on the array: order them.  The call is synchronous: it
  * waits for `stream` before returning the new state (and `res`, if not NULL).
  * The first call on a device looks up the array's address and the launch
  * geometry with that device current; make it before any stream capture. */

@@ -1,5 +1,5 @@
-// synth.cu -- seeded synthetic inputs for the ZeRO shard step, generated
-// bit-identically on the host (threads) and on the GPU.
+// synth.cu -- seeded synthetic inputs for the ZeRO shard step, generated on
+// the GPU (and, for host-side samples of the same workload, on host threads).
 //
 // This module holds none of the optimizer's arithmetic.  It draws:
 //   * fp32 tensors ~ N(0, sigma) (optionally |N|) for master weights and
@@ -17,12 +17,15 @@
 // key = (seed, stream id).  Every element is one Philox block, so any element
 // can be regenerated on its own.
 //
-// Normal variates: Irwin-Hall with four terms.  The four 32-bit words give
-// four uniforms u_k = w_k >> 8 on [0, 2^24); their integer sum minus its mean
-// 2*(2^24 - 1), times sqrt(3) / 2^24, has mean 0 and variance 1 (support
-// +-2*sqrt(3)).  The sum is exact in int64, the two scalings are single fp64
-// multiplies and the final rounding to fp32 is one conversion, so host and
-// device produce the same bits.
+// Normal variates: Box-Muller (G. E. P. Box and M. E. Muller, "A Note on the
+// Generation of Random Normal Deviates", Ann. Math. Statist. 29(2), 1958).
+// Two words of the element's block give u1 = ((w0 >> 8) + 1) / 2^24 in
+// (0, 1] and u2 = (w1 >> 8) / 2^24 in [0, 1), both exact in fp32, and
+// z = sqrt(-2 ln u1) cos(2 pi u2) is N(0, 1) (|z| <= sqrt(2 ln 2^24) = 5.77).
+// The logarithm, square root and cosine are the platform's own library
+// functions (CUDA's logf, sqrtf and cospif on the GPU; the C library's on the
+// host), so host and device values agree to a few ulp but not bit for bit;
+// tests that compare the GPU with the oracle hand the oracle the GPU's bytes.
 #include <cstdint>
 #include <cstring>
 #include <cmath>
@@ -61,22 +64,20 @@ __host__ __device__ inline void philox4x32_10(uint32_t c[4], uint32_t k0, uint32
     }
 }
 
-// sqrt(3) / 2^24 as an fp64 constant (sqrt(3) correctly rounded to fp64).
-constexpr double kIrwinHallScale = 1.7320508075688772 / 16777216.0;
-
 __host__ __device__ inline float normal_at(uint32_t seed, uint32_t stream, uint64_t idx,
                                            double sigma) {
     uint32_t c[4] = {(uint32_t)idx, (uint32_t)(idx >> 32), 0u, 0u};
     philox4x32_10(c, seed, stream);
-    const int64_t s = (int64_t)(c[0] >> 8) + (int64_t)(c[1] >> 8) +
-                      (int64_t)(c[2] >> 8) + (int64_t)(c[3] >> 8);
-    const int64_t d = s - (int64_t)2 * ((int64_t)(1 << 24) - 1);
+    const float u1 = (float)((c[0] >> 8) + 1u) * 0x1p-24f;
+    const float u2 = (float)(c[1] >> 8) * 0x1p-24f;
 #ifdef __CUDA_ARCH__
-    const double z = __dmul_rn((double)d, kIrwinHallScale);
-    return (float)__dmul_rn(z, sigma);
+    const float r = sqrtf(__fmul_rn(-2.0f, logf(u1)));
+    const float z = __fmul_rn(r, cospif(__fmul_rn(2.0f, u2)));
+    return (float)__dmul_rn((double)z, sigma);
 #else
-    const double z = (double)d * kIrwinHallScale;      // one rounding per multiply
-    return (float)(z * sigma);
+    const float r = std::sqrt(-2.0f * std::log(u1));
+    const float z = r * (float)std::cos(6.283185307179586 * (double)u2);
+    return (float)((double)z * sigma);
 #endif
 }
 

@@ -1,5 +1,7 @@
-"""The device generator gives the host generator's bits (so the oracle can
-regenerate any input the GPU consumed)."""
+"""The device generator draws the host generator's distribution: the same
+Philox words, and the platform's own logf / sqrtf / cos in Box-Muller, so
+values agree to a few ulp (tests that compare the GPU with the oracle hand the
+oracle the GPU's bytes, so bit identity is not needed)."""
 import numpy as np
 import pytest
 
@@ -9,7 +11,12 @@ import synth  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 
-def test_device_equals_host_generator():
+def _key16(u):
+    u = u.astype(np.int32)
+    return np.where(u & 0x8000, -(u & 0x7FFF), u & 0x7FFF)
+
+
+def test_device_matches_host_generator():
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
     n = 3_000_017
@@ -17,8 +24,10 @@ def test_device_equals_host_generator():
                                        (synth.MOMENT_V, 5 * 10 ** 9, 1e-8, True)):
         t = torch.empty(n, dtype=torch.float32, device="cuda")
         synth.normal_device(t, 11, kind, first, sigma, absval=absval)
-        h = synth.normal_host(11, kind, first, n, sigma, absval=absval)
-        assert np.array_equal(t.cpu().numpy().view(np.uint32), h.view(np.uint32))
+        d = t.cpu().numpy().astype(np.float64)
+        h = synth.normal_host(11, kind, first, n, sigma, absval=absval).astype(np.float64)
+        # a few ulp of the value, or of sigma where the cosine is near zero
+        assert np.all(np.abs(d - h) <= 1e-6 * np.abs(h) + 1e-6 * sigma)
     for dtype in (synth.F16, synth.BF16):
         g = torch.empty((3, n + 5), dtype=torch.float16, device="cuda")
         synth.grads_device(g, 4, 7, 10 ** 9, n, 1e-3, 2e-3, scale=4096.0 if dtype == 0 else 1.0,
@@ -26,4 +35,7 @@ def test_device_equals_host_generator():
         d = g[:, :n].view(torch.int16).cpu().numpy().view(np.uint16)
         h = synth.grads_host(4, 7, 3, 10 ** 9, n, 1e-3, 2e-3, scale=4096.0 if dtype == 0 else 1.0,
                              dtype=dtype, zero_from=10 ** 9 + n - 10)
-        assert np.array_equal(d, h)
+        # the 16-bit casts of values a few fp32 ulp apart: equal, or 1 ulp apart
+        assert np.abs(_key16(d) - _key16(h)).max() <= 1
+        assert np.mean(d == h) > 0.99
+        assert not d[:, n - 10:].any()

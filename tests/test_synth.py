@@ -1,6 +1,6 @@
 """The seeded input generator: Philox4x32-10 against the published
-known-answer vectors, the Irwin-Hall normal's moments, counter-based
-regeneration of single elements, thread-count independence."""
+known-answer vectors, the Box-Muller normal's moments and tails,
+counter-based regeneration of single elements, thread-count independence."""
 import numpy as np
 import pytest
 
@@ -21,15 +21,20 @@ def test_philox_known_answers(ctr, key, want):
     assert tuple(synth.philox(ctr, key)) == want
 
 
-def test_irwin_hall_moments():
-    x = synth.normal_host(0, synth.MASTER, 0, 2_000_000, 1.0).astype(np.float64)
+def test_normal_moments_and_tails():
+    n = 4_000_000
+    x = synth.normal_host(0, synth.MASTER, 0, n, 1.0).astype(np.float64)
     assert abs(x.mean()) < 3e-3
     assert abs(x.var() - 1.0) < 5e-3
     kurt = ((x - x.mean()) ** 4).mean() / x.var() ** 2 - 3.0
-    assert abs(kurt - (-0.3)) < 0.02                  # Irwin-Hall, n=4: -6/(5n)
-    assert np.abs(x).max() <= 2 * np.sqrt(3) + 1e-6
+    assert abs(kurt) < 0.03                           # a normal has excess kurtosis 0
+    assert np.abs(x).max() <= np.sqrt(2 * 24 * np.log(2)) + 1e-5   # u1 >= 2^-24
+    # tail mass beyond 3 and 4 sigma: 2.70e-3 and 6.33e-5 for a normal
+    # (binomial standard errors ~2.6e-5 and ~4e-6 at this n)
+    assert abs(np.mean(np.abs(x) > 3.0) - 2.6998e-3) < 2e-4
+    assert abs(np.mean(np.abs(x) > 4.0) - 6.334e-5) < 2.5e-5
     y = synth.normal_host(0, synth.MASTER, 0, 1000, 0.02)
-    assert np.allclose(y, (x[:1000] * 0.02).astype(np.float32), rtol=1e-6, atol=0)
+    assert np.array_equal(y, (x[:1000] * 0.02).astype(np.float32))
 
 
 def test_counter_based_regeneration_and_threads():
