@@ -75,6 +75,11 @@ def parse_args(argv=None):
                         "stepped with one global decision, against per-FlatParameter steps")
     p.add_argument("--group-params", type=int, default=1_000_000,
                    help="params in each group member's shard")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip the other configs' steps (gpt2_small, gpt_1p5b_rank17, "
+                        "llama_7b_rank0) reported beside the headline workload")
+    p.add_argument("--workload-steps", type=int, default=20,
+                   help="timed steps of each of those configs")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -453,6 +458,21 @@ def run_ours(args, w):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.cpu_seconds)
+    side = None
+    if (world == 1 and not args.no_workloads and w.name == "10b_rank7" and K == 1
+            and not args.q8 and not args.graph):
+        from synth.workloads import BY_NAME
+        l2_note = (dw.flat.device_bytes() / 1e9 + (dw.grads.numel() * esize +
+                   (3 + (K > 1)) * params * 4 + dw.out.numel() * 2) / 1e9)
+        dw.close()
+        del dw
+        torch.cuda.empty_cache()
+        dw = None
+        side = {name: measure_workload(BY_NAME[name], args.workload_steps, 3, dev)
+                for name in SIDE_WORKLOADS}
+    else:
+        l2_note = (dw.flat.device_bytes() / 1e9 + (dw.grads.numel() * esize +
+                   (3 + (K > 1)) * params * 4 + dw.out.numel() * 2) / 1e9)
 
     if rank == 0:
         line = {
@@ -468,9 +488,7 @@ def run_ours(args, w):
                        "micro_steps": K,
                        "q8_payload": bool(args.q8),
                        "cuda_graph": bool(args.graph),
-                       "l2": "inputs larger than L2 (%.0f GB resident vs 129 MB)" %
-                             (dw.flat.device_bytes() / 1e9 + (dw.grads.numel() * esize +
-                              (3 + (K > 1)) * params * 4 + dw.out.numel() * 2) / 1e9),
+                       "l2": "inputs larger than L2 (%.0f GB resident vs 129 MB)" % l2_note,
                        "parallelism": "replicas%d" % world},
             "step_hbm": {"min_bytes_per_param": K * N * esize + 26, "achieved_gbs": step_gbs,
                          "frac_of_measured": step_gbs / peak,
@@ -482,9 +500,84 @@ def run_ours(args, w):
             "clocks": clocks,
             "gpu_launches": launches_per_step * args.steps,
         }
+        if side is not None:
+            line["workloads"] = side
         print(json.dumps(line), flush=True)
-    dw.close()
+    if dw is not None:
+        dw.close()
     group.close()
+
+
+# The configs reported beside the headline step (each its own FlatParameter,
+# stepped alone on the device after the headline workload has been freed).
+SIDE_WORKLOADS = ("gpt2_small", "gpt_1p5b_rank17", "llama_7b_rank0")
+
+
+def measure_workload(w, steps, warmup, dev):
+    """Device-timed steps of one more config: ms per step, Gparams/s, each
+    kernel's event-timed duration and achieved GB/s (algorithmic bytes), the
+    step's HBM rate at the method's minimum bytes, and the dominant kernel's
+    fraction of the measured copy peak."""
+    import torch
+
+    import fsdp_sharded_mixed_zero_gb300 as Z
+    from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
+    peak, peak_kind = measured_peaks()
+    dw = DeviceWorkload(w, device=dev)
+    try:
+        stream = torch.cuda.current_stream(dev)
+        dw.gen_grads(0, dw.scaler().scale)
+        for _ in range(warmup):
+            dw.step(want_result=False, stream=stream)
+        Z.zero_flat_profile_enable(dw.flat.handle, True)
+        Z.zero_flat_profile_read(dw.flat.handle)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            dw.step(want_result=False, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        Z.zero_flat_profile_enable(dw.flat.handle, False)
+        ms_red, _, ms_adam, nrec = Z.zero_flat_profile_read(dw.flat.handle)
+        ms = e0.elapsed_time(e1) / steps
+        res = dw.step(want_result=True, stream=stream)
+        assert res.skipped == 0 and res.overflow == 0, "%s inputs overflowed" % w.name
+        params = dw.S * len(w.ranks)
+        N = w.world_size
+        esize = 4 if w.grad_dtype == 2 else 2
+        kernels = {"reduce_kernel": {"ms_mean": ms_red / max(nrec, 1),
+                                     "bytes_per_param": N * esize + 4},
+                   "adamw_kernel": {"ms_mean": ms_adam / max(nrec, 1), "bytes_per_param": 30}}
+        for k in kernels.values():
+            k["achieved_gbs"] = k["bytes_per_param"] * params / (k["ms_mean"] / 1e3) / 1e9
+            k["frac_of_measured"] = k["achieved_gbs"] / peak
+        dom = max(kernels, key=lambda n: kernels[n]["ms_mean"])
+        min_b = (N * esize + 26) * params
+        moved_b = (N * esize + 34) * params
+        return {"ms_per_step": ms, "value": params / (ms / 1e3) / 1e9, "unit": "Gparams/s",
+                "params_stepped": params, "emulated_world_size": N, "stepped_ranks": w.ranks,
+                "steps": steps, "warmup": warmup,
+                "step_hbm": {"min_bytes_per_param": N * esize + 26,
+                             "achieved_gbs_at_min_bytes": min_b / (ms / 1e3) / 1e9,
+                             "frac_of_nominal_8tbs_at_min_bytes":
+                                 min_b / (ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+                             "moved_bytes_per_param": N * esize + 34,
+                             "achieved_gbs_moved": moved_b / (ms / 1e3) / 1e9,
+                             "frac_of_nominal_8tbs_moved":
+                                 moved_b / (ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+                             "frac_of_measured_moved": moved_b / (ms / 1e3) / 1e9 / peak},
+                "kernels": kernels,
+                "roofline": {"bound": "hbm", "kernel": dom,
+                             "achieved": kernels[dom]["achieved_gbs"], "peak": peak,
+                             "unit": "GB/s", "frac": kernels[dom]["achieved_gbs"] / peak,
+                             "peak_kind": peak_kind},
+                "launches_per_step": 2}
+    finally:
+        dw.close()
+        del dw
+        torch.cuda.empty_cache()
 
 
 def measure_e2e(args, dw, stream, dev, params, barrier, max_over_ranks, world):

@@ -613,17 +613,21 @@ ZERO_API zero_status zero_shard_reduce(zero_flat *h, const int32_t *ranks, int32
     return ZERO_OK;
 }
 
-ZERO_API zero_status zero_shard_apply(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
-                                      float *const *master, float *const *m, float *const *v,
-                                      void *flat_param_out, const double *norm_sq,
-                                      const int32_t *overflow, void *stream,
-                                      zero_step_result *res) {
+// The second half of a split step: the decision over n_parts (norm_sq[k],
+// overflow[k]) pairs in device memory, then AdamW and the cast.
+static zero_status apply_parts(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                               float *const *master, float *const *m, float *const *v,
+                               void *flat_param_out, const double *norm_sq,
+                               const int32_t *overflow, int32_t n_parts, void *stream,
+                               zero_step_result *res) {
     if (!h) return fail(ZERO_ERR_INVALID_ARG, "handle is NULL");
     int32_t max_rank = 0;
     zero_status s;
     if ((s = check_ranks(h, ranks, n_ranks, &max_rank))) return s;
     if ((s = check_update(h, n_ranks, master, m, v, flat_param_out, 0.0))) return s;
     if (!norm_sq || !overflow) return fail(ZERO_ERR_INVALID_ARG, "NULL total");
+    if (n_parts < 1 || n_parts > (1 << 20))
+        return fail(ZERO_ERR_INVALID_ARG, "n_parts must be in [1, 2^20]");
     if ((uintptr_t)norm_sq % 8 || (uintptr_t)overflow % 4)
         return fail(ZERO_ERR_ALIGNMENT, "norm_sq must be 8-byte, overflow 4-byte aligned");
     if (h->reduced_ranks.size() != (size_t)n_ranks ||
@@ -639,13 +643,35 @@ ZERO_API zero_status zero_shard_apply(zero_flat *h, const int32_t *ranks, int32_
     ap.v = v;
     ap.out = flat_param_out;
     plan_adamw(h, ap, ranks, n_ranks);
-    // the decision from the caller's totals: one "partial" holding them
-    const zg::FinalizeArgs f = decision_args(h, norm_sq, overflow, 1, 0.0);
+    // the decision from the caller's partials, totalled by the decision kernel
+    // in its fixed order
+    const zg::FinalizeArgs f = decision_args(h, norm_sq, overflow, n_parts, 0.0);
     cudaError_t e;
     if ((e = zg::launch_finalize(f, st))) return cuda_fail(e, "finalize kernel launch");
     if ((e = zg::run_adamw(ap, st))) return cuda_fail(e, "adamw kernel launch");
     h->reduced_ranks.clear();
     return res ? read_result(h, st, res) : ZERO_OK;
+}
+
+ZERO_API zero_status zero_shard_apply(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                                      float *const *master, float *const *m, float *const *v,
+                                      void *flat_param_out, const double *norm_sq,
+                                      const int32_t *overflow, void *stream,
+                                      zero_step_result *res) {
+    // one "partial" holding the caller's totals
+    return apply_parts(h, ranks, n_ranks, master, m, v, flat_param_out, norm_sq, overflow, 1,
+                       stream, res);
+}
+
+ZERO_API zero_status zero_shard_apply_partials(zero_flat *h, const int32_t *ranks,
+                                               int32_t n_ranks, float *const *master,
+                                               float *const *m, float *const *v,
+                                               void *flat_param_out,
+                                               const double *norm_sq_parts,
+                                               const int32_t *overflow_parts, int32_t n_parts,
+                                               void *stream, zero_step_result *res) {
+    return apply_parts(h, ranks, n_ranks, master, m, v, flat_param_out, norm_sq_parts,
+                       overflow_parts, n_parts, stream, res);
 }
 
 ZERO_API zero_status zero_shard_step_q8(zero_flat *h, const int32_t *ranks, int32_t n_ranks,

@@ -283,6 +283,23 @@ zero_status zero_shard_apply(zero_flat *h, const int32_t *ranks, int32_t n_ranks
                              void *flat_param_out, const double *norm_sq,
                              const int32_t *overflow, void *stream, zero_step_result *res);
 
+/* zero_shard_apply with the cross-rank exchange left as an all-gather: the
+ * one global decision of the ZeRO reading §5.3 (overflow and clipping taken
+ * over every rank's gradient) from n_parts per-rank partials in device
+ * memory -- norm_sq_parts[k] (fp64) and overflow_parts[k] (int32), k <
+ * n_parts, e.g. every rank's zero_shard_reduce outputs gathered in rank order
+ * -- totalled on the device (the squared norms summed in one fixed order, the
+ * flags OR-ed), so every rank that applies the same gathered arrays takes
+ * bit for bit the same skip / clip / scale decision, whatever the collective
+ * library's reduction order.  Then AdamW and the cast as zero_shard_apply.
+ * Other arguments, requirements and errors as for zero_shard_apply;
+ * INVALID_ARG for n_parts outside [1, 2^20]. */
+zero_status zero_shard_apply_partials(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                                      float *const *master, float *const *m, float *const *v,
+                                      void *flat_param_out, const double *norm_sq_parts,
+                                      const int32_t *overflow_parts, int32_t n_parts,
+                                      void *stream, zero_step_result *res);
+
 /* A group: the FlatParameters one rank steps together ("PyTorch FSDP ...
  * 深度解析" §3.1: one FlatParameter per wrapped module) with one clip norm and
  * one loss-scale decision (ZeRO reading §5.3), in one reduce launch and one

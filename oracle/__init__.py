@@ -103,6 +103,8 @@ def lib():
                                          C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
                                          C.POINTER(C.c_void_p), C.c_void_p, C.c_double,
                                          C.POINTER(Result)]
+        L.ora_unscale_acc.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_int64, C.c_float,
+                                      C.c_void_p]
         L.ora_quantize_q8.argtypes = [C.c_void_p, C.c_int64, C.c_int32, C.c_void_p, C.c_void_p]
         L.ora_ddp_step.argtypes = [C.POINTER(Hparams), C.POINTER(Scaler), C.c_int32,
                                    C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
@@ -321,6 +323,17 @@ def grad_accumulate(world_size, full_numel, shard_size, ranks, grads, ld, rank_m
                                    _ptr_array(acc, shard_size), int(bool(first)))
     if rc:
         raise ValueError("ora_grad_accumulate failed: %d" % rc)
+
+
+def unscale_acc(acc, first_flat_index, full_numel, scale, out=None):
+    """g = acc / scale for real elements, 0 for padding (flat index >= full_numel)."""
+    _check(acc, np.float32)
+    out = np.empty(acc.size, np.float32) if out is None else out
+    _check(out, np.float32)
+    assert out.size == acc.size
+    lib().ora_unscale_acc(_ptr(acc), acc.size, first_flat_index, full_numel, float(scale),
+                          _ptr(out))
+    return out
 
 
 def shard_step_acc(hp, st, world_size, full_numel, shard_size, ranks, acc, master, m, v,

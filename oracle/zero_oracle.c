@@ -580,8 +580,19 @@ int ora_grad_accumulate(int32_t world_size, int64_t full_numel, int64_t shard_si
     return ORA_OK;
 }
 
-/* The optimizer step on accumulated shards: g = acc / scale (padding
- * elements, flat index >= full_numel, count as zero), then apply_step.      */
+/* The gradient of a step taken from accumulators: the loss scale comes out
+ * once, at the optimizer step ([P1] §实践要点, gradient accumulation):
+ * g = acc / scale for the `count` elements from flat index first_flat_index;
+ * padding elements (flat index >= full_numel) count as zero.               */
+void ora_unscale_acc(const float *acc, int64_t count, int64_t first_flat_index,
+                     int64_t full_numel, float scale, float *g_out)
+{
+    for (int64_t i = 0; i < count; ++i)
+        g_out[i] = first_flat_index + i >= full_numel ? 0.0f : acc[i] / scale;
+}
+
+/* The optimizer step on accumulated shards: ora_unscale_acc, then
+ * apply_step.                                                               */
 int ora_shard_step_acc(const ora_hparams *hp, ora_scaler *st, int32_t world_size,
                        int64_t full_numel, int64_t shard_size, int32_t param_is_bf16,
                        const int32_t *ranks, int32_t n_ranks, const float *const *acc,
@@ -593,12 +604,9 @@ int ora_shard_step_acc(const ora_hparams *hp, ora_scaler *st, int32_t world_size
     float *g = alloc_rows(shard_size, n_ranks);
     if (!g) return ORA_EOVERFLOW;
     const float scale_used = st->scale;
-    for (int32_t j = 0; j < n_ranks; ++j) {
-        const int64_t first = (int64_t)ranks[j] * shard_size;
-        for (int64_t i = 0; i < shard_size; ++i)
-            g[(int64_t)j * shard_size + i] =
-                first + i >= full_numel ? 0.0f : acc[j][i] / scale_used;
-    }
+    for (int32_t j = 0; j < n_ranks; ++j)
+        ora_unscale_acc(acc[j], shard_size, (int64_t)ranks[j] * shard_size, full_numel,
+                        scale_used, g + (int64_t)j * shard_size);
     apply_step(hp, st, shard_size, param_is_bf16, ranks, n_ranks, g, master, m, v,
                flat_out, extra_norm_sq, scale_used, res);
     free(g);

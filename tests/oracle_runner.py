@@ -55,6 +55,31 @@ def norm_exact(arrays, acc=None, overflow=0):
     return acc, overflow
 
 
+def adamw_slot(hp, t, coef, g, master, m, v, out, param_is_bf16=False):
+    """oracle.adamw_cast over one shard, chunk-parallel (the update is
+    elementwise, so the chunking changes no result); out: the shard's 16-bit
+    slot (uint16, same length)."""
+    def job(ab):
+        a, b = ab
+        oracle.adamw_cast(hp, t, coef, g[a:b], master[a:b], m[a:b], v[a:b],
+                          param_is_bf16=param_is_bf16, out=out[a:b])
+
+    list(_pool().map(job, _chunks(g.size)))
+
+
+def _decide_and_apply(hp, st, S, ranks, gs, master, m, v, out, param_is_bf16, extra_norm_sq,
+                      coef_override, scale):
+    acc, of = norm_exact(gs)
+    norm = math.sqrt(oracle.norm_sum(acc) + extra_norm_sq)
+    coef, skip = oracle.scaler_decide(hp, st, of, norm)
+    if not skip:
+        c = coef if coef_override is None else float(coef_override)
+        for j, r in enumerate(ranks):
+            adamw_slot(hp, st.step_t, c, gs[j], master[j], m[j], v[j], out[r * S:(r + 1) * S],
+                       param_is_bf16)
+    return of, skip, norm, coef, scale
+
+
 def shard_step(hp, st, world_size, full, S, ranks, grads, ld, mul, master, m, v, out,
                avg=True, grad_is_bf16=False, param_is_bf16=False, extra_norm_sq=0.0,
                coef_override=None):
@@ -68,21 +93,32 @@ def shard_step(hp, st, world_size, full, S, ranks, grads, ld, mul, master, m, v,
         g = np.empty(max(S, 1), np.float32)[:S]
         reduce_rank(grads, ld, r * mul, world_size, S, r * S, full, avg, scale, grad_is_bf16, g)
         gs.append(g)
-    acc, of = norm_exact(gs)
-    norm = math.sqrt(oracle.norm_sum(acc) + extra_norm_sq)
-    coef, skip = oracle.scaler_decide(hp, st, of, norm)
-    if not skip:
-        t = st.step_t
-        c = coef if coef_override is None else float(coef_override)
+    return _decide_and_apply(hp, st, S, ranks, gs, master, m, v, out, param_is_bf16,
+                             extra_norm_sq, coef_override, scale)
 
-        def job(args):
-            j, a, b = args
-            r = ranks[j]
-            oracle.adamw_cast(hp, t, c, gs[j][a:b], master[j][a:b], m[j][a:b], v[j][a:b],
-                              param_is_bf16=param_is_bf16, out=out[r * S + a:r * S + b])
 
-        list(_pool().map(job, [(j, a, b) for j in range(len(ranks)) for a, b in _chunks(S)]))
-    return of, skip, norm, coef, scale
+def unscale_acc(acc, first, full, scale, g):
+    """g[:] = oracle.unscale_acc of the accumulator acc (flat indices from
+    `first`), chunk-parallel."""
+    def job(ab):
+        a, b = ab
+        oracle.unscale_acc(acc[a:b], first + a, full, scale, out=g[a:b])
+
+    list(_pool().map(job, _chunks(acc.size)))
+
+
+def shard_step_acc(hp, st, world_size, full, S, ranks, acc, master, m, v, out,
+                   param_is_bf16=False, extra_norm_sq=0.0):
+    """Equivalent of oracle.shard_step_acc (the step from fp32 accumulators);
+    returns (overflow, skipped, norm, coef, scale_used)."""
+    scale = st.scale
+    gs = []
+    for j, r in enumerate(ranks):
+        g = np.empty(max(S, 1), np.float32)[:S]
+        unscale_acc(acc[j], r * S, full, scale, g)
+        gs.append(g)
+    return _decide_and_apply(hp, st, S, ranks, gs, master, m, v, out, param_is_bf16,
+                             extra_norm_sq, None, scale)
 
 
 def accumulate_rows(grads, ld, n_contrib, count, full, avg, bf16, acc, first):

@@ -120,7 +120,11 @@ def test_accumulation_then_step(ora, w):
 
 def test_one_micro_step_equals_direct_step():
     """Accumulate once, step from the accumulator: the same bits as the direct
-    step on the same contributions (two handles, same inputs)."""
+    step on the same contributions (two handles, same inputs).  The two norms
+    are summed over different partitions (the direct step's odd shard takes
+    the staged reduce, the accumulated step the plain norm pass), so they
+    agree to ~1e-16 relative rather than bit for bit; the clip coefficient
+    derived from them, and so every state bit, is the same."""
     _need_gpu()
     from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
     w = _wl("one_micro", [(100_003,)], 4, [0, 1, 2, 3], steps=2)
@@ -132,8 +136,8 @@ def test_one_micro_step_equals_direct_step():
         ra = a.step()
         b.accumulate(first=True)
         rb = b.step_accumulated()
-        assert (ra.overflow, ra.skipped, ra.grad_norm, ra.clip_coef) == \
-               (rb.overflow, rb.skipped, rb.grad_norm, rb.clip_coef)
+        assert (ra.overflow, ra.skipped, ra.clip_coef) == (rb.overflow, rb.skipped, rb.clip_coef)
+        assert abs(ra.grad_norm - rb.grad_norm) <= 1e-14 * ra.grad_norm
     for x, y in zip(a.master + a.m + a.v, b.master + b.m + b.v):
         assert torch.equal(x, y)
     assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))

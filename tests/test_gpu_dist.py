@@ -1,0 +1,113 @@
+"""The multi-rank step with the library's kernels: two processes, one rank
+each, joined by a gloo group on 127.0.0.1 and sharing this one GPU.  Each
+process steps only its own shard (RankStep: the all-to-all of the
+reduce-scatter, zero_shard_reduce, the all-gather of the two scalars,
+zero_shard_apply_partials, the all-gather of the 16-bit slots); every
+exchange goes through gloo on host-staged buffers, so no kernel of one
+process waits on the other.  On every rank and every step, the result, the
+loss-scale state, the rank's master / m / v and the whole gathered flat
+buffer are compared with the oracle's step of all shards at once on the
+stacked contributions, at the parity tolerances; one rank's inf must make
+both ranks skip and halve the scale."""
+import os
+import socket
+import sys
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as tdist  # noqa: E402
+import torch.multiprocessing as mp  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+F16, BF16, SUM, AVG = 0, 1, 0, 1
+
+CASES = [
+    # odd shard: rank 1's slice and the received rows are off 16-byte boundaries
+    dict(name="fp16_avg_dynamic_ragged", full=1_000_003, dtype=F16, op=AVG, dynamic=True),
+    # every row 64-byte aligned: the vectorised reduce
+    dict(name="bf16_sum_static_aligned", full=2 * 262_144, dtype=BF16, op=SUM, dynamic=False),
+]
+WORLD, STEPS, INF_STEP = 2, 4, 2
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, port, case):
+    if ROOT not in sys.path:
+        sys.path.insert(0, ROOT)
+    torch.cuda.set_device(0)
+    tdist.init_process_group("gloo", init_method="tcp://127.0.0.1:%d" % port, rank=rank,
+                             world_size=WORLD)
+    import fsdp_sharded_mixed_zero_gb300 as Z
+    import oracle
+    import synth
+    from fsdp_sharded_mixed_zero_gb300.dist import RankStep
+    from tests.gpu_helpers import assert_params_close, assert_result, assert_state, f32, u16
+
+    full, dt, bf16 = case["full"], case["dtype"], case["dtype"] == BF16
+    kw = dict(dynamic=case["dynamic"], lr=1e-3, window=3, initial_scale_power=12)
+    flat = Z.ZeroFlat([(full,)], WORLD, dt, dt, case["op"], Z.hparams(**kw))
+    ohp = oracle.hparams(**kw)
+    S, padded = flat.shard_size, flat.padded_numel
+    tdt = torch.bfloat16 if bf16 else torch.float16
+    sdt = synth.BF16 if bf16 else synth.F16
+    step_of = RankStep(flat, rank, grad_dtype=dt)
+    # this rank's shard, and the oracle's copy of every shard
+    master_all = torch.empty(padded, device="cuda")
+    synth.normal_device(master_all, 41, synth.MASTER, 0, 0.02)
+    master_all[full:].zero_()
+    master = master_all[rank * S:(rank + 1) * S].clone()
+    m = torch.zeros(S, device="cuda")
+    v = torch.zeros(S, device="cuda")
+    out = torch.zeros(padded, dtype=tdt, device="cuda")
+    o_state = [[f32(master_all[k * S:(k + 1) * S]).copy() for k in range(WORLD)],
+               [np.zeros(S, np.float32) for _ in range(WORLD)],
+               [np.zeros(S, np.float32) for _ in range(WORLD)]]
+    o_out = np.zeros(padded, np.uint16)
+    o_st = oracle.scaler_init(ohp)
+    mine = torch.empty((1, padded), dtype=tdt, device="cuda")
+    everyone = torch.empty((WORLD, padded), dtype=tdt, device="cuda")
+    for step in range(STEPS):
+        scale = flat.scaler_state().scale
+        assert scale == o_st.scale
+        # this rank's own gradient (contributor `rank`), and all of them for the oracle
+        synth.grads_device(mine, 41, step, 0, padded, 1e-3, 1e-3, scale, sdt, zero_from=full,
+                           c0=rank, n_contrib=1)
+        synth.grads_device(everyone, 41, step, 0, padded, 1e-3, 1e-3, scale, sdt,
+                           zero_from=full)
+        if step == INF_STEP:                 # rank 1's gradient, inside rank 0's slice
+            everyone[1, 777] = float("inf")
+            if rank == 1:
+                mine[0, 777] = float("inf")
+        assert torch.equal(mine[0].view(torch.int16), everyone[rank].view(torch.int16))
+        g_host = u16(everyone)
+        scale_used = o_st.scale
+        ro = oracle.shard_step(ohp, o_st, WORLD, full, S, list(range(WORLD)), g_host, padded, S,
+                               *o_state, o_out, avg=case["op"] == AVG, grad_is_bf16=bf16,
+                               param_is_bf16=bf16)
+        res = step_of.step(mine.view(-1), master, m, v, out)
+        torch.cuda.synchronize()
+        tag = " (rank %d, step %d)" % (rank, step)
+        assert_result(res, (ro.overflow, ro.skipped, ro.grad_norm, ro.clip_coef, scale_used))
+        assert flat.scaler_state().as_tuple() == o_st.as_tuple(), tag
+        assert_state(f32(master), f32(m), f32(v), o_state[0][rank], o_state[1][rank],
+                     o_state[2][rank], tag=tag)
+        assert_params_close(u16(out), o_out, bf16, "gathered flat buffer" + tag)
+        assert res.skipped == (step == INF_STEP), tag
+    assert o_st.overflow_count == 1
+    flat.close()
+    tdist.destroy_process_group()
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: c["name"])
+def test_two_ranks_on_gloo_match_the_all_shards_step(case):
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    mp.start_processes(_worker, args=(_free_port(), case), nprocs=WORLD, start_method="spawn")

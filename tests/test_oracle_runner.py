@@ -1,5 +1,5 @@
-"""The threaded composition of the oracle's pieces equals ora_shard_step bit
-for bit (so large GPU parity runs may use it)."""
+"""The threaded composition of the oracle's pieces equals ora_shard_step
+(and ora_shard_step_acc) bit for bit, so large GPU parity runs may use it."""
 import numpy as np
 import pytest
 
@@ -88,3 +88,38 @@ def test_group_composition_equals_the_concatenated_step(ora):
             assert np.array_equal(cat[i], np.concatenate([m[i] for m in grp]))
         assert np.array_equal(out_cat, np.concatenate(out_grp))
     assert st_cat.overflow_count == 1
+
+
+@pytest.mark.parametrize("N,n,ranks", [(4, 2_000_003, [0, 3]), (8, 1_000_000, [5])])
+def test_threaded_matches_shard_step_acc(ora, monkeypatch, N, n, ranks):
+    monkeypatch.setattr(runner, "CHUNK", 1 << 18)
+    rng = np.random.default_rng(n + 1)
+    full, S, padded = ora.layout([n], N)
+    hp = ora.hparams(lr=1e-3, max_grad_norm=1.0, window=2, initial_scale_power=4)
+    sa, sb = ora.scaler_init(hp), ora.scaler_init(hp)
+    th = [(rng.standard_normal(S) * 0.02).astype(np.float32) for _ in ranks]
+    st_a = [[t.copy() for t in th], [np.zeros(S, np.float32) for _ in ranks],
+            [np.zeros(S, np.float32) for _ in ranks]]
+    st_b = [[t.copy() for t in th], [np.zeros(S, np.float32) for _ in ranks],
+            [np.zeros(S, np.float32) for _ in ranks]]
+    oa = np.zeros(padded, np.uint16)
+    ob = np.zeros(padded, np.uint16)
+    for step in range(3):
+        # accumulators as the accumulation leaves them: garbage in the padding
+        # (the step must ignore it), an inf at step 1
+        acc = [(rng.standard_normal(S) * 64).astype(np.float32) for _ in ranks]
+        if step == 1:
+            acc[-1][3] = np.inf
+        ra = ora.shard_step_acc(hp, sa, N, full, S, ranks, acc, *st_a, oa, extra_norm_sq=0.5)
+        rb = runner.shard_step_acc(hp, sb, N, full, S, ranks, acc, *st_b, ob, extra_norm_sq=0.5)
+        assert (ra.overflow, ra.skipped, ra.grad_norm, ra.clip_coef, ra.scale_used) == rb
+        assert sa.as_tuple() == sb.as_tuple()
+        for x, y in zip(st_a[0] + st_a[1] + st_a[2] + [oa], st_b[0] + st_b[1] + st_b[2] + [ob]):
+            assert np.array_equal(x, y)
+    assert sa.overflow_count == 1
+
+
+def test_unscale_acc_pads_with_zero(ora):
+    acc = np.array([2.0, -6.0, 1.0, 5.0], np.float32)
+    g = ora.unscale_acc(acc, 10, 12, 4.0)             # flat indices 10..13, full_numel 12
+    assert g.tolist() == [0.5, -1.5, 0.0, 0.0]
