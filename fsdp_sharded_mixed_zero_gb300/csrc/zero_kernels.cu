@@ -192,7 +192,7 @@ struct NormAcc {
 // Block total of per-thread fp64 sums and flags, in a fixed order.
 __device__ __forceinline__ void block_partial(double ss, int of, double *out_ss,
                                               int32_t *out_of) {
-    __shared__ double warp_ss[kBlock / 32];
+    __shared__ double warp_ss[32];
     of = __syncthreads_or(of);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_down_sync(0xFFFFFFFFu, ss, o);
@@ -521,20 +521,26 @@ reduce_kernel(const __grid_constant__ ReduceArgs a) {
 // covers the tile into a shared-memory slot, so DRAM sees only whole 64-byte
 // units.  A thread then re-aligns its 8 elements from the slot (one 16-byte
 // shared load when the row's offset is a multiple of 16 bytes, else two and a
-// funnel shift).  Rows come in groups of kRows per stage, two stages in
-// flight, completion tracked by one mbarrier per stage.  The arithmetic per
-// element is that of reduce_kernel: contributions added in contributor order.
-// Every mbarrier wait is bounded (one second); a block that gives up sets the
-// error word, counts as an overflow (so the step is skipped) and waits, again
-// bounded, for its copies before it exits.
+// funnel shift).  Rows come in groups of kRows per stage, kStages stages in a
+// ring.  One producer warp issues the copies -- one row per lane, after one
+// lane has posted the stage's byte count on its `full` mbarrier -- and waits
+// on the stage's `empty` mbarrier, on which each of the eight consumer warps
+// arrives once it has read the stage; consumers wait on `full`.  No block-wide
+// barrier sits inside the loop.  The arithmetic per element is that of
+// reduce_kernel: contributions added in contributor order.
+// Every wait is bounded (one second) and also ends when another warp has
+// raised the block's abort flag; a block that gives up sets the error word,
+// counts as an overflow (so the step is skipped) and waits, again bounded, for
+// the copies it issued before it exits.
 template <int kIn> struct StageTraits {
     static constexpr int kE = kIn == kInF32 ? 4 : 2;          // bytes per element
     static constexpr int kRows = kIn == kInF32 ? 4 : 8;       // rows per stage
     static constexpr int kSlot = kStageTile * kE + 64;        // bytes per row slot
     static constexpr int kStages = 2;
-    static constexpr int kHeader = 128;                       // the mbarriers
+    static constexpr int kHeader = 128;                       // mbarriers, abort flag
     static constexpr int kSmem = kHeader + kStages * kRows * kSlot;
 };
+constexpr int kStagedThreads = kBlock + 32;                   // 8 consumer warps + 1 producer
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -545,9 +551,12 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_init_fence() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     uint32_t done;
@@ -571,6 +580,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     const uint64_t t0 = global_ns();
     while (!mbar_test(bar, parity))
         if (global_ns() - t0 > 1000000000ull) return false;
+    return true;
+}
+// The same, giving up early once *abort is set; a wait that runs out sets it.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity,
+                                                   volatile int *abort) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_test(bar, parity)) {
+        if (*abort) return false;
+        if (global_ns() - t0 > 1000000000ull) {
+            *abort = 1;
+            return false;
+        }
+    }
     return true;
 }
 // Order this thread's earlier generic-proxy accesses of shared memory before
@@ -650,13 +673,17 @@ __device__ __forceinline__ void staged_elems(const unsigned char *slot, uint32_t
 }
 
 template <int kIn, int kMode>
-__global__ void __launch_bounds__(kBlock, 3) reduce_staged_kernel(const __grid_constant__ ReduceArgs a) {
+__global__ void __launch_bounds__(kStagedThreads, 3)
+reduce_staged_kernel(const __grid_constant__ ReduceArgs a) {
     using T = typename InTraits<kIn>::T;
     using ST = StageTraits<kIn>;
-    constexpr int kE = ST::kE, kR = ST::kRows, kSlot = ST::kSlot;
+    constexpr int kE = ST::kE, kR = ST::kRows, kSlot = ST::kSlot, kS = ST::kStages;
     constexpr bool kNorm = kMode == kModeStep;
+    constexpr uint32_t kFull = 0xFFFFFFFFu;
     extern __shared__ __align__(128) unsigned char smem[];
-    const uint32_t bar0 = smem_u32(smem);                     // stage s barrier at bar0 + 8*s
+    const uint32_t full0 = smem_u32(smem);                    // full[s] at full0 + 8*s
+    const uint32_t empty0 = full0 + 8u * kS;                  // empty[s] at empty0 + 8*s
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + 16 * kS);
     unsigned char *slots = smem + ST::kHeader;
 
     const int j = blockIdx.y;
@@ -678,58 +705,65 @@ __global__ void __launch_bounds__(kBlock, 3) reduce_staged_kernel(const __grid_c
     const int64_t my_tiles =
         (int64_t)blockIdx.x < n_tiles ? (n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     const int64_t n_jobs = my_tiles * groups;           // job = (tile of this block, row group)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool producer = warp == kBlock / 32;
 
     // byte address of row c's element i (of this rank's slice)
     auto row_addr = [&](int c, int64_t i) {
         return bbase + ((int64_t)c * ld + i) * kE;
     };
-    auto issue = [&](int64_t job, int stage) {          // thread 0
-        const int64_t q = job / groups;
-        const int gi = (int)(job - q * groups);
-        const int64_t i0 = (blockIdx.x + q * gridDim.x) * (int64_t)kStageTile;
-        const int c0 = gi * kR;
-        const int nr = N - c0 < kR ? N - c0 : kR;
-        uint32_t total = 0;
-        for (int r = 0; r < nr; ++r) {
-            const uintptr_t A = (uintptr_t)row_addr(c0 + r, i0);
-            const uintptr_t lo = A & ~(uintptr_t)63;
-            const uintptr_t hi = (A + (uintptr_t)kStageTile * kE + 63) & ~(uintptr_t)63;
-            total += (uint32_t)(hi - lo);
-        }
-        const uint32_t bar = bar0 + 8u * stage;
-        mbar_expect_tx(bar, total + a.tx_pad);
-        for (int r = 0; r < nr; ++r) {
-            const uintptr_t A = (uintptr_t)row_addr(c0 + r, i0);
-            const uintptr_t lo = A & ~(uintptr_t)63;
-            const uintptr_t hi = (A + (uintptr_t)kStageTile * kE + 63) & ~(uintptr_t)63;
-            bulk_g2s(smem_u32(slots + (stage * kR + r) * kSlot), reinterpret_cast<const void *>(lo),
-                     (uint32_t)(hi - lo), bar);
-        }
-    };
 
     if (threadIdx.x == 0) {
-        mbar_init(bar0, 1);
-        mbar_init(bar0 + 8, 1);
+        for (int s = 0; s < kS; ++s) {
+            mbar_init(full0 + 8u * s, 1);                     // the producer's one arrive
+            mbar_init(empty0 + 8u * s, kBlock / 32);          // one arrive per consumer warp
+        }
+        *abort = 0;
         mbar_init_fence();
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        if (n_jobs > 0) issue(0, 0);
-        if (n_jobs > 1) issue(1, 1);
-    }
 
     NormAcc na;
     int of = 0;
-    float x[kVec];
-    uint32_t parity = 0u;                                       // bit s: stage s's wait parity
-    int64_t job = 0;
-    bool failed = false;
-    bool my_ok = true;                                          // this thread's last wait
-    for (; job < n_jobs; ++job) {
-        const int stage = (int)(job & 1);
-        my_ok = mbar_wait_bounded(bar0 + 8u * stage, (parity >> stage) & 1u);
-        if (my_ok) {
-            parity ^= 1u << stage;
+    int64_t issued = 0;                                       // producer: jobs issued
+    if (producer) {
+        for (int64_t job = 0; job < n_jobs; ++job) {
+            const int stage = (int)(job % kS);
+            if (job >= kS) {                                  // the stage's last readers are done
+                const bool ok = mbar_wait_or_abort(empty0 + 8u * stage,
+                                                   (uint32_t)((job / kS - 1) & 1), abort);
+                if (!__all_sync(kFull, ok)) break;
+            }
+            const int64_t q = job / groups;
+            const int gi = (int)(job - q * groups);
+            const int64_t i0 = (blockIdx.x + q * gridDim.x) * (int64_t)kStageTile;
+            const int c0 = gi * kR;
+            const int nr = N - c0 < kR ? N - c0 : kR;
+            uintptr_t lo = 0;
+            uint32_t bytes = 0;
+            if (lane < nr) {
+                const uintptr_t A = (uintptr_t)row_addr(c0 + lane, i0);
+                lo = A & ~(uintptr_t)63;
+                bytes = (uint32_t)(((A + (uintptr_t)kStageTile * kE + 63) & ~(uintptr_t)63) - lo);
+            }
+            const uint32_t total = __reduce_add_sync(kFull, bytes);
+            const uint32_t bar = full0 + 8u * stage;
+            if (lane == 0) mbar_arrive_expect_tx(bar, total + a.tx_pad);
+            __syncwarp();
+            if (lane < nr) {
+                fence_proxy_async();
+                bulk_g2s(smem_u32(slots + (stage * kR + lane) * kSlot),
+                         reinterpret_cast<const void *>(lo), bytes, bar);
+            }
+            issued = job + 1;
+        }
+    } else {
+        float x[kVec];
+        for (int64_t job = 0; job < n_jobs; ++job) {
+            const int stage = (int)(job % kS);
+            const bool ok = mbar_wait_or_abort(full0 + 8u * stage, (uint32_t)((job / kS) & 1),
+                                               abort);
+            if (!__all_sync(kFull, ok)) break;
             const int64_t q = job / groups;
             const int gi = (int)(job - q * groups);
             const int64_t t0 = (blockIdx.x + q * gridDim.x) * (int64_t)kStageTile;
@@ -748,6 +782,8 @@ __global__ void __launch_bounds__(kBlock, 3) reduce_staged_kernel(const __grid_c
                     for (int e = 0; e < kVec; ++e) x[e] = __fadd_rn(x[e], f[e]);
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8u * stage);   // this warp is done reading
             if (gi == groups - 1) {                             // the tile's elements are reduced
                 const int64_t i0 = t0 + (int64_t)threadIdx.x * kVec;
 #pragma unroll
@@ -773,23 +809,17 @@ __global__ void __launch_bounds__(kBlock, 3) reduce_staged_kernel(const __grid_c
                 }
             }
         }
-        // one barrier per job: every read of the stage is done (it may be
-        // refilled) and a timed-out wait anywhere in the block is seen by all
-        if (__syncthreads_or(!my_ok)) { failed = true; break; }
-        if (threadIdx.x == 0 && job + 2 < n_jobs) {
-            fence_proxy_async();
-            issue(job + 2, stage);
-        }
     }
-    if (failed) {
+    __syncthreads();                                            // every warp is out of its loop
+    if (*abort) {
         // give the copies still in flight a bounded chance to land before the
-        // block's shared memory goes away: this job's (unless thread 0 saw it
-        // complete) and the next one's
-        if (threadIdx.x == 0) {
-            for (int64_t k = my_ok ? job + 1 : job; k < job + 2 && k < n_jobs; ++k)
-                mbar_wait_bounded(bar0 + 8u * (uint32_t)(k & 1), (parity >> (k & 1)) & 1u);
-            atomicExch(a.err, 1);
+        // block's shared memory goes away: the last job issued on each stage
+        // (no later job was issued there, so its phase parity identifies it)
+        if (producer && lane == 0) {
+            for (int64_t k = issued > kS ? issued - kS : 0; k < issued; ++k)
+                mbar_wait_bounded(full0 + 8u * (uint32_t)(k % kS), (uint32_t)((k / kS) & 1));
         }
+        if (threadIdx.x == 0) atomicExch(a.err, 1);
         of = 1;
         __syncthreads();
     }
@@ -1122,7 +1152,7 @@ static cudaError_t launch_staged(const ReduceArgs &a, dim3 grid, cudaStream_t s)
     cudaError_t e = cudaFuncSetAttribute(reduce_staged_kernel<kIn, kMode>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    reduce_staged_kernel<kIn, kMode><<<grid, kBlock, kSmem, s>>>(a);
+    reduce_staged_kernel<kIn, kMode><<<grid, kStagedThreads, kSmem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -1232,7 +1262,7 @@ static cudaError_t occ(bool staged, int *bps) {
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return e;
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, reduce_staged_kernel<kIn, kMode>,
-                                                             kBlock, kSmem);
+                                                             kStagedThreads, kSmem);
     }
 }
 
