@@ -539,6 +539,9 @@ template <int kIn> struct StageTraits {
     static constexpr int kStages = 2;
     static constexpr int kHeader = 128;                       // mbarriers, abort flag
     static constexpr int kSmem = kHeader + kStages * kRows * kSlot;
+    // full[kStages] and empty[kStages] (8 bytes each), then the abort flag:
+    // all before the first slot
+    static_assert(16 * kStages + 4 <= kHeader, "stage header overlaps the slots");
 };
 constexpr int kStagedThreads = kBlock + 32;                   // 8 consumer warps + 1 producer
 
@@ -862,6 +865,26 @@ struct AdamConst {
     float b1, b2, omb1, omb2, lr, eps, decay, coef, bc1, bc2;
 };
 
+// a / b, correctly rounded, given y = RN(1/b) (the int8 quantizer divides a
+// block's values by its scale), by Markstein's correction
+// (P. Markstein, IBM J. Res. Dev. 34(1), 1990): when q is a faithful
+// approximation of a/b and y approximates 1/b within a relative 2^-24, the
+// remainder r = a - q*b is exact in one fma and RN(q + r*y) = RN(a/b).
+// q0 = RN(a*y) can be up to ~1.5 ulp off (not always faithful), so one
+// correction brings q1 within ~2e-7 ulp of a/b (faithful) and a second one
+// gives the IEEE quotient.  Taken while a, the quotient and the remainders
+// stay normal (2^-100 <= |a| <= 2^100, b and y in [2^-100, 2^100]);
+// otherwise IEEE division.
+__device__ __forceinline__ float div_known_recip(float a, float b, float y) {
+    const float aa = fabsf(a);
+    if (aa >= 0x1p-100f && aa <= 0x1p100f) {
+        const float q0 = __fmul_rn(a, y);
+        const float q1 = __fmaf_rn(__fmaf_rn(-q0, b, a), y, q0);
+        return __fmaf_rn(__fmaf_rn(-q1, b, a), y, q1);
+    }
+    return __fdiv_rn(a, b);
+}
+
 // One element, in the order of the equations: clip, moments, bias
 // correction, decoupled decay, Adam step (lr*mh)/(sqrt(vh)+eps).
 __device__ __forceinline__ void adam_elem(float g, float &th, float &m, float &v,
@@ -1099,11 +1122,9 @@ __global__ void __launch_bounds__(kBlock) adamw_q8_kernel(const __grid_constant_
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
         const float scale = __fdiv_rn(amax, 127.0f);
-        // p / scale, correctly rounded, by Markstein's correction (P. Markstein,
-        // IBM J. Res. Dev. 34(1), 1990): with y = RN(1/scale) and q0 = RN(p*y)
-        // within an ulp of p/scale, RN(q0 + r*y) with the exact remainder
-        // r = p - q0*scale (one fma) is the IEEE quotient.  Used when scale,
-        // 1/scale and the quotients stay normal; IEEE division otherwise.
+        // p / scale, correctly rounded: Markstein's correction from
+        // y = RN(1/scale) (div_known_recip) while scale, 1/scale and the
+        // quotients stay normal; IEEE division otherwise.
         const bool fast = scale >= 0x1p-100f && scale <= 0x1p100f;
         const float y = fast ? __frcp_rn(scale) : 0.0f;
         int8_t q[kVec];
@@ -1111,15 +1132,8 @@ __global__ void __launch_bounds__(kBlock) adamw_q8_kernel(const __grid_constant_
         for (int e = 0; e < kVec; ++e) {
             int code = 0;
             if (scale != 0.0f) {
-                float v;
                 const float pe = P[e];
-                if (fast && fabsf(pe) >= 0x1p-100f) {
-                    const float q0 = __fmul_rn(pe, y);
-                    const float r = __fmaf_rn(-q0, scale, pe);
-                    v = __fmaf_rn(r, y, q0);
-                } else {
-                    v = __fdiv_rn(pe, scale);
-                }
+                const float v = fast ? div_known_recip(pe, scale, y) : __fdiv_rn(pe, scale);
                 if (!isnan(v)) {
                     code = __float2int_rn(v);                  // half to even; saturates
                     code = code > 127 ? 127 : (code < -127 ? -127 : code);
