@@ -76,7 +76,7 @@ def parse_args(argv=None):
     p.add_argument("--group-params", type=int, default=1_000_000,
                    help="params in each group member's shard")
     p.add_argument("--no-workloads", action="store_true",
-                   help="skip the other configs' steps (gpt2_small, gpt_1p5b_rank17, "
+                   help="skip the other configs' steps (tiny_mlp, gpt2_small, gpt_1p5b_rank17, "
                         "llama_7b_rank0) reported beside the headline workload")
     p.add_argument("--workload-steps", type=int, default=20,
                    help="timed steps of each of those configs")
@@ -510,7 +510,7 @@ def run_ours(args, w):
 
 # The configs reported beside the headline step (each its own FlatParameter,
 # stepped alone on the device after the headline workload has been freed).
-SIDE_WORKLOADS = ("gpt2_small", "gpt_1p5b_rank17", "llama_7b_rank0")
+SIDE_WORKLOADS = ("tiny_mlp", "gpt2_small", "gpt_1p5b_rank17", "llama_7b_rank0")
 
 
 def measure_workload(w, steps, warmup, dev):
