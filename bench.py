@@ -80,6 +80,11 @@ def parse_args(argv=None):
                         "llama_7b_rank0) reported beside the headline workload")
     p.add_argument("--workload-steps", type=int, default=20,
                    help="timed steps of each of those configs")
+    p.add_argument("--collective", action="store_true",
+                   help="time the rank step among real processes (RankStep over NCCL, one "
+                        "rank per GPU under torchrun) instead of the single-GPU emulation")
+    p.add_argument("--collective-shard", type=int, default=1_250_000_000,
+                   help="params in each rank's shard for --collective (weak scaling)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -87,8 +92,8 @@ def parse_args(argv=None):
     p.add_argument("--ref-seconds", type=float, default=120.0,
                    help="target length of the whole --impl reference run")
     args = p.parse_args(argv)
-    if bool(args.q8) + (args.micro_steps > 1) + bool(args.offload) > 1:
-        p.error("--q8, --micro-steps K > 1 and --offload exclude one another")
+    if bool(args.q8) + (args.micro_steps > 1) + bool(args.offload) + bool(args.collective) > 1:
+        p.error("--q8, --micro-steps K > 1, --offload and --collective exclude one another")
     return args
 
 
@@ -282,6 +287,85 @@ def cpu_baseline(w, target_s):
 
 
 # ---------------------------------------------------------------- arms
+def run_collective(args):
+    """The rank step among real processes: each rank (one process per GPU,
+    NCCL) steps its own shard of an N-rank FlatParameter with RankStep -- the
+    all-to-all of the gradient slices, the fp32 reduce over the N received
+    rows, the all-gather of every rank's norm^2 and overflow flag, the
+    decision, AdamW, and the all-gather of the 16-bit slots.  Weak scaling:
+    every rank's shard holds --collective-shard params (the 10B config's 1.25e9
+    by default), so the model is N times that; each rank generates its own
+    contribution (the whole flat fp16 gradient of N shards)."""
+    import torch
+    import torch.distributed as dist
+
+    import fsdp_sharded_mixed_zero_gb300 as Z
+    import synth
+    from fsdp_sharded_mixed_zero_gb300.dist import RankStep
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    else:
+        dist.init_process_group("nccl", init_method="tcp://127.0.0.1:%d" % _free_port(),
+                                rank=0, world_size=1, device_id=dev)
+    S = args.collective_shard
+    full = S * world
+    flat = Z.ZeroFlat([(full,)], world, Z.ZERO_F16, Z.ZERO_F16, Z.ZERO_AVG, Z.hparams())
+    stream = torch.cuda.current_stream(dev)
+    scale = flat.scaler_state().scale
+    grads = torch.empty((1, full), dtype=torch.float16, device=dev)
+    synth.grads_device(grads, 11, 0, 0, full, 2e-4, 2e-4, scale, synth.F16, c0=rank, n_contrib=1)
+    master = torch.empty(S, device=dev)
+    synth.normal_device(master, 11, synth.MASTER, rank * S, 0.02)
+    m = torch.zeros(S, device=dev)
+    v = torch.zeros(S, device=dev)
+    out = torch.zeros(full, dtype=torch.float16, device=dev)
+    step = RankStep(flat, rank, grad_dtype=Z.ZERO_F16, device=dev)
+    for _ in range(args.warmup):
+        step.step(grads.view(-1), master, m, v, out, stream=stream, want_result=False)
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step.step(grads.view(-1), master, m, v, out, stream=stream, want_result=False)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    t = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    elapsed_ms = float(t.item())
+    res = step.step(grads.view(-1), master, m, v, out, stream=stream, want_result=True)
+    assert res.skipped == 0 and res.overflow == 0, "benchmark inputs overflowed"
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": whole_job_value(S, args.steps, world, elapsed_ms),
+            "unit": "Gparams/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "rank_step_%d_params_per_rank" % S,
+                       "params_stepped_per_gpu": S, "world_size": world,
+                       "storage": "f16 grads, f16 params, f32 master/m/v",
+                       "exchanges": "NCCL all-to-all of 16-bit slices, all-gather of "
+                                    "(norm^2, flag), all-gather of 16-bit slots",
+                       "parallelism": "zero%d" % world},
+            # per step: the reduce, the decision, AdamW (the NCCL kernels are not ours)
+            "gpu_launches": 3 * args.steps}), flush=True)
+    flat.close()
+    dist.destroy_process_group()
+
+
+def _free_port():
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
 def run_reference(args, w):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -925,6 +1009,8 @@ def main():
         run_group(args)
     elif args.offload:
         run_offload(args, w)
+    elif args.collective:
+        run_collective(args)
     else:
         run_ours(args, w)
 

@@ -8,7 +8,9 @@ process waits on the other.  On every rank and every step, the result, the
 loss-scale state, the rank's master / m / v and the whole gathered flat
 buffer are compared with the oracle's step of all shards at once on the
 stacked contributions, at the parity tolerances; one rank's inf must make
-both ranks skip and halve the scale."""
+both ranks skip and halve the scale.  A last test runs one rank over NCCL
+(a one-rank communicator on this GPU): the device-tensor branch of every
+exchange, with no host staging, against the oracle."""
 import os
 import socket
 import sys
@@ -111,3 +113,59 @@ def test_two_ranks_on_gloo_match_the_all_shards_step(case):
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
     mp.start_processes(_worker, args=(_free_port(), case), nprocs=WORLD, start_method="spawn")
+
+
+def _nccl_worker(rank, port):
+    """One rank over NCCL (a one-rank communicator on this GPU): the device-
+    tensor branch of every exchange (no host staging, in-place slot all-gather)
+    against the oracle's step."""
+    if ROOT not in sys.path:
+        sys.path.insert(0, ROOT)
+    torch.cuda.set_device(0)
+    tdist.init_process_group("nccl", init_method="tcp://127.0.0.1:%d" % port, rank=0,
+                             world_size=1, device_id=torch.device("cuda", 0))
+    import fsdp_sharded_mixed_zero_gb300 as Z
+    import oracle
+    import synth
+    from fsdp_sharded_mixed_zero_gb300.dist import RankStep
+    from tests.gpu_helpers import assert_params_close, assert_result, assert_state, f32, u16
+
+    assert tdist.get_backend() == "nccl"
+    full = 300_007
+    kw = dict(lr=1e-3, window=2, initial_scale_power=10)
+    flat = Z.ZeroFlat([(full,)], 1, F16, F16, AVG, Z.hparams(**kw))
+    ohp = oracle.hparams(**kw)
+    S = flat.shard_size
+    step_of = RankStep(flat, 0, grad_dtype=F16)
+    master = torch.empty(S, device="cuda")
+    synth.normal_device(master, 43, synth.MASTER, 0, 0.02)
+    m = torch.zeros(S, device="cuda")
+    v = torch.zeros(S, device="cuda")
+    out = torch.zeros(S, dtype=torch.float16, device="cuda")
+    o_state = [[f32(master).copy()], [np.zeros(S, np.float32)], [np.zeros(S, np.float32)]]
+    o_out = np.zeros(S, np.uint16)
+    o_st = oracle.scaler_init(ohp)
+    g = torch.empty((1, S), dtype=torch.float16, device="cuda")
+    for step in range(3):
+        scale = flat.scaler_state().scale
+        synth.grads_device(g, 43, step, 0, S, 1e-3, 1e-3, scale, synth.F16)
+        if step == 1:
+            g[0, 5] = float("inf")
+        scale_used = o_st.scale
+        ro = oracle.shard_step(ohp, o_st, 1, full, S, [0], u16(g), S, 0, *o_state, o_out)
+        res = step_of.step(g.view(-1), master, m, v, out)
+        assert_result(res, (ro.overflow, ro.skipped, ro.grad_norm, ro.clip_coef, scale_used))
+        assert flat.scaler_state().as_tuple() == o_st.as_tuple()
+        assert_state(f32(master), f32(m), f32(v), *(x[0] for x in o_state), tag=" %d" % step)
+        assert_params_close(u16(out), o_out, False, "flat buffer (step %d)" % step)
+    assert o_st.overflow_count == 1
+    flat.close()
+    tdist.destroy_process_group()
+
+
+def test_one_rank_over_nccl_matches_the_oracle():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    if not tdist.is_nccl_available():
+        pytest.skip("no NCCL in this torch build")
+    mp.start_processes(_nccl_worker, args=(_free_port(),), nprocs=1, start_method="spawn")
