@@ -20,12 +20,19 @@ roofline: the dominant kernel's algorithmic bytes per launch over its mean
 event-timed duration, against the measured HBM copy peak.
 cpu_baseline: the oracle (plain single-threaded C) on a bounded sample of the
 same workload, timed on this host.
+workloads (default workload, N = 1): the tiny MLP, GPT-2-small, 1.5B and 7B
+configs' steps measured in the same run, each with its kernels' achieved GB/s
+and its dominant kernel's fraction of the measured copy peak.
 --impl reference: the oracle on the host cores as the reference arm.
 --offload: the ZeRO-Offload step instead (zero_shard_step_offload: reduce and
 decision on the GPU, AdamW over host-resident fp32 state on the host cores),
 its own JSON line with the per-phase times and the host update against the
 host copy bandwidth measured in the same run.
-Under torchrun each rank runs an independent replica (weak scaling).
+--collective: the rank step among real processes (RankStep over NCCL: the
+all-to-all of the gradient slices, the reduce, the all-gather of every rank's
+norm^2 and overflow flag, AdamW, the all-gather of the 16-bit slots), one
+rank per GPU under torchrun, weak scaling.
+Otherwise, under torchrun each rank runs an independent replica (weak scaling).
 """
 import argparse
 import hashlib
