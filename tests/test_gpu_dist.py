@@ -24,13 +24,16 @@ import torch.multiprocessing as mp  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-F16, BF16, SUM, AVG = 0, 1, 0, 1
+F16, BF16, F32, SUM, AVG = 0, 1, 2, 0, 1
 
 CASES = [
     # odd shard: rank 1's slice and the received rows are off 16-byte boundaries
     dict(name="fp16_avg_dynamic_ragged", full=1_000_003, dtype=F16, op=AVG, dynamic=True),
     # every row 64-byte aligned: the vectorised reduce
     dict(name="bf16_sum_static_aligned", full=2 * 262_144, dtype=BF16, op=SUM, dynamic=False),
+    # fp32 contributions (a reduce_dtype=float32 reduce-scatter), fp16 parameters
+    dict(name="fp32_contributions_avg", full=700_001, dtype=F16, gdtype=F32, op=AVG,
+         dynamic=True),
 ]
 WORLD, STEPS, INF_STEP = 2, 4, 2
 
@@ -54,13 +57,15 @@ def _worker(rank, port, case):
     from tests.gpu_helpers import assert_params_close, assert_result, assert_state, f32, u16
 
     full, dt, bf16 = case["full"], case["dtype"], case["dtype"] == BF16
+    gdt = case.get("gdtype", dt)
     kw = dict(dynamic=case["dynamic"], lr=1e-3, window=3, initial_scale_power=12)
-    flat = Z.ZeroFlat([(full,)], WORLD, dt, dt, case["op"], Z.hparams(**kw))
+    flat = Z.ZeroFlat([(full,)], WORLD, gdt, dt, case["op"], Z.hparams(**kw))
     ohp = oracle.hparams(**kw)
     S, padded = flat.shard_size, flat.padded_numel
     tdt = torch.bfloat16 if bf16 else torch.float16
-    sdt = synth.BF16 if bf16 else synth.F16
-    step_of = RankStep(flat, rank, grad_dtype=dt)
+    gtdt = torch.float32 if gdt == F32 else tdt
+    sdt = synth.F32 if gdt == F32 else (synth.BF16 if bf16 else synth.F16)
+    step_of = RankStep(flat, rank, grad_dtype=gdt)
     # this rank's shard, and the oracle's copy of every shard
     master_all = torch.empty(padded, device="cuda")
     synth.normal_device(master_all, 41, synth.MASTER, 0, 0.02)
@@ -74,8 +79,8 @@ def _worker(rank, port, case):
                [np.zeros(S, np.float32) for _ in range(WORLD)]]
     o_out = np.zeros(padded, np.uint16)
     o_st = oracle.scaler_init(ohp)
-    mine = torch.empty((1, padded), dtype=tdt, device="cuda")
-    everyone = torch.empty((WORLD, padded), dtype=tdt, device="cuda")
+    mine = torch.empty((1, padded), dtype=gtdt, device="cuda")
+    everyone = torch.empty((WORLD, padded), dtype=gtdt, device="cuda")
     for step in range(STEPS):
         scale = flat.scaler_state().scale
         assert scale == o_st.scale
@@ -88,8 +93,9 @@ def _worker(rank, port, case):
             everyone[1, 777] = float("inf")
             if rank == 1:
                 mine[0, 777] = float("inf")
-        assert torch.equal(mine[0].view(torch.int16), everyone[rank].view(torch.int16))
-        g_host = u16(everyone)
+        assert torch.equal(mine[0], everyone[rank]) if gdt == F32 else \
+            torch.equal(mine[0].view(torch.int16), everyone[rank].view(torch.int16))
+        g_host = everyone.cpu().numpy() if gdt == F32 else u16(everyone)
         scale_used = o_st.scale
         ro = oracle.shard_step(ohp, o_st, WORLD, full, S, list(range(WORLD)), g_host, padded, S,
                                *o_state, o_out, avg=case["op"] == AVG, grad_is_bf16=bf16,
