@@ -134,15 +134,21 @@ class RankStep:
         grad dtype); master, m, v: this rank's fp32 shard (S elements each);
         out: the flat 16-bit parameter buffer (padded_numel elements), slot
         `rank` written by the update and, with gather, every slot refreshed
-        from its owner.  Returns the step result (want_result) or None."""
+        from its owner.  stream: the CUDA stream every part of the step runs
+        on -- the library's kernels, the collectives and the staging copies
+        (None: the current stream).  Returns the step result (want_result)
+        or None."""
+        stream = stream if stream is not None else torch.cuda.current_stream()
         r = [self.rank]
-        exchange_contributions(grads, self.recv, self.group, self.staging)
-        self.flat.reduce(r, self.recv, self.norm_sq, self.overflow, grad_rank_offset_mul=0,
-                         stream=stream)
-        gather_partials(self.norm_sq, self.all_norm_sq, self.group, self.staging, "ss")
-        gather_partials(self.overflow, self.all_overflow, self.group, self.staging, "of")
-        res = self.flat.apply_partials(r, [master], [m], [v], out, self.all_norm_sq,
-                                       self.all_overflow, stream=stream, want_result=want_result)
-        if gather:
-            gather_slots(out, self.rank, self.S, self.group, self.staging)
+        with torch.cuda.stream(stream):
+            exchange_contributions(grads, self.recv, self.group, self.staging)
+            self.flat.reduce(r, self.recv, self.norm_sq, self.overflow, grad_rank_offset_mul=0,
+                             stream=stream)
+            gather_partials(self.norm_sq, self.all_norm_sq, self.group, self.staging, "ss")
+            gather_partials(self.overflow, self.all_overflow, self.group, self.staging, "of")
+            res = self.flat.apply_partials(r, [master], [m], [v], out, self.all_norm_sq,
+                                           self.all_overflow, stream=stream,
+                                           want_result=want_result)
+            if gather:
+                gather_slots(out, self.rank, self.S, self.group, self.staging)
         return res
