@@ -152,6 +152,7 @@ def _nccl_worker(rank, port):
     o_out = np.zeros(S, np.uint16)
     o_st = oracle.scaler_init(ohp)
     g = torch.empty((1, S), dtype=torch.float16, device="cuda")
+    side = torch.cuda.Stream()
     for step in range(3):
         scale = flat.scaler_state().scale
         synth.grads_device(g, 43, step, 0, S, 1e-3, 1e-3, scale, synth.F16)
@@ -159,7 +160,9 @@ def _nccl_worker(rank, port):
             g[0, 5] = float("inf")
         scale_used = o_st.scale
         ro = oracle.shard_step(ohp, o_st, 1, full, S, [0], u16(g), S, 0, *o_state, o_out)
-        res = step_of.step(g.view(-1), master, m, v, out)
+        side.wait_stream(torch.cuda.current_stream())
+        res = step_of.step(g.view(-1), master, m, v, out, stream=side)   # not the current stream
+        side.synchronize()
         assert_result(res, (ro.overflow, ro.skipped, ro.grad_norm, ro.clip_coef, scale_used))
         assert flat.scaler_state().as_tuple() == o_st.as_tuple()
         assert_state(f32(master), f32(m), f32(v), *(x[0] for x in o_state), tag=" %d" % step)
