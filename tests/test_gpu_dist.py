@@ -1,5 +1,5 @@
-"""The multi-rank step with the library's kernels: two processes, one rank
-each, joined by a gloo group on 127.0.0.1 and sharing this one GPU.  Each
+"""The multi-rank step with the library's kernels: two (or three) processes,
+one rank each, joined by a gloo group on 127.0.0.1 and sharing this one GPU.  Each
 process steps only its own shard (RankStep: the all-to-all of the
 reduce-scatter, zero_shard_reduce, the all-gather of the two scalars,
 zero_shard_apply_partials, the all-gather of the 16-bit slots); every
@@ -34,8 +34,10 @@ CASES = [
     # fp32 contributions (a reduce_dtype=float32 reduce-scatter), fp16 parameters
     dict(name="fp32_contributions_avg", full=700_001, dtype=F16, gdtype=F32, op=AVG,
          dynamic=True),
+    # three ranks, three processes
+    dict(name="three_ranks_fp16_avg", full=900_005, dtype=F16, op=AVG, dynamic=True, world=3),
 ]
-WORLD, STEPS, INF_STEP = 2, 4, 2
+STEPS, INF_STEP = 4, 2
 
 
 def _free_port():
@@ -48,6 +50,7 @@ def _worker(rank, port, case):
     if ROOT not in sys.path:
         sys.path.insert(0, ROOT)
     torch.cuda.set_device(0)
+    WORLD = case.get("world", 2)
     tdist.init_process_group("gloo", init_method="tcp://127.0.0.1:%d" % port, rank=rank,
                              world_size=WORLD)
     import fsdp_sharded_mixed_zero_gb300 as Z
@@ -118,7 +121,8 @@ def _worker(rank, port, case):
 def test_two_ranks_on_gloo_match_the_all_shards_step(case):
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
-    mp.start_processes(_worker, args=(_free_port(), case), nprocs=WORLD, start_method="spawn")
+    mp.start_processes(_worker, args=(_free_port(), case), nprocs=case.get("world", 2),
+                       start_method="spawn")
 
 
 def _nccl_worker(rank, port):

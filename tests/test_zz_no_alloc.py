@@ -30,7 +30,7 @@ from tests.gpu_helpers import (assert_params_close, assert_result, assert_state,
 
 pytestmark = pytest.mark.gpu
 
-F16, BF16, SUM, AVG = 0, 1, 0, 1
+F16, BF16, F32, SUM, AVG = 0, 1, 2, 0, 1
 INF_CALL = 1
 CASES = [
     # all four shards of a ragged FlatParameter, fp16, AVG, dynamic loss scale;
@@ -45,6 +45,10 @@ CASES = [
     # vectorised reduce), fp16, AVG, dynamic
     dict(name="all_shards_fp16_aligned", full=4 * 65_536, N=4, ranks=[0, 1, 2, 3], dtype=F16,
          op=AVG, dynamic=True, layout="full"),
+    # fp32 contributions (reduce_dtype=float32) and fp16 parameters; odd shard:
+    # 4-byte-aligned rank slices (the staged reduce's fp32 form)
+    dict(name="two_shards_fp32_contributions", full=400_001, N=3, ranks=[0, 2], dtype=F16,
+         gdtype=F32, op=AVG, dynamic=True, layout="full"),
 ]
 
 
@@ -54,7 +58,8 @@ def _setup(case):
     padded = S * N
     tdt = torch.float16 if case["dtype"] == F16 else torch.bfloat16
     ld = padded if case["layout"] == "full" else -(-S // 8) * 8
-    grads = torch.empty((N, ld), dtype=tdt, device="cuda")
+    gtdt = torch.float32 if case.get("gdtype") == F32 else tdt
+    grads = torch.empty((N, ld), dtype=gtdt, device="cuda")
     states = []
     for _ in range(2):                                   # identical copies: A and B
         master = []
@@ -72,7 +77,8 @@ def _setup(case):
 
 
 def _gen(case, grads, S, step, scale):
-    dt = synth.F16 if case["dtype"] == F16 else synth.BF16
+    dt = synth.F32 if case.get("gdtype") == F32 else (
+        synth.F16 if case["dtype"] == F16 else synth.BF16)
     r0 = case["ranks"][0]
     if case["layout"] == "full":
         synth.grads_device(grads, 21, step, 0, grads.shape[1], 1e-3, 1e-3, scale, dt,
@@ -99,8 +105,9 @@ def test_noalloc_matches_handle_step_and_oracle(ora, case):
     hp = Z.hparams(**kw)
     ohp = ora.hparams(**kw)
     bf16 = case["dtype"] == BF16
+    gdt = case.get("gdtype", case["dtype"])
     S, padded, ld, grads, (A, B) = _setup(case)
-    flat = Z.ZeroFlat([(case["full"],)], case["N"], case["dtype"], case["dtype"], case["op"], hp)
+    flat = Z.ZeroFlat([(case["full"],)], case["N"], gdt, case["dtype"], case["op"], hp)
     state = Z.ScalerState(65536.0 if case["dynamic"] else 1.0, 0, 0, 0)
     mul = S if case["layout"] == "full" else 0
     stream = torch.cuda.current_stream()
@@ -120,7 +127,7 @@ def test_noalloc_matches_handle_step_and_oracle(ora, case):
             ra = flat.step(case["ranks"], grads, A[0], A[1], A[2], A[3],
                            grad_rank_offset_mul=mul)
             rb = Z.zero_shard_step_noalloc(
-                case["full"], case["N"], case["dtype"], case["dtype"], case["op"], hp, state,
+                case["full"], case["N"], gdt, case["dtype"], case["op"], hp, state,
                 case["ranks"], grads.data_ptr(), ld, mul, [t.data_ptr() for t in B[0]],
                 [t.data_ptr() for t in B[1]], [t.data_ptr() for t in B[2]], B[3].data_ptr(),
                 0.0, stream.cuda_stream)
