@@ -80,7 +80,8 @@ def test_torchrun_reference_arm_two_ranks():
 
 
 @pytest.mark.parametrize("argv", [["--q8", "--micro-steps", "2"], ["--offload", "--q8"],
-                                  ["--group", "4", "--offload", "--micro-steps", "3"]])
+                                  ["--group", "4", "--offload", "--micro-steps", "3"],
+                                  ["--collective", "--q8"], ["--collective", "--offload"]])
 def test_bench_rejects_step_forms_that_exclude_one_another(argv):
     """The step forms are refused at argument parsing, before any device work."""
     import bench
@@ -91,5 +92,6 @@ def test_bench_rejects_step_forms_that_exclude_one_another(argv):
 
 def test_bench_accepts_each_step_form_alone():
     import bench
-    for argv in ([], ["--q8"], ["--micro-steps", "4"], ["--offload"], ["--group", "8", "--q8"]):
+    for argv in ([], ["--q8"], ["--micro-steps", "4"], ["--offload"], ["--group", "8", "--q8"],
+                 ["--collective", "--collective-shard", "1000"]):
         bench.parse_args(argv)
