@@ -151,3 +151,40 @@ def test_split_misuse_is_refused():
         assert e.value.status == 3
     finally:
         d.close()
+
+
+def test_apply_partials_totals_thousands_of_partials():
+    """zero_shard_apply_partials with 5000 per-rank partials (the all-gathered
+    form of the cross-rank exchange): the decision kernel's fixed-order fp64
+    total matches the exactly rounded sum to ~1e-15, the clip coefficient
+    follows from it, and one set flag among them skips the step."""
+    _need_gpu()
+    import math
+    from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
+    w = _wl("partials", [(50_000,)], 1, [0], steps=1, layout="slice")
+    dw = DeviceWorkload(w)
+    ss, of = _totals()
+    rng = np.random.default_rng(3)
+    n = 5000
+    parts = rng.random(n) * rng.choice([1e-6, 1e-3, 1.0], n)       # magnitudes far apart
+    norm_sq = torch.from_numpy(parts).cuda()
+    try:
+        for overflow_at in (None, 4321):
+            flags = torch.zeros(n, dtype=torch.int32, device="cuda")
+            if overflow_at is not None:
+                flags[overflow_at] = 1
+            sc = dw.scaler()
+            dw.gen_grads(0, sc.scale)
+            dw.flat.reduce(w.ranks, dw.grads, ss, of, grad_rank_offset_mul=0)
+            res = dw.flat.apply_partials(w.ranks, dw.master, dw.m, dw.v, dw.out, norm_sq, flags)
+            if overflow_at is None:
+                norm = math.sqrt(math.fsum(parts))
+                assert (res.overflow, res.skipped) == (0, 0)
+                assert abs(res.grad_norm - norm) <= 1e-14 * norm, (res.grad_norm, norm)
+                coef = float(np.float32(1.0 / (norm + 1e-6)))
+                assert abs(res.clip_coef - coef) <= NORM_RTOL * coef
+            else:
+                assert (res.overflow, res.skipped) == (1, 1)
+                assert dw.scaler().scale == sc.scale / 2
+    finally:
+        dw.close()
