@@ -20,7 +20,8 @@ __all__ = [
     "zero_shard_step_noalloc", "zero_grad_accumulate", "zero_shard_step_accumulated",
     "zero_shard_step_q8", "ZERO_Q8_BLOCK", "zero_flat_set_lr", "zero_shard_step_offload",
     "zero_offload_adamw_host", "zero_debug_set_stage_tx_pad", "zero_shard_reduce",
-    "zero_shard_apply", "zero_shard_apply_partials", "GroupMember", "ZeroGroup", "zero_group_init", "zero_group_step",
+    "zero_shard_apply", "zero_shard_apply_partials", "zero_shard_apply_partials_q8",
+    "GroupMember", "ZeroGroup", "zero_group_init", "zero_group_step",
     "zero_group_step_q8", "zero_group_step_accumulated", "zero_group_step_offload",
     "zero_group_accumulate", "zero_group_loss_scaler_state", "zero_group_set_loss_scaler_state",
     "zero_group_set_lr", "zero_group_free",
@@ -134,6 +135,9 @@ def _load():
     L.zero_shard_apply_partials.argtypes = [vp, C.POINTER(i32), i32, C.POINTER(vp),
                                             C.POINTER(vp), C.POINTER(vp), vp, vp, vp, i32, vp,
                                             C.POINTER(StepResult)]
+    L.zero_shard_apply_partials_q8.argtypes = [vp, C.POINTER(i32), i32, C.POINTER(vp),
+                                               C.POINTER(vp), C.POINTER(vp), vp, vp, vp, vp, vp,
+                                               i32, vp, C.POINTER(StepResult)]
     L.zero_shard_step_offload.argtypes = [vp, C.POINTER(i32), i32, vp, i64, i64, C.POINTER(vp),
                                           C.POINTER(vp), C.POINTER(vp), vp, C.c_double, i32,
                                           C.c_double, vp, C.POINTER(StepResult)]
@@ -150,7 +154,7 @@ def _load():
                  "zero_shard_step_q8", "zero_flat_set_lr", "zero_shard_step_offload",
                  "zero_offload_adamw_host", "zero_debug_set_stage_tx_pad",
                  "zero_shard_reduce", "zero_shard_apply", "zero_shard_apply_partials",
-                 "zero_group_init", "zero_group_step",
+                 "zero_shard_apply_partials_q8", "zero_group_init", "zero_group_step",
                  "zero_group_loss_scaler_state", "zero_group_set_loss_scaler_state",
                  "zero_group_set_lr", "zero_group_free", "zero_group_accumulate",
                  "zero_group_step_accumulated", "zero_group_step_q8",
@@ -361,6 +365,24 @@ def zero_shard_apply_partials(h, ranks, master_ptrs, m_ptrs, v_ptrs, out_ptr, no
                                           C.c_void_p(stream),
                                           C.byref(res) if res is not None else None),
            "zero_shard_apply_partials")
+    return res
+
+
+def zero_shard_apply_partials_q8(h, ranks, master_ptrs, m_ptrs, v_ptrs, out_ptr, q8_ptr,
+                                 q8_scales_ptr, norm_sq_parts_ptr, overflow_parts_ptr, n_parts,
+                                 stream=0, want_result=True):
+    """zero_shard_apply_partials that also writes the int8 payload (out_ptr may be 0)."""
+    n = len(ranks)
+    r = (C.c_int32 * n)(*ranks)
+    arrs = [(C.c_void_p * n)(*p) for p in (master_ptrs, m_ptrs, v_ptrs)]
+    res = StepResult() if want_result else None
+    _check(_lib.zero_shard_apply_partials_q8(h, r, n, *arrs, C.c_void_p(out_ptr or None),
+                                             C.c_void_p(q8_ptr), C.c_void_p(q8_scales_ptr),
+                                             C.c_void_p(norm_sq_parts_ptr),
+                                             C.c_void_p(overflow_parts_ptr), n_parts,
+                                             C.c_void_p(stream),
+                                             C.byref(res) if res is not None else None),
+           "zero_shard_apply_partials_q8")
     return res
 
 
@@ -709,19 +731,26 @@ class ZeroFlat:
                                 stream.cuda_stream, want_result)
 
     def apply_partials(self, ranks, master, m, v, out, norm_sq_parts, overflow_parts,
-                       stream=None, want_result=True):
+                       stream=None, want_result=True, q8=None, q8_scales=None):
         """Second half from per-rank partials: norm_sq_parts float64 and
-        overflow_parts int32 CUDA tensors of equal length."""
+        overflow_parts int32 CUDA tensors of equal length.  q8 / q8_scales:
+        also write the int8 payload (out may then be None)."""
         import torch
         if stream is None:
             stream = torch.cuda.current_stream()
         assert norm_sq_parts.numel() == overflow_parts.numel()
         assert norm_sq_parts.is_contiguous() and overflow_parts.is_contiguous()
-        return zero_shard_apply_partials(self.handle, list(ranks), [t.data_ptr() for t in master],
-                                         [t.data_ptr() for t in m], [t.data_ptr() for t in v],
-                                         out.data_ptr(), norm_sq_parts.data_ptr(),
-                                         overflow_parts.data_ptr(), norm_sq_parts.numel(),
-                                         stream.cuda_stream, want_result)
+        ptrs = ([t.data_ptr() for t in master], [t.data_ptr() for t in m],
+                [t.data_ptr() for t in v])
+        if q8 is not None:
+            return zero_shard_apply_partials_q8(
+                self.handle, list(ranks), *ptrs, out.data_ptr() if out is not None else 0,
+                q8.data_ptr(), q8_scales.data_ptr(), norm_sq_parts.data_ptr(),
+                overflow_parts.data_ptr(), norm_sq_parts.numel(), stream.cuda_stream,
+                want_result)
+        return zero_shard_apply_partials(self.handle, list(ranks), *ptrs, out.data_ptr(),
+                                         norm_sq_parts.data_ptr(), overflow_parts.data_ptr(),
+                                         norm_sq_parts.numel(), stream.cuda_stream, want_result)
 
     def set_lr(self, lr):
         zero_flat_set_lr(self.handle, lr)

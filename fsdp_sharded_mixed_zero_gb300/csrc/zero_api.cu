@@ -614,17 +614,23 @@ ZERO_API zero_status zero_shard_reduce(zero_flat *h, const int32_t *ranks, int32
 }
 
 // The second half of a split step: the decision over n_parts (norm_sq[k],
-// overflow[k]) pairs in device memory, then AdamW and the cast.
+// overflow[k]) pairs in device memory, then AdamW and the cast (and, with
+// q8, the int8 payload: flat_param_out may then be NULL).
 static zero_status apply_parts(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
                                float *const *master, float *const *m, float *const *v,
                                void *flat_param_out, const double *norm_sq,
                                const int32_t *overflow, int32_t n_parts, void *stream,
-                               zero_step_result *res) {
+                               zero_step_result *res, bool q8 = false,
+                               int8_t *flat_q8_out = nullptr, float *q8_scales = nullptr) {
     if (!h) return fail(ZERO_ERR_INVALID_ARG, "handle is NULL");
     int32_t max_rank = 0;
     zero_status s;
     if ((s = check_ranks(h, ranks, n_ranks, &max_rank))) return s;
-    if ((s = check_update(h, n_ranks, master, m, v, flat_param_out, 0.0))) return s;
+    if ((s = check_update(h, n_ranks, master, m, v, flat_param_out, 0.0, q8))) return s;
+    if (q8 && (!flat_q8_out || !q8_scales))
+        return fail(ZERO_ERR_INVALID_ARG, "int8 outputs are NULL");
+    if (q8 && (uintptr_t)q8_scales % 4)
+        return fail(ZERO_ERR_ALIGNMENT, "q8_scales must be 4-byte aligned");
     if (!norm_sq || !overflow) return fail(ZERO_ERR_INVALID_ARG, "NULL total");
     if (n_parts < 1 || n_parts > (1 << 20))
         return fail(ZERO_ERR_INVALID_ARG, "n_parts must be in [1, 2^20]");
@@ -642,6 +648,10 @@ static zero_status apply_parts(zero_flat *h, const int32_t *ranks, int32_t n_ran
     ap.m = m;
     ap.v = v;
     ap.out = flat_param_out;
+    if (q8) {
+        ap.q8 = flat_q8_out;
+        ap.q8_scales = q8_scales;
+    }
     plan_adamw(h, ap, ranks, n_ranks);
     // the decision from the caller's partials, totalled by the decision kernel
     // in its fixed order
@@ -661,6 +671,15 @@ ZERO_API zero_status zero_shard_apply(zero_flat *h, const int32_t *ranks, int32_
     // one "partial" holding the caller's totals
     return apply_parts(h, ranks, n_ranks, master, m, v, flat_param_out, norm_sq, overflow, 1,
                        stream, res);
+}
+
+ZERO_API zero_status zero_shard_apply_partials_q8(
+    zero_flat *h, const int32_t *ranks, int32_t n_ranks, float *const *master, float *const *m,
+    float *const *v, void *flat_param_out, int8_t *flat_q8_out, float *q8_scales,
+    const double *norm_sq_parts, const int32_t *overflow_parts, int32_t n_parts, void *stream,
+    zero_step_result *res) {
+    return apply_parts(h, ranks, n_ranks, master, m, v, flat_param_out, norm_sq_parts,
+                       overflow_parts, n_parts, stream, res, true, flat_q8_out, q8_scales);
 }
 
 ZERO_API zero_status zero_shard_apply_partials(zero_flat *h, const int32_t *ranks,

@@ -21,7 +21,9 @@ Per step, on rank r of N (shard size S, flat buffer of N*S elements):
      loss-scale decision; AdamW and the cast into slot r of the flat buffer;
   5. the all-gather of the 16-bit slots ("DeepSpeed 与 FSDP" §ZeRO-1 step 3;
      "PyTorch FSDP ... 深度解析" §3.2): every rank's flat buffer holds every
-     rank's new parameters.
+     rank's new parameters -- or, in the ZeRO++ form ("DeepSpeed 与 FSDP"
+     §ZeRO++; ZeRO reading §4.2), the all-gather of every rank's int8 codes
+     and block scales, half the bytes of the 16-bit slots.
 
 The collectives are the process group's (NCCL moves device tensors; a gloo
 group moves host tensors, so the step stages its buffers through pinned host
@@ -97,7 +99,8 @@ def gather_slots(flat, rank, shard_size, group=None, staging=None):
     slot = flat[rank * shard_size:(rank + 1) * shard_size]
     if _stages_on_host(flat, group):
         staging = staging or _Staging()
-        hs, hf = staging.host("slot", slot), staging.host("flat", flat)
+        tag = "%s_%d" % (flat.dtype, flat.numel())
+        hs, hf = staging.host("slot_" + tag, slot), staging.host("flat_" + tag, flat)
         hs.copy_(slot)
         dist.all_gather_into_tensor(hf, hs, group=group)
         flat.copy_(hf)
@@ -129,15 +132,20 @@ class RankStep:
         self.all_overflow = torch.zeros(n, dtype=torch.int32, device=dev)
         self.staging = _Staging()
 
-    def step(self, grads, master, m, v, out, stream=None, want_result=True, gather=True):
+    def step(self, grads, master, m, v, out, stream=None, want_result=True, gather=True,
+             q8=None, q8_scales=None):
         """grads: this rank's whole flat gradient (padded_numel elements of the
         grad dtype); master, m, v: this rank's fp32 shard (S elements each);
         out: the flat 16-bit parameter buffer (padded_numel elements), slot
         `rank` written by the update and, with gather, every slot refreshed
-        from its owner.  stream: the CUDA stream every part of the step runs
-        on -- the library's kernels, the collectives and the staging copies
-        (None: the current stream).  Returns the step result (want_result)
-        or None."""
+        from its owner.  q8, q8_scales: the int8 weight payload (int8
+        codes, padded_numel; fp32 block scales, world_size * ceil(S/256)),
+        written for this rank as zero_shard_step_q8 writes it and, with
+        gather, all-gathered; out may then be None (only the payload is
+        written and exchanged).  stream: the CUDA stream every part of the
+        step runs on -- the library's kernels, the collectives and the
+        staging copies (None: the current stream).  Returns the step result
+        (want_result) or None."""
         stream = stream if stream is not None else torch.cuda.current_stream()
         r = [self.rank]
         with torch.cuda.stream(stream):
@@ -148,7 +156,12 @@ class RankStep:
             gather_partials(self.overflow, self.all_overflow, self.group, self.staging, "of")
             res = self.flat.apply_partials(r, [master], [m], [v], out, self.all_norm_sq,
                                            self.all_overflow, stream=stream,
-                                           want_result=want_result)
+                                           want_result=want_result, q8=q8, q8_scales=q8_scales)
             if gather:
-                gather_slots(out, self.rank, self.S, self.group, self.staging)
+                if out is not None:
+                    gather_slots(out, self.rank, self.S, self.group, self.staging)
+                if q8 is not None:
+                    nb = -(-self.S // 256)
+                    gather_slots(q8, self.rank, self.S, self.group, self.staging)
+                    gather_slots(q8_scales, self.rank, nb, self.group, self.staging)
         return res

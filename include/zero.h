@@ -300,6 +300,24 @@ zero_status zero_shard_apply_partials(zero_flat *h, const int32_t *ranks, int32_
                                       const int32_t *overflow_parts, int32_t n_parts,
                                       void *stream, zero_step_result *res);
 
+/* zero_shard_apply_partials that also writes the ZeRO++ int8 weight payload
+ * ("DeepSpeed 与 FSDP" §ZeRO++; ZeRO reading §4.2: the parameter shard goes
+ * to the all-gather as int8 codes and block scales, half the bytes of fp16),
+ * exactly as zero_shard_step_q8 writes it: flat_q8_out (device int8,
+ * padded_numel elements, rank r's codes at [r*S, (r+1)*S)) and q8_scales
+ * (device fp32, world_size * ceil(S/256), rank r's at [r*nb, (r+1)*nb)).
+ * flat_param_out may be NULL (only the payload is written).  The decision
+ * from the gathered partials as in zero_shard_apply_partials.  Errors: as for
+ * zero_shard_apply_partials; INVALID_ARG for NULL int8 outputs, ALIGNMENT for
+ * q8_scales not 4-byte aligned. */
+zero_status zero_shard_apply_partials_q8(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                                         float *const *master, float *const *m,
+                                         float *const *v, void *flat_param_out,
+                                         int8_t *flat_q8_out, float *q8_scales,
+                                         const double *norm_sq_parts,
+                                         const int32_t *overflow_parts, int32_t n_parts,
+                                         void *stream, zero_step_result *res);
+
 /* A group: the FlatParameters one rank steps together ("PyTorch FSDP ...
  * 深度解析" §3.1: one FlatParameter per wrapped module) with one clip norm and
  * one loss-scale decision (ZeRO reading §5.3), in one reduce launch and one

@@ -68,6 +68,16 @@ def _exchange_worker(rank, world, port, S):
     flat[rank * S:(rank + 1) * S] = rank + 1
     D.gather_slots(flat, rank, S)
     assert flat.tolist() == sum([[k + 1] * S for k in range(world)], [])
+    # the int8 payload: codes (1 byte) and block scales (fp32) per rank
+    codes = torch.full((padded,), -1, dtype=torch.int8)
+    codes[rank * S:(rank + 1) * S] = rank + 3
+    D.gather_slots(codes, rank, S)
+    assert codes.tolist() == sum([[k + 3] * S for k in range(world)], [])
+    nb = -(-S // 256)
+    scales = torch.full((world * nb,), -1.0)
+    scales[rank * nb:(rank + 1) * nb] = rank + 0.5
+    D.gather_slots(scales, rank, nb)
+    assert scales.tolist() == sum([[k + 0.5] * nb for k in range(world)], [])
     tdist.destroy_process_group()
 
 

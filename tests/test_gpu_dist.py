@@ -8,7 +8,9 @@ process waits on the other.  On every rank and every step, the result, the
 loss-scale state, the rank's master / m / v and the whole gathered flat
 buffer are compared with the oracle's step of all shards at once on the
 stacked contributions, at the parity tolerances; one rank's inf must make
-both ranks skip and halve the scale.  A last test runs one rank over NCCL
+both ranks skip and halve the scale.  The ZeRO++ form exchanges only the int8
+payload: every gathered code and block scale must equal the oracle's
+quantization of every rank's parameters.  A last test runs one rank over NCCL
 (a one-rank communicator on this GPU): the device-tensor branch of every
 exchange, with no host staging, against the oracle."""
 import os
@@ -182,3 +184,77 @@ def test_one_rank_over_nccl_matches_the_oracle():
     if not tdist.is_nccl_available():
         pytest.skip("no NCCL in this torch build")
     mp.start_processes(_nccl_worker, args=(_free_port(),), nprocs=1, start_method="spawn")
+
+
+def _q8_worker(rank, port):
+    """The ZeRO++ form: each rank writes only the int8 payload of its slot and
+    the ranks all-gather codes and block scales (no 16-bit buffer)."""
+    if ROOT not in sys.path:
+        sys.path.insert(0, ROOT)
+    torch.cuda.set_device(0)
+    world = 2
+    tdist.init_process_group("gloo", init_method="tcp://127.0.0.1:%d" % port, rank=rank,
+                             world_size=world)
+    import fsdp_sharded_mixed_zero_gb300 as Z
+    import oracle
+    import synth
+    from fsdp_sharded_mixed_zero_gb300.dist import RankStep
+    from tests.gpu_helpers import assert_result, assert_state, f32, u16
+
+    full, B = 600_001, 256
+    kw = dict(lr=1e-3, window=3, initial_scale_power=12)
+    flat = Z.ZeroFlat([(full,)], world, F16, F16, AVG, Z.hparams(**kw))
+    ohp = oracle.hparams(**kw)
+    S, padded = flat.shard_size, flat.padded_numel
+    nb = -(-S // B)
+    step_of = RankStep(flat, rank, grad_dtype=F16)
+    master_all = torch.empty(padded, device="cuda")
+    synth.normal_device(master_all, 45, synth.MASTER, 0, 0.02)
+    master_all[full:].zero_()
+    master = master_all[rank * S:(rank + 1) * S].clone()
+    m = torch.zeros(S, device="cuda")
+    v = torch.zeros(S, device="cuda")
+    q8 = torch.zeros(padded, dtype=torch.int8, device="cuda")
+    scales = torch.zeros(world * nb, device="cuda")
+    o_state = [[f32(master_all[k * S:(k + 1) * S]).copy() for k in range(world)],
+               [np.zeros(S, np.float32) for _ in range(world)],
+               [np.zeros(S, np.float32) for _ in range(world)]]
+    o_out = np.zeros(padded, np.uint16)
+    o_st = oracle.scaler_init(ohp)
+    mine = torch.empty((1, padded), dtype=torch.float16, device="cuda")
+    everyone = torch.empty((world, padded), dtype=torch.float16, device="cuda")
+    for step in range(STEPS):
+        scale = flat.scaler_state().scale
+        synth.grads_device(mine, 45, step, 0, padded, 1e-3, 1e-3, scale, synth.F16,
+                           zero_from=full, c0=rank, n_contrib=1)
+        synth.grads_device(everyone, 45, step, 0, padded, 1e-3, 1e-3, scale, synth.F16,
+                           zero_from=full)
+        if step == INF_STEP:
+            everyone[1, 777] = float("inf")
+            if rank == 1:
+                mine[0, 777] = float("inf")
+        scale_used = o_st.scale
+        ro = oracle.shard_step(ohp, o_st, world, full, S, list(range(world)), u16(everyone),
+                               padded, S, *o_state, o_out)
+        res = step_of.step(mine.view(-1), master, m, v, None, q8=q8, q8_scales=scales)
+        torch.cuda.synchronize()
+        tag = " (rank %d, step %d)" % (rank, step)
+        assert_result(res, (ro.overflow, ro.skipped, ro.grad_norm, ro.clip_coef, scale_used))
+        assert_state(f32(master), f32(m), f32(v), o_state[0][rank], o_state[1][rank],
+                     o_state[2][rank], tag=tag)
+        got_q, got_s = q8.cpu().numpy(), scales.cpu().numpy()
+        for k in range(world):                            # every rank's payload, gathered
+            p = oracle.decode_array(np.ascontiguousarray(o_out[k * S:(k + 1) * S]))
+            want_q, want_s = oracle.quantize_q8(p, B)
+            assert np.array_equal(got_q[k * S:(k + 1) * S], want_q), "codes of rank %d" % k + tag
+            assert np.array_equal(got_s[k * nb:(k + 1) * nb].view(np.uint32),
+                                  want_s.view(np.uint32)), "scales of rank %d" % k + tag
+    assert o_st.overflow_count == 1
+    flat.close()
+    tdist.destroy_process_group()
+
+
+def test_two_ranks_exchange_the_int8_payload():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    mp.start_processes(_q8_worker, args=(_free_port(),), nprocs=2, start_method="spawn")
