@@ -21,6 +21,7 @@ __all__ = [
     "zero_shard_step_q8", "ZERO_Q8_BLOCK", "zero_flat_set_lr", "zero_shard_step_offload",
     "zero_offload_adamw_host", "zero_debug_set_stage_tx_pad", "zero_shard_reduce",
     "zero_shard_apply", "zero_shard_apply_partials", "zero_shard_apply_partials_q8",
+    "zero_shard_reduce_accumulated",
     "GroupMember", "ZeroGroup", "zero_group_init", "zero_group_step",
     "zero_group_step_q8", "zero_group_step_accumulated", "zero_group_step_offload",
     "zero_group_accumulate", "zero_group_loss_scaler_state", "zero_group_set_loss_scaler_state",
@@ -135,6 +136,8 @@ def _load():
     L.zero_shard_apply_partials.argtypes = [vp, C.POINTER(i32), i32, C.POINTER(vp),
                                             C.POINTER(vp), C.POINTER(vp), vp, vp, vp, i32, vp,
                                             C.POINTER(StepResult)]
+    L.zero_shard_reduce_accumulated.argtypes = [vp, C.POINTER(i32), i32, C.POINTER(vp), vp, vp,
+                                                vp]
     L.zero_shard_apply_partials_q8.argtypes = [vp, C.POINTER(i32), i32, C.POINTER(vp),
                                                C.POINTER(vp), C.POINTER(vp), vp, vp, vp, vp, vp,
                                                i32, vp, C.POINTER(StepResult)]
@@ -154,7 +157,8 @@ def _load():
                  "zero_shard_step_q8", "zero_flat_set_lr", "zero_shard_step_offload",
                  "zero_offload_adamw_host", "zero_debug_set_stage_tx_pad",
                  "zero_shard_reduce", "zero_shard_apply", "zero_shard_apply_partials",
-                 "zero_shard_apply_partials_q8", "zero_group_init", "zero_group_step",
+                 "zero_shard_apply_partials_q8", "zero_shard_reduce_accumulated",
+                 "zero_group_init", "zero_group_step",
                  "zero_group_loss_scaler_state", "zero_group_set_loss_scaler_state",
                  "zero_group_set_lr", "zero_group_free", "zero_group_accumulate",
                  "zero_group_step_accumulated", "zero_group_step_q8",
@@ -366,6 +370,17 @@ def zero_shard_apply_partials(h, ranks, master_ptrs, m_ptrs, v_ptrs, out_ptr, no
                                           C.byref(res) if res is not None else None),
            "zero_shard_apply_partials")
     return res
+
+
+def zero_shard_reduce_accumulated(h, ranks, acc_ptrs, norm_sq_ptr, overflow_ptr, stream=0):
+    """First half of a split step from micro-step accumulators: g = acc / scale
+    into the handle's rows, this handle's norm^2 and overflow flag on the device."""
+    n = len(ranks)
+    r = (C.c_int32 * n)(*ranks)
+    _check(_lib.zero_shard_reduce_accumulated(h, r, n, (C.c_void_p * n)(*acc_ptrs),
+                                              C.c_void_p(norm_sq_ptr), C.c_void_p(overflow_ptr),
+                                              C.c_void_p(stream)),
+           "zero_shard_reduce_accumulated")
 
 
 def zero_shard_apply_partials_q8(h, ranks, master_ptrs, m_ptrs, v_ptrs, out_ptr, q8_ptr,
@@ -719,6 +734,15 @@ class ZeroFlat:
         zero_shard_reduce(self.handle, list(ranks), grads.data_ptr(), grads.stride(0),
                           grad_rank_offset_mul, norm_sq.data_ptr(), overflow.data_ptr(),
                           stream.cuda_stream)
+
+    def reduce_accumulated(self, ranks, acc, norm_sq, overflow, stream=None):
+        """First half of a split step from fp32 accumulators (one CUDA tensor
+        of shard_size per stepped rank)."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        zero_shard_reduce_accumulated(self.handle, list(ranks), [t.data_ptr() for t in acc],
+                                      norm_sq.data_ptr(), overflow.data_ptr(), stream.cuda_stream)
 
     def apply(self, ranks, master, m, v, out, norm_sq, overflow, stream=None, want_result=True):
         """Second half: the decision from the (summed) totals, then AdamW."""

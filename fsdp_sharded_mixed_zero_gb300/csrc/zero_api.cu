@@ -613,6 +613,66 @@ ZERO_API zero_status zero_shard_reduce(zero_flat *h, const int32_t *ranks, int32
     return ZERO_OK;
 }
 
+ZERO_API zero_status zero_shard_reduce_accumulated(zero_flat *h, const int32_t *ranks,
+                                                   int32_t n_ranks, const float *const *acc,
+                                                   double *norm_sq_out, int32_t *overflow_out,
+                                                   void *stream) {
+    if (!h) return fail(ZERO_ERR_INVALID_ARG, "handle is NULL");
+    int32_t max_rank = 0;
+    zero_status s;
+    if ((s = check_ranks(h, ranks, n_ranks, &max_rank))) return s;
+    if ((s = check_rows(h, const_cast<float *const *>(acc), n_ranks, "acc"))) return s;
+    if (!norm_sq_out || !overflow_out) return fail(ZERO_ERR_INVALID_ARG, "NULL output");
+    if ((uintptr_t)norm_sq_out % 8 || (uintptr_t)overflow_out % 4)
+        return fail(ZERO_ERR_ALIGNMENT, "norm_sq_out must be 8-byte, overflow_out 4-byte aligned");
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return fail(ZERO_ERR_CUDA, "cannot select the handle's device");
+    const cudaStream_t st = (cudaStream_t)stream;
+    // the step's reduce with each accumulator as the one fp32 contribution of
+    // its row: g = acc / scale (padding zero) into the handle's gradient rows,
+    // the overflow check and the norm partials
+    zg::ReducePlan rp;
+    rp.mode = zg::kModeStep;
+    rp.ranks = ranks;
+    rp.n_ranks = n_ranks;
+    int64_t parts = 0;
+    if ((s = plan_reduce(h, rp, &parts))) return s;
+    rp.in_kind = zg::kInF32;
+    rp.n_contrib = 1;
+    rp.avg = 0;
+    rp.staged = false;
+    int bps = 1;
+    cudaError_t e = zg::reduce_blocks_per_sm(zg::kInF32, zg::kModeStep, false, &bps);
+    if (e) return cuda_fail(e, "occupancy query");
+    const int64_t batch = std::min<int64_t>(n_ranks, zg::kMaxRanksPerLaunch);
+    rp.grid_x = std::min(rp.grid_x, zg::grid_x_for(h->shard, batch, h->sm_count, bps));
+    parts = (int64_t)rp.grid_x * n_ranks;
+    if (h->shard > 0) {
+        std::vector<zg::ReduceRow> rows(n_ranks);
+        for (int32_t j = 0; j < n_ranks; ++j) {
+            zg::ReduceRow &w = rows[j];
+            const int64_t first = (int64_t)ranks[j] * h->shard;
+            w.in = acc[j];
+            w.S = h->shard;
+            w.valid = std::max<int64_t>(0, std::min<int64_t>(h->shard, h->full_numel - first));
+            w.first = first;
+            w.g = h->d_g + (int64_t)j * h->g_stride;
+        }
+        zg::FinalizeArgs f = decision_args(h, h->d_part_ss, h->d_part_of, (int32_t)parts, 0.0);
+        f.sum_out = norm_sq_out;           // the last block totals the partials
+        f.of_out = overflow_out;
+        rp.fuse_finalize = true;
+        rp.fin = f;
+        e = zg::run_reduce_rows(rp, rows.data(), n_ranks, st, true);
+    } else {
+        e = cudaMemsetAsync(norm_sq_out, 0, sizeof(double), st);
+        if (!e) e = cudaMemsetAsync(overflow_out, 0, sizeof(int32_t), st);
+    }
+    if (e) return cuda_fail(e, "reduce kernel launch");
+    h->reduced_ranks.assign(ranks, ranks + n_ranks);
+    return ZERO_OK;
+}
+
 // The second half of a split step: the decision over n_parts (norm_sq[k],
 // overflow[k]) pairs in device memory, then AdamW and the cast (and, with
 // q8, the int8 payload: flat_param_out may then be NULL).

@@ -132,6 +132,35 @@ class RankStep:
         self.all_overflow = torch.zeros(n, dtype=torch.int32, device=dev)
         self.staging = _Staging()
 
+    def accumulate(self, grads, acc, first_micro_step, stream=None):
+        """One micro-step ("DeepSpeed 与 FSDP" §实践要点, gradient
+        accumulation): the all-to-all of this micro-step's gradient slices,
+        then zero_grad_accumulate of the N received rows into this rank's
+        fp32 accumulator (acc = r on the first micro-step, acc += r after)."""
+        stream = stream if stream is not None else torch.cuda.current_stream()
+        with torch.cuda.stream(stream):
+            exchange_contributions(grads, self.recv, self.group, self.staging)
+            self.flat.accumulate([self.rank], self.recv, [acc], first_micro_step,
+                                 grad_rank_offset_mul=0, stream=stream)
+
+    def step_accumulated(self, acc, master, m, v, out, stream=None, want_result=True,
+                         gather=True):
+        """The optimizer step from the accumulator: this rank's norm^2 and flag
+        (zero_shard_reduce_accumulated), their all-gather, the one decision
+        (zero_shard_apply_partials), AdamW and the slot all-gather."""
+        stream = stream if stream is not None else torch.cuda.current_stream()
+        r = [self.rank]
+        with torch.cuda.stream(stream):
+            self.flat.reduce_accumulated(r, [acc], self.norm_sq, self.overflow, stream=stream)
+            gather_partials(self.norm_sq, self.all_norm_sq, self.group, self.staging, "ss")
+            gather_partials(self.overflow, self.all_overflow, self.group, self.staging, "of")
+            res = self.flat.apply_partials(r, [master], [m], [v], out, self.all_norm_sq,
+                                           self.all_overflow, stream=stream,
+                                           want_result=want_result)
+            if gather:
+                gather_slots(out, self.rank, self.S, self.group, self.staging)
+        return res
+
     def step(self, grads, master, m, v, out, stream=None, want_result=True, gather=True,
              q8=None, q8_scales=None):
         """grads: this rank's whole flat gradient (padded_numel elements of the

@@ -278,6 +278,21 @@ zero_status zero_shard_step_accumulated(zero_flat *h, const int32_t *ranks, int3
 zero_status zero_shard_reduce(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
                               const void *grads, int64_t grad_ld, int64_t grad_rank_offset_mul,
                               double *norm_sq_out, int32_t *overflow_out, void *stream);
+
+/* The first half of a split step taken from micro-step accumulators
+ * ("DeepSpeed 与 FSDP" §实践要点, gradient accumulation; ZeRO reading §5.1,
+ * contiguous_gradients, and §5.3, one decision): for each stepped rank j,
+ * g = acc[j] / scale (the handle's current loss scale; padding elements
+ * zero) into the handle's gradient rows, the overflow check and this
+ * handle's norm^2 and flag written to DEVICE memory as zero_shard_reduce
+ * writes them.  zero_shard_apply / zero_shard_apply_partials then decide and
+ * update as after zero_shard_reduce; the pair equals
+ * zero_shard_step_accumulated on the same accumulators.  acc: device fp32,
+ * shard_size elements per stepped rank (4-byte aligned), only read.  Errors:
+ * as for zero_shard_reduce. */
+zero_status zero_shard_reduce_accumulated(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
+                                          const float *const *acc, double *norm_sq_out,
+                                          int32_t *overflow_out, void *stream);
 zero_status zero_shard_apply(zero_flat *h, const int32_t *ranks, int32_t n_ranks,
                              float *const *master, float *const *m, float *const *v,
                              void *flat_param_out, const double *norm_sq,

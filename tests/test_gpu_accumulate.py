@@ -229,3 +229,38 @@ def test_norm_extreme_magnitudes(ora, scales):
     for j in range(N):
         assert_state(f32(master[j]), f32(m[j]), f32(v[j]), hm[j], hmm[j], hv[j])
     f.close()
+
+
+def test_split_accumulated_step_equals_the_accumulated_step():
+    """zero_shard_reduce_accumulated followed by zero_shard_apply (the split
+    form a multi-rank caller uses) gives the bits of zero_shard_step_accumulated
+    on the same accumulators -- ragged shard, four stepped ranks, an
+    overflowing micro-step."""
+    _need_gpu()
+    from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
+    w = _wl("split_acc", [(400_003,)], 4, [0, 1, 2, 3], steps=3, micro=2, inf_at=(2, 3, 11))
+    a, b = DeviceWorkload(w), DeviceWorkload(w)
+    a.alloc_acc()
+    b.alloc_acc()
+    ss = torch.zeros((), dtype=torch.float64, device="cuda")
+    of = torch.zeros((), dtype=torch.int32, device="cuda")
+    for step in range(w.steps):
+        for k in range(2):
+            a.gen_grads(2 * step + k, a.scaler().scale)
+            b.grads.copy_(a.grads)
+            a.accumulate(first=(k == 0))
+            b.accumulate(first=(k == 0))
+        ra = a.step_accumulated()
+        b.flat.reduce_accumulated(w.ranks, b.acc, ss, of)
+        rb = b.flat.apply(w.ranks, b.master, b.m, b.v, b.out, ss, of)
+        assert (ra.overflow, ra.skipped, ra.clip_coef, ra.scale_used) == \
+               (rb.overflow, rb.skipped, rb.clip_coef, rb.scale_used)
+        if not ra.overflow:
+            assert abs(ra.grad_norm - rb.grad_norm) <= 1e-14 * ra.grad_norm
+        assert rb.skipped == (step == 1)
+    for x, y in zip(a.master + a.m + a.v, b.master + b.m + b.v):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+    assert a.scaler().as_tuple() == b.scaler().as_tuple()
+    a.close()
+    b.close()

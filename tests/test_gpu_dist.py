@@ -258,3 +258,81 @@ def test_two_ranks_exchange_the_int8_payload():
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
     mp.start_processes(_q8_worker, args=(_free_port(),), nprocs=2, start_method="spawn")
+
+
+def _acc_worker(rank, port):
+    """Micro-step accumulation among real ranks: per micro-step the all-to-all
+    and zero_grad_accumulate of the received rows, then the step from the
+    accumulator with one decision over both ranks -- against the oracle's
+    accumulation and accumulated step of all shards at once."""
+    if ROOT not in sys.path:
+        sys.path.insert(0, ROOT)
+    torch.cuda.set_device(0)
+    world, K = 2, 2
+    tdist.init_process_group("gloo", init_method="tcp://127.0.0.1:%d" % port, rank=rank,
+                             world_size=world)
+    import fsdp_sharded_mixed_zero_gb300 as Z
+    import oracle
+    import synth
+    from fsdp_sharded_mixed_zero_gb300.dist import RankStep
+    from tests.gpu_helpers import assert_params_close, assert_result, assert_state, f32, u16
+
+    full = 500_003
+    kw = dict(lr=1e-3, window=3, initial_scale_power=12)
+    flat = Z.ZeroFlat([(full,)], world, F16, F16, AVG, Z.hparams(**kw))
+    ohp = oracle.hparams(**kw)
+    S, padded = flat.shard_size, flat.padded_numel
+    step_of = RankStep(flat, rank, grad_dtype=F16)
+    master_all = torch.empty(padded, device="cuda")
+    synth.normal_device(master_all, 47, synth.MASTER, 0, 0.02)
+    master_all[full:].zero_()
+    master = master_all[rank * S:(rank + 1) * S].clone()
+    m = torch.zeros(S, device="cuda")
+    v = torch.zeros(S, device="cuda")
+    acc = torch.empty(S, device="cuda")
+    out = torch.zeros(padded, dtype=torch.float16, device="cuda")
+    o_state = [[f32(master_all[k * S:(k + 1) * S]).copy() for k in range(world)],
+               [np.zeros(S, np.float32) for _ in range(world)],
+               [np.zeros(S, np.float32) for _ in range(world)]]
+    o_acc = [np.zeros(S, np.float32) for _ in range(world)]
+    o_out = np.zeros(padded, np.uint16)
+    o_st = oracle.scaler_init(ohp)
+    mine = torch.empty((1, padded), dtype=torch.float16, device="cuda")
+    everyone = torch.empty((world, padded), dtype=torch.float16, device="cuda")
+    for step in range(3):
+        scale = flat.scaler_state().scale
+        for k in range(K):
+            micro = K * step + k
+            synth.grads_device(mine, 47, micro, 0, padded, 1e-3, 1e-3, scale, synth.F16,
+                               zero_from=full, c0=rank, n_contrib=1)
+            synth.grads_device(everyone, 47, micro, 0, padded, 1e-3, 1e-3, scale, synth.F16,
+                               zero_from=full)
+            if micro == 3:                    # rank 1's gradient, inside rank 0's slice
+                everyone[1, 99] = float("inf")
+                if rank == 1:
+                    mine[0, 99] = float("inf")
+            oracle.grad_accumulate(world, full, S, list(range(world)), u16(everyone), padded, S,
+                                   o_acc, k == 0)
+            step_of.accumulate(mine.view(-1), acc, k == 0)
+        torch.cuda.synchronize()
+        tag = " (rank %d, step %d)" % (rank, step)
+        assert np.array_equal(f32(acc).view(np.uint32), o_acc[rank].view(np.uint32)), tag
+        scale_used = o_st.scale
+        ro = oracle.shard_step_acc(ohp, o_st, world, full, S, list(range(world)), o_acc,
+                                   *o_state, o_out)
+        res = step_of.step_accumulated(acc, master, m, v, out)
+        torch.cuda.synchronize()
+        assert_result(res, (ro.overflow, ro.skipped, ro.grad_norm, ro.clip_coef, scale_used))
+        assert flat.scaler_state().as_tuple() == o_st.as_tuple(), tag
+        assert_state(f32(master), f32(m), f32(v), o_state[0][rank], o_state[1][rank],
+                     o_state[2][rank], tag=tag)
+        assert_params_close(u16(out), o_out, False, "gathered flat buffer" + tag)
+        assert res.skipped == (step == 1), tag
+    flat.close()
+    tdist.destroy_process_group()
+
+
+def test_two_ranks_accumulate_micro_steps():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    mp.start_processes(_acc_worker, args=(_free_port(),), nprocs=2, start_method="spawn")
