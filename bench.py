@@ -38,6 +38,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import re
 import statistics
 import subprocess
@@ -277,6 +278,45 @@ def oracle_sample_step(w, k):
     return run, k
 
 
+_ARM_PARTS = {0xd40: "Neoverse-V1", 0xd49: "Neoverse-N2", 0xd4f: "Neoverse-V2",
+              0xd84: "Neoverse-V3", 0xd0c: "Neoverse-N1"}
+
+
+def host_cpu(cpuinfo=None):
+    """The host's CPU model (from /proc/cpuinfo, or the text `cpuinfo`: "model
+    name" where the kernel gives one, else the Arm implementer/part pair), its
+    online CPU count and the CPUs this process may run on."""
+    model, impl, part = None, None, None
+    try:
+        if cpuinfo is None:
+            with open("/proc/cpuinfo") as f:
+                cpuinfo = f.read()
+        for line in cpuinfo.splitlines():
+            k, _, v = line.partition(":")
+            k, v = k.strip(), v.strip()
+            if k == "model name" and model is None:
+                model = v
+            elif k == "CPU implementer" and impl is None:
+                impl = v
+            elif k == "CPU part" and part is None:
+                part = v
+    except OSError:
+        pass
+    if model is None and part is not None:
+        try:
+            name = _ARM_PARTS.get(int(part, 16))
+        except ValueError:
+            name = None
+        model = ("Arm " + name) if impl == "0x41" and name else \
+            "implementer %s part %s" % (impl, part)
+    try:
+        usable = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        usable = os.cpu_count()
+    return {"cpu_model": model or platform.processor() or platform.machine(),
+            "nproc": os.cpu_count(), "usable_cpus": usable}
+
+
 def cpu_baseline(w, target_s):
     run, k0 = oracle_sample_step(w, 1 << 20)
     t = time.perf_counter()
@@ -290,7 +330,7 @@ def cpu_baseline(w, target_s):
     return {"value": k / dt / 1e9, "unit": "Gparams/s", "cores": 1, "kind": "oracle",
             "sample": "%d params of the %s shard (%d fp16/bf16 contributions each), one full "
                       "oracle step (reduce, norm, decision, AdamW, cast), single thread, "
-                      "%.1f s" % (k, w.name, w.world_size, dt)}
+                      "%.1f s" % (k, w.name, w.world_size, dt), "host": host_cpu()}
 
 
 # ---------------------------------------------------------------- arms
@@ -402,7 +442,7 @@ def run_reference(args, w):
         "config": {"workload": w.name, "sample_params_per_step": k},
         "cpu_baseline": {"value": value, "unit": "Gparams/s", "cores": 1, "kind": "oracle",
                          "sample": "%d params of the %s shard per step, single thread" %
-                                   (k, w.name)},
+                                   (k, w.name), "host": host_cpu()},
         "e2e": {"value": value, "unit": "Gparams/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -95,3 +95,16 @@ def test_bench_accepts_each_step_form_alone():
     for argv in ([], ["--q8"], ["--micro-steps", "4"], ["--offload"], ["--group", "8", "--q8"],
                  ["--collective", "--collective-shard", "1000"]):
         bench.parse_args(argv)
+
+
+def test_host_cpu_names_the_model():
+    import bench
+    arm = ("processor\t: 0\nBogoMIPS\t: 2000.00\nCPU implementer\t: 0x41\n"
+           "CPU architecture: 8\nCPU variant\t: 0x0\nCPU part\t: 0xd4f\n\n"
+           "processor\t: 1\nCPU implementer\t: 0x41\nCPU part\t: 0xd4f\n")
+    h = bench.host_cpu(arm)
+    assert h["cpu_model"] == "Arm Neoverse-V2"
+    assert h["nproc"] >= 1 and 1 <= h["usable_cpus"] <= h["nproc"]
+    assert bench.host_cpu("processor\t: 0\nCPU implementer\t: 0x51\nCPU part\t: 0x001\n")[
+        "cpu_model"] == "implementer 0x51 part 0x001"
+    assert bench.host_cpu("model name\t: Some CPU @ 3GHz\n")["cpu_model"] == "Some CPU @ 3GHz"
