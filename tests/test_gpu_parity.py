@@ -109,6 +109,13 @@ EDGE = [
     _wl("no_clip_no_wd", [(9999,)], 2, [0, 1], hp=dict(max_grad_norm=0.0, weight_decay=0.0)),
     # every step overflows until the scale reaches its floor
     _wl("floor", [(4096,)], 2, [0, 1], steps=3, hp=dict(initial_scale_power=1, min_scale=1.0)),
+    # a large world: 1000 contributions (AVG by true division) of a 38-element
+    # shard; rank 973 holds 31 elements and 7 of padding, rank 999's slice is
+    # all padding (full_numel = 37,005 < 999 * 38)
+    _wl("n1000_tiny_shards", [(37_005,)], 1000, [0, 973, 999], steps=3, inf_at=(1, 640, 5)),
+    # 256 contributions through the staged reduce: odd shard (4,097), rows
+    # 8,208 bytes apart (16 bytes off a 64-byte boundary)
+    _wl("n256_staged", [(256 * 4_097,)], 256, [201], layout="slice", steps=3),
 ]
 
 
