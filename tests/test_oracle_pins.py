@@ -285,6 +285,31 @@ def test_sum_of_squares_is_exact(ora):
     assert ora.sum_of_squares(g)[1] == 1
 
 
+def test_exact_accumulators_merge_with_carries(ora):
+    # Merging two exact accumulators carries between 64-bit limbs.  Units are
+    # 2^-298, so 2^84 sits at bit 382 (limb 5); two squares of 2^42 make 2^85
+    # (limb 5's top bit) in each accumulator, and their merge 2^86 (limb 6).
+    x = np.full(2, 2.0 ** 42, np.float32)
+    a, b = ora.norm_accumulate(x)[0], ora.norm_accumulate(x)[0]
+    assert ora.norm_sum(ora.acc_merge(a, b)) == 2.0 ** 86
+    # Random magnitudes over the whole fp32 range, many squares of one binade
+    # (so limbs fill and carry), split at random and merged in random order:
+    # the exact sum rounded once (Fraction -> nearest double).
+    rng = np.random.default_rng(11)
+    for _ in range(10):
+        wide = np.ldexp(rng.uniform(1.0, 2.0, 200), rng.integers(-149, 127, 200))
+        same = np.ldexp(rng.uniform(1.9, 2.0, 300), 42)
+        g = (np.concatenate([wide, same]) * rng.choice([-1.0, 1.0], 500)).astype(np.float32)
+        rng.shuffle(g)
+        exact = float(sum((Fr(float(v)) ** 2 for v in g), Fr(0)))
+        cuts = np.sort(rng.choice(np.arange(1, g.size), 6, replace=False))
+        parts = [ora.norm_accumulate(p)[0] for p in np.split(g, cuts)]
+        tot = ora.ExactAcc()
+        for k in rng.permutation(len(parts)):
+            ora.acc_merge(tot, parts[k])
+        assert ora.norm_sum(tot) == exact == ora.sum_of_squares(g)[0]
+
+
 def test_sum_of_squares_rounding_ties(ora):
     # (2^26)^2 + (2^26)^2 + 1 = 2^53 + 1 is halfway between two doubles
     x = np.array([2.0 ** 26, 2.0 ** 26, 1.0], np.float32)   # 2^53 + 1 exactly
