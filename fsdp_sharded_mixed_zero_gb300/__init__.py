@@ -646,6 +646,7 @@ class ZeroFlat:
                  else param_infos(shapes_or_infos, param_dtype))
         self.hp = hp if hp is not None else hparams()
         self.world_size = world_size
+        self.grad_dtype, self.param_dtype, self.op = grad_dtype, param_dtype, op
         self.handle = zero_flat_init(infos, world_size, grad_dtype, param_dtype, op, self.hp)
         self.full_numel, self.shard_size, self.padded_numel = zero_flat_layout(self.handle)
 

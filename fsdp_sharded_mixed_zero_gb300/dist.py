@@ -113,15 +113,21 @@ def gather_slots(flat, rank, shard_size, group=None, staging=None):
 class RankStep:
     """The ZeRO step of rank `rank` of a process group whose size is the
     handle's world size.  flat: a ZeroFlat of the FlatParameter (world size N,
-    grad dtype, op and hyper-parameters as every other rank's)."""
+    grad dtype, op and hyper-parameters as every other rank's); grad_dtype,
+    if given, must be the handle's."""
 
-    def __init__(self, flat, rank, grad_dtype=ZERO_F16, group=None, device=None):
+    def __init__(self, flat, rank, grad_dtype=None, group=None, device=None):
         n = dist.get_world_size(group)
         if n != flat.world_size:
             raise ValueError("process group of %d ranks for a FlatParameter sharded %d ways"
                              % (n, flat.world_size))
         if not 0 <= rank < n:
             raise ValueError("rank %d out of range" % rank)
+        if grad_dtype is None:
+            grad_dtype = flat.grad_dtype
+        elif grad_dtype != flat.grad_dtype:
+            raise ValueError("grad dtype %d differs from the handle's (%d)"
+                             % (grad_dtype, flat.grad_dtype))
         self.flat, self.rank, self.group = flat, rank, group
         self.N, self.S = n, flat.shard_size
         dev = torch.device(device) if device is not None else torch.device("cuda")

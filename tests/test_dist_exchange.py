@@ -78,6 +78,16 @@ def _exchange_worker(rank, world, port, S):
     scales[rank * nb:(rank + 1) * nb] = rank + 0.5
     D.gather_slots(scales, rank, nb)
     assert scales.tolist() == sum([[k + 0.5] * nb for k in range(world)], [])
+    # RankStep refuses a handle that does not fit the group (checked before
+    # anything is allocated)
+    from types import SimpleNamespace
+    fake = SimpleNamespace(world_size=world, grad_dtype=0, shard_size=S)
+    with pytest.raises(ValueError, match="grad dtype"):
+        D.RankStep(fake, rank, grad_dtype=1)
+    with pytest.raises(ValueError, match="sharded"):
+        D.RankStep(SimpleNamespace(world_size=world + 1, grad_dtype=0, shard_size=S), rank)
+    with pytest.raises(ValueError, match="out of range"):
+        D.RankStep(fake, world)
     tdist.destroy_process_group()
 
 
