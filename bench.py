@@ -173,6 +173,12 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
+def reduce_name(flat):
+    """The name of the reduce kernel the handle's last contribution reduce
+    launched (the planner stages misaligned rows and large launches)."""
+    return "reduce_staged_kernel" if flat.reduce_form() == "staged" else "reduce_kernel"
+
+
 def profiled_traffic(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source; else None."""
@@ -564,8 +570,9 @@ def run_ours(args, w):
     # accumulator (4) and the accumulate launches read N*esize, read (after
     # the first) and write the accumulator.
     kernels = {
-        "reduce_kernel": {"ms_mean": ms_red / max(nrec, 1),
-                          "bytes_per_param": N * esize + 4 if K == 1 else 4},
+        (reduce_name(dw.flat) if K == 1 else "reduce_kernel"): {
+            "ms_mean": ms_red / max(nrec, 1),
+            "bytes_per_param": N * esize + 4 if K == 1 else 4},
         ("adamw_q8_kernel" if args.q8 else "adamw_kernel"): {
             "ms_mean": ms_adam / max(nrec, 1),
             "bytes_per_param": 30 + (1 + 4 / 256 if args.q8 else 0)},
@@ -574,7 +581,8 @@ def run_ours(args, w):
     if K > 1:
         kernels["accumulate_launch"] = {
             "ms_mean": ms_acc / max(len(acc_events), 1) / K,
-            "bytes_per_param": N * esize + (4 + 8 * (K - 1)) / K}
+            "bytes_per_param": N * esize + (4 + 8 * (K - 1)) / K,
+            "kernel": reduce_name(dw.flat)}
     for k in kernels.values():
         k["achieved_gbs"] = (k["bytes_per_param"] * params / (k["ms_mean"] / 1e3) / 1e9
                              if k["ms_mean"] > 0 else None)
@@ -686,8 +694,8 @@ def measure_workload(w, steps, warmup, dev):
         params = dw.S * len(w.ranks)
         N = w.world_size
         esize = 4 if w.grad_dtype == 2 else 2
-        kernels = {"reduce_kernel": {"ms_mean": ms_red / max(nrec, 1),
-                                     "bytes_per_param": N * esize + 4},
+        kernels = {reduce_name(dw.flat): {"ms_mean": ms_red / max(nrec, 1),
+                                          "bytes_per_param": N * esize + 4},
                    "adamw_kernel": {"ms_mean": ms_adam / max(nrec, 1), "bytes_per_param": 30}}
         for k in kernels.values():
             k["achieved_gbs"] = k["bytes_per_param"] * params / (k["ms_mean"] / 1e3) / 1e9
@@ -852,7 +860,8 @@ def run_offload(args, w):
     f = max(0.0, min(1.0, args.offload_gpu_share))
     host_bpp = f * 24 + (1 - f) * 36
     kernels = {
-        "reduce_kernel": {"ms_mean": ms_red / max(nrec, 1), "bytes_per_param": N * esize + 4},
+        reduce_name(dw.flat): {"ms_mean": ms_red / max(nrec, 1),
+                               "bytes_per_param": N * esize + 4},
         "finalize_kernel": {"ms_mean": ms_fin / max(nrec, 1), "bytes_per_param": 0},
         "host_update": {"ms_mean": ms_host / max(nrec, 1), "bytes_per_param": host_bpp,
                         "link_bytes_per_param": f * 24 + (1 - f) * 6},

@@ -17,6 +17,7 @@ __all__ = [
     "zero_flat_init", "zero_flat_layout", "zero_shard_step", "zero_loss_scaler_state",
     "zero_set_loss_scaler_state", "zero_memory_bytes", "zero_flat_device_bytes",
     "zero_flat_free", "zero_flat_profile_enable", "zero_flat_profile_read",
+    "zero_flat_profile_reduce_form",
     "zero_shard_step_noalloc", "zero_grad_accumulate", "zero_shard_step_accumulated",
     "zero_shard_step_q8", "ZERO_Q8_BLOCK", "zero_flat_set_lr", "zero_shard_step_offload",
     "zero_offload_adamw_host", "zero_debug_set_stage_tx_pad", "zero_shard_reduce",
@@ -102,6 +103,7 @@ def _load():
     L.zero_flat_free.argtypes = [vp]
     L.zero_flat_profile_enable.argtypes = [vp, i32]
     L.zero_flat_profile_read.argtypes = [vp] + [C.POINTER(C.c_double)] * 3 + [C.POINTER(i64)]
+    L.zero_flat_profile_reduce_form.argtypes = [vp, C.POINTER(i32)]
     L.zero_shard_step_noalloc.argtypes = [i64, i32, i32, i32, i32, C.POINTER(Hparams),
                                           C.POINTER(ScalerState), C.POINTER(i32), i32, vp, i64,
                                           i64, C.POINTER(vp), C.POINTER(vp), C.POINTER(vp), vp,
@@ -153,7 +155,8 @@ def _load():
     for name in ("zero_flat_init", "zero_flat_layout", "zero_shard_step",
                  "zero_loss_scaler_state", "zero_set_loss_scaler_state", "zero_memory_bytes",
                  "zero_flat_device_bytes", "zero_flat_free", "zero_flat_profile_enable",
-                 "zero_flat_profile_read", "zero_shard_step_noalloc", "zero_grad_accumulate",
+                 "zero_flat_profile_read", "zero_flat_profile_reduce_form",
+                 "zero_shard_step_noalloc", "zero_grad_accumulate",
                  "zero_shard_step_q8", "zero_flat_set_lr", "zero_shard_step_offload",
                  "zero_offload_adamw_host", "zero_debug_set_stage_tx_pad",
                  "zero_shard_reduce", "zero_shard_apply", "zero_shard_apply_partials",
@@ -622,6 +625,14 @@ def zero_flat_profile_read(h):
     return t[0].value, t[1].value, t[2].value, n.value
 
 
+def zero_flat_profile_reduce_form(h):
+    """The last contribution reduce's kernel: "staged", "plain", or None
+    before the first."""
+    v = C.c_int32()
+    _check(_lib.zero_flat_profile_reduce_form(h, C.byref(v)), "zero_flat_profile_reduce_form")
+    return {1: "staged", 0: "plain"}.get(v.value)
+
+
 def zero_status_string(status):
     return _lib.zero_status_string(status).decode()
 
@@ -649,6 +660,10 @@ class ZeroFlat:
         self.grad_dtype, self.param_dtype, self.op = grad_dtype, param_dtype, op
         self.handle = zero_flat_init(infos, world_size, grad_dtype, param_dtype, op, self.hp)
         self.full_numel, self.shard_size, self.padded_numel = zero_flat_layout(self.handle)
+
+    def reduce_form(self):
+        """The kernel of the last contribution reduce: "staged", "plain" or None."""
+        return zero_flat_profile_reduce_form(self.handle)
 
     def step(self, ranks, grads, master, m, v, out, grad_rank_offset_mul=None,
              extra_norm_sq=0.0, stream=None, want_result=True):

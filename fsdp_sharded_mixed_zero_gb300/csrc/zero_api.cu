@@ -441,6 +441,7 @@ zero_status plan_reduce(zero_flat *h, zg::ReducePlan &rp, int64_t *parts) {
     rp.S = S;
     rp.n_contrib = h->world;
     rp.staged = zg::reduce_wants_staging(rp);
+    if (rp.grads) h->last_reduce_staged = rp.staged ? 1 : 0;
     rp.grid_x = zg::grid_x_for(S, batch, h->sm_count,
                                rp.staged ? h->staged_bps[rp.mode] : h->reduce_bps[rp.mode]);
     *parts = (int64_t)rp.grid_x * rp.n_ranks;
@@ -815,6 +816,7 @@ ZERO_API zero_status zero_grad_accumulate(zero_flat *h, const int32_t *ranks, in
     rp.avg = h->op == ZERO_AVG;
     rp.st = h->d_state;
     rp.staged = zg::reduce_wants_staging(rp);
+    h->last_reduce_staged = rp.staged ? 1 : 0;
     const int64_t batch = std::min<int64_t>(n_ranks, zg::kMaxRanksPerLaunch);
     rp.grid_x = zg::grid_x_for(h->shard, batch, h->sm_count,
                                rp.staged ? h->staged_bps[rp.mode] : h->reduce_bps[rp.mode]);
@@ -1250,6 +1252,12 @@ ZERO_API zero_status zero_flat_profile_read(zero_flat *h, double *ms_reduce, dou
     if (ms_finalize) *ms_finalize = t[1];
     if (ms_adamw) *ms_adamw = t[2];
     if (steps) *steps = (int64_t)n;
+    return ZERO_OK;
+}
+
+ZERO_API zero_status zero_flat_profile_reduce_form(const zero_flat *h, int32_t *staged) {
+    if (!h || !staged) return fail(ZERO_ERR_INVALID_ARG, "handle or output is NULL");
+    *staged = h->last_reduce_staged;
     return ZERO_OK;
 }
 

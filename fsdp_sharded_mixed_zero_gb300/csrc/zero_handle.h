@@ -57,6 +57,7 @@ struct zero_flat {
     int sm_count = 0;
     int reduce_bps[4] = {1, 1, 1, 1}; // resident reduce blocks per SM, per ReduceMode
     int staged_bps[3] = {1, 1, 1};    // the same for the staged reduce (no kModeNormOnly)
+    int32_t last_reduce_staged = -1;  // the form of the last contribution reduce (-1: none yet)
     int32_t world = 1;
     zero_dtype grad_dtype = ZERO_F16, param_dtype = ZERO_F16;
     zero_reduce_op op = ZERO_AVG;

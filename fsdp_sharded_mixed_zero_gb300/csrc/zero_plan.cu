@@ -39,6 +39,7 @@ bool rows_want_staging(int mode, int in_kind, int32_t n_contrib, const ReduceRow
     if (mode == kModeNormOnly) return false;
     const size_t esize = in_kind == kInF32 ? 4 : 2;
     bool any = false, tile = false;
+    size_t bytes = 0;
     for (int32_t j = 0; j < n_rows; ++j) {
         const ReduceRow &w = rows[j];
         if (!w.in) return false;
@@ -46,8 +47,9 @@ bool rows_want_staging(int mode, int in_kind, int32_t n_contrib, const ReduceRow
         const bool rows_vary = n_contrib > 1 && ((size_t)w.ld * esize) % 64 != 0;
         any = any || rows_vary || (uintptr_t)w.in % 64 != 0;
         tile = tile || w.S >= kStageTile;
+        bytes += (size_t)(n_contrib > 0 ? n_contrib : 0) * (size_t)(w.S > 0 ? w.S : 0) * esize;
     }
-    return any && tile;
+    return tile && (any || bytes >= kStageAlignedBytes);
 }
 
 bool reduce_wants_staging(const ReducePlan &p) {

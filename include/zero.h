@@ -557,6 +557,12 @@ zero_status zero_flat_profile_enable(zero_flat *h, int32_t enable);
 zero_status zero_flat_profile_read(zero_flat *h, double *ms_reduce, double *ms_finalize,
                                    double *ms_adamw, int64_t *steps);
 
+/* Which reduce kernel the handle's last contribution reduce (a step, a split
+ * step's first half, or a micro-step accumulation) launched, for measurement
+ * tools that name it: *staged = 1 for the bulk-copy (staged) reduce, 0 for
+ * the plain one, -1 before the first.  Errors: INVALID_ARG (NULL). */
+zero_status zero_flat_profile_reduce_form(const zero_flat *h, int32_t *staged);
+
 /* Size of the device array that zero_shard_step_noalloc uses as scratch. */
 #define ZERO_NOALLOC_SCRATCH_BYTES (32u << 20)
 

@@ -1,14 +1,15 @@
 """GPU parity of the staged reduce (reduce_staged_kernel): contributor rows
-whose starts are not 64-byte aligned go through TMA bulk copies of aligned
-spans into shared memory and are re-aligned there.  Every case is compared
-with the oracle element by element on every step, and the CUDA profiler
-confirms that the staged kernel is the one that ran.
+go through TMA bulk copies of 64-byte-aligned spans into shared memory and
+are re-aligned there.  The planner takes it for rows whose starts are not
+64-byte aligned, and for aligned rows once a launch reads at least 1 GiB of
+contributions.  Every case is compared with the oracle element by element on
+every step, and the CUDA profiler confirms which kernel ran.
 
 Layouts: the full [N, padded] layout with an odd shard size (rank slices
 2-byte aligned, or 4-byte for fp32 contributions), a slice layout whose
 row stride is 32 bytes off a 64-byte multiple, fewer contributors than one
-stage holds, more contributors than several stages hold, padding, and the
-micro-step accumulation modes."""
+stage holds, more contributors than several stages hold, padding, the
+micro-step accumulation modes, and aligned rows below and above 1 GiB."""
 import warnings
 
 import pytest
@@ -131,11 +132,38 @@ def test_staged_accumulation_matches_oracle(ora, w):
         assert skipped[w.inf_at[0] // w.micro_steps] == 1
 
 
-def test_aligned_rows_keep_the_plain_kernel():
-    """The 10B-style slice layout (rows 128-byte aligned) must not be staged."""
+def test_small_aligned_launch_keeps_the_plain_kernel():
+    """Rows 128-byte aligned and 1 MB of contributions: the plain reduce
+    (its fixed cost is lower; staging pays off from 1 GiB per launch)."""
     _need_gpu()
     names = _step_kernels(_wl("aligned_slice", 8 * 64 * 1000, 8, [3], layout="slice"))
     if not names:
         pytest.skip("the CUDA profiler recorded no kernels")
     assert not any("reduce_staged_kernel" in n for n in names)
     assert any("reduce_kernel" in n for n in names)
+
+
+def test_large_aligned_launch_is_staged_and_matches_oracle(ora):
+    """Rows 64-byte aligned (slice layout, 8 contributions of 70M elements,
+    1.12 GB): at least 1 GiB of contributions takes the staged reduce; the
+    step must match the oracle, and the handle must report the form."""
+    _need_gpu()
+    from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
+    w = _wl("aligned_slice_1gib", 8 * 70_000_000, 8, [3], layout="slice", steps=2)
+    _assert_staged(w)
+    run_parity(ora, w)
+    dw = DeviceWorkload(w)
+    try:
+        assert dw.flat.reduce_form() is None
+        dw.gen_grads(0, dw.scaler().scale)
+        dw.step()
+        assert dw.flat.reduce_form() == "staged"
+    finally:
+        dw.close()
+    small = DeviceWorkload(_wl("aligned_small", 8 * 64 * 1000, 8, [3], layout="slice"))
+    try:
+        small.gen_grads(0, small.scaler().scale)
+        small.step()
+        assert small.flat.reduce_form() == "plain"
+    finally:
+        small.close()

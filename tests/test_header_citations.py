@@ -11,7 +11,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "zero.h")
 
 EXEMPT = {"zero_flat_free", "zero_group_free", "zero_status_string", "zero_last_error",
-          "zero_flat_profile_enable", "zero_flat_profile_read", "zero_flat_device_bytes",
+          "zero_flat_profile_enable", "zero_flat_profile_read", "zero_flat_profile_reduce_form",
+          "zero_flat_device_bytes",
           "zero_shard_step_noalloc"}
 
 DECL = re.compile(r"^(?:const\s+)?(?:zero_status|uint64_t|const char)\s*\*?\s*(zero_\w+)\s*\(",
