@@ -53,19 +53,21 @@ struct ReduceRow {
 };
 // The rows of a single-FlatParameter plan (its ranks, in order).
 void reduce_rows_of(const ReducePlan &p, std::vector<ReduceRow> &rows);
-// Launches that read at least this many contribution bytes take the staged
-// reduce even when every row is 64-byte aligned.  Measured on GB300 (same box,
-// three alternations): the bulk-copy reduce streams 6.8-6.9 TB/s whatever the
-// contributor rows' stride, the plain one 5.97-6.67 TB/s depending on it
-// (10B shard 3.78 -> 3.66 ms, 7B 2.53 -> 2.48, GPT-2's eight shards
-// 0.417 -> 0.391, fp32 contributions at 10B 7.05 -> 6.49, a 10B accumulation
-// launch 4.15 -> 3.98), but the staged launch costs ~10-20 us more in fixed
-// time: slower for the 1-MB tiny step (15.9 -> 17.5 us) and, by 1-3 %, for
-// launches of 1e8-param shards or groups of a few M-param members.
+// A reduce whose rows (over all its launches) hold at least this many
+// contribution bytes takes the staged kernel even when every row is 64-byte
+// aligned.  Measured on GB300 (same box, three alternations, 8 rows x 2
+// stages): the bulk-copy reduce streams 6.8-6.9 TB/s whatever the contributor
+// rows' stride, the plain one 5.97-6.67 TB/s depending on it (10B shard
+// 3.78 -> 3.66 ms, 7B 2.53 -> 2.48, GPT-2's eight shards 0.417 -> 0.391, fp32
+// contributions at 10B 7.05 -> 6.49, a 10B accumulation launch
+// 4.15 -> 3.98), but the staged launch costs more fixed time: slower for the
+// 1-MB tiny step (15.9 -> 17.5 us) and, by 1-3 %, for 1e8-param shards or
+// groups of a few M-param members.  With 4 rows x 3 stages the staged reduce
+// is still 1-6 % slower for reduces of 16 MB-512 MB and equal at 768 MB.
 constexpr size_t kStageAlignedBytes = size_t(1) << 30;
 // Whether rows should take the staged reduce: a row with a full tile, every
 // accumulator 16-byte aligned, and either a row start off a 64-byte boundary
-// or at least kStageAlignedBytes of contributions in the launch.
+// or at least kStageAlignedBytes of contributions over all the rows.
 bool rows_want_staging(int mode, int in_kind, int32_t n_contrib, const ReduceRow *rows,
                        int32_t n_rows);
 // The launches of a reduce over any rows: p supplies the launch-wide settings
@@ -82,7 +84,7 @@ void set_stage_tx_pad(uint32_t bytes);
 
 // Whether a plan's contributions should go through the staged reduce: the
 // shard holds at least one full tile, and some stepped rank has a contributor
-// row whose start is not 64-byte aligned or the launch reads at least
+// row whose start is not 64-byte aligned or the rows hold at least
 // kStageAlignedBytes.  (A 16-byte vector load that starts inside a 64-byte
 // DRAM access unit makes the unit's other half a separate request, which is
 // fetched again: 7 % extra traffic with 32-byte aligned rows; 2-byte aligned

@@ -1,7 +1,7 @@
 """GPU parity of the staged reduce (reduce_staged_kernel): contributor rows
 go through TMA bulk copies of 64-byte-aligned spans into shared memory and
 are re-aligned there.  The planner takes it for rows whose starts are not
-64-byte aligned, and for aligned rows once a launch reads at least 1 GiB of
+64-byte aligned, and for aligned rows once a reduce reads at least 1 GiB of
 contributions.  Every case is compared with the oracle element by element on
 every step, and the CUDA profiler confirms which kernel ran.
 
@@ -134,7 +134,7 @@ def test_staged_accumulation_matches_oracle(ora, w):
 
 def test_small_aligned_launch_keeps_the_plain_kernel():
     """Rows 128-byte aligned and 1 MB of contributions: the plain reduce
-    (its fixed cost is lower; staging pays off from 1 GiB per launch)."""
+    (its fixed cost is lower; staging pays off from 1 GiB per reduce)."""
     _need_gpu()
     names = _step_kernels(_wl("aligned_slice", 8 * 64 * 1000, 8, [3], layout="slice"))
     if not names:
