@@ -89,12 +89,16 @@ def test_bf16_grads_fp16_params(ora):
     run_parity(ora, w)
 
 
-def test_gradients_in_pinned_host_memory():
+@pytest.mark.parametrize("numel,form", [(2_000_017, "staged"), (8 * 65_536, "plain")],
+                         ids=["staged_bulk_copies", "plain_loads"])
+def test_gradients_in_pinned_host_memory(numel, form):
     """The contributions read straight from page-locked host memory (no copy):
-    the bits of the device-resident step."""
+    the bits of the device-resident step -- through the staged reduce's bulk
+    copies (slice rows 16 bytes off 64-byte boundaries) and through the plain
+    reduce's 16-byte loads (aligned rows, a small reduce)."""
     _need_gpu()
     from fsdp_sharded_mixed_zero_gb300.harness import DeviceWorkload
-    w = Workload(name="hostgrads", description="hostgrads", shapes=[(2_000_017,)], world_size=8,
+    w = Workload(name="hostgrads", description="hostgrads", shapes=[(numel,)], world_size=8,
                  ranks=[5], grad_dtype=F16, op=AVG, dynamic=True, steps=3, sigma_g=1e-3,
                  sigma_n=1e-3, grads_layout="slice")
     dev, hst = DeviceWorkload(w), DeviceWorkload(w)
@@ -107,6 +111,7 @@ def test_gradients_in_pinned_host_memory():
                            grad_rank_offset_mul=0)
         assert (ra.overflow, ra.skipped, ra.grad_norm, ra.clip_coef) == \
                (rb.overflow, rb.skipped, rb.grad_norm, rb.clip_coef)
+        assert dev.flat.reduce_form() == hst.flat.reduce_form() == form
     _same(dev.master + dev.m + dev.v + [dev.out], hst.master + hst.m + hst.v + [hst.out])
     dev.close()
     hst.close()
