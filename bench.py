@@ -166,10 +166,16 @@ def measured_peaks():
 
 
 def kernel_source_sha():
+    """Hash of the kernels' code (comments and blank lines left out, so that a
+    comment edit does not void the profiles taken on the same code)."""
     h = hashlib.sha256()
     for name in ("zero_kernels.cu", "zero_kernels.cuh"):
-        with open(os.path.join(ROOT, "fsdp_sharded_mixed_zero_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "fsdp_sharded_mixed_zero_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
+        h.update(code.encode())
     return h.hexdigest()[:16]
 
 

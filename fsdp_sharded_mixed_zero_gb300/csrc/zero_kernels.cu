@@ -8,8 +8,10 @@
 //                       sum-then-split in the numpy demo of "DeepSpeed 与
 //                       FSDP"; fp32 reduce per its MixedPrecision example).
 //   K1 reduce_staged_kernel  the same for contributor rows that are not
-//                       64-byte aligned: TMA bulk copies of aligned spans into
-//                       shared memory, re-aligned there.
+//                       64-byte aligned, and for reduces that read at least
+//                       1 GiB of contributions: a producer warp's TMA bulk
+//                       copies of 64-byte-aligned spans into shared memory,
+//                       re-aligned there by the consumer warps.
 //   K2 the decision     fixed-order total of the partials, global norm, clip
 //                       coefficient, overflow skip and the dynamic loss-scale
 //                       state machine (ZeRO reading §5.1, §5.3): made by the
