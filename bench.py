@@ -365,11 +365,11 @@ def run_collective(args):
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if world > 1:
+    init = rendezvous_method(os.environ, world)
+    if init == "env://":
         dist.init_process_group("nccl", device_id=dev)
     else:
-        dist.init_process_group("nccl", init_method="tcp://127.0.0.1:%d" % _free_port(),
-                                rank=0, world_size=1, device_id=dev)
+        dist.init_process_group("nccl", init_method=init, rank=0, world_size=1, device_id=dev)
     S = args.collective_shard
     full = S * world
     flat = Z.ZeroFlat([(full,)], world, Z.ZERO_F16, Z.ZERO_F16, Z.ZERO_AVG, Z.hparams())
@@ -416,6 +416,17 @@ def run_collective(args):
             "gpu_launches": 3 * args.steps}), flush=True)
     flat.close()
     dist.destroy_process_group()
+
+
+def rendezvous_method(env, world):
+    """How a rank finds the others: the launcher's store ("env://") whenever
+    torchrun started the process -- even for one rank, since under its agent
+    a tcp:// address makes every rank a client of a store that nobody serves
+    -- else, for a single process started directly, a private store on a free
+    local port."""
+    if world > 1 or ("MASTER_ADDR" in env and "MASTER_PORT" in env):
+        return "env://"
+    return "tcp://127.0.0.1:%d" % _free_port()
 
 
 def _free_port():

@@ -108,3 +108,15 @@ def test_host_cpu_names_the_model():
     assert bench.host_cpu("processor\t: 0\nCPU implementer\t: 0x51\nCPU part\t: 0x001\n")[
         "cpu_model"] == "implementer 0x51 part 0x001"
     assert bench.host_cpu("model name\t: Some CPU @ 3GHz\n")["cpu_model"] == "Some CPU @ 3GHz"
+
+
+def test_collective_rendezvous_under_torchrun_uses_the_launchers_store():
+    # one rank under torchrun: the agent's store (a tcp:// address would make
+    # the rank a client of a store nobody serves and wait for its timeout)
+    import bench
+    env = {"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": "29500", "WORLD_SIZE": "1",
+           "TORCHELASTIC_USE_AGENT_STORE": "True"}
+    assert bench.rendezvous_method(env, 1) == "env://"
+    assert bench.rendezvous_method({}, 2) == "env://"
+    m = bench.rendezvous_method({}, 1)                   # started directly: a private store
+    assert m.startswith("tcp://127.0.0.1:") and int(m.rsplit(":", 1)[1]) > 0
