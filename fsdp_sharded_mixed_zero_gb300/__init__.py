@@ -20,7 +20,8 @@ __all__ = [
     "zero_flat_profile_reduce_form",
     "zero_shard_step_noalloc", "zero_grad_accumulate", "zero_shard_step_accumulated",
     "zero_shard_step_q8", "ZERO_Q8_BLOCK", "zero_flat_set_lr", "zero_shard_step_offload",
-    "zero_offload_adamw_host", "zero_debug_set_stage_tx_pad", "zero_shard_reduce",
+    "zero_offload_adamw_host", "zero_debug_set_stage_tx_pad", "zero_debug_reduce_form",
+    "zero_shard_reduce",
     "zero_shard_apply", "zero_shard_apply_partials", "zero_shard_apply_partials_q8",
     "zero_shard_reduce_accumulated",
     "GroupMember", "ZeroGroup", "zero_group_init", "zero_group_step",
@@ -118,6 +119,8 @@ def _load():
                                               C.c_double, vp, C.POINTER(StepResult)]
     L.zero_flat_set_lr.argtypes = [vp, C.c_double]
     L.zero_debug_set_stage_tx_pad.argtypes = [C.c_uint32]
+    L.zero_debug_reduce_form.argtypes = [i32, i32, i32, C.POINTER(u64), C.POINTER(i64),
+                                         C.POINTER(i64), C.POINTER(u64), i32, C.POINTER(i32)]
     L.zero_shard_reduce.argtypes = [vp, C.POINTER(i32), i32, vp, i64, i64, vp, vp, vp]
     L.zero_group_init.argtypes = [C.POINTER(vp), i32, C.POINTER(vp)]
     L.zero_group_step.argtypes = [vp, C.POINTER(GroupMember), C.c_double, vp,
@@ -159,6 +162,7 @@ def _load():
                  "zero_shard_step_noalloc", "zero_grad_accumulate",
                  "zero_shard_step_q8", "zero_flat_set_lr", "zero_shard_step_offload",
                  "zero_offload_adamw_host", "zero_debug_set_stage_tx_pad",
+                 "zero_debug_reduce_form",
                  "zero_shard_reduce", "zero_shard_apply", "zero_shard_apply_partials",
                  "zero_shard_apply_partials_q8", "zero_shard_reduce_accumulated",
                  "zero_group_init", "zero_group_step",
@@ -575,6 +579,22 @@ class ZeroGroup:
 def zero_debug_set_stage_tx_pad(nbytes):
     """Test hook: the staged reduce's waits run out (see include/zero_debug.h)."""
     _check(_lib.zero_debug_set_stage_tx_pad(int(nbytes)), "zero_debug_set_stage_tx_pad")
+
+
+def zero_debug_reduce_form(grad_dtype, n_contrib, rows, mode=0):
+    """The planner's reduce for rows [(contribution address, row stride in
+    elements, shard size[, accumulator address]), ...]: "staged" or "plain".
+    Host logic only (no GPU, nothing dereferenced); mode 0 step, 1 first
+    micro-step, 2 later micro-step."""
+    n = len(rows)
+    ins = (C.c_uint64 * n)(*[int(r[0]) for r in rows])
+    lds = (C.c_int64 * n)(*[int(r[1]) for r in rows])
+    ss = (C.c_int64 * n)(*[int(r[2]) for r in rows])
+    accs = (C.c_uint64 * n)(*[int(r[3]) if len(r) > 3 else 0 for r in rows]) if mode else None
+    out = C.c_int32()
+    _check(_lib.zero_debug_reduce_form(grad_dtype, n_contrib, n, ins, lds, ss, accs, mode,
+                                       C.byref(out)), "zero_debug_reduce_form")
+    return "staged" if out.value else "plain"
 
 
 def zero_flat_set_lr(h, lr):

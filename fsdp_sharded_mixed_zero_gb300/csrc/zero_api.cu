@@ -1176,6 +1176,32 @@ ZERO_API zero_status zero_debug_set_stage_tx_pad(uint32_t bytes) {
     return ZERO_OK;
 }
 
+ZERO_API zero_status zero_debug_reduce_form(zero_dtype grad_dtype, int32_t n_contrib,
+                                            int32_t n_rows, const uint64_t *in_addr,
+                                            const int64_t *ld, const int64_t *shard,
+                                            const uint64_t *acc_addr, int32_t mode,
+                                            int32_t *staged) {
+    if (!staged || !in_addr || !ld || !shard || n_rows < 1 || n_contrib < 1)
+        return fail(ZERO_ERR_INVALID_ARG, "NULL output or rows, or no rows or contributors");
+    if (grad_dtype != ZERO_F16 && grad_dtype != ZERO_BF16 && grad_dtype != ZERO_F32)
+        return fail(ZERO_ERR_INVALID_ARG, "unknown contribution dtype");
+    if (mode < 0 || mode > 2) return fail(ZERO_ERR_INVALID_ARG, "mode must be 0, 1 or 2");
+    if (mode != 0 && !acc_addr) return fail(ZERO_ERR_INVALID_ARG, "accumulator addresses missing");
+    std::vector<zg::ReduceRow> rows((size_t)n_rows);
+    for (int32_t j = 0; j < n_rows; ++j) {
+        rows[j].in = reinterpret_cast<const void *>((uintptr_t)in_addr[j]);
+        rows[j].ld = ld[j];
+        rows[j].S = shard[j];
+        rows[j].valid = shard[j];
+        rows[j].acc = mode ? reinterpret_cast<float *>((uintptr_t)acc_addr[j]) : nullptr;
+    }
+    const int kind = grad_dtype == ZERO_F32 ? zg::kInF32
+                                            : (grad_dtype == ZERO_BF16 ? zg::kInBF16 : zg::kInF16);
+    const int m = mode == 0 ? zg::kModeStep : (mode == 1 ? zg::kModeAccFirst : zg::kModeAccAdd);
+    *staged = zg::rows_want_staging(m, kind, n_contrib, rows.data(), n_rows) ? 1 : 0;
+    return ZERO_OK;
+}
+
 ZERO_API zero_status zero_flat_set_lr(zero_flat *h, double lr) {
     if (!h) return fail(ZERO_ERR_INVALID_ARG, "handle is NULL");
     if (!std::isfinite(lr) || lr < 0) return fail(ZERO_ERR_INVALID_ARG, "lr must be finite and >= 0");
