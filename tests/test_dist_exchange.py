@@ -1,7 +1,8 @@
 """The multi-rank step's exchanges on CPU ranks (gloo, 2 and 3 processes):
 
 - the all-to-all of the reduce-scatter delivers, on rank r, slice r of every
-  rank's gradient in contributor order;
+  rank's gradient in contributor order, bit for bit for fp16, bf16 (every
+  2-byte pattern) and fp32 contributions;
 - the partials' all-gather delivers every rank's values in rank order;
 - the slot all-gather leaves every rank with every owner's slot;
 - the composition: every rank reduces the rows it received, the ranks
@@ -56,6 +57,23 @@ def _exchange_worker(rank, world, port, S):
     got = recv.view(torch.int16).numpy().view(np.uint16)
     for c in range(world):
         assert np.array_equal(got[c], _grad_of(c, padded)[rank * S:(rank + 1) * S]), (rank, c)
+    # bf16 contributions travel as the same 2-byte words (every bit pattern,
+    # NaN payloads included), fp32 ones as they are
+    bits = np.random.default_rng(77 + rank).integers(0, 1 << 16, padded, dtype=np.uint16)
+    mine_b = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16)
+    recv_b = torch.empty((world, S), dtype=torch.bfloat16)
+    D.exchange_contributions(mine_b, recv_b)
+    got_b = recv_b.view(torch.int16).numpy().view(np.uint16)
+    for c in range(world):
+        want = np.random.default_rng(77 + c).integers(0, 1 << 16, padded, dtype=np.uint16)
+        assert np.array_equal(got_b[c], want[rank * S:(rank + 1) * S]), ("bf16", rank, c)
+    f32 = np.random.default_rng(99 + rank).standard_normal(padded).astype(np.float32)
+    recv_f = torch.empty((world, S), dtype=torch.float32)
+    D.exchange_contributions(torch.from_numpy(f32), recv_f)
+    for c in range(world):
+        want = np.random.default_rng(99 + c).standard_normal(padded).astype(np.float32)
+        assert np.array_equal(recv_f[c].numpy().view(np.uint32),
+                              want[rank * S:(rank + 1) * S].view(np.uint32)), ("f32", rank, c)
     ss = torch.tensor([rank + 0.25], dtype=torch.float64)
     of = torch.tensor([rank % 2], dtype=torch.int32)
     all_ss = torch.empty(world, dtype=torch.float64)
