@@ -13,7 +13,7 @@ micro-step accumulation, and the int8 payload quantizer.
 
 CPU only; the copies run in parallel subprocesses.  The two slowest cast pins
 (every fp16 and bf16 rounding pattern) are left out of the mutant runs, except
-for the mistake in the cast itself."""
+for the mistakes in the casts and the decode."""
 import os
 import shutil
 import subprocess
@@ -90,6 +90,46 @@ MISTAKES = {
                           "const float scale = amax / 128.0f;"),
     "q8_rounds_half_away": ("const float r = rintf(v);", "const float r = roundf(v);"),
     "q8_truncates": ("const float r = rintf(v);", "const float r = truncf(v);"),
+    "q8_nan_in_amax": ("if (a > amax) amax = a;", "if (!(a <= amax)) amax = a;"),
+    # more of the casts and the decode (IEEE-754 binary16 / bfloat16)
+    "cast_subnormal_cutoff": ("if (shift >= 25) {", "if (shift >= 24) {"),
+    "cast_overflow_threshold": ("if (e > 15) return sign | 0x7c00u;",
+                                "if (e > 16) return sign | 0x7c00u;"),
+    "cast_nan_to_inf": ("return (uint16_t)(sign | 0x7e00u | (man >> 13));",
+                        "return (uint16_t)(sign | 0x7c00u);"),
+    "cast_bf16_ties_up": ("if (lo > 0x8000u || (lo == 0x8000u && (hi & 1u))) hi += 1u;",
+                          "if (lo >= 0x8000u) hi += 1u;"),
+    "decode_f16_subnormal_scale": ("mag = (float)ldexp((double)man, -24);",
+                                   "mag = (float)ldexp((double)man, -25);"),
+    # more of AdamW
+    "decay_without_lr": ("const float decay = (float)(1.0 - hp->lr * hp->weight_decay);",
+                         "const float decay = (float)(1.0 - hp->weight_decay);"),
+    "eps_inside_sqrt": ("th = th - (lr * mh) / (sqrtf(vh) + eps);",
+                        "th = th - (lr * mh) / sqrtf(vh + eps);"),
+    "bc2_with_beta1": ("const float bc2 = (float)(1.0 - pow(hp->beta2, (double)t));",
+                       "const float bc2 = (float)(1.0 - pow(hp->beta1, (double)t));"),
+    # more of the reduce, the norm and the decision
+    "contributors_reversed": (
+        "for (int32_t c = 0; c < n_contrib; ++c)\n"
+        "            acc = acc + contribution(grads, grad_kind, (int64_t)c * ld + rank_off + i);",
+        "for (int32_t c = n_contrib - 1; c >= 0; --c)\n"
+        "            acc = acc + contribution(grads, grad_kind, (int64_t)c * ld + rank_off + i);"),
+    "unscale_before_avg": ("if (avg) acc = acc / (float)n_contrib;\n        g_out[i] = acc / scale;",
+                           "acc = acc / scale;\n        if (avg) acc = acc / (float)n_contrib;\n"
+                           "        g_out[i] = acc;"),
+    "extra_norm_dropped": ("const double norm = sqrt(ora_norm_sum(&acc) + extra_norm_sq);",
+                           "const double norm = sqrt(ora_norm_sum(&acc));"),
+    "norm_bit_position": ("int off = q - 53 - ORA_ACC_UNIT_EXP;",
+                          "int off = q - 52 - ORA_ACC_UNIT_EXP;"),
+    "norm_high_part_shift": ("if (sh) acc_add_at(a, limb + 1, m >> (64 - sh));",
+                             "if (sh) acc_add_at(a, limb + 1, m >> (63 - sh));"),
+    "norm_sticky_skips_bit0": (
+        "for (int i = low - 1; i >= 0 && !sticky; --i) sticky = acc_bit(a, i);",
+        "for (int i = low - 1; i > 0 && !sticky; --i) sticky = acc_bit(a, i);"),
+    "clip_epsilon": ("const double q = hp->max_grad_norm / (norm + 1e-6);",
+                     "const double q = hp->max_grad_norm / (norm + 1e-5);"),
+    "static_scale_ignored": (": (float)hp->static_loss_scale;", ": 1.0f;"),
+    "overflow_not_counted": ("st->overflow_count += 1;", ""),
 }
 
 
@@ -113,7 +153,7 @@ def _run_pins(tmp, name, mistake):
             f.write(src.replace(old, new))
     cmd = [sys.executable, "-m", "pytest", "tests/test_oracle_pins.py", "-x", "-q",
            "-p", "no:cacheprovider"]
-    if name != "cast_ties_away":
+    if not name.startswith(("cast_", "decode_")):
         for t in SLOW_CASTS:
             cmd += ["--deselect", t]
     env = dict(os.environ, PYTHONDONTWRITEBYTECODE="1")

@@ -316,6 +316,11 @@ def test_sum_of_squares_rounding_ties(ora):
     assert ora.sum_of_squares(x)[0] == float(Fr(2 ** 53 + 1))   # ties to even: 2^53
     y = np.array([2.0 ** 26, 2.0 ** 26, 1.0, 1.0, 1.0], np.float32)  # 2^53 + 3
     assert ora.sum_of_squares(y)[0] == float(Fr(2 ** 53 + 3))   # ties to even: 2^53 + 4
+    # a tie broken by the smallest possible square: (2^-149)^2 = 2^-298, the
+    # lowest bit the exact sum can hold, lifts 2^53 + 1 above the halfway point
+    z = np.array([2.0 ** 26, 2.0 ** 26, 1.0, 2.0 ** -149], np.float32)
+    exact = Fr(2 ** 53 + 1) + Fr(1, 2 ** 298)
+    assert ora.sum_of_squares(z)[0] == float(exact) == 2.0 ** 53 + 2
 
 
 # --------------------------------------------------------------------------
@@ -576,7 +581,10 @@ def _brute_step(hp, grads, N, S, full, ranks, master, m, v, scale, t, avg, extra
 
 
 @pytest.mark.parametrize("N,n,avg,scale", [(2, 8, True, 1024.0), (3, 8, False, 1.0),
-                                           (3, 8, True, 65536.0)])
+                                           (3, 8, True, 65536.0),
+                                           # a static scale that is not a power of two:
+                                           # the AVG division and the unscale each round
+                                           (3, 8, True, 5.0)])
 def test_brute_force_tiny(ora, N, n, avg, scale):
     rng = np.random.default_rng(N * 100 + n)
     full, S, padded = ora.layout([n], N)
@@ -605,6 +613,41 @@ def test_brute_force_tiny(ora, N, n, avg, scale):
         want_out = np.array(outs, np.float32).astype(np.float16).view(np.uint16)
         assert np.array_equal(out, want_out)
         grads = (rng.standard_normal((N, padded)) * scale * 0.1).astype(np.float16)
+
+
+def test_one_rank_with_the_others_norm_share_steps_like_all_ranks(ora):
+    # The clip / skip decision is one decision over every rank's gradient (ZeRO
+    # reading §5.3): a rank stepped alone with extra_norm_sq = the other ranks'
+    # sum of squares (here math.fsum over their reduced gradients) takes the
+    # decision of the all-ranks step and updates its shard the same way.
+    rng = np.random.default_rng(21)
+    N, n = 4, 4001
+    full, S, padded = ora.layout([n], N)
+    hp = ora.hparams(lr=1e-3, max_grad_norm=1.0, dynamic=False, static_scale=1.0)
+    grads = (rng.standard_normal((N, padded)) * 0.05).astype(np.float16)
+    grads[:, full:] = 0
+    theta = (rng.standard_normal(padded) * 0.02).astype(np.float32)
+    r = 2
+    others = [ora.reduce_unscale(grads.view(np.uint16), padded, k * S, N, S, k * S, full,
+                                 avg=True, scale=1.0) for k in range(N) if k != r]
+    extra = math.fsum(float(x) * float(x) for g in others for x in g)
+    st_all, st_one = ora.scaler_init(hp), ora.scaler_init(hp)
+    all_state = [[theta[k * S:(k + 1) * S].copy() for k in range(N)],
+                 [np.zeros(S, np.float32) for _ in range(N)],
+                 [np.zeros(S, np.float32) for _ in range(N)]]
+    one_state = [[theta[r * S:(r + 1) * S].copy()], [np.zeros(S, np.float32)],
+                 [np.zeros(S, np.float32)]]
+    out_all, out_one = np.zeros(padded, np.uint16), np.zeros(padded, np.uint16)
+    ra = ora.shard_step(hp, st_all, N, full, S, list(range(N)), grads.view(np.uint16), padded,
+                        S, *all_state, out_all)
+    ro = ora.shard_step(hp, st_one, N, full, S, [r], grads.view(np.uint16), padded, S,
+                        *one_state, out_one, extra_norm_sq=extra)
+    assert ra.clip_coef < 1.0                                  # clipping is active
+    assert abs(ro.grad_norm - ra.grad_norm) <= 4e-16 * ra.grad_norm
+    assert (ro.overflow, ro.skipped, ro.clip_coef) == (ra.overflow, ra.skipped, ra.clip_coef)
+    for x, y in zip(one_state, all_state):
+        assert np.array_equal(x[0], y[r])
+    assert np.array_equal(out_one[r * S:(r + 1) * S], out_all[r * S:(r + 1) * S])
 
 
 # --------------------------------------------------------------------------
