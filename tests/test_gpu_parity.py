@@ -116,6 +116,13 @@ EDGE = [
     # 256 contributions through the staged reduce: odd shard (4,097), rows
     # 8,208 bytes apart (16 bytes off a 64-byte boundary)
     _wl("n256_staged", [(256 * 4_097,)], 256, [201], layout="slice", steps=3),
+    # a static loss scale that is not a power of two: the unscale is an IEEE
+    # division (not an exact reciprocal multiply) after the AVG division by 3;
+    # plain reduce (aligned rows) and staged reduce (odd shard) both
+    _wl("static_scale5_n3_aligned", [(3 * 65_536,)], 3, [0, 1, 2], dynamic=False,
+        hp=dict(static_scale=5.0)),
+    _wl("static_scale5_n3_staged", [(3 * 30_001,)], 3, [0, 1, 2], dynamic=False,
+        hp=dict(static_scale=5.0)),
 ]
 
 
