@@ -108,6 +108,12 @@ ACCUM = [
         steps=2),
     # more ranks than one launch takes
     _wl("accum_n70", [(70 * 33 + 1,)], 70, list(range(70)), micro=2, steps=2),
+    # a static loss scale of 5: the norm pass and AdamW divide the accumulator
+    # by a scale that is not a power of two (an IEEE division); rank slices
+    # 8 bytes off 64-byte boundaries and 16-byte-aligned accumulator rows, so
+    # the accumulation launches are staged
+    _wl("accum_static_scale5", [(3 * 40_004 - 1,)], 3, [0, 1, 2], dynamic=False, micro=2,
+        steps=2, hp=dict(static_scale=5.0)),
 ]
 
 
