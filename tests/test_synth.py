@@ -60,3 +60,18 @@ def test_grads_recipe():
     assert b.shape == (2, n) and b.dtype == np.uint16
     z = synth.grads_host(5, 1, 2, 0, 10, 1.0, 1.0, zero_from=6)
     assert not z[:, 6:].any() and z[:, :6].all()
+
+
+def test_workload_shapes_are_the_architectures():
+    # the FlatParameters of the synthetic workloads hold exactly the parameters of
+    # the architectures they stand for (element counts and tensor counts):
+    # GPT-2 small with a tied head 124,439,808 in 148 tensors; the 48-layer,
+    # d=1600 GPT-2 (the 1.5B model) 1,557,611,200 in 580; the Llama-shaped 7B
+    # with an untied head 6,738,415,616 in 291
+    from synth import workloads as W
+    for w, numel, tensors in ((W.GPT2, 124_439_808, 148), (W.GPT_1P5B, 1_557_611_200, 580),
+                              (W.LLAMA_7B, 6_738_415_616, 291)):
+        assert sum(int(np.prod(s)) for s in w.shapes) == numel, w.name
+        assert len(w.shapes) == tensors, w.name
+    # the tiny MLP: [512x1024, 1024, 1024x512, 512]
+    assert sum(int(np.prod(s)) for s in W.TINY.shapes) == 1_050_112
