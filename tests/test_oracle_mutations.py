@@ -6,10 +6,11 @@ order, a rounding rule changed, a carry lost), rebuilds that copy and runs
 the pin suite (tests/test_oracle_pins.py) against it: at least one pin must
 fail.  The untouched copy must pass, so a failure is the mistake's doing.
 
-The mistakes cover every function of the step: the reduce and unscale, the
-exact norm accumulator, the decision (clipping, loss-scale state machine),
-AdamW with bias correction and decoupled decay, the RNE casts, the
-micro-step accumulation, and the int8 payload quantizer.
+The mistakes cover every function of the oracle: the layout and the memory
+accounting, the reduce and unscale, the exact norm accumulator, the decision
+(clipping, loss-scale state machine), AdamW with bias correction and
+decoupled decay, the RNE casts and decodes, the micro-step accumulation, and
+the int8 payload quantizer.
 
 CPU only; the copies run in parallel subprocesses.  The two slowest cast pins
 (every fp16 and bf16 rounding pattern) are left out of the mutant runs, except
@@ -130,6 +131,18 @@ MISTAKES = {
                      "const double q = hp->max_grad_norm / (norm + 1e-5);"),
     "static_scale_ignored": (": (float)hp->static_loss_scale;", ": 1.0f;"),
     "overflow_not_counted": ("st->overflow_count += 1;", ""),
+    # the layout ("PyTorch FSDP ..." §3.1, §3.3) and the memory accounting
+    # ("DeepSpeed 与 FSDP" §逐步推导, §ZeRO-3 的数学总结)
+    "shard_size_floor": ("int64_t s = total / world_size + (total % world_size != 0);",
+                         "int64_t s = total / world_size;"),
+    "layout_gap_accepted": ("if (starts[k] != total) return ORA_EINVAL;", ""),
+    "zero2_grads_not_split": ("    {0, 1, 1},   /* ZeRO-2: + gradients */",
+                              "    {0, 0, 1},   /* ZeRO-2: + gradients */"),
+    "zero1_params_split": ("    {0, 0, 1},   /* ZeRO-1: optimizer states */",
+                           "    {1, 0, 1},   /* ZeRO-1: optimizer states */"),
+    "optimizer_8_bytes": ("const uint64_t per[3] = {2, 2, 12};",
+                          "const uint64_t per[3] = {2, 2, 8};"),
+    "memory_rounds_down": ("u128 q = num / den + (num % den != 0);", "u128 q = num / den;"),
 }
 
 
